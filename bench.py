@@ -1,0 +1,357 @@
+"""Benchmark of one sparse MoE layer's forward pass on B300 (the decode workload by default).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload decode]
+
+A step is one whole pass (router + top-k, bucketing, slot-table lookup inside the expert
+FFN, SwiGLU experts, combine) over one batch of T tokens. Batches rotate over 16 seeded
+inputs, so each step routes to its own experts. A 512 MiB buffer (larger than the 126 MB
+L2) is written between timed steps, outside the timed events. Times are CUDA events on
+the launching stream, and the maximum is taken over ranks. One JSON line is printed by rank 0.
+
+--impl reference times the CPU oracle on this host's cores instead, over the same
+workload and metric (one oracle layer pass per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill int8 TOPS as % of B300 peak"
+N_BATCHES = 16
+FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6400.0, 1800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks ----------------
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            self.path = f"/tmp/moe_bench_clocks_{os.getpid()}.csv"
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [c.strip() for c in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx = float(f[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle ------------
+
+def _gen_expert(args):
+    import synth
+    seed, layer, e, d, f, sigma = args
+    return e, synth.expert_arrays(seed, layer, e, d, f, sigma)
+
+
+def oracle_experts(w, layer: int, ids, workers: int):
+    """Expert arrays for the oracle, made by the numpy generator in a spawn process pool."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    ids = sorted(set(int(e) for e in ids))
+    jobs = [(w.seed, layer, e, w.d, w.f, w.expert_sigma) for e in ids]
+    with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+        return dict(ex.map(_gen_expert, jobs))
+
+
+def prepare_oracle(w, batches):
+    """Inputs of the timed oracle passes: activations, router and every expert the batches
+    route to (made before, and outside, the timing)."""
+    from oracle import moe_oracle as O
+    router = w.router(0)
+    xs = [w.x_f64(b) for b in batches]
+    need = set()
+    for x in xs:
+        need |= set(O.select_topk(O.router_logits(x, router), w.k).reshape(-1).tolist())
+    need |= {w.E + s for s in range(w.n_shared)}
+    ex = oracle_experts(w, 0, need, workers=max(1, min(16, os.cpu_count() or 1)))
+    return xs, router, ex
+
+
+def time_oracle(w, prep, budget_s: float, max_steps: int | None = None):
+    """Times the oracle's layer pass over the prepared batches, one batch per step, with one
+    BLAS thread. Returns (tokens/s, steps, seconds, threads)."""
+    from threadpoolctl import threadpool_limits
+    from oracle import moe_oracle as O
+    xs, router, ex = prep
+    shared = [ex[w.E + s] for s in range(w.n_shared)]
+    steps, t0 = 0, time.perf_counter()
+    with threadpool_limits(limits=1):
+        while True:
+            O.moe_layer(xs[steps % len(xs)], router, w.k, lambda e: ex[e], shared)
+            steps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or (max_steps is not None and steps >= max_steps):
+                break
+    return w.T * steps / el, steps, el, 1
+
+
+# ------------------------------------------------------------------ distributed -----------
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("MOE_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def dist_max(v: float, ws: int, device) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ reference arm ---------
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    from synth.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    batches = list(range(4))
+    prep = prepare_oracle(w, batches)
+    # W untimed oracle passes, then K timed ones (one batch of T tokens per step), stopping
+    # early once 150 s have passed so that the run stays within a few minutes
+    time_oracle(w, prep, budget_s=1e9, max_steps=max(W, 1))
+    tps, steps, el, cores = time_oracle(w, prep, budget_s=150.0, max_steps=K)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps,
+        "warmup": W, "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.describe(), "tokens_per_step": w.T},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{steps} oracle layer passes over {len(batches)} rotating batches of T={w.T}"},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm ---------------
+
+def run_ours(args, ws, rank, local):
+    import torch
+    from routed_expert_ffn_bucketing_b300 import _lib as L
+    from routed_expert_ffn_bucketing_b300 import layer as lay
+    from synth.device import DeviceLayer
+    from synth.workloads import WORKLOADS
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    hbm_peak, _, peak_kind = peaks()
+
+    dl = DeviceLayer(w, device=str(dev))
+    xs = [dl.x(b) for b in range(N_BATCHES)]
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    buf = lay.alloc_buffers(s, device=dev, ydt=L.MOE_F32, odt=L.MOE_BF16, keep_logits=False)
+    table = L.expert_table(dl.pool, dl.slot_bytes, dl.slot_of, dl.shared_ptr)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    xdt = L.MOE_BF16
+
+    def step(x):
+        lay.forward(buf, x, dl.router, table, L.MOE_MODE_AUTO, stream=stream)
+
+    # active experts per batch (for the algorithmic byte count), from untimed passes
+    n_active = []
+    for b in range(N_BATCHES):
+        step(xs[b])
+        torch.cuda.synchronize(dev)
+        n_active.append(int(buf.active[0].item()))
+        assert L.moe_read_status(buf.ws) == 0
+    for i in range(W):
+        flush.fill_(i & 0xFF)
+        step(xs[i % N_BATCHES])
+    torch.cuda.synchronize(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        x = xs[i % N_BATCHES]
+        e0, e1, e2, e3 = ev[i]
+        e0.record(stream)
+        L.moe_route(s, x, xdt, dl.router, buf.topk_idx, buf.topk_w, None, buf.ws, buf.ws_bytes, stream)
+        L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
+                      buf.ws_bytes, stream)
+        e1.record(stream)
+        L.moe_expert_ffn(s, L.MOE_MODE_AUTO, x, xdt, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm,
+                         buf.ydt, buf.ws, buf.ws_bytes, stream)
+        e2.record(stream)
+        L.moe_combine(s, buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, stream)
+        e3.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(d) for a, _, _, d in ev]
+    ffn_ms = [b.elapsed_time(c) for _, b, c, _ in ev]
+    route_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
+    comb_ms = [c.elapsed_time(d) for _, _, c, d in ev]
+    total_s = dist_max(sum(step_ms) / 1e3, ws, dev)
+    value = ws * w.T * K / total_s
+
+    # algorithmic bytes of the expert-FFN launch: each selected expert's record once, x rows
+    # staged, h written and read (fp32), y_perm written (fp32)
+    rows = w.P + w.T * w.n_shared
+    small = rows * (w.d * 2 + 2 * w.f * 4 + w.d * 4)
+    ffn_bytes = [(n_active[i % N_BATCHES] + w.n_shared) * w.record_bytes + small for i in range(K)]
+    achieved = sum(ffn_bytes) / (sum(ffn_ms) / 1e3) / 1e9
+    router_bytes = w.d * w.E * 4
+    step_bytes = [b + router_bytes for b in ffn_bytes]
+    step_gbs = sum(step_bytes) / (sum(step_ms) / 1e3) / 1e9
+
+    # end to end through the public API with host buffers: pinned x in, bf16 out back, per step
+    x_host = [x.cpu().pin_memory() for x in xs]
+    out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(xs[0])
+    e2e_s = 0.0
+    for i in range(W + K):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        x_dev.copy_(x_host[i % N_BATCHES], non_blocking=True)
+        step(x_dev)
+        out_host.copy_(buf.out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        if i >= W:
+            e2e_s += time.perf_counter() - t0
+    e2e_s = dist_max(e2e_s, ws, dev)
+    e2e = {"value": ws * w.T * K / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
+           "d2h_bytes_per_step": w.T * w.d * 2}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tps, steps, el, cores = time_oracle(w, prepare_oracle(w, list(range(4))), budget_s=args.cpu_seconds)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{steps} oracle layer passes ({el:.1f} s) over 4 rotating batches of T={w.T}"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": sum(step_ms) / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": w.describe(), "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
+                   "activations": "bf16", "l2": "512 MiB buffer written between timed steps (outside events)",
+                   "batches": N_BATCHES, "mean_active_experts": float(np.mean(n_active)),
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"kernel": "moe_expert_ffn (gate/up + SwiGLU, down)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                     "bytes_per_launch": float(np.mean(ffn_bytes)), "ms_per_launch": sum(ffn_ms) / K},
+        "stages_ms": {"route_permute": sum(route_ms) / K, "expert_ffn": sum(ffn_ms) / K,
+                      "combine": sum(comb_ms) / K},
+        "step_hbm_gbs": step_gbs,
+        "wall_s": wall,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": 6 * K,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

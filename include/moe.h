@@ -1,0 +1,233 @@
+/*
+ * moe.h: C-ABI of the B300 (sm_103a) sparse MoE layer forward pass.
+ *
+ * One MoE layer's forward pass runs as five calls on one CUDA stream:
+ *
+ *   moe_route       router logits (fp32), top-k and renormalised gate weights
+ *   moe_permute     bucketing: group the (token, slot) pairs by expert
+ *   moe_expert_ffn  each selected expert's SwiGLU FFN over int8 block-32 weights, looked up
+ *                   through the resident slot table, plus the always-on shared experts
+ *   moe_combine     weighted sum of the expert outputs per token (unpermute)
+ *   slot_table_*    host-side slot pool for experts that do not all fit on the device: a miss
+ *                   is copied from pinned host memory on a side stream
+ *
+ * Sources. The pages on the Strata engine describe the method:
+ *   [P5] "单张RTX 5090跑125B大模型：Strata实测Qwen3.8 Flash Next", section "MoE专家按需调度":
+ *        a light router picks the top-K experts per token and the other experts take no part;
+ *        experts not selected can leave VRAM and are brought back when the router picks them.
+ *   [P2] "Strata 工作原理图解GPU内存SSD三级存储如何让125B模型塞进消费级显卡":
+ *        section "三级存储分工": router and shared expert resident in VRAM, all experts pinned in RAM;
+ *        section "专家缓存": a VRAM expert cache of the most used experts; misses live in RAM;
+ *        section "长文本": the next layer's experts stream over PCIe while the current layer computes.
+ *   [P3] "Strata 性能基准与论文导读125B MoE在消费级硬件上的极限测量与瓶颈分析", section "瓶颈分析 1️⃣":
+ *        quantised expert matmuls on tensor cores without a separate dequantisation pass.
+ * The pages leave the FFN form, weight format, gate and tie-break open. The readings taken
+ * here are: SwiGLU without biases; int8 codes with one fp16 scale per 32 elements of the
+ * reduction dimension; softmax over all E restricted to the top k and renormalised; ties to
+ * the lowest expert index; and shared experts added with weight 1.
+ *
+ * Conventions for every call:
+ *  - All pointers are DEVICE pointers unless the name starts with h_. The caller owns all
+ *    memory, and the library allocates nothing on any of these calls.
+ *  - Arrays are dense and row-major. x, y_perm, out, w_router and the workspace must be
+ *    16-byte aligned (the workspace 256-byte aligned). Expert records are 256-byte aligned.
+ *  - Calls are asynchronous on `stream` and return at once. A negative moe_status is a
+ *    host-side error found before any launch (nothing was enqueued) or a failed launch.
+ *  - Errors found by kernels (a NaN logit, an expert index out of range, a routed expert
+ *    with no resident slot) set bits of a device status word in the workspace. Nothing
+ *    traps. moe_read_status() returns that word.
+ *  - T == 0 is valid: each call checks its arguments and enqueues nothing.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
+typedef struct CUevent_st* moe_event_t;   /* the same type as cudaEvent_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,        /* null pointer, bad shape, misalignment, k > E, d or f not a multiple of 32 */
+  MOE_EUNSUPPORTED = -2,  /* valid but outside what the kernels handle (e.g. k > 32, E > 1024) */
+  MOE_ECUDA = -3,         /* a CUDA launch or copy failed; moe_last_error_string() has the detail */
+  MOE_ENOSLOT = -4,       /* slot_table_update: more misses than evictable slots */
+  MOE_EDEVICE = -5        /* moe_read_status: the device status word is non-zero */
+} moe_status;
+
+/* device status word bits (moe_read_status) */
+#define MOE_DEV_NAN_LOGIT    0x1  /* a router logit was NaN; it was ranked below every number */
+#define MOE_DEV_BAD_EXPERT   0x2  /* a topk_idx entry was outside [0, E); outputs are undefined */
+#define MOE_DEV_MISSING_SLOT 0x4  /* a routed expert had slot_of[e] < 0; its rows were left unwritten */
+
+typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
+
+/* moe_expert_ffn kernel family. AUTO: DECODE when T <= 16 or x is fp32, else PREFILL.
+ * DECODE streams each selected expert's int8 rows once per group of up to 8 of its tokens
+ * (fp32 arithmetic on exactly dequantised weights). PREFILL is the tensor-core grouped
+ * GEMM (bf16 operands after shared-memory dequantisation, fp32 accumulation); it
+ * requires bf16 x. */
+typedef enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL = 2 } moe_mode;
+
+/* Problem shape. T tokens, model width d, expert hidden width f, E routed experts,
+ * top-k, n_shared always-on experts. P = T * k routed (token, slot) pairs. */
+typedef struct {
+  int32_t T, d, f, E, k, n_shared;
+} moe_shape;
+
+/* Byte offsets of one expert record. Each section starts on a 256-byte boundary:
+ *   gate_q [f][d] int8, up_q [f][d] int8, down_q [d][f] int8,
+ *   gate_s [f][d/32] fp16, up_s [f][d/32] fp16, down_s [d][f/32] fp16.
+ * Weight W[r][i] = q[r][i] * s[r][i/32]; blocks run along the reduction dimension. */
+typedef struct {
+  uint64_t gate_q, up_q, down_q, gate_s, up_s, down_s, record_bytes;
+} moe_expert_layout;
+
+/* Fills *out for (d, f). Host only, no CUDA call. MOE_EINVAL if d or f is not a positive
+ * multiple of 32 or out is NULL. */
+moe_status moe_get_expert_layout(int32_t d, int32_t f, moe_expert_layout* out);
+
+/* Where the experts of one layer live.
+ *  pool       device: slot records, slot s at pool + s * slot_bytes
+ *  slot_bytes stride of the pool: >= record_bytes and a multiple of 256
+ *  slot_of    device int32 [E]: slot of routed expert e, or -1 when it is not resident
+ *             (the row of one layer of the slot table; [P2] "专家缓存")
+ *  shared     device: n_shared records at shared + s * slot_bytes; NULL iff n_shared == 0
+ * The table is only read. It is the caller's (or slot_table_update's) job to keep it current. */
+typedef struct {
+  const void* pool;
+  uint64_t slot_bytes;
+  const int32_t* slot_of;
+  const void* shared;
+} moe_expert_table;
+
+/* Bytes of workspace that moe_route / moe_permute / moe_expert_ffn need for this shape
+ * (any mode, either dtype). One workspace serves one layer's calls from moe_route to
+ * moe_combine. Its first 256 bytes hold the device status word. Host only. */
+moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes);
+
+/* Router and top-k ([P5] "MoE专家按需调度": the router picks the top-K experts per token).
+ *  x          [T][d], bf16 (xdt = MOE_BF16) or fp32 (MOE_F32)
+ *  w_router   fp32 [d][E]
+ *  topk_idx   out int32 [T][k]: the k experts with the largest fp32 logits, descending
+ *             logit, ties to the lowest index, -0.0 equal to +0.0, NaN below every number
+ *  topk_w     out fp32 [T][k]: exp(l_j - l_0) / sum_j' exp(l_j' - l_0) over the selected
+ *             logits (equal to softmax over all E, restricted and renormalised)
+ *  logits_opt out fp32 [T][E] or NULL: logit[t][e] = sum_i x[t][i] * w_router[i][e], fp32
+ *             accumulation in a fixed order (deterministic)
+ *  ws         workspace of moe_workspace_size bytes. The status word is cleared here.
+ * Limits: k <= 32 and E <= 1024 (else MOE_EUNSUPPORTED). */
+moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                     int32_t* topk_idx, float* topk_w, float* logits_opt, void* ws, size_t ws_bytes,
+                     moe_stream_t stream);
+
+/* Bucketing and permutation of the P = T*k pairs by expert, so that each selected expert's
+ * weights are streamed once for all of its tokens ([P2] "专家缓存": the GPU computes the
+ * experts the cache holds). Deterministic and free of atomics.
+ *  topk_idx    int32 [T][k]; pair p = t*k + j routes token t to expert topk_idx[p]
+ *  counts      out int32 [E]: pairs routed to each expert
+ *  offsets     out int32 [E+1]: exclusive prefix sum of counts (offsets[E] = P)
+ *  sorted_pair out int32 [P]: pair ids grouped by expert, ascending pair id inside a group
+ *  inv_pos     out int32 [P]: position of pair p in sorted_pair
+ *  active      out int32 [1 + min(E, P)]: active[0] = number of experts with a pair, then
+ *              those experts in ascending order
+ * An index outside [0, E) sets MOE_DEV_BAD_EXPERT (outputs then undefined, all writes in bounds). */
+moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t* counts,
+                       int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int32_t* active,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Expert FFN: for every expert in `active` (and every shared expert), for each of its rows
+ * y = W_down (silu(W_gate x) * (W_up x)), silu(z) = z / (1 + e^-z), W = q * s per block of 32.
+ * The expert's record is found through the slot table (experts->slot_of).
+ *  x           [T][d] (xdt), the same activations given to moe_route
+ *  offsets, sorted_pair, active: from moe_permute (active may also be any caller list in
+ *              the same format, e.g. only the experts already resident)
+ *  y_perm      out [P + T*n_shared][d] (ydt): row offsets[e] + i holds expert e's output for
+ *              pair sorted_pair[offsets[e] + i]; row P + s*T + t holds shared expert s for token t
+ *  ydt         MOE_F32 or MOE_BF16 (a bf16 y_perm halves the combine's reads)
+ * PREFILL mode needs xdt = MOE_BF16. A routed expert with slot_of[e] < 0 sets
+ * MOE_DEV_MISSING_SLOT and its rows are not written. */
+moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, moe_dtype xdt,
+                          const moe_expert_table* experts, const int32_t* offsets,
+                          const int32_t* sorted_pair, const int32_t* active, void* y_perm,
+                          moe_dtype ydt, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Combine / unpermute ([P5]: the token's output is the gated mixture of its selected
+ * experts; [P2] "三级存储分工": the shared expert applies to every token):
+ *   out[t] = sum_{j=0..k-1} topk_w[t][j] * y_perm[inv_pos[t*k+j]]
+ *            + sum_s y_perm[P + s*T + t] + (residual_opt ? residual_opt[t] : 0)
+ * summed in fp32 in exactly that order, then rounded once to odt (bf16: nearest-even).
+ *  residual_opt [T][d] in odt's type, or NULL. out may alias residual_opt. */
+moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt,
+                       const int32_t* inv_pos, const float* topk_w, const void* residual_opt,
+                       void* out, moe_dtype odt, moe_stream_t stream);
+
+/* Waits for `stream`, then returns the device status word of workspace `ws` in *h_status.
+ * MOE_OK if it is zero, MOE_EDEVICE if not, MOE_ECUDA if the copy failed. */
+moe_status moe_read_status(const void* ws, moe_stream_t stream, int32_t* h_status);
+
+/* Message of the last MOE_ECUDA / MOE_EINVAL returned on this host thread ("" if none). */
+const char* moe_last_error_string(void);
+
+/* ------------------------------------------------------------------------------------
+ * Slot table: an expert cache for experts that do not all fit in device memory
+ * ([P2] "专家缓存" and "三级存储分工": the most used experts stay in VRAM, all experts
+ * sit pinned in host RAM; [P2] "长文本": expert copies overlap with computation).
+ * The table keeps, on the host, an LRU order over n_slots device slots and the owner
+ * (layer, expert) of each slot. The device table d_slot_of [L][E] lives in caller memory.
+ * Row `layer` of it is what moe_expert_ffn reads through moe_expert_table.slot_of.
+ * ------------------------------------------------------------------------------------ */
+typedef struct moe_slot_table moe_slot_table;
+
+typedef struct {
+  uint64_t hits, misses, evictions, bytes_h2d;
+} moe_slot_stats;
+
+/* Copies `bytes` from host `h_src` to device `d_dst` on `stream`; returns 0 on success.
+ * The default copier is cudaMemcpyAsync. A caller can pass its own (e.g. to add tracing,
+ * or in tests to inject a failure). */
+typedef int (*moe_copy_fn)(void* d_dst, const void* h_src, size_t bytes, moe_stream_t stream,
+                           void* user);
+
+/* Creates a table over n_slots slots of slot_bytes at d_pool (device), for L layers of E
+ * experts whose records sit at h_records[l*E + e] (pinned host memory, slot_bytes each;
+ * the same pointer may repeat). All slots start empty and d_slot_of is set to -1 (a
+ * synchronous cudaMemset). copy_fn may be NULL (cudaMemcpyAsync). */
+moe_status slot_table_create(moe_slot_table** out, int32_t L, int32_t E, int32_t n_slots,
+                             uint64_t slot_bytes, void* d_pool, int32_t* d_slot_of,
+                             const void* const* h_records, moe_copy_fn copy_fn, void* copy_user);
+
+/* Makes every expert of h_active[0..n_active) (host array) resident for `layer`:
+ *  - a resident expert is a hit; it moves to the most-recently-used end;
+ *  - a miss takes the least-recently-used slot whose owner is not in h_active (an empty
+ *    slot first), is copied from h_records on copy_stream, and is marked most recent;
+ *  - the changed entries of row `layer` of d_slot_of are then written on copy_stream, and
+ *    `ready` (if not NULL) is recorded on copy_stream after all copies.
+ * A compute stream that waits on `ready` sees the new row. Hits can run before `ready`.
+ * Optional outputs: h_hits / h_misses (host int32 arrays of capacity n_active) receive
+ * the hit and miss expert ids in h_active order, with their counts in *n_hits / *n_misses.
+ * MOE_ENOSLOT if the misses outnumber the slots not owned by h_active (the table is left
+ * unchanged), MOE_ECUDA if a copy fails (the failed expert is not marked resident),
+ * MOE_EINVAL for a bad layer or expert id or a repeated id. */
+moe_status slot_table_update(moe_slot_table* table, int32_t layer, const int32_t* h_active,
+                             int32_t n_active, moe_stream_t copy_stream, moe_event_t ready,
+                             int32_t* h_hits, int32_t* n_hits, int32_t* h_misses,
+                             int32_t* n_misses, moe_slot_stats* stats_opt);
+
+/* Cumulative counters since creation. */
+moe_status slot_table_stats(const moe_slot_table* table, moe_slot_stats* out);
+
+/* Host mirror of d_slot_of [L][E]: copies L*E int32 into h_out. */
+moe_status slot_table_snapshot(const moe_slot_table* table, int32_t* h_out);
+
+moe_status slot_table_destroy(moe_slot_table* table);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

@@ -1,0 +1,204 @@
+"""ctypes binding of libmoe_b300.so (include/moe.h): argument marshalling only.
+
+Every function here has the name of its C entry point and forwards to it. A pointer
+argument may be a torch tensor (its data_ptr()), an int (a raw address) or None (NULL). A
+stream may be a torch.cuda.Stream, a raw handle (int) or None (the current torch stream).
+A negative moe_status raises MoeError with the library's message. Loading fails loudly
+when the library has not been built: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+
+MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA, MOE_ENOSLOT, MOE_EDEVICE = 0, -1, -2, -3, -4, -5
+MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_EXPERT, MOE_DEV_MISSING_SLOT = 0x1, 0x2, 0x4
+MOE_BF16, MOE_F32 = 0, 1
+MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
+
+_STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_EUNSUPPORTED", -3: "MOE_ECUDA", -4: "MOE_ENOSLOT",
+                 -5: "MOE_EDEVICE"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__(f"{where}: {_STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class moe_shape(C.Structure):
+    _fields_ = [("T", C.c_int32), ("d", C.c_int32), ("f", C.c_int32), ("E", C.c_int32), ("k", C.c_int32),
+                ("n_shared", C.c_int32)]
+
+
+class moe_expert_layout(C.Structure):
+    _fields_ = [(n, C.c_uint64) for n in ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s", "record_bytes")]
+
+
+class moe_expert_table(C.Structure):
+    _fields_ = [("pool", C.c_void_p), ("slot_bytes", C.c_uint64), ("slot_of", C.c_void_p), ("shared", C.c_void_p)]
+
+
+class moe_slot_stats(C.Structure):
+    _fields_ = [(n, C.c_uint64) for n in ("hits", "misses", "evictions", "bytes_h2d")]
+
+
+MOE_COPY_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p)
+
+_P = C.c_void_p
+_SIGS = {
+    "moe_get_expert_layout": (C.c_int, [C.c_int32, C.c_int32, C.POINTER(moe_expert_layout)]),
+    "moe_workspace_size": (C.c_int, [C.POINTER(moe_shape), C.POINTER(C.c_size_t)]),
+    "moe_route": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, _P, C.c_size_t, _P]),
+    "moe_permute": (C.c_int, [C.POINTER(moe_shape), _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
+    "moe_expert_ffn": (C.c_int, [C.POINTER(moe_shape), C.c_int, _P, C.c_int, C.POINTER(moe_expert_table), _P, _P, _P,
+                                 _P, C.c_int, _P, C.c_size_t, _P]),
+    "moe_combine": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, C.c_int, _P]),
+    "moe_read_status": (C.c_int, [_P, _P, C.POINTER(C.c_int32)]),
+    "moe_last_error_string": (C.c_char_p, []),
+    "slot_table_create": (C.c_int, [C.POINTER(_P), C.c_int32, C.c_int32, C.c_int32, C.c_uint64, _P, _P, _P,
+                                    MOE_COPY_FN, _P]),
+    "slot_table_update": (C.c_int, [_P, C.c_int32, _P, C.c_int32, _P, _P, _P, _P, _P, _P,
+                                    C.POINTER(moe_slot_stats)]),
+    "slot_table_stats": (C.c_int, [_P, C.POINTER(moe_slot_stats)]),
+    "slot_table_snapshot": (C.c_int, [_P, _P]),
+    "slot_table_destroy": (C.c_int, [_P]),
+}
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded library (loaded on first use)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m routed_expert_ffn_bucketing_b300.build`")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def stream_handle(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(st: int, where: str) -> int:
+    if st < 0:
+        raise MoeError(st, where, (lib().moe_last_error_string() or b"").decode())
+    return st
+
+
+def shape(T: int, d: int, f: int, E: int, k: int, n_shared: int = 0) -> moe_shape:
+    return moe_shape(T, d, f, E, k, n_shared)
+
+
+def moe_get_expert_layout(d: int, f: int) -> moe_expert_layout:
+    out = moe_expert_layout()
+    _check(lib().moe_get_expert_layout(d, f, C.byref(out)), "moe_get_expert_layout")
+    return out
+
+
+def moe_workspace_size(s: moe_shape) -> int:
+    n = C.c_size_t()
+    _check(lib().moe_workspace_size(C.byref(s), C.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_route(s, x, xdt, w_router, topk_idx, topk_w, logits_opt, ws, ws_bytes, stream=None) -> int:
+    return _check(lib().moe_route(C.byref(s), ptr(x), xdt, ptr(w_router), ptr(topk_idx), ptr(topk_w),
+                                  ptr(logits_opt), ptr(ws), ws_bytes, stream_handle(stream)), "moe_route")
+
+
+def moe_permute(s, topk_idx, counts, offsets, sorted_pair, inv_pos, active, ws, ws_bytes, stream=None) -> int:
+    return _check(lib().moe_permute(C.byref(s), ptr(topk_idx), ptr(counts), ptr(offsets), ptr(sorted_pair),
+                                    ptr(inv_pos), ptr(active), ptr(ws), ws_bytes, stream_handle(stream)),
+                  "moe_permute")
+
+
+def expert_table(pool, slot_bytes: int, slot_of, shared=None) -> moe_expert_table:
+    return moe_expert_table(ptr(pool), slot_bytes, ptr(slot_of), ptr(shared))
+
+
+def moe_expert_ffn(s, mode, x, xdt, table: moe_expert_table, offsets, sorted_pair, active, y_perm, ydt, ws,
+                   ws_bytes, stream=None) -> int:
+    return _check(lib().moe_expert_ffn(C.byref(s), mode, ptr(x), xdt, C.byref(table), ptr(offsets),
+                                       ptr(sorted_pair), ptr(active), ptr(y_perm), ydt, ptr(ws), ws_bytes,
+                                       stream_handle(stream)), "moe_expert_ffn")
+
+
+def moe_combine(s, y_perm, ydt, inv_pos, topk_w, residual_opt, out, odt, stream=None) -> int:
+    return _check(lib().moe_combine(C.byref(s), ptr(y_perm), ydt, ptr(inv_pos), ptr(topk_w), ptr(residual_opt),
+                                    ptr(out), odt, stream_handle(stream)), "moe_combine")
+
+
+def moe_read_status(ws, stream=None) -> int:
+    """Returns the device status word (0 when clean); raises only on MOE_ECUDA / MOE_EINVAL."""
+    v = C.c_int32()
+    st = lib().moe_read_status(ptr(ws), stream_handle(stream), C.byref(v))
+    if st not in (MOE_OK, MOE_EDEVICE):
+        _check(st, "moe_read_status")
+    return v.value
+
+
+def moe_last_error_string() -> str:
+    return (lib().moe_last_error_string() or b"").decode()
+
+
+# ------------------------------------------------------------------ slot table ------------
+
+def slot_table_create(L, E, n_slots, slot_bytes, d_pool, d_slot_of, h_records, copy_fn=None, copy_user=None):
+    """h_records: sequence of L*E host addresses (ints). copy_fn: a MOE_COPY_FN or None.
+    Returns the opaque handle (int)."""
+    arr = (C.c_void_p * (L * E))(*h_records)
+    out = C.c_void_p()
+    fn = copy_fn if copy_fn is not None else MOE_COPY_FN()
+    st = lib().slot_table_create(C.byref(out), L, E, n_slots, slot_bytes, ptr(d_pool), ptr(d_slot_of), arr, fn,
+                                 copy_user)
+    if st < 0:
+        raise MoeError(st, "slot_table_create", "")
+    return out.value
+
+
+def slot_table_update(table, layer, h_active, n_active, copy_stream, ready, h_hits=None, n_hits=None,
+                      h_misses=None, n_misses=None, stats=None) -> int:
+    """Pointer arguments are raw host addresses (ints) or None; stats a moe_slot_stats or None."""
+    st = lib().slot_table_update(table, layer, h_active, n_active, copy_stream, ready, h_hits, n_hits, h_misses,
+                                 n_misses, C.byref(stats) if stats is not None else None)
+    if st < 0 and st != MOE_ENOSLOT:
+        raise MoeError(st, "slot_table_update", "")
+    return st
+
+
+def slot_table_stats(table) -> moe_slot_stats:
+    out = moe_slot_stats()
+    _check(lib().slot_table_stats(table, C.byref(out)), "slot_table_stats")
+    return out
+
+
+def slot_table_snapshot(table, h_out) -> None:
+    _check(lib().slot_table_snapshot(table, h_out), "slot_table_snapshot")
+
+
+def slot_table_destroy(table) -> None:
+    _check(lib().slot_table_destroy(table), "slot_table_destroy")

@@ -1,0 +1,279 @@
+// C-ABI entry points (include/moe.h): argument checks, workspace layout, kernel dispatch.
+// Every check happens on the host before any launch; a failed check enqueues nothing.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+static thread_local char g_err[512] = "";
+
+static moe_status fail(moe_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+static moe_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(MOE_ECUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+int route_splits(int d) { return (d + kRouteRowsPerSplit - 1) / kRouteRowsPerSplit; }
+int perm_chunks(int P) { return (P + kPermChunk - 1) / kPermChunk; }
+
+WsLayout ws_layout(const moe_shape& s) {
+  WsLayout L{};
+  const size_t T = (size_t)s.T, P = (size_t)s.T * s.k;
+  size_t o = 0;
+  L.status = o;
+  o += 256;
+  L.route_partial = o;
+  if (s.T <= kRouteGemvMaxT) o = align256(o + sizeof(float) * route_splits(s.d) * T * s.E);
+  L.logits = o;
+  if (s.T > kRouteGemvMaxT) o = align256(o + sizeof(float) * T * s.E);
+  L.perm_cnt = o;
+  const size_t C = P > (size_t)kPermChunk ? (size_t)perm_chunks((int)P) : 0;
+  o = align256(o + sizeof(int32_t) * C * s.E);
+  L.perm_keys = o;
+  o = align256(o + sizeof(uint32_t) * C * kPermChunk);
+  L.h = o;
+  o = align256(o + sizeof(float) * (P + T * s.n_shared) * s.f);
+  L.tiles = o;
+  L.total = o;
+  return L;
+}
+
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (bytes > (size_t)optin) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e != cudaSuccess) return e;
+  done.insert({kernel, dev});
+  return cudaSuccess;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static moe_status check_shape(const moe_shape* s) {
+  if (!s) return fail(MOE_EINVAL, "shape is NULL");
+  if (s->T < 0 || s->d <= 0 || s->f <= 0 || s->E <= 0 || s->k <= 0 || s->n_shared < 0)
+    return fail(MOE_EINVAL, "shape has a negative or zero field (T=%d d=%d f=%d E=%d k=%d n_shared=%d)", s->T,
+                s->d, s->f, s->E, s->k, s->n_shared);
+  if (s->d % 32 || s->f % 32) return fail(MOE_EINVAL, "d=%d and f=%d must be multiples of 32", s->d, s->f);
+  if (s->k > s->E) return fail(MOE_EINVAL, "k=%d exceeds E=%d", s->k, s->E);
+  if (s->k > 32) return fail(MOE_EUNSUPPORTED, "k=%d > 32", s->k);
+  if (s->E > 1024) return fail(MOE_EUNSUPPORTED, "E=%d > 1024", s->E);
+  if (s->T > 65535) return fail(MOE_EUNSUPPORTED, "T=%d > 65535", s->T);
+  if (s->n_shared > 8) return fail(MOE_EUNSUPPORTED, "n_shared=%d > 8", s->n_shared);
+  if ((int64_t)s->d * s->f > (int64_t)1 << 30) return fail(MOE_EUNSUPPORTED, "d*f too large");
+  return MOE_OK;
+}
+
+static moe_status check_ws(const moe_shape* s, const void* ws, size_t ws_bytes) {
+  if (!ws) return fail(MOE_EINVAL, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(MOE_EINVAL, "workspace must be 256-byte aligned");
+  const size_t need = ws_layout(*s).total;
+  if (ws_bytes < need) return fail(MOE_EINVAL, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return MOE_OK;
+}
+
+static moe_status check_dtype(int dt, const char* what) {
+  if (dt != MOE_BF16 && dt != MOE_F32) return fail(MOE_EINVAL, "%s dtype %d is not MOE_BF16 or MOE_F32", what, dt);
+  return MOE_OK;
+}
+
+template <typename T>
+static T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_last_error_string(void) { return g_err; }
+
+moe_status moe_get_expert_layout(int32_t d, int32_t f, moe_expert_layout* out) {
+  if (!out) return fail(MOE_EINVAL, "out is NULL");
+  if (d <= 0 || f <= 0 || d % 32 || f % 32) return fail(MOE_EINVAL, "d=%d f=%d must be positive multiples of 32", d, f);
+  const uint64_t q = (uint64_t)d * f, sgu = (uint64_t)f * (d / 32) * 2, sd = (uint64_t)d * (f / 32) * 2;
+  uint64_t o = 0;
+  auto take = [&](uint64_t n) {
+    const uint64_t r = o;
+    o = (o + n + 255) & ~(uint64_t)255;
+    return r;
+  };
+  out->gate_q = take(q);
+  out->up_q = take(q);
+  out->down_q = take(q);
+  out->gate_s = take(sgu);
+  out->up_s = take(sgu);
+  out->down_s = take(sd);
+  out->record_bytes = o;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!bytes) return fail(MOE_EINVAL, "bytes is NULL");
+  *bytes = ws_layout(*shape).total;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                     int32_t* topk_idx, float* topk_w, float* logits_opt, void* ws, size_t ws_bytes,
+                     moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_dtype(xdt, "x")) != MOE_OK) return st;
+  if ((st = check_ws(shape, ws, ws_bytes)) != MOE_OK) return st;
+  if (shape->T > 0) {
+    if (!x || !w_router || !topk_idx || !topk_w) return fail(MOE_EINVAL, "moe_route: NULL argument");
+    if (!aligned(x, 16) || !aligned(w_router, 16))
+      return fail(MOE_EINVAL, "moe_route: x and w_router must be 16-byte aligned");
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(*shape);
+  int* status = at<int>(ws, L.status);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_route: clearing the status word");
+  if (shape->T == 0) return MOE_OK;
+  if (shape->T <= kRouteGemvMaxT) {
+    float* partial = at<float>(ws, L.route_partial);
+    e = launch_route_gemv(*shape, x, xdt, w_router, partial, s);
+    if (e == cudaSuccess)
+      e = launch_topk(*shape, partial, route_splits(shape->d), topk_idx, topk_w, logits_opt, status, s);
+  } else {
+    float* logits = logits_opt ? logits_opt : at<float>(ws, L.logits);
+    e = launch_route_gemm(*shape, x, xdt, w_router, logits, s);
+    if (e == cudaSuccess) e = launch_topk(*shape, logits, 1, topk_idx, topk_w, nullptr, status, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "moe_route: launch");
+  return MOE_OK;
+}
+
+moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                       int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(shape, ws, ws_bytes)) != MOE_OK) return st;
+  if (!counts || !offsets || !active || (shape->T > 0 && (!topk_idx || !sorted_pair || !inv_pos)))
+    return fail(MOE_EINVAL, "moe_permute: NULL argument");
+  const WsLayout L = ws_layout(*shape);
+  cudaError_t e = launch_permute(*shape, topk_idx, counts, offsets, sorted_pair, inv_pos, active,
+                                 at<int32_t>(ws, L.perm_cnt), at<uint32_t>(ws, L.perm_keys), at<int>(ws, L.status),
+                                 reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_permute: launch");
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, moe_dtype xdt,
+                          const moe_expert_table* experts, const int32_t* offsets, const int32_t* sorted_pair,
+                          const int32_t* active, void* y_perm, moe_dtype ydt, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_dtype(xdt, "x")) != MOE_OK) return st;
+  if ((st = check_dtype(ydt, "y_perm")) != MOE_OK) return st;
+  if ((st = check_ws(shape, ws, ws_bytes)) != MOE_OK) return st;
+  if (mode != MOE_MODE_AUTO && mode != MOE_MODE_DECODE && mode != MOE_MODE_PREFILL)
+    return fail(MOE_EINVAL, "moe_expert_ffn: bad mode %d", (int)mode);
+  if (shape->T == 0) return MOE_OK;
+  if (!x || !experts || !offsets || !sorted_pair || !active || !y_perm)
+    return fail(MOE_EINVAL, "moe_expert_ffn: NULL argument");
+  if (!experts->pool || !experts->slot_of) return fail(MOE_EINVAL, "moe_expert_ffn: NULL pool or slot_of");
+  if ((shape->n_shared > 0) != (experts->shared != nullptr))
+    return fail(MOE_EINVAL, "moe_expert_ffn: shared must be non-NULL exactly when n_shared > 0");
+  moe_expert_layout lay;
+  moe_get_expert_layout(shape->d, shape->f, &lay);
+  if (experts->slot_bytes < lay.record_bytes || experts->slot_bytes % 256)
+    return fail(MOE_EINVAL, "moe_expert_ffn: slot_bytes %llu must be >= %llu and a multiple of 256",
+                (unsigned long long)experts->slot_bytes, (unsigned long long)lay.record_bytes);
+  if (!aligned(x, 16) || !aligned(y_perm, 16) || !aligned(experts->pool, 256) ||
+      (experts->shared && !aligned(experts->shared, 256)))
+    return fail(MOE_EINVAL, "moe_expert_ffn: misaligned x, y_perm, pool or shared");
+  if (mode == MOE_MODE_PREFILL) return fail(MOE_EUNSUPPORTED, "moe_expert_ffn: PREFILL kernels not built");
+  if (shape->T == 0) return MOE_OK;
+  const WsLayout L = ws_layout(*shape);
+  FfnArgs a{};
+  a.x = x;
+  a.xdt = xdt;
+  a.pool = static_cast<const uint8_t*>(experts->pool);
+  a.slot_bytes = experts->slot_bytes;
+  a.slot_of = experts->slot_of;
+  a.shared = static_cast<const uint8_t*>(experts->shared);
+  a.offsets = offsets;
+  a.sorted_pair = sorted_pair;
+  a.active = active;
+  a.y = y_perm;
+  a.ydt = ydt;
+  a.h = at<float>(ws, L.h);
+  a.status = at<int>(ws, L.status);
+  a.T = shape->T;
+  a.d = shape->d;
+  a.f = shape->f;
+  a.E = shape->E;
+  a.k = shape->k;
+  a.n_shared = shape->n_shared;
+  a.P = shape->T * shape->k;
+  a.o_gate_q = lay.gate_q;
+  a.o_up_q = lay.up_q;
+  a.o_down_q = lay.down_q;
+  a.o_gate_s = lay.gate_s;
+  a.o_up_s = lay.up_s;
+  a.o_down_s = lay.down_s;
+  cudaError_t e = launch_ffn_decode(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_expert_ffn: launch");
+  return MOE_OK;
+}
+
+moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt, const int32_t* inv_pos,
+                       const float* topk_w, const void* residual_opt, void* out, moe_dtype odt,
+                       moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_dtype(ydt, "y_perm")) != MOE_OK) return st;
+  if ((st = check_dtype(odt, "out")) != MOE_OK) return st;
+  if (shape->T == 0) return MOE_OK;
+  if (!y_perm || !inv_pos || !topk_w || !out) return fail(MOE_EINVAL, "moe_combine: NULL argument");
+  if (!aligned(y_perm, 16) || !aligned(out, 16) || (residual_opt && !aligned(residual_opt, 16)))
+    return fail(MOE_EINVAL, "moe_combine: misaligned y_perm, out or residual");
+  if (shape->T == 0) return MOE_OK;
+  cudaError_t e = launch_combine(*shape, y_perm, ydt, inv_pos, topk_w, residual_opt, out, odt,
+                                 reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_combine: launch");
+  return MOE_OK;
+}
+
+moe_status moe_read_status(const void* ws, moe_stream_t stream, int32_t* h_status) {
+  if (!ws || !h_status) return fail(MOE_EINVAL, "moe_read_status: NULL argument");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(h_status, ws, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_read_status");
+  return *h_status ? MOE_EDEVICE : MOE_OK;
+}
+
+}  // extern "C"

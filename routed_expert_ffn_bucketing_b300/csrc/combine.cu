@@ -1,0 +1,66 @@
+// Combine / unpermute: each token's output is the gated mixture of its selected experts
+// ("单张RTX 5090跑125B大模型：Strata实测Qwen3.8 Flash Next", section "MoE专家按需调度"), plus the
+// shared expert applied to every token ("Strata 工作原理图解GPU内存SSD三级存储如何让125B模型塞进消费级显卡",
+// section "三级存储分工"):
+//   out[t] = sum_j w[t][j] * y_perm[inv_pos[t*k + j]] + sum_s y_perm[P + s*T + t] (+ residual[t])
+// The sum is fp32 in exactly that order (deterministic) and is rounded once to the output type.
+// One thread produces 4 consecutive columns of one token.
+#include "moe_common.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ float4 load4(const void* p, int dt, size_t off) {
+  if (dt == 1) return *reinterpret_cast<const float4*>(static_cast<const float*>(p) + off);
+  const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p) + off);
+  return make_float4(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16),
+                     bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16));
+}
+
+__device__ __forceinline__ void fma4(float w, const float4& v, float4& a) {
+  a.x = fmaf(w, v.x, a.x); a.y = fmaf(w, v.y, a.y); a.z = fmaf(w, v.z, a.z); a.w = fmaf(w, v.w, a.w);
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y, int ydt,
+                                                      const int32_t* __restrict__ inv_pos,
+                                                      const float* __restrict__ topk_w,
+                                                      const void* residual, void* out, int odt, int T, int d,
+                                                      int k, int n_shared) {
+  const int t = blockIdx.y;
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (c >= d) return;
+  const size_t P = (size_t)T * k;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const int row = inv_pos[(size_t)t * k + j];
+    fma4(topk_w[(size_t)t * k + j], load4(y, ydt, (size_t)row * d + c), acc);
+  }
+  for (int s = 0; s < n_shared; ++s) {
+    const float4 v = load4(y, ydt, (P + (size_t)s * T + t) * d + c);
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  if (residual) {
+    const float4 v = load4(residual, odt, (size_t)t * d + c);
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  const size_t o = (size_t)t * d + c;
+  if (odt == 1) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = acc;
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + o) = v;
+  }
+}
+
+cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,
+                           const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st) {
+  const int threads = 256;
+  dim3 grid((s.d / 4 + threads - 1) / threads, s.T);
+  combine_kernel<<<grid, threads, 0, st>>>(y, ydt, inv_pos, topk_w, residual, out, odt, s.T, s.d, s.k,
+                                           s.n_shared);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

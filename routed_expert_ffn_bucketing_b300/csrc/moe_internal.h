@@ -1,0 +1,75 @@
+// Internal interface between the C-ABI layer (capi.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int MOE_DEV_NAN_LOGIT_BIT = MOE_DEV_NAN_LOGIT;
+constexpr int MOE_DEV_BAD_EXPERT_BIT = MOE_DEV_BAD_EXPERT;
+constexpr int MOE_DEV_MISSING_SLOT_BIT = MOE_DEV_MISSING_SLOT;
+
+constexpr int kRouteGemvMaxT = 16;   // tokens up to which the router runs as a split-d GEMV
+constexpr int kRouteRowsPerSplit = 64;
+constexpr int kPermChunk = 1024;     // pairs per bucketing chunk (one CTA)
+constexpr int kDecodeMaxT = 16;      // AUTO picks the decode kernels up to this many tokens
+constexpr int kDecodeTokGroup = 4;   // decode kernels stream weights once per group of tokens
+
+// Byte offsets of the workspace regions (all 256-byte aligned).
+struct WsLayout {
+  size_t status;         // int32 device status word
+  size_t route_partial;  // fp32 [S][T][E]: split-d router partial sums (T <= kRouteGemvMaxT)
+  size_t logits;         // fp32 [T][E]: router GEMM output (T > kRouteGemvMaxT)
+  size_t perm_cnt;       // int32 [C][E]: per-chunk counts, then per-chunk bases
+  size_t perm_keys;      // uint32 [C * kPermChunk]: chunk-sorted (expert, pair) keys
+  size_t h;              // [P + T*n_shared][f] fp32: SwiGLU activations between the FFN kernels
+  size_t tiles;          // int32 [..]: prefill tile list
+  size_t total;
+};
+
+WsLayout ws_layout(const moe_shape& s);
+
+// Raises a kernel's dynamic shared memory limit to at least `bytes` on the current device
+// (once per kernel and device).
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+int route_splits(int d);
+int perm_chunks(int P);
+
+// Arguments of the expert FFN kernels (device pointers, already validated).
+struct FfnArgs {
+  const void* x;
+  int xdt;  // 0 bf16, 1 fp32
+  const uint8_t* pool;
+  uint64_t slot_bytes;
+  const int32_t* slot_of;
+  const uint8_t* shared;
+  const int32_t* offsets;
+  const int32_t* sorted_pair;
+  const int32_t* active;
+  void* y;
+  int ydt;
+  float* h;  // fp32 [P + T*n_shared][f]
+  int* status;
+  int T, d, f, E, k, n_shared, P;
+  // record layout
+  uint64_t o_gate_q, o_up_q, o_down_q, o_gate_s, o_up_s, o_down_s;
+};
+
+// Launchers; each returns cudaSuccess or the launch error.
+cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
+                              cudaStream_t st);
+cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const float* w, float* logits,
+                              cudaStream_t st);
+cudaError_t launch_topk(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
+                        float* logits_out, int* status, cudaStream_t st);
+cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                           int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
+                           uint32_t* keys, int* status, cudaStream_t st);
+cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);
+cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,
+                           const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,304 @@
+// Router logits and top-k gate of the MoE layer.
+//
+// The router picks the top-K experts of each token; the other experts take no part
+// ("单张RTX 5090跑125B大模型：Strata实测Qwen3.8 Flash Next", section "MoE专家按需调度"). It is
+// resident in VRAM ("Strata 工作原理图解GPU内存SSD三级存储如何让125B模型塞进消费级显卡", section
+// "三级存储分工"). Logits are fp32 with a fixed summation order, so results are deterministic.
+//
+//  * T <= 16 (decode, spec-verify): the router is a GEMV that streams w_router [d][E] once.
+//    The d rows are split into chunks of 64 so that the whole matrix is in flight at
+//    once (one CTA per 64 rows x 128 experts). Each chunk writes a partial sum, and the top-k
+//    kernel adds the chunks in ascending order.
+//  * T > 16 (prefill): a tiled fp32 GEMM, 128 x 128 outputs per CTA. Each output sums its
+//    32-long k-blocks separately before adding them up, which keeps the fp32 error of a
+//    2048-long dot product near that of a tree sum.
+//  * top-k: one warp per token. Each lane holds E/32 logits as order-preserving integer
+//    keys, and k rounds of warp max (redux.sync) pick the experts. A tie goes to the lowest
+//    index.
+#include "moe_common.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ split-d GEMV ----------
+
+template <int TT, int VEC>
+__global__ void __launch_bounds__(256) router_gemv_kernel(const void* __restrict__ x, int xdt,
+                                                          const float* __restrict__ w,
+                                                          float* __restrict__ partial, int T, int d,
+                                                          int E) {
+  constexpr int R = kRouteRowsPerSplit;  // rows of d per CTA
+  constexpr int COLS = 32 * VEC;         // experts per CTA
+  extern __shared__ float sm[];
+  float* xs = sm;            // [TT][R]
+  float* red = sm + TT * R;  // [8][TT][COLS]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i0 = blockIdx.y * R;
+  const int rows = min(R, d - i0);
+  for (int j = threadIdx.x; j < TT * R; j += blockDim.x) {
+    const int t = j / R, i = j % R;
+    xs[j] = (t < T && i < rows) ? load_act(x, xdt, (size_t)t * d + i0 + i) : 0.0f;
+  }
+  __syncthreads();
+
+  const int c0 = blockIdx.x * COLS + lane * VEC;
+  float acc[TT][VEC];
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[t][v] = 0.0f;
+
+  float wv[R / 8][VEC];
+#pragma unroll
+  for (int rr = 0; rr < R / 8; ++rr) {  // all loads first: R/8 independent rows in flight
+    const int i = warp + rr * 8;
+    const float* row = w + (size_t)(i0 + i) * E;
+    if constexpr (VEC == 4) {
+      if (i < rows && c0 + 3 < E) {
+        const float4 v4 = __ldg(reinterpret_cast<const float4*>(row + c0));
+        wv[rr][0] = v4.x; wv[rr][1] = v4.y; wv[rr][2] = v4.z; wv[rr][3] = v4.w;
+        continue;
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) wv[rr][v] = (i < rows && c0 + v < E) ? __ldg(row + c0 + v) : 0.0f;
+  }
+#pragma unroll
+  for (int rr = 0; rr < R / 8; ++rr) {
+    const int i = warp + rr * 8;
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      const float xv = xs[t * R + i];
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) acc[t][v] = fmaf(xv, wv[rr][v], acc[t][v]);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) red[(warp * TT + t) * COLS + lane * VEC + v] = acc[t][v];
+  __syncthreads();
+  for (int j = threadIdx.x; j < TT * COLS; j += blockDim.x) {
+    const int t = j / COLS, c = j % COLS;
+    float s = 0.0f;
+#pragma unroll
+    for (int w8 = 0; w8 < 8; ++w8) s += red[(w8 * TT + t) * COLS + c];
+    const int e = blockIdx.x * COLS + c;
+    if (t < T && e < E) partial[((size_t)blockIdx.y * T + t) * E + e] = s;
+  }
+}
+
+template <int TT, int VEC>
+static cudaError_t gemv_launch(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
+                               cudaStream_t st) {
+  constexpr int COLS = 32 * VEC;
+  const size_t smem = sizeof(float) * (TT * kRouteRowsPerSplit + 8 * TT * COLS);
+  auto kern = router_gemv_kernel<TT, VEC>;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((s.E + COLS - 1) / COLS, route_splits(s.d));
+  kern<<<grid, 256, smem, st>>>(x, xdt, w, partial, s.T, s.d, s.E);
+  return cudaGetLastError();
+}
+
+template <int VEC>
+static cudaError_t gemv_dispatch_t(const moe_shape& s, const void* x, int xdt, const float* w, float* p,
+                                   cudaStream_t st) {
+  if (s.T <= 1) return gemv_launch<1, VEC>(s, x, xdt, w, p, st);
+  if (s.T <= 2) return gemv_launch<2, VEC>(s, x, xdt, w, p, st);
+  if (s.T <= 4) return gemv_launch<4, VEC>(s, x, xdt, w, p, st);
+  if (s.T <= 8) return gemv_launch<8, VEC>(s, x, xdt, w, p, st);
+  return gemv_launch<16, VEC>(s, x, xdt, w, p, st);
+}
+
+cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
+                              cudaStream_t st) {
+  if (s.E % 4 == 0) return gemv_dispatch_t<4>(s, x, xdt, w, partial, st);
+  return gemv_dispatch_t<1>(s, x, xdt, w, partial, st);
+}
+
+// ------------------------------------------------------------------ tiled GEMM -------------
+
+// out[T][E] = x[T][d] . w[d][E]; CTA tile 128 x 128, k-tile 8, 256 threads with 8 x 8 outputs.
+// Every 32 k the block sum is added to the running total (two-level accumulation).
+__global__ void __launch_bounds__(256) router_gemm_kernel(const void* __restrict__ x, int xdt,
+                                                          const float* __restrict__ w,
+                                                          float* __restrict__ out, int T, int d, int E) {
+  __shared__ __align__(16) float As[2][8][128];  // [k][token]
+  __shared__ __align__(16) float Bs[2][8][128];  // [k][expert]
+  const int tid = threadIdx.x;
+  const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
+  const int ty = tid >> 4, tx = tid & 15;
+  // global->shared mapping: A: token row tid/2, k 4*(tid%2)..+4; B: k row tid/32, experts 4*(tid%32)..+4
+  const int a_row = tid >> 1, a_k = (tid & 1) * 4;
+  const int b_k = tid >> 5, b_col = (tid & 31) * 4;
+
+  float acc[8][8], blk[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = blk[i][j] = 0.0f;
+
+  float ra[4], rb[4];
+  auto load_tile = [&](int kt) {
+    const int tok = m0 + a_row;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      ra[q] = tok < T ? load_act(x, xdt, (size_t)tok * d + kt * 8 + a_k + q) : 0.0f;
+    const int krow = kt * 8 + b_k;
+    const float* wr = w + (size_t)krow * E + n0 + b_col;
+    if (n0 + b_col + 3 < E && (E % 4) == 0) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(wr));
+      rb[0] = v.x; rb[1] = v.y; rb[2] = v.z; rb[3] = v.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) rb[q] = (n0 + b_col + q < E) ? __ldg(wr + q) : 0.0f;
+    }
+  };
+  auto store_tile = [&](int buf) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) As[buf][a_k + q][a_row] = ra[q];
+    *reinterpret_cast<float4*>(&Bs[buf][b_k][b_col]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+  };
+
+  const int nk = d / 8;
+  load_tile(0);
+  store_tile(0);
+  __syncthreads();
+  for (int kt = 0; kt < nk; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < nk) load_tile(kt + 1);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      float a[8], b[8];
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 8]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 8 + 4]);
+      a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w; a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+      b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w; b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) blk[i][j] = fmaf(a[i], b[j], blk[i][j]);
+    }
+    if ((kt & 3) == 3 || kt + 1 == nk) {  // close a 32-long k-block
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          acc[i][j] += blk[i][j];
+          blk[i][j] = 0.0f;
+        }
+    }
+    if (kt + 1 < nk) store_tile(buf ^ 1);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int tok = m0 + ty * 8 + i;
+    if (tok >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = n0 + tx * 8 + j;
+      if (e < E) out[(size_t)tok * E + e] = acc[i][j];
+    }
+  }
+}
+
+cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const float* w, float* logits,
+                              cudaStream_t st) {
+  dim3 grid((s.E + 127) / 128, (s.T + 127) / 128);
+  router_gemm_kernel<<<grid, 256, 0, st>>>(x, xdt, w, logits, s.T, s.d, s.E);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ top-k ------------------
+
+// Order-preserving key of an fp32 logit: larger float, larger key. -0.0 maps like +0.0 and
+// NaN maps to 0, below every number (-inf has key 0x007FFFFF).
+__device__ __forceinline__ uint32_t logit_key(float v, bool* nan) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
+  if (v != v) {
+    *nan = true;
+    return 0u;
+  }
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
+template <int PER>
+__global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ partial, int S, int T, int E,
+                                                   int k, int32_t* __restrict__ idx, float* __restrict__ wts,
+                                                   float* __restrict__ logits_out, int* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 4 + warp;
+  if (t >= T) return;
+  uint32_t key[PER];
+  bool nan = false;
+#pragma unroll
+  for (int p = 0; p < PER; ++p) {
+    const int e = lane + 32 * p;
+    key[p] = 0u;
+    if (e < E) {
+      float v = partial[(size_t)t * E + e];
+      for (int sp = 1; sp < S; ++sp) v += partial[((size_t)sp * T + t) * E + e];
+      if (logits_out) logits_out[(size_t)t * E + e] = v;
+      key[p] = logit_key(v, &nan);
+    }
+  }
+  uint32_t taken = 0u;
+  int my_e = 0;
+  uint32_t my_key = 0u;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u;
+    int be = 0x7FFFFFFF;
+    bool found = false;
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const bool free_ = !((taken >> p) & 1u) && (lane + 32 * p) < E;
+      if (free_ && (!found || key[p] > bk)) {
+        bk = key[p];
+        be = lane + 32 * p;
+        found = true;
+      }
+    }
+    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const uint32_t cand = (found && bk == mk) ? (uint32_t)be : 0x7FFFFFFFu;
+    const int sel = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
+    if (lane == (sel & 31)) taken |= 1u << (sel >> 5);
+    if (lane == j) {
+      my_e = sel;
+      my_key = mk;
+    }
+  }
+  const float v = key_logit(my_key);
+  const float m = __shfl_sync(0xFFFFFFFFu, v, 0);
+  float ex = lane < k ? expf(v - m) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_e;
+    wts[(size_t)t * k + lane] = ex / sum;
+  }
+  if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) flag_status(status, MOE_DEV_NAN_LOGIT_BIT);
+}
+
+cudaError_t launch_topk(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
+                        float* logits_out, int* status, cudaStream_t st) {
+  const dim3 grid((s.T + 3) / 4);
+  const int per = (s.E + 31) / 32;
+  if (per <= 1) topk_kernel<1><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
+  else if (per <= 2) topk_kernel<2><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
+  else if (per <= 4) topk_kernel<4><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
+  else if (per <= 8) topk_kernel<8><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
+  else if (per <= 16) topk_kernel<16><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
+  else topk_kernel<32><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,87 @@
+"""The workloads: shapes and input recipes of the MoE layer configurations.
+
+Each workload is seeded and synthetic. No dataset is involved, and the pages measure none
+for this path.
+  tiny     T=16, d=256, f=128, E=16, top-2, no shared expert; router N(0, 0.02)
+  decode   T=4 (one token plus three drafts), d=2048, f=768, E=512, top-10 + 1 shared; router N(0, 1)
+  stack    48 decode layers, router columns scaled for Zipf(1.1) popularity, residual stream
+  prefill  T=8192 chunk, d=2048, f=768, E=512, top-10 + 1 shared, Zipf(1.1) routing
+  tiered   the stack with a 4,500-slot device pool, the rest in pinned host memory
+Experts are N(0, 0.02) quantised to int8 blocks of 32 with fp16 scales. Activations are
+N(0, 1) rounded to bf16.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import numpy as np
+
+from . import (activations_bf16, activations_f32, bf16_bits_to_f32, expert_arrays, record_layout,
+               router_weights)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    d: int
+    f: int
+    E: int
+    k: int
+    n_shared: int
+    router_sigma: float
+    zipf_s: float | None = None
+    layers: int = 1
+    residual: bool = False
+    slots: int | None = None       # device slot pool size (tiered); None = every expert resident
+    seed: int = 0
+    expert_sigma: float = 0.02
+
+    @property
+    def P(self) -> int:
+        return self.T * self.k
+
+    @property
+    def record_bytes(self) -> int:
+        return record_layout(self.d, self.f).record_bytes
+
+    def describe(self) -> str:
+        s = f"{self.name}: T={self.T} d={self.d} f={self.f} E={self.E} top-{self.k}"
+        s += f" + {self.n_shared} shared" if self.n_shared else ""
+        if self.layers > 1:
+            s += f", {self.layers} layers"
+        if self.zipf_s:
+            s += f", Zipf({self.zipf_s}) routing"
+        return s
+
+    # ---- inputs -------------------------------------------------------------------------
+    def x_bits(self, batch: int = 0) -> np.ndarray:
+        """bf16 bit patterns [T][d] of input batch `batch`."""
+        return activations_bf16(self.seed, batch, self.T, self.d)
+
+    def x_f64(self, batch: int = 0) -> np.ndarray:
+        return bf16_bits_to_f32(self.x_bits(batch)).astype(np.float64)
+
+    def x_f32(self, batch: int = 0) -> np.ndarray:
+        """fp32 activations (the fp32 debug mode's input)."""
+        return activations_f32(self.seed, batch, self.T, self.d)
+
+    def router(self, layer: int = 0) -> np.ndarray:
+        return router_weights(self.seed, layer, self.d, self.E, self.router_sigma, self.zipf_s, self.k)
+
+    def expert(self, layer: int, e: int):
+        """Routed expert e < E, or shared expert s as e = E + s."""
+        return expert_arrays(self.seed, layer, e, self.d, self.f, self.expert_sigma)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 16, 256, 128, 16, 2, 0, 0.02),
+    "decode": Workload("decode", 4, 2048, 768, 512, 10, 1, 1.0),
+    "stack": Workload("stack", 4, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1, layers=48, residual=True),
+    "prefill": Workload("prefill", 8192, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1),
+    "tiered": Workload("tiered", 4, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1, layers=48, residual=True, slots=4500),
+}
+
+
+def custom(base: str, **kw) -> Workload:
+    return replace(WORKLOADS[base], **kw)

@@ -1,0 +1,226 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol include/moe.h declares,
+agrees with the generator on the record layout, rejects bad arguments on the host before
+any CUDA call, and runs the slot table's LRU policy with an injected copier."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from routed_expert_ffn_bucketing_b300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:moe_status|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)
+    assert len(names) >= 12
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = L.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(L._SIGS), "binding misses a declared entry point"
+
+
+def test_generator_library_exports_fill():
+    lib = C.CDLL(os.path.join(ROOT, "synth", "libsynth_b300.so"))
+    assert hasattr(lib, "synth_fill_expert_records")
+
+
+@pytest.mark.parametrize("d,f", [(32, 32), (256, 128), (2048, 768), (96, 160), (4096, 1536)])
+def test_expert_layout_matches_generator(d, f):
+    a = L.moe_get_expert_layout(d, f)
+    b = synth.record_layout(d, f)
+    assert (a.gate_q, a.up_q, a.down_q, a.gate_s, a.up_s, a.down_s, a.record_bytes) == (
+        b.gate_q, b.up_q, b.down_q, b.gate_s, b.up_s, b.down_s, b.record_bytes)
+    assert a.record_bytes % 256 == 0
+
+
+def test_layout_rejects_bad_sizes():
+    for d, f in [(0, 32), (33, 32), (32, 48), (-32, 32)]:
+        with pytest.raises(L.MoeError) as e:
+            L.moe_get_expert_layout(d, f)
+        assert e.value.status == L.MOE_EINVAL
+
+
+def test_workspace_size_covers_activation_buffer():
+    for T in (0, 1, 4, 16, 17, 8192):
+        s = L.moe_workspace_size(L.shape(T, 2048, 768, 512, 10, 1))
+        assert s % 256 == 0
+        assert s >= 256 + 4 * (T * 10 + T) * 768   # status word + fp32 h rows
+
+
+BAD_SHAPES = [
+    (L.shape(4, 100, 768, 512, 10, 1), L.MOE_EINVAL),   # d % 32
+    (L.shape(4, 2048, 770, 512, 10, 1), L.MOE_EINVAL),  # f % 32
+    (L.shape(4, 2048, 768, 8, 10, 1), L.MOE_EINVAL),    # k > E
+    (L.shape(-1, 2048, 768, 512, 10, 1), L.MOE_EINVAL),
+    (L.shape(4, 2048, 768, 512, 0, 1), L.MOE_EINVAL),
+    (L.shape(4, 2048, 768, 512, 33, 1), L.MOE_EUNSUPPORTED),
+    (L.shape(4, 2048, 768, 2048, 10, 1), L.MOE_EUNSUPPORTED),
+    (L.shape(70000, 2048, 768, 512, 10, 1), L.MOE_EUNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("s,code", BAD_SHAPES)
+def test_bad_shapes_rejected_before_any_launch(s, code):
+    # fake, never dereferenced addresses: the checks fail before any CUDA call
+    fake = 0x10000
+    with pytest.raises(L.MoeError) as e:
+        L.moe_route(s, fake, L.MOE_BF16, fake, fake, fake, None, fake, 1 << 30, 0)
+    assert e.value.status == code
+    with pytest.raises(L.MoeError) as e:
+        L.moe_workspace_size(s)
+    assert e.value.status == code
+
+
+def test_null_and_misaligned_arguments():
+    s = L.shape(4, 256, 128, 16, 2, 0)
+    need = L.moe_workspace_size(s)
+    fake = 0x10000
+    cases = [
+        lambda: L.moe_route(s, None, L.MOE_BF16, fake, fake, fake, None, fake, need, 0),
+        lambda: L.moe_route(s, fake, L.MOE_BF16, fake, fake, fake, None, fake + 16, need, 0),   # ws not 256-aligned
+        lambda: L.moe_route(s, fake, L.MOE_BF16, fake, fake, fake, None, fake, need - 1, 0),    # ws too small
+        lambda: L.moe_route(s, fake + 2, L.MOE_BF16, fake, fake, fake, None, fake, need, 0),    # x misaligned
+        lambda: L.moe_route(s, fake, 7, fake, fake, fake, None, fake, need, 0),                 # bad dtype
+        lambda: L.moe_permute(s, fake, None, fake, fake, fake, fake, fake, need, 0),
+        lambda: L.moe_combine(s, fake, L.MOE_F32, fake, fake, None, fake + 4, L.MOE_BF16, 0),
+        lambda: L.moe_expert_ffn(s, 9, fake, L.MOE_BF16, L.expert_table(fake, 104448, fake), fake, fake, fake,
+                                 fake, L.MOE_F32, fake, need, 0),
+        lambda: L.moe_expert_ffn(s, 0, fake, L.MOE_BF16, L.expert_table(fake, 1000, fake), fake, fake, fake,
+                                 fake, L.MOE_F32, fake, need, 0),                              # slot_bytes too small
+        lambda: L.moe_expert_ffn(s, 0, fake, L.MOE_BF16, L.expert_table(fake, 104448, fake, fake), fake, fake,
+                                 fake, fake, L.MOE_F32, fake, need, 0),                        # shared with n_shared 0
+    ]
+    for fn in cases:
+        with pytest.raises(L.MoeError) as e:
+            fn()
+        assert e.value.status == L.MOE_EINVAL, L.moe_last_error_string()
+        assert L.moe_last_error_string()
+
+
+# ------------------------------------------------------------------ slot table ------------
+
+class FakeCopier:
+    """Records every copy the table asks for; optionally fails the n-th record copy."""
+
+    def __init__(self, pool, table, slot_bytes, fail_at=None):
+        self.pool, self.table, self.slot_bytes = pool, table, slot_bytes
+        self.records, self.entries = [], {}
+        self.fail_at, self.n_record_copies = fail_at, 0
+        self.fn = L.MOE_COPY_FN(self._copy)
+
+    def _copy(self, dst, src, nbytes, stream, user):
+        dst = dst or 0
+        if self.table <= dst < self.table + (1 << 20):
+            vals = np.ctypeslib.as_array((C.c_int32 * (nbytes // 4)).from_address(src))
+            for i, v in enumerate(vals):
+                self.entries[(dst - self.table) // 4 + i] = int(v)
+            return 0
+        self.n_record_copies += 1
+        if self.fail_at is not None and self.n_record_copies == self.fail_at:
+            return 1
+        assert (dst - self.pool) % self.slot_bytes == 0 and nbytes == self.slot_bytes
+        self.records.append(((dst - self.pool) // self.slot_bytes, src))
+        return 0
+
+
+def _make_table(Lyr, E, n_slots, fail_at=None):
+    pool, tab, sb = 0x100000, 0x40000000, 256
+    hrec = [0x7000000 + 4096 * i for i in range(Lyr * E)]
+    cp = FakeCopier(pool, tab, sb, fail_at)
+    h = L.slot_table_create(Lyr, E, n_slots, sb, pool, tab, hrec, cp.fn, None)
+    return h, cp, hrec
+
+
+def _update(h, layer, ids):
+    a = (C.c_int32 * max(1, len(ids)))(*ids)
+    hits = (C.c_int32 * max(1, len(ids)))()
+    miss = (C.c_int32 * max(1, len(ids)))()
+    nh, nm = C.c_int32(), C.c_int32()
+    st = L.slot_table_update(h, layer, C.addressof(a), len(ids), None, None, C.addressof(hits), C.addressof(nh),
+                             C.addressof(miss), C.addressof(nm), None)
+    return st, list(hits[:nh.value]), list(miss[:nm.value])
+
+
+def _snapshot(h, Lyr, E):
+    out = (C.c_int32 * (Lyr * E))()
+    L.slot_table_snapshot(h, C.addressof(out))
+    return np.array(out[:]).reshape(Lyr, E)
+
+
+def test_slot_table_fills_empty_slots_then_evicts_lru():
+    h, cp, hrec = _make_table(2, 8, 4)
+    assert all(v == -1 for v in cp.entries.values()) and len(cp.entries) == 16
+    st, hits, miss = _update(h, 0, [3, 5])
+    assert st == 0 and hits == [] and miss == [3, 5]
+    assert [s for s, _ in cp.records] == [0, 1] and [src for _, src in cp.records] == [hrec[3], hrec[5]]
+    st, hits, miss = _update(h, 0, [5, 6])
+    assert hits == [5] and miss == [6] and cp.records[-1] == (2, hrec[6])
+    st, hits, miss = _update(h, 1, [0])        # last empty slot
+    assert miss == [0] and cp.records[-1] == (3, hrec[8])
+    # LRU now: slot 0 (layer0 e3), slot 1 (e5), slot 2 (e6), slot 3 (layer1 e0), with e5/e6 touched after e3
+    st, hits, miss = _update(h, 1, [1])
+    assert miss == [1] and cp.records[-1][0] == 0   # evicts layer 0 expert 3
+    snap = _snapshot(h, 2, 8)
+    assert snap[0, 3] == -1 and snap[1, 1] == 0 and snap[0, 5] == 1 and snap[0, 6] == 2 and snap[1, 0] == 3
+    # the evicted entry of the other layer was written to the device table too
+    assert cp.entries[0 * 8 + 3] == -1 and cp.entries[1 * 8 + 1] == 0
+    s = L.slot_table_stats(h)
+    assert (s.hits, s.misses, s.evictions, s.bytes_h2d) == (1, 5, 1, 5 * 256)
+    L.slot_table_destroy(h)
+
+
+def test_slot_table_never_evicts_current_experts():
+    h, cp, _ = _make_table(1, 16, 3)
+    _update(h, 0, [0, 1, 2])
+    st, hits, miss = _update(h, 0, [2, 0, 9])   # 9 must evict expert 1 (not 0 or 2)
+    assert hits == [2, 0] and miss == [9]
+    snap = _snapshot(h, 1, 16)
+    assert snap[0, 1] == -1 and snap[0, 9] >= 0 and snap[0, 0] >= 0 and snap[0, 2] >= 0
+    L.slot_table_destroy(h)
+
+
+def test_slot_table_reports_no_slot_and_leaves_table_unchanged():
+    h, cp, _ = _make_table(1, 16, 3)
+    _update(h, 0, [0, 1])
+    before = _snapshot(h, 1, 16).copy()
+    n_before = len(cp.records)
+    st, _, _ = _update(h, 0, [0, 1, 2, 3])    # 2 misses, 1 evictable slot
+    assert st == L.MOE_ENOSLOT
+    assert np.array_equal(before, _snapshot(h, 1, 16)) and len(cp.records) == n_before
+    L.slot_table_destroy(h)
+
+
+def test_slot_table_rejects_bad_ids():
+    h, cp, _ = _make_table(2, 8, 4)
+    for layer, ids in [(0, [1, 1]), (0, [8]), (0, [-1]), (2, [0]), (-1, [0])]:
+        a = (C.c_int32 * len(ids))(*ids)
+        with pytest.raises(L.MoeError) as e:
+            L.slot_table_update(h, layer, C.addressof(a), len(ids), None, None)
+        assert e.value.status == L.MOE_EINVAL
+    L.slot_table_destroy(h)
+
+
+def test_slot_table_copy_failure_is_reported_and_not_resident():
+    h, cp, _ = _make_table(1, 8, 4, fail_at=2)
+    a = (C.c_int32 * 3)(4, 5, 6)
+    with pytest.raises(L.MoeError) as e:
+        L.slot_table_update(h, 0, C.addressof(a), 3, None, None)
+    assert e.value.status == L.MOE_ECUDA
+    snap = _snapshot(h, 1, 8)
+    assert snap[0, 4] >= 0 and snap[0, 5] == -1 and snap[0, 6] == -1
+    assert cp.entries[4] == snap[0, 4]
+    # a retry succeeds once the copier works again
+    cp.fail_at = None
+    st, hits, miss = _update(h, 0, [4, 5, 6])
+    assert st == 0 and hits == [4] and miss == [5, 6]
+    L.slot_table_destroy(h)

@@ -1,0 +1,170 @@
+"""GPU parity of the whole layer pass through the C-ABI against the CPU oracle, on the same
+seeded inputs: routing (indices where the logit gap allows, weights), bucketing (bit-exact),
+outputs (bf16: max |err| <= 2e-2 rms; fp32 debug mode: <= 1e-4 rms), and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import moe_oracle as O
+from routed_expert_ffn_bucketing_b300 import _lib as L
+from synth.device import DeviceLayer
+from synth.workloads import WORKLOADS, custom
+
+from gpu_util import check_bucketing, check_output, check_routing, run_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return DeviceLayer(WORKLOADS["tiny"])
+
+
+@pytest.fixture(scope="module")
+def decode():
+    return DeviceLayer(WORKLOADS["decode"])
+
+
+def test_device_generator_matches_numpy():
+    w = custom("decode", E=3, n_shared=1)
+    dl = DeviceLayer(w, layer=5)
+    for e in range(4):
+        assert np.array_equal(dl.record_bytes_of(e), synth.pack_record(w.expert(5, e))), e
+    w1 = WORKLOADS["tiny"]
+    dl1 = DeviceLayer(w1)
+    for e in (0, 7, 15):
+        assert np.array_equal(dl1.record_bytes_of(e), synth.pack_record(w1.expert(0, e)))
+
+
+def test_tiny_layer_bf16(tiny):
+    for batch in range(3):
+        run = run_layer(tiny, batch)
+        assert run.status == 0
+        check_routing(run, tiny.w)
+        check_bucketing(run, tiny.w)
+        check_output(run, tiny.w)
+
+
+def test_tiny_layer_fp32_debug(tiny):
+    run = run_layer(tiny, 1, f32=True)
+    assert run.status == 0
+    check_routing(run, tiny.w)
+    check_bucketing(run, tiny.w)
+    check_output(run, tiny.w, f32=True)
+
+
+def test_tiny_layer_residual_and_bf16_y(tiny):
+    run = run_layer(tiny, 2, residual=True, ydt=L.MOE_BF16)
+    check_output(run, tiny.w, residual=True)
+
+
+def test_decode_layer_full_size(decode):
+    w = decode.w
+    # the oracle sees the bytes the GPU holds, for every expert it uses
+    for batch in range(2):
+        run = run_layer(decode, batch)
+        assert run.status == 0
+        _, idx_g, n_checked = check_routing(run, w)
+        assert n_checked == w.T
+        check_bucketing(run, w)
+        for e in list(np.unique(idx_g)[:3]) + [w.E]:
+            assert np.array_equal(decode.record_bytes_of(int(e)), synth.pack_record(w.expert(0, int(e))))
+        check_output(run, w)
+
+
+def test_decode_layer_fp32_debug(decode):
+    run = run_layer(decode, 3, f32=True)
+    check_routing(run, decode.w)
+    check_output(run, decode.w, f32=True)
+
+
+@pytest.mark.parametrize("T,E,k,ns", [(1, 16, 2, 0), (3, 8, 8, 1), (16, 1, 1, 0), (7, 40, 5, 2), (16, 64, 32, 0)])
+def test_small_shapes(T, E, k, ns):
+    w = custom("tiny", T=T, E=E, k=k, n_shared=ns, d=96, f=64, router_sigma=1.0)
+    dl = DeviceLayer(w, fill="host")
+    run = run_layer(dl, 0)
+    assert run.status == 0
+    check_routing(run, w)
+    check_bucketing(run, w)
+    check_output(run, w)
+
+
+@pytest.mark.parametrize("T", [17, 300])
+def test_router_gemm_and_multichunk_bucketing(T):
+    # T > 16 takes the tiled router GEMM; T*k > 1024 takes the multi-chunk bucketing
+    w = custom("tiny", T=T, E=64, k=10, n_shared=1, router_sigma=1.0)
+    dl = DeviceLayer(w)
+    run = run_layer(dl, 0, mode=L.MOE_MODE_DECODE)
+    assert run.status == 0
+    check_routing(run, w)
+    check_bucketing(run, w)
+    check_output(run, w, tokens=np.arange(0, T, 7))
+
+
+def test_empty_batch(tiny):
+    w = custom("tiny", T=0)
+    dl = DeviceLayer(w)
+    run = run_layer(dl, 0)
+    assert run.status == 0
+    assert run.buf.active.cpu().numpy()[0] == 0
+    assert np.all(run.buf.offsets.cpu().numpy() == 0)
+
+
+def test_exact_ties_go_to_lowest_index():
+    w = custom("tiny", T=8, E=32, k=4, router_sigma=1.0)
+    dl = DeviceLayer(w)
+    r = dl.router.clone()
+    r[:, 20] = r[:, 3]     # experts 3 and 20 always tie exactly; so do 5, 6 and 30
+    r[:, 6] = r[:, 5]
+    r[:, 30] = r[:, 5]
+    dl.router = r
+    run = run_layer(dl, 0)
+    idx = run.buf.topk_idx.cpu().numpy()
+    for t in range(w.T):
+        s = set(idx[t])
+        assert not (20 in s and 3 not in s)
+        assert not (6 in s and 5 not in s) and not (30 in s and 6 not in s)
+    lg = run.buf.logits.cpu().numpy()
+    assert np.all(lg[:, 3] == lg[:, 20]) and np.all(lg[:, 5] == lg[:, 30])
+    # the GPU's selection equals the oracle's rule applied to the GPU's own (exactly tied) logits
+    assert np.array_equal(idx, O.select_topk(lg, w.k))
+
+
+def test_missing_slot_sets_status_and_skips(tiny):
+    so = tiny.slot_of.clone()
+    so[:] = -1
+    run = run_layer(tiny, 0, slot_of=so)
+    assert run.status & L.MOE_DEV_MISSING_SLOT
+
+
+def test_bad_expert_index_sets_status(tiny):
+    w = tiny.w
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, 0)
+    from routed_expert_ffn_bucketing_b300 import layer as lay
+    buf = lay.alloc_buffers(s)
+    idx = torch.zeros((w.T, w.k), dtype=torch.int32, device="cuda")
+    idx[:, 1] = 1
+    idx[3, 0] = w.E + 5
+    torch.cuda.synchronize()
+    L.moe_route(s, tiny.x(0), L.MOE_BF16, tiny.router, buf.topk_idx, buf.topk_w, None, buf.ws, buf.ws_bytes)
+    L.moe_permute(s, idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws, buf.ws_bytes)
+    assert L.moe_read_status(buf.ws) & L.MOE_DEV_BAD_EXPERT
+
+
+def test_nan_logit_sets_status(tiny):
+    w = tiny.w
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, 0)
+    from routed_expert_ffn_bucketing_b300 import layer as lay
+    buf = lay.alloc_buffers(s)
+    r = tiny.router.clone()
+    r[0, 4] = float("nan")
+    L.moe_route(s, tiny.x(0), L.MOE_BF16, r, buf.topk_idx, buf.topk_w, None, buf.ws, buf.ws_bytes)
+    assert L.moe_read_status(buf.ws) & L.MOE_DEV_NAN_LOGIT
+    assert not np.any(buf.topk_idx.cpu().numpy() == 4)
+
+
+def test_deterministic(decode):
+    a = run_layer(decode, 5)
+    b = run_layer(decode, 5)
+    assert torch.equal(a.buf.out, b.buf.out) and torch.equal(a.buf.topk_w, b.buf.topk_w)
