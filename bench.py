@@ -21,7 +21,11 @@ import subprocess
 import sys
 import time
 
-import numpy as np
+# the CPU oracle is timed on one core: fix the BLAS thread count before numpy loads
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -44,7 +48,7 @@ def peaks():
 # ------------------------------------------------------------------ clocks ----------------
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    """nvidia-smi clock/throttle samples every 100 ms while the timed region runs."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -56,7 +60,7 @@ class ClockSampler:
         try:
             self.path = f"/tmp/moe_bench_clocks_{os.getpid()}.csv"
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -125,21 +129,19 @@ def prepare_oracle(w, batches):
 
 
 def time_oracle(w, prep, budget_s: float, max_steps: int | None = None):
-    """Times the oracle's layer pass over the prepared batches, one batch per step, with one
-    BLAS thread. Returns (tokens/s, steps, seconds, threads)."""
-    from threadpoolctl import threadpool_limits
+    """Times the oracle's layer pass over the prepared batches, one batch per step, on one
+    thread. Returns (tokens/s, steps, seconds, threads)."""
     from oracle import moe_oracle as O
     xs, router, ex = prep
     shared = [ex[w.E + s] for s in range(w.n_shared)]
     steps, t0 = 0, time.perf_counter()
-    with threadpool_limits(limits=1):
-        while True:
-            O.moe_layer(xs[steps % len(xs)], router, w.k, lambda e: ex[e], shared)
-            steps += 1
-            el = time.perf_counter() - t0
-            if el >= budget_s or (max_steps is not None and steps >= max_steps):
-                break
-    return w.T * steps / el, steps, el, 1
+    while True:
+        O.moe_layer(xs[steps % len(xs)], router, w.k, lambda e: ex[e], shared)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps is not None and steps >= max_steps):
+            break
+    return w.T * steps / el, steps, el, int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
 
 
 # ------------------------------------------------------------------ distributed -----------
@@ -334,7 +336,7 @@ def run_ours(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")

@@ -36,7 +36,8 @@
  *  - Errors found by kernels (a NaN logit, an expert index out of range, a routed expert
  *    with no resident slot) set bits of a device status word in the workspace. Nothing
  *    traps. moe_read_status() returns that word.
- *  - T == 0 is valid: each call checks its arguments and enqueues nothing.
+ *  - T == 0 is valid: moe_route clears the status word, moe_permute writes zero counts and
+ *    an empty active list, and the other calls check their arguments and enqueue nothing.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -64,6 +65,7 @@ typedef enum {
 #define MOE_DEV_NAN_LOGIT    0x1  /* a router logit was NaN; it was ranked below every number */
 #define MOE_DEV_BAD_EXPERT   0x2  /* a topk_idx entry was outside [0, E); outputs are undefined */
 #define MOE_DEV_MISSING_SLOT 0x4  /* a routed expert had slot_of[e] < 0; its rows were left unwritten */
+#define MOE_DEV_TIMEOUT      0x8  /* a kernel's bounded wait ran out; that kernel's outputs are incomplete */
 
 typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
 

@@ -15,7 +15,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
 MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA, MOE_ENOSLOT, MOE_EDEVICE = 0, -1, -2, -3, -4, -5
-MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_EXPERT, MOE_DEV_MISSING_SLOT = 0x1, 0x2, 0x4
+MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_EXPERT, MOE_DEV_MISSING_SLOT, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 MOE_BF16, MOE_F32 = 0, 1
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
 

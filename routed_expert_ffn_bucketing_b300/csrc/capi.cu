@@ -63,8 +63,12 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
   int optin = 0;
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  if (bytes > (size_t)optin) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  const size_t room = (size_t)optin - fa.sharedSizeBytes;  // static shared memory counts too
+  if (bytes > room) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)room);
   if (e != cudaSuccess) return e;
   done.insert({kernel, dev});
   return cudaSuccess;

@@ -66,7 +66,7 @@ __device__ __forceinline__ bool resolve_item(int a, const FfnArgs& A, FfnItem* i
     const int e = A.active[1 + a];
     const int s = A.slot_of[e];
     if (s < 0) {
-      if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(A.status, MOE_DEV_MISSING_SLOT_BIT);
+      if (threadIdx.x == 0) flag_status(A.status, MOE_DEV_MISSING_SLOT_BIT);  // any CTA that meets it
       return false;
     }
     it->rec = A.pool + (uint64_t)s * A.slot_bytes;

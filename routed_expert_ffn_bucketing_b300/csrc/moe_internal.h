@@ -11,6 +11,7 @@ namespace moe {
 constexpr int MOE_DEV_NAN_LOGIT_BIT = MOE_DEV_NAN_LOGIT;
 constexpr int MOE_DEV_BAD_EXPERT_BIT = MOE_DEV_BAD_EXPERT;
 constexpr int MOE_DEV_MISSING_SLOT_BIT = MOE_DEV_MISSING_SLOT;
+constexpr int MOE_DEV_TIMEOUT_BIT = MOE_DEV_TIMEOUT;
 
 constexpr int kRouteGemvMaxT = 16;   // tokens up to which the router runs as a split-d GEMV
 constexpr int kRouteRowsPerSplit = 64;

@@ -18,9 +18,10 @@ namespace moe {
 
 constexpr int CH = kPermChunk;  // 1024
 
-__device__ __forceinline__ void bitonic_sort_1024(uint32_t* keys) {
-  const int i = threadIdx.x;
-  for (int size = 2; size <= CH; size <<= 1) {
+// Ascending bitonic sort of n = blockDim.x keys (a power of two), one key per thread.
+__device__ __forceinline__ void bitonic_sort_block(uint32_t* keys) {
+  const int i = threadIdx.x, n = blockDim.x;
+  for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const int j = i ^ stride;
       if (j > i) {
@@ -47,7 +48,8 @@ __device__ __forceinline__ int lower_bound_u32(const uint32_t* keys, int n, uint
   return lo;
 }
 
-// Block-wide exclusive scan of one int per thread (1024 threads); returns the total in *total.
+// Block-wide exclusive scan of one int per thread (a multiple of 32 threads, at most 1024);
+// returns the total in *total.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -59,7 +61,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_sums[lane];
+    int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -87,7 +89,8 @@ __device__ __forceinline__ uint32_t load_pair_key(const int32_t* topk_idx, int p
   return ((uint32_t)e << 10) | (uint32_t)local;
 }
 
-// All P <= 1024 pairs in one CTA: sort, offsets, active list, scatter.
+// All P <= 1024 pairs in one CTA of n >= P threads (a power of two, at least 32): sort,
+// offsets, active list, scatter.
 __global__ void __launch_bounds__(CH) bucket_single_kernel(const int32_t* __restrict__ topk_idx, int P, int E,
                                                            int32_t* __restrict__ counts,
                                                            int32_t* __restrict__ offsets,
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(CH) bucket_single_kernel(const int32_t* __rest
   const int i = threadIdx.x;
   keys[i] = load_pair_key(topk_idx, i, i, P, E, status);
   __syncthreads();
-  bitonic_sort_1024(keys);
+  bitonic_sort_block(keys);
   const uint32_t key = keys[i];
   const int e = (int)(key >> 10);
   if (i < P) {
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(CH) bucket_single_kernel(const int32_t* __rest
   const int rank = block_exclusive_scan(start, warp_sums, &n_active);
   if (start) active[1 + rank] = e;
   if (i == 0) active[0] = n_active;
-  for (int ee = i; ee <= E; ee += CH) {
+  for (int ee = i; ee <= E; ee += blockDim.x) {
     const int lb = lower_bound_u32(keys, P, (uint32_t)ee << 10);
     offsets[ee] = lb;
     if (ee < E) counts[ee] = lower_bound_u32(keys, P, (uint32_t)(ee + 1) << 10) - lb;
@@ -131,7 +134,7 @@ __global__ void __launch_bounds__(CH) bucket_chunk_kernel(const int32_t* __restr
   int32_t* row = cnt + (size_t)c * E;
   for (int ee = i; ee < E; ee += CH) row[ee] = 0;
   __syncthreads();
-  bitonic_sort_1024(keys);
+  bitonic_sort_block(keys);
   const uint32_t key = keys[i];
   chunk_keys[base + i] = key;  // the workspace holds C * 1024 keys
   if (i < n) {
@@ -205,7 +208,9 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
                            uint32_t* keys, int* status, cudaStream_t st) {
   const int P = s.T * s.k;
   if (P <= CH) {
-    bucket_single_kernel<<<1, CH, 0, st>>>(topk_idx, P, s.E, counts, offsets, sorted_pair, inv_pos, active,
+    int n = 32;
+    while (n < P) n <<= 1;
+    bucket_single_kernel<<<1, n, 0, st>>>(topk_idx, P, s.E, counts, offsets, sorted_pair, inv_pos, active,
                                            status);
     return cudaGetLastError();
   }

@@ -12,9 +12,10 @@
 //  * T > 16 (prefill): a tiled fp32 GEMM, 128 x 128 outputs per CTA. Each output sums its
 //    32-long k-blocks separately before adding them up, which keeps the fp32 error of a
 //    2048-long dot product near that of a tree sum.
-//  * top-k: one warp per token. Each lane holds E/32 logits as order-preserving integer
-//    keys, and k rounds of warp max (redux.sync) pick the experts. A tie goes to the lowest
-//    index.
+//  * top-k: one warp per token selects. Each lane holds E/32 logits as order-preserving
+//    integer keys, and k rounds of warp max (redux.sync) pick the experts. A tie goes to the
+//    lowest index. After the GEMV, one CTA per token first adds the split partial sums with
+//    all loads independent (a warp adding them one after another waited for each load in turn).
 #include "moe_common.cuh"
 
 namespace moe {
@@ -230,26 +231,12 @@ __device__ __forceinline__ float key_logit(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
 }
 
+// Selection of the k largest keys among the E logits held as PER keys per lane (logit e in
+// lane e % 32, slot e / 32), then the renormalised gate weights; one warp, one token.
 template <int PER>
-__global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ partial, int S, int T, int E,
-                                                   int k, int32_t* __restrict__ idx, float* __restrict__ wts,
-                                                   float* __restrict__ logits_out, int* status) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 4 + warp;
-  if (t >= T) return;
-  uint32_t key[PER];
-  bool nan = false;
-#pragma unroll
-  for (int p = 0; p < PER; ++p) {
-    const int e = lane + 32 * p;
-    key[p] = 0u;
-    if (e < E) {
-      float v = partial[(size_t)t * E + e];
-      for (int sp = 1; sp < S; ++sp) v += partial[((size_t)sp * T + t) * E + e];
-      if (logits_out) logits_out[(size_t)t * E + e] = v;
-      key[p] = logit_key(v, &nan);
-    }
-  }
+__device__ __forceinline__ void select_topk_warp(uint32_t (&key)[PER], int E, int k, int t, int32_t* idx,
+                                                 float* wts) {
+  const int lane = threadIdx.x & 31;
   uint32_t taken = 0u;
   int my_e = 0;
   uint32_t my_key = 0u;
@@ -277,7 +264,7 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
   }
   const float v = key_logit(my_key);
   const float m = __shfl_sync(0xFFFFFFFFu, v, 0);
-  float ex = lane < k ? expf(v - m) : 0.0f;
+  const float ex = lane < k ? expf(v - m) : 0.0f;
   float sum = ex;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
@@ -285,19 +272,95 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
     idx[(size_t)t * k + lane] = my_e;
     wts[(size_t)t * k + lane] = ex / sum;
   }
+}
+
+// Logits already summed (router GEMM): one warp per token.
+template <int PER>
+__global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                   int32_t* __restrict__ idx, float* __restrict__ wts,
+                                                   int* status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  uint32_t key[PER];
+  bool nan = false;
+#pragma unroll
+  for (int p = 0; p < PER; ++p) {
+    const int e = lane + 32 * p;
+    key[p] = e < E ? logit_key(logits[(size_t)t * E + e], &nan) : 0u;
+  }
+  select_topk_warp<PER>(key, E, k, t, idx, wts);
   if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) flag_status(status, MOE_DEV_NAN_LOGIT_BIT);
 }
 
+// Split-d partial sums (router GEMV): one CTA per token. Thread e adds expert e's S partial
+// sums in four interleaved chains, then adds the chains (a fixed order), with all loads
+// independent; warp 0 then selects from shared memory.
+template <int PER>
+__global__ void __launch_bounds__(1024) topk_split_kernel(const float* __restrict__ partial, int S, int T, int E,
+                                                          int k, int32_t* __restrict__ idx,
+                                                          float* __restrict__ wts, float* __restrict__ logits_out,
+                                                          int* status) {
+  __shared__ float lg[32 * PER];
+  __shared__ int nan_any;
+  const int t = blockIdx.x;
+  if (threadIdx.x == 0) nan_any = 0;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+    int sp = 0;
+    for (; sp + 4 <= S; sp += 4) {
+      c0 += partial[((size_t)(sp + 0) * T + t) * E + e];
+      c1 += partial[((size_t)(sp + 1) * T + t) * E + e];
+      c2 += partial[((size_t)(sp + 2) * T + t) * E + e];
+      c3 += partial[((size_t)(sp + 3) * T + t) * E + e];
+    }
+    for (; sp < S; ++sp) c0 += partial[((size_t)sp * T + t) * E + e];
+    const float v = (c0 + c1) + (c2 + c3);
+    lg[e] = v;
+    if (logits_out) logits_out[(size_t)t * E + e] = v;
+    if (v != v) nan_any = 1;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    uint32_t key[PER];
+    bool nan = false;
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const int e = lane + 32 * p;
+      key[p] = e < E ? logit_key(lg[e], &nan) : 0u;
+    }
+    select_topk_warp<PER>(key, E, k, t, idx, wts);
+    if (lane == 0 && nan_any) flag_status(status, MOE_DEV_NAN_LOGIT_BIT);
+  }
+}
+
+#define MOE_TOPK_DISPATCH(LAUNCH)    \
+  do {                               \
+    const int per = (s.E + 31) / 32; \
+    if (per <= 1) LAUNCH(1);         \
+    else if (per <= 2) LAUNCH(2);    \
+    else if (per <= 4) LAUNCH(4);    \
+    else if (per <= 8) LAUNCH(8);    \
+    else if (per <= 16) LAUNCH(16);  \
+    else LAUNCH(32);                 \
+  } while (0)
+
 cudaError_t launch_topk(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
                         float* logits_out, int* status, cudaStream_t st) {
-  const dim3 grid((s.T + 3) / 4);
-  const int per = (s.E + 31) / 32;
-  if (per <= 1) topk_kernel<1><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
-  else if (per <= 2) topk_kernel<2><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
-  else if (per <= 4) topk_kernel<4><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
-  else if (per <= 8) topk_kernel<8><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
-  else if (per <= 16) topk_kernel<16><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
-  else topk_kernel<32><<<grid, 128, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status);
+  if (splits > 1) {
+    const int threads = (s.E + 31) / 32 * 32;
+#define L_SPLIT(P) \
+  topk_split_kernel<P><<<s.T, threads, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status)
+    MOE_TOPK_DISPATCH(L_SPLIT);
+#undef L_SPLIT
+  } else {
+    const dim3 grid((s.T + 3) / 4);
+#define L_ONE(P) topk_kernel<P><<<grid, 128, 0, st>>>(partial, s.T, s.E, s.k, idx, wts, status)
+    MOE_TOPK_DISPATCH(L_ONE);
+#undef L_ONE
+  }
   return cudaGetLastError();
 }
 
