@@ -143,6 +143,24 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t*
                        int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int32_t* active,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Bucketing without a workspace, for callers that cannot allocate device memory where they
+ * bucket: for example an engine that sizes all device memory once at start-up and lets no
+ * library add to it, or a serving path where a cudaMalloc could stall the device. The pages
+ * have no counterpart: this is the same computation as moe_permute, with the same outputs,
+ * kernels and error bits, but its scratch is a fixed array inside this library. The array
+ * is 512 KiB on every GPU that loads the library and is held until the process exits.
+ *  status  out int32 (device): cleared by this call, then receives the MOE_DEV_* bits
+ * Limits: T*k <= 65536 pairs and E <= 1024, else MOE_EUNSUPPORTED (nothing enqueued).
+ * The first call on a device looks up the array's device address with that device current
+ * (cudaGetSymbolAddress). Make that first call before any stream capture. It allocates nothing
+ * (no cudaMalloc, no cudaFree). All calls in the process share the one array and every call
+ * rewrites all of the scratch it reads, so nothing carries over from an earlier call. Two
+ * calls whose work overlaps on the GPU (e.g. on two streams) race on the array and give
+ * undefined results: order them on one stream or with events. */
+moe_status moe_permute_static(const moe_shape* shape, const int32_t* topk_idx, int32_t* counts,
+                              int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos,
+                              int32_t* active, int32_t* status, moe_stream_t stream);
+
 /* Expert FFN: for every expert in `active` (and every shared expert), for each of its rows
  * y = W_down (silu(W_gate x) * (W_up x)), silu(z) = z / (1 + e^-z), W = q * s per block of 32.
  * The expert's record is found through the slot table (experts->slot_of).

@@ -54,6 +54,7 @@ _SIGS = {
     "moe_workspace_size": (C.c_int, [C.POINTER(moe_shape), C.POINTER(C.c_size_t)]),
     "moe_route": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "moe_permute": (C.c_int, [C.POINTER(moe_shape), _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
+    "moe_permute_static": (C.c_int, [C.POINTER(moe_shape), _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (C.c_int, [C.POINTER(moe_shape), C.c_int, _P, C.c_int, C.POINTER(moe_expert_table), _P, _P, _P,
                                  _P, C.c_int, _P, C.c_size_t, _P]),
     "moe_combine": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, C.c_int, _P]),
@@ -134,6 +135,14 @@ def moe_permute(s, topk_idx, counts, offsets, sorted_pair, inv_pos, active, ws, 
     return _check(lib().moe_permute(C.byref(s), ptr(topk_idx), ptr(counts), ptr(offsets), ptr(sorted_pair),
                                     ptr(inv_pos), ptr(active), ptr(ws), ws_bytes, stream_handle(stream)),
                   "moe_permute")
+
+
+def moe_permute_static(s, topk_idx, counts, offsets, sorted_pair, inv_pos, active, status, stream=None) -> int:
+    """moe_permute with the library's fixed scratch instead of a workspace; `status` is a
+    device int32 that receives the MOE_DEV_* bits."""
+    return _check(lib().moe_permute_static(C.byref(s), ptr(topk_idx), ptr(counts), ptr(offsets), ptr(sorted_pair),
+                                           ptr(inv_pos), ptr(active), ptr(status), stream_handle(stream)),
+                  "moe_permute_static")
 
 
 def expert_table(pool, slot_bytes: int, slot_of, shared=None) -> moe_expert_table:

@@ -21,6 +21,8 @@ static moe_status fail(moe_status st, const char* fmt, ...) {
   return st;
 }
 
+moe_status report_error(moe_status st, const char* msg) { return fail(st, "%s", msg); }
+
 static moe_status cuda_fail(cudaError_t e, const char* where) {
   return fail(MOE_ECUDA, "%s: %s", where, cudaGetErrorString(e));
 }

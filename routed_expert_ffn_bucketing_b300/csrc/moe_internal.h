@@ -33,6 +33,9 @@ struct WsLayout {
 
 WsLayout ws_layout(const moe_shape& s);
 
+// Records `msg` as this host thread's moe_last_error_string() and returns st.
+moe_status report_error(moe_status st, const char* msg);
+
 // Raises a kernel's dynamic shared memory limit to at least `bytes` on the current device
 // (once per kernel and device).
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
