@@ -49,6 +49,12 @@ WsLayout ws_layout(const moe_shape& s) {
   o = align256(o + sizeof(uint32_t) * C * kPermChunk);
   L.h = o;
   o = align256(o + sizeof(float) * (P + T * s.n_shared) * s.f);
+  L.x16 = o;
+  o = align256(o + sizeof(uint16_t) * T * s.d);
+  L.xunscale = o;
+  o = align256(o + sizeof(float) * T);
+  L.hmax = o;
+  o = align256(o + sizeof(uint32_t) * (P + T * s.n_shared));
   L.tiles = o;
   L.total = o;
   return L;
@@ -74,6 +80,20 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
   if (e != cudaSuccess) return e;
   done.insert({kernel, dev});
   return cudaSuccess;
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
 }
 
 static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
@@ -250,7 +270,12 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
   a.o_gate_s = lay.gate_s;
   a.o_up_s = lay.up_s;
   a.o_down_s = lay.down_s;
-  cudaError_t e = launch_ffn_decode(a, reinterpret_cast<cudaStream_t>(stream));
+  // bf16 activations: TMA-streamed tensor-core kernels; fp32 (debug mode): fp32 SIMT throughout
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = (xdt == MOE_BF16 && stream_supported(a))
+                      ? launch_ffn_decode_tc(a, at<__half>(ws, L.x16), at<float>(ws, L.xunscale),
+                                             at<uint32_t>(ws, L.hmax), device_sm_count(), cs)
+                      : launch_ffn_decode(a, cs);
   if (e != cudaSuccess) return cuda_fail(e, "moe_expert_ffn: launch");
   return MOE_OK;
 }

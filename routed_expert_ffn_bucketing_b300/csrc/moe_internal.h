@@ -4,6 +4,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda_fp16.h>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -27,6 +29,9 @@ struct WsLayout {
   size_t perm_cnt;       // int32 [C][E]: per-chunk counts, then per-chunk bases
   size_t perm_keys;      // uint32 [C * kPermChunk]: chunk-sorted (expert, pair) keys
   size_t h;              // [P + T*n_shared][f] fp32: SwiGLU activations between the FFN kernels
+  size_t x16;            // f16 [T][d]: activations rescaled per token by a power of two
+  size_t xunscale;       // fp32 [T]: the power of two that undoes that rescale
+  size_t hmax;           // uint32 [P + T*n_shared]: bits of max |h| per h row
   size_t tiles;          // int32 [..]: prefill tile list
   size_t total;
 };
@@ -72,7 +77,12 @@ cudaError_t launch_topk(const moe_shape& s, const float* partial, int splits, in
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
                            uint32_t* keys, int* status, cudaStream_t st);
-cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);
+cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);  // fp32 SIMT (any x dtype)
+// TMA-streamed tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
+cudaError_t launch_ffn_decode_tc(const FfnArgs& a, __half* x16, float* xunscale, uint32_t* hmax, int sm_count,
+                                 cudaStream_t st);
+bool stream_supported(const FfnArgs& a);
+int device_sm_count();
 cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,
                            const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st);
 
