@@ -327,7 +327,7 @@ def run_ours(args, ws, rank, local):
         "wall_s": wall,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": 6 * K,
+        "gpu_launches": 7 * K,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

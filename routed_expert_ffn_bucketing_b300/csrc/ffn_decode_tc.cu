@@ -24,7 +24,7 @@
 // Exactness. Weight codes become f16 pairs exactly (a byte permute into 1024 + (q + 128),
 // then one packed subtraction). Each MMA stays inside one 32-element block, so the block's
 // fp16 scale multiplies the fp32 MMA result. Activations are f16 copies, exact after a
-// per-token power-of-two rescale that keeps |x| below 2^15 (bf16 has 8 significant bits).
+// per-token power-of-two rescale that puts max |x| in [2^14, 2^15) (bf16 has 8 significant bits).
 // h is rescaled per row by a power of two from max |h| of that row and rounded once to f16
 // (11 bits). That max is an atomic max of non-negative floats, so it does not depend on order.
 //
@@ -35,6 +35,7 @@
 // Every wait is bounded. A wait that runs out sets MOE_DEV_TIMEOUT in the status word; the
 // CTA then stops its work, lets its copies in flight land and returns.
 #include "moe_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 
@@ -48,45 +49,8 @@ constexpr int kDownKSplit = kConsumerWarps / kDownSub;
 constexpr int kHPad = 32;                   // f16 padding per staged h row
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemBudget = 227 * 1024;  // dynamic shared memory per CTA
-constexpr long long kWaitLimit = 1ll << 26;  // try_wait rounds before a wait is abandoned
 
 // ------------------------------------------------------------------ PTX helpers ----------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Waits for the completion of the phase with parity `parity`; false if the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
-  for (long long i = 0; i < kWaitLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // Barrier of the consumer warps only (the producer warp does not take part).
 __device__ __forceinline__ void consumer_sync() {
@@ -124,9 +88,13 @@ __device__ __forceinline__ void block_mma(float* d, uint2 wg, uint2 wg8, const u
 
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
-// e >= 0 with m * 2^-e < 2^15 (m finite, >= 0)
+// e with m * 2^-e in [2^14, 2^15) for a normal m > 0 (clamped to [-100, 100]); 0 for m == 0.
+// Scaling a row by 2^-e puts its largest magnitude near the top of the f16 range, so values
+// down to 2^-28 of that maximum stay normal f16 numbers.
 __device__ __forceinline__ int f16_exp_for(float m) {
-  return m >= 32768.0f ? (int)((__float_as_uint(m) >> 23) & 0xFF) - 127 - 14 : 0;
+  if (!(m > 0.0f)) return 0;
+  const int e = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127 - 14;
+  return e < -100 ? -100 : (e > 100 ? 100 : e);
 }
 
 // Contiguous range [t0, t1) of this CTA's tiles out of n, split over gridDim.x CTAs.
@@ -197,7 +165,7 @@ __device__ __forceinline__ void init_barriers(StreamSmem& S, int NS) {
       mbar_init(&S.empty[s], 1);
     }
     S.abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_mbar_init();
   }
   __syncthreads();
 }
