@@ -66,6 +66,7 @@ typedef enum {
 #define MOE_DEV_BAD_EXPERT   0x2  /* a topk_idx entry was outside [0, E); outputs are undefined */
 #define MOE_DEV_MISSING_SLOT 0x4  /* a routed expert had slot_of[e] < 0; its rows were left unwritten */
 #define MOE_DEV_TIMEOUT      0x8  /* a kernel's bounded wait ran out; that kernel's outputs are incomplete */
+#define MOE_DEV_BAD_SLOT     0x10 /* a routed expert had slot_of[e] >= n_slots; its rows were left unwritten */
 
 typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
 
@@ -95,17 +96,20 @@ typedef struct {
 moe_status moe_get_expert_layout(int32_t d, int32_t f, moe_expert_layout* out);
 
 /* Where the experts of one layer live.
- *  pool       device: slot records, slot s at pool + s * slot_bytes
+ *  pool       device: slot records, slot s at pool + s * slot_bytes, s < n_slots
  *  slot_bytes stride of the pool: >= record_bytes and a multiple of 256
  *  slot_of    device int32 [E]: slot of routed expert e, or -1 when it is not resident
  *             (the row of one layer of the slot table; [P2] "专家缓存")
  *  shared     device: n_shared records at shared + s * slot_bytes; NULL iff n_shared == 0
+ *  n_slots    number of slots in the pool (> 0). A slot_of entry >= n_slots is an error
+ *             (MOE_DEV_BAD_SLOT) and that expert's rows are not written.
  * The table is only read. It is the caller's (or slot_table_update's) job to keep it current. */
 typedef struct {
   const void* pool;
   uint64_t slot_bytes;
   const int32_t* slot_of;
   const void* shared;
+  uint64_t n_slots;
 } moe_expert_table;
 
 /* Bytes of workspace that moe_route / moe_permute / moe_expert_ffn need for this shape

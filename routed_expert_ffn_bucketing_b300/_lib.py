@@ -15,7 +15,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
 MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA, MOE_ENOSLOT, MOE_EDEVICE = 0, -1, -2, -3, -4, -5
-MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_EXPERT, MOE_DEV_MISSING_SLOT, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_EXPERT, MOE_DEV_MISSING_SLOT, MOE_DEV_TIMEOUT, MOE_DEV_BAD_SLOT = 0x1, 0x2, 0x4, 0x8, 0x10
 MOE_BF16, MOE_F32 = 0, 1
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
 
@@ -39,7 +39,8 @@ class moe_expert_layout(C.Structure):
 
 
 class moe_expert_table(C.Structure):
-    _fields_ = [("pool", C.c_void_p), ("slot_bytes", C.c_uint64), ("slot_of", C.c_void_p), ("shared", C.c_void_p)]
+    _fields_ = [("pool", C.c_void_p), ("slot_bytes", C.c_uint64), ("slot_of", C.c_void_p), ("shared", C.c_void_p),
+                ("n_slots", C.c_uint64)]
 
 
 class moe_slot_stats(C.Structure):
@@ -145,8 +146,8 @@ def moe_permute_static(s, topk_idx, counts, offsets, sorted_pair, inv_pos, activ
                   "moe_permute_static")
 
 
-def expert_table(pool, slot_bytes: int, slot_of, shared=None) -> moe_expert_table:
-    return moe_expert_table(ptr(pool), slot_bytes, ptr(slot_of), ptr(shared))
+def expert_table(pool, slot_bytes: int, n_slots: int, slot_of, shared=None) -> moe_expert_table:
+    return moe_expert_table(ptr(pool), slot_bytes, ptr(slot_of), ptr(shared), n_slots)
 
 
 def moe_expert_ffn(s, mode, x, xdt, table: moe_expert_table, offsets, sorted_pair, active, y_perm, ydt, ws,

@@ -55,7 +55,16 @@ WsLayout ws_layout(const moe_shape& s) {
   o = align256(o + sizeof(float) * T);
   L.hmax = o;
   o = align256(o + sizeof(uint32_t) * (P + T * s.n_shared));
-  L.tiles = o;
+  L.items = o;
+  o = align256(o + sizeof(ItemRec) * ((P < (size_t)s.E ? P : (size_t)s.E) + s.n_shared));
+  L.row_tok = o;
+  o = align256(o + sizeof(int32_t) * (P + T * s.n_shared));
+  L.h16 = o;
+  o = align256(o + sizeof(uint16_t) * (P + T * s.n_shared) * s.f);
+  L.hexp = o;
+  o = align256(o + sizeof(int32_t) * (P + T * s.n_shared));
+  L.item_cnt = o;
+  o = align256(o + sizeof(int32_t) * ((P < (size_t)s.E ? P : (size_t)s.E) + s.n_shared));
   L.total = o;
   return L;
 }
@@ -230,6 +239,8 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
   if (!x || !experts || !offsets || !sorted_pair || !active || !y_perm)
     return fail(MOE_EINVAL, "moe_expert_ffn: NULL argument");
   if (!experts->pool || !experts->slot_of) return fail(MOE_EINVAL, "moe_expert_ffn: NULL pool or slot_of");
+  if (experts->n_slots == 0 || experts->n_slots > ((uint64_t)1 << 31))
+    return fail(MOE_EINVAL, "moe_expert_ffn: n_slots %llu must be in [1, 2^31]", (unsigned long long)experts->n_slots);
   if ((shape->n_shared > 0) != (experts->shared != nullptr))
     return fail(MOE_EINVAL, "moe_expert_ffn: shared must be non-NULL exactly when n_shared > 0");
   moe_expert_layout lay;
@@ -250,6 +261,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
   a.slot_bytes = experts->slot_bytes;
   a.slot_of = experts->slot_of;
   a.shared = static_cast<const uint8_t*>(experts->shared);
+  a.n_slots = experts->n_slots;
   a.offsets = offsets;
   a.sorted_pair = sorted_pair;
   a.active = active;
@@ -270,12 +282,18 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
   a.o_gate_s = lay.gate_s;
   a.o_up_s = lay.up_s;
   a.o_down_s = lay.down_s;
-  // bf16 activations: TMA-streamed tensor-core kernels; fp32 (debug mode): fp32 SIMT throughout
+  // bf16 activations: bulk-copy-streamed tensor-core kernels; fp32 (debug mode): fp32 SIMT throughout
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = (xdt == MOE_BF16 && stream_supported(a))
-                      ? launch_ffn_decode_tc(a, at<__half>(ws, L.x16), at<float>(ws, L.xunscale),
-                                             at<uint32_t>(ws, L.hmax), device_sm_count(), cs)
-                      : launch_ffn_decode(a, cs);
+  cudaError_t e;
+  if (xdt == MOE_BF16 && stream_supported(a)) {
+    const StreamAux aux{at<__half>(ws, L.x16),    at<float>(ws, L.xunscale), at<uint32_t>(ws, L.hmax),
+                        at<ItemRec>(ws, L.items), at<int32_t>(ws, L.row_tok), at<__half>(ws, L.h16),
+                        at<int32_t>(ws, L.hexp),  at<int32_t>(ws, L.item_cnt)};
+    const PoolView pv{experts->pool, experts->shared, experts->n_slots, experts->slot_bytes};
+    e = launch_ffn_stream(a, aux, pv, device_sm_count(), cs);
+  } else {
+    e = launch_ffn_decode(a, cs);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "moe_expert_ffn: launch");
   return MOE_OK;
 }

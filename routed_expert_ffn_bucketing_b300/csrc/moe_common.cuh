@@ -58,6 +58,7 @@ struct FfnItem {
   int row0;            // first y_perm / h row of this expert
   int ntok;            // rows (tokens) of this expert
   int routed;          // 1: tokens come from sorted_pair; 0: shared expert, tokens 0..T-1
+  int slot;            // pool slot (routed) or shared-expert index
 };
 
 __device__ __forceinline__ bool resolve_item(int a, const FfnArgs& A, FfnItem* it) {
@@ -66,10 +67,15 @@ __device__ __forceinline__ bool resolve_item(int a, const FfnArgs& A, FfnItem* i
     const int e = A.active[1 + a];
     const int s = A.slot_of[e];
     if (s < 0) {
-      if (threadIdx.x == 0) flag_status(A.status, MOE_DEV_MISSING_SLOT_BIT);  // any CTA that meets it
+      flag_status(A.status, MOE_DEV_MISSING_SLOT_BIT);
+      return false;
+    }
+    if ((uint64_t)s >= A.n_slots) {
+      flag_status(A.status, MOE_DEV_BAD_SLOT_BIT);
       return false;
     }
     it->rec = A.pool + (uint64_t)s * A.slot_bytes;
+    it->slot = s;
     it->row0 = A.offsets[e];
     it->ntok = A.offsets[e + 1] - A.offsets[e];
     it->routed = 1;
@@ -78,6 +84,7 @@ __device__ __forceinline__ bool resolve_item(int a, const FfnArgs& A, FfnItem* i
   const int sh = a - n_active;
   if (sh < A.n_shared) {
     it->rec = A.shared + (uint64_t)sh * A.slot_bytes;
+    it->slot = sh;
     it->row0 = A.P + sh * A.T;
     it->ntok = A.T;
     it->routed = 0;

@@ -14,6 +14,7 @@ constexpr int MOE_DEV_NAN_LOGIT_BIT = MOE_DEV_NAN_LOGIT;
 constexpr int MOE_DEV_BAD_EXPERT_BIT = MOE_DEV_BAD_EXPERT;
 constexpr int MOE_DEV_MISSING_SLOT_BIT = MOE_DEV_MISSING_SLOT;
 constexpr int MOE_DEV_TIMEOUT_BIT = MOE_DEV_TIMEOUT;
+constexpr int MOE_DEV_BAD_SLOT_BIT = MOE_DEV_BAD_SLOT;
 
 constexpr int kRouteGemvMaxT = 16;   // tokens up to which the router runs as a split-d GEMV
 constexpr int kRouteRowsPerSplit = 64;
@@ -32,7 +33,11 @@ struct WsLayout {
   size_t x16;            // f16 [T][d]: activations rescaled per token by a power of two
   size_t xunscale;       // fp32 [T]: the power of two that undoes that rescale
   size_t hmax;           // uint32 [P + T*n_shared]: bits of max |h| per h row
-  size_t tiles;          // int32 [..]: prefill tile list
+  size_t items;          // ItemRec [min(E, P) + n_shared]: work items of the expert FFN
+  size_t row_tok;        // int32 [P + T*n_shared]: token of each y_perm / h row
+  size_t h16;            // f16 [P + T*n_shared][f]: h rescaled per row by a power of two
+  size_t hexp;           // int32 [P + T*n_shared]: the exponent e of that rescale (h = h16 * 2^e)
+  size_t item_cnt;       // int32 [min(E, P) + n_shared]: finished gate/up units per work item
   size_t total;
 };
 
@@ -55,6 +60,7 @@ struct FfnArgs {
   uint64_t slot_bytes;
   const int32_t* slot_of;
   const uint8_t* shared;
+  uint64_t n_slots;
   const int32_t* offsets;
   const int32_t* sorted_pair;
   const int32_t* active;
@@ -65,6 +71,36 @@ struct FfnArgs {
   int T, d, f, E, k, n_shared, P;
   // record layout
   uint64_t o_gate_q, o_up_q, o_down_q, o_gate_s, o_up_s, o_down_s;
+};
+
+// One work item of the expert FFN as the streaming kernels see it: the expert's record (NULL
+// when the expert has no resident slot), its first y_perm / h row and its number of rows.
+struct ItemRec {
+  const uint8_t* rec;
+  int row0;
+  int ntok;
+  int slot;    // slot in the pool, or the index of the shared expert
+  int shared;  // 1: a shared expert (its record is in the shared array)
+  int pad[2];
+};
+
+// Workspace buffers of the streaming expert-FFN kernels.
+struct StreamAux {
+  __half* x16;
+  float* xunscale;
+  uint32_t* hmax;
+  ItemRec* items;
+  int32_t* row_tok;
+  __half* h16;
+  int32_t* hexp;
+  int32_t* item_cnt;
+};
+
+// Where the expert records are, for the host code that builds the tensor maps.
+struct PoolView {
+  const void* pool;
+  const void* shared;
+  uint64_t n_slots, slot_bytes;
 };
 
 // Launchers; each returns cudaSuccess or the launch error.
@@ -78,9 +114,9 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
                            int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
                            uint32_t* keys, int* status, cudaStream_t st);
 cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);  // fp32 SIMT (any x dtype)
-// TMA-streamed tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
-cudaError_t launch_ffn_decode_tc(const FfnArgs& a, __half* x16, float* xunscale, uint32_t* hmax, int sm_count,
-                                 cudaStream_t st);
+// Bulk-copy-streamed tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
+cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, const PoolView& pv, int sm_count,
+                              cudaStream_t st);
 bool stream_supported(const FfnArgs& a);
 int device_sm_count();
 cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,

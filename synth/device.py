@@ -32,6 +32,11 @@ class DeviceLayer:
         self.router = torch.from_numpy(w.router(layer)).to(device)
 
     @property
+    def n_slots(self) -> int:
+        """Slots of the routed-expert pool (the shared records follow them)."""
+        return self.w.E
+
+    @property
     def shared_ptr(self) -> int | None:
         return self.pool.data_ptr() + self.w.E * self.slot_bytes if self.w.n_shared else None
 

@@ -31,7 +31,8 @@ def run_layer(dl: DeviceLayer, batch: int = 0, mode: int = L.MOE_MODE_AUTO, f32:
     odt = L.MOE_F32 if f32 else L.MOE_BF16
     buf = lay.alloc_buffers(s, ydt=L.MOE_F32 if f32 else ydt, odt=odt)
     x = dl.x(batch, torch.float32 if f32 else torch.bfloat16)
-    table = L.expert_table(dl.pool, dl.slot_bytes, dl.slot_of if slot_of is None else slot_of, dl.shared_ptr)
+    table = L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of if slot_of is None else slot_of,
+                           dl.shared_ptr)
     lay.forward(buf, x, dl.router, table, mode, residual=x if residual else None)
     status = L.moe_read_status(buf.ws)
     torch.cuda.synchronize()

@@ -93,11 +93,11 @@ def test_null_and_misaligned_arguments():
         lambda: L.moe_route(s, fake, 7, fake, fake, fake, None, fake, need, 0),                 # bad dtype
         lambda: L.moe_permute(s, fake, None, fake, fake, fake, fake, fake, need, 0),
         lambda: L.moe_combine(s, fake, L.MOE_F32, fake, fake, None, fake + 4, L.MOE_BF16, 0),
-        lambda: L.moe_expert_ffn(s, 9, fake, L.MOE_BF16, L.expert_table(fake, 104448, fake), fake, fake, fake,
+        lambda: L.moe_expert_ffn(s, 9, fake, L.MOE_BF16, L.expert_table(fake, 104448, 16, fake), fake, fake, fake,
                                  fake, L.MOE_F32, fake, need, 0),
-        lambda: L.moe_expert_ffn(s, 0, fake, L.MOE_BF16, L.expert_table(fake, 1000, fake), fake, fake, fake,
+        lambda: L.moe_expert_ffn(s, 0, fake, L.MOE_BF16, L.expert_table(fake, 1000, 16, fake), fake, fake, fake,
                                  fake, L.MOE_F32, fake, need, 0),                              # slot_bytes too small
-        lambda: L.moe_expert_ffn(s, 0, fake, L.MOE_BF16, L.expert_table(fake, 104448, fake, fake), fake, fake,
+        lambda: L.moe_expert_ffn(s, 0, fake, L.MOE_BF16, L.expert_table(fake, 104448, 16, fake, fake), fake, fake,
                                  fake, fake, L.MOE_F32, fake, need, 0),                        # shared with n_shared 0
     ]
     for fn in cases:
