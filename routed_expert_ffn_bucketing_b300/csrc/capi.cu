@@ -29,6 +29,12 @@ static moe_status cuda_fail(cudaError_t e, const char* where) {
 
 static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
+// Routed work items at most: experts with at least one pair.
+static size_t P_items(const moe_shape& s) {
+  const size_t P = (size_t)s.T * s.k;
+  return P < (size_t)s.E ? P : (size_t)s.E;
+}
+
 int route_splits(int d) { return (d + kRouteRowsPerSplit - 1) / kRouteRowsPerSplit; }
 int perm_chunks(int P) { return (P + kPermChunk - 1) / kPermChunk; }
 
@@ -64,7 +70,11 @@ WsLayout ws_layout(const moe_shape& s) {
   L.hexp = o;
   o = align256(o + sizeof(int32_t) * (P + T * s.n_shared));
   L.item_cnt = o;
-  o = align256(o + sizeof(int32_t) * ((P < (size_t)s.E ? P : (size_t)s.E) + s.n_shared));
+  o = align256(o + sizeof(int32_t) * ((P < (size_t)s.E ? P : (size_t)s.E) + s.n_shared + 2));
+  L.cx = o;
+  o = align256(o + sizeof(float) * T * (s.d / 32));
+  L.ch = o;
+  o = align256(o + sizeof(float) * (P + T * s.n_shared) * (s.f / 32));
   L.total = o;
   return L;
 }
@@ -286,11 +296,12 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (xdt == MOE_BF16 && stream_supported(a)) {
+    const size_t items_max = (P_items(*shape)) + shape->n_shared;
     const StreamAux aux{at<__half>(ws, L.x16),    at<float>(ws, L.xunscale), at<uint32_t>(ws, L.hmax),
                         at<ItemRec>(ws, L.items), at<int32_t>(ws, L.row_tok), at<__half>(ws, L.h16),
-                        at<int32_t>(ws, L.hexp),  at<int32_t>(ws, L.item_cnt)};
-    const PoolView pv{experts->pool, experts->shared, experts->n_slots, experts->slot_bytes};
-    e = launch_ffn_stream(a, aux, pv, device_sm_count(), cs);
+                        at<int32_t>(ws, L.hexp),  at<int32_t>(ws, L.item_cnt), at<float>(ws, L.cx),
+                        at<float>(ws, L.ch),      at<int32_t>(ws, L.item_cnt) + items_max};
+    e = launch_ffn_stream(a, aux, device_sm_count(), cs);
   } else {
     e = launch_ffn_decode(a, cs);
   }

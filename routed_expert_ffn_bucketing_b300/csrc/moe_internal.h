@@ -30,14 +30,17 @@ struct WsLayout {
   size_t perm_cnt;       // int32 [C][E]: per-chunk counts, then per-chunk bases
   size_t perm_keys;      // uint32 [C * kPermChunk]: chunk-sorted (expert, pair) keys
   size_t h;              // [P + T*n_shared][f] fp32: SwiGLU activations between the FFN kernels
-  size_t x16;            // f16 [T][d]: activations rescaled per token by a power of two
+  size_t x16;            // f16 [T][d]: activations rescaled per token by a power of two (permuted)
   size_t xunscale;       // fp32 [T]: the power of two that undoes that rescale
   size_t hmax;           // uint32 [P + T*n_shared]: bits of max |h| per h row
   size_t items;          // ItemRec [min(E, P) + n_shared]: work items of the expert FFN
   size_t row_tok;        // int32 [P + T*n_shared]: token of each y_perm / h row
-  size_t h16;            // f16 [P + T*n_shared][f]: h rescaled per row by a power of two
+  size_t h16;            // f16 [P + T*n_shared][f]: h rescaled per row by a power of two (permuted)
   size_t hexp;           // int32 [P + T*n_shared]: the exponent e of that rescale (h = h16 * 2^e)
-  size_t item_cnt;       // int32 [min(E, P) + n_shared]: finished gate/up units per work item
+  size_t item_cnt;       // int32 [min(E, P) + n_shared + 2]: finished gate/up tasks per work item,
+                         // then the task counters of the two streaming kernels
+  size_t cx;             // fp32 [T][d/32]: MMA accumulator inputs of the x16 blocks
+  size_t ch;             // fp32 [P + T*n_shared][f/32]: MMA accumulator inputs of the h16 blocks
   size_t total;
 };
 
@@ -94,14 +97,11 @@ struct StreamAux {
   __half* h16;
   int32_t* hexp;
   int32_t* item_cnt;
+  float* cx;  // [T][d/32]: -1152 * (sum of each block of x16), the MMA accumulator input
+  float* ch;  // [P + T*n_shared][f/32]: the same for h16
+  int32_t* sched;  // [2]: next task of the gate/up and of the down kernel
 };
 
-// Where the expert records are, for the host code that builds the tensor maps.
-struct PoolView {
-  const void* pool;
-  const void* shared;
-  uint64_t n_slots, slot_bytes;
-};
 
 // Launchers; each returns cudaSuccess or the launch error.
 cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
@@ -114,9 +114,8 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
                            int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
                            uint32_t* keys, int* status, cudaStream_t st);
 cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);  // fp32 SIMT (any x dtype)
-// Bulk-copy-streamed tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
-cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, const PoolView& pv, int sm_count,
-                              cudaStream_t st);
+// Streaming tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
+cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, int sm_count, cudaStream_t st);
 bool stream_supported(const FfnArgs& a);
 int device_sm_count();
 cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,

@@ -93,6 +93,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int x, 
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, int x, int y, int z, int w, int v,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
+      "%6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Asks L2 to fetch [src, src + bytes) (16-byte aligned, bytes a multiple of 16); no completion.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
