@@ -71,6 +71,12 @@ WsLayout ws_layout(const moe_shape& s) {
   o = align256(o + sizeof(int32_t) * (P + T * s.n_shared));
   L.item_cnt = o;
   o = align256(o + sizeof(int32_t) * ((P < (size_t)s.E ? P : (size_t)s.E) + s.n_shared + 2));
+  L.xp16 = o;
+  o = align256(o + sizeof(uint16_t) * (P + T * s.n_shared) * s.d);
+  L.xexp = o;
+  o = align256(o + sizeof(int32_t) * T);
+  L.tiles = o;
+  o = align256(o + sizeof(int32_t) * 2 * ((P + T * s.n_shared) / 128 + P_items(s) + s.n_shared + 2));
   L.cx = o;
   o = align256(o + sizeof(float) * T * (s.d / 32));
   L.ch = o;
@@ -261,7 +267,6 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
   if (!aligned(x, 16) || !aligned(y_perm, 16) || !aligned(experts->pool, 256) ||
       (experts->shared && !aligned(experts->shared, 256)))
     return fail(MOE_EINVAL, "moe_expert_ffn: misaligned x, y_perm, pool or shared");
-  if (mode == MOE_MODE_PREFILL) return fail(MOE_EUNSUPPORTED, "moe_expert_ffn: PREFILL kernels not built");
   if (shape->T == 0) return MOE_OK;
   const WsLayout L = ws_layout(*shape);
   FfnArgs a{};
@@ -292,10 +297,22 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
   a.o_gate_s = lay.gate_s;
   a.o_up_s = lay.up_s;
   a.o_down_s = lay.down_s;
-  // bf16 activations: bulk-copy-streamed tensor-core kernels; fp32 (debug mode): fp32 SIMT throughout
+  // PREFILL (and AUTO for T > 16 with bf16 x): tensor-core grouped GEMM. DECODE (and AUTO for few
+  // tokens): streaming tensor-core kernels for bf16 x, fp32 SIMT kernels in the fp32 debug mode.
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (xdt == MOE_BF16 && stream_supported(a)) {
+  const bool want_prefill = mode == MOE_MODE_PREFILL || (mode == MOE_MODE_AUTO && shape->T > kDecodeMaxT && xdt == MOE_BF16);
+  if (want_prefill && prefill_supported(a)) {
+    const PrefillAux px{at<__half>(ws, L.xp16),    at<float>(ws, L.xunscale), at<int32_t>(ws, L.xexp),
+                        at<uint32_t>(ws, L.hmax),   at<ItemRec>(ws, L.items),  at<int32_t>(ws, L.row_tok),
+                        at<__half>(ws, L.h16),      at<int32_t>(ws, L.hexp),   at<int2>(ws, L.tiles),
+                        at<int32_t>(ws, L.tiles) + 2 * ((size_t)(shape->T * shape->k + shape->T * shape->n_shared) / 128 +
+                                                        P_items(*shape) + shape->n_shared + 1)};
+    e = launch_ffn_prefill(a, px, experts->pool, experts->shared, experts->n_slots, experts->slot_bytes,
+                           device_sm_count(), cs);
+  } else if (mode == MOE_MODE_PREFILL) {
+    return fail(MOE_EUNSUPPORTED, "moe_expert_ffn: PREFILL needs bf16 x, d a multiple of 256 and f of 128");
+  } else if (xdt == MOE_BF16 && stream_supported(a)) {
     const size_t items_max = (P_items(*shape)) + shape->n_shared;
     const StreamAux aux{at<__half>(ws, L.x16),    at<float>(ws, L.xunscale), at<uint32_t>(ws, L.hmax),
                         at<ItemRec>(ws, L.items), at<int32_t>(ws, L.row_tok), at<__half>(ws, L.h16),

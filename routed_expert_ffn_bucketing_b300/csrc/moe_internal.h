@@ -39,6 +39,9 @@ struct WsLayout {
   size_t hexp;           // int32 [P + T*n_shared]: the exponent e of that rescale (h = h16 * 2^e)
   size_t item_cnt;       // int32 [min(E, P) + n_shared + 2]: finished gate/up tasks per work item,
                          // then the task counters of the two streaming kernels
+  size_t xp16;           // f16 [P + T*n_shared][d]: prefill activations gathered by row, rescaled per token
+  size_t xexp;           // int32 [T]: the exponent of each token's rescale (prefill)
+  size_t tiles;          // int2 [P/128 + items + 2]: prefill M tiles (item, first row), then the count
   size_t cx;             // fp32 [T][d/32]: MMA accumulator inputs of the x16 blocks
   size_t ch;             // fp32 [P + T*n_shared][f/32]: MMA accumulator inputs of the h16 blocks
   size_t total;
@@ -103,6 +106,20 @@ struct StreamAux {
 };
 
 
+// Workspace buffers of the prefill (tensor-core GEMM) expert FFN.
+struct PrefillAux {
+  __half* xp16;       // [P + T*n_shared][d]: activation rows in expert order, f16, rescaled per token
+  float* xunscale;    // [T]: 2^e of each token's rescale
+  int32_t* xexp;      // [T]: e
+  uint32_t* hmax;     // [P + T*n_shared]: bits of max |h| per row
+  ItemRec* items;
+  int32_t* row_tok;
+  __half* h16;        // [P + T*n_shared][f]: h rescaled per row (natural order)
+  int32_t* hexp;      // [P + T*n_shared]
+  int2* tiles;        // M tiles: (item, first row within the item)
+  int32_t* n_tiles;   // [1]
+};
+
 // Launchers; each returns cudaSuccess or the launch error.
 cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
                               cudaStream_t st);
@@ -117,6 +134,11 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);  // fp32 SIMT 
 // Streaming tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
 cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, int sm_count, cudaStream_t st);
 bool stream_supported(const FfnArgs& a);
+// Tensor-core grouped GEMM for many tokens per expert (bf16 x); prefill_supported() says whether
+// the shape fits (d a multiple of 256, f of 128).
+cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, const void* pool, const void* shared,
+                               uint64_t n_slots, uint64_t slot_bytes, int sm_count, cudaStream_t st);
+bool prefill_supported(const FfnArgs& a);
 int device_sm_count();
 cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,
                            const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st);

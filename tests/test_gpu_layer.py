@@ -168,3 +168,43 @@ def test_deterministic(decode):
     a = run_layer(decode, 5)
     b = run_layer(decode, 5)
     assert torch.equal(a.buf.out, b.buf.out) and torch.equal(a.buf.topk_w, b.buf.topk_w)
+
+
+@pytest.mark.parametrize("T,E,k,ns", [(300, 64, 10, 1), (200, 16, 2, 0), (97, 8, 8, 2)])
+def test_prefill_gemm_small(T, E, k, ns):
+    # the tensor-core grouped GEMM on shapes with partial 128-row tiles, several experts with
+    # more than one tile and experts with one token
+    w = custom("tiny", T=T, E=E, k=k, n_shared=ns, router_sigma=1.0)
+    dl = DeviceLayer(w)
+    run = run_layer(dl, 0, mode=L.MOE_MODE_PREFILL)
+    assert run.status == 0
+    check_routing(run, w)
+    check_bucketing(run, w)
+    check_output(run, w, tokens=np.arange(0, T, 3))
+
+
+def test_prefill_gemm_matches_decode_kernels():
+    # the same layer through the prefill GEMM and through the decode kernels: both within the
+    # tolerance of the oracle, and within 2e-2 rms of each other everywhere
+    w = custom("tiny", T=64, E=32, k=4, n_shared=1, router_sigma=1.0)
+    dl = DeviceLayer(w)
+    a = run_layer(dl, 0, mode=L.MOE_MODE_PREFILL)
+    b = run_layer(dl, 0, mode=L.MOE_MODE_DECODE)
+    assert torch.equal(a.buf.topk_idx, b.buf.topk_idx)
+    oa, ob = a.buf.out.float(), b.buf.out.float()
+    rms = float(torch.sqrt(torch.mean(ob * ob)))
+    assert float(torch.max(torch.abs(oa - ob))) <= 2e-2 * rms
+    check_output(a, w)
+
+
+def test_prefill_layer_full_size():
+    # the prefill chunk: T = 8192 tokens, Zipf(1.1) routing, tiles from one token to thousands;
+    # routing and bucketing are checked for every token, outputs on a sample of tokens
+    w = WORKLOADS["prefill"]
+    dl = DeviceLayer(w)
+    run = run_layer(dl, 0)  # AUTO takes the tensor-core GEMM for T > 16
+    assert run.status == 0
+    _, _, n_checked = check_routing(run, w)
+    assert n_checked >= w.T - 8
+    check_bucketing(run, w)
+    check_output(run, w, tokens=np.array([0, 1, 77, 1023, 3333, 4096, 5000, 8191]))
