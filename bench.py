@@ -114,12 +114,15 @@ def oracle_experts(w, layer: int, ids, workers: int):
         return dict(ex.map(_gen_expert, jobs))
 
 
+ORACLE_MAX_TOKENS = 64  # tokens per oracle pass: large batches are timed on their first rows
+
+
 def prepare_oracle(w, batches):
-    """Inputs of the timed oracle passes: activations, router and every expert the batches
-    route to (made before, and outside, the timing)."""
+    """Inputs of the timed oracle passes: activations (at most ORACLE_MAX_TOKENS rows of each
+    batch), router and every expert those rows route to (made before, and outside, the timing)."""
     from oracle import moe_oracle as O
     router = w.router(0)
-    xs = [w.x_f64(b) for b in batches]
+    xs = [w.x_f64(b)[:ORACLE_MAX_TOKENS] for b in batches]
     need = set()
     for x in xs:
         need |= set(O.select_topk(O.router_logits(x, router), w.k).reshape(-1).tolist())
@@ -141,7 +144,7 @@ def time_oracle(w, prep, budget_s: float, max_steps: int | None = None):
         el = time.perf_counter() - t0
         if el >= budget_s or (max_steps is not None and steps >= max_steps):
             break
-    return w.T * steps / el, steps, el, int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
+    return xs[0].shape[0] * steps / el, steps, el, int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
 
 
 # ------------------------------------------------------------------ distributed -----------
@@ -193,7 +196,8 @@ def run_reference(args, ws, rank):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": w.describe(), "tokens_per_step": w.T},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{steps} oracle layer passes over {len(batches)} rotating batches of T={w.T}"},
+                         "sample": f"{steps} oracle layer passes over {len(batches)} rotating batches of "
+                                   f"{min(w.T, ORACLE_MAX_TOKENS)} tokens of T={w.T}"},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -214,12 +218,16 @@ def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
-    hbm_peak, _, peak_kind = peaks()
+    hbm_peak, bf16_peak, peak_kind = peaks()
 
+    prefill = w.T > 16
+    n_batches = 4 if prefill else N_BATCHES
     dl = DeviceLayer(w, device=str(dev))
-    xs = [dl.x(b) for b in range(N_BATCHES)]
+    xs = [dl.x(b) for b in range(n_batches)]
     s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
-    buf = lay.alloc_buffers(s, device=dev, ydt=L.MOE_F32, odt=L.MOE_BF16, keep_logits=False)
+    # prefill writes y_perm in bf16 (half the combine's reads); decode keeps fp32
+    buf = lay.alloc_buffers(s, device=dev, ydt=L.MOE_BF16 if prefill else L.MOE_F32, odt=L.MOE_BF16,
+                            keep_logits=False)
     table = L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -230,14 +238,14 @@ def run_ours(args, ws, rank, local):
 
     # active experts per batch (for the algorithmic byte count), from untimed passes
     n_active = []
-    for b in range(N_BATCHES):
+    for b in range(n_batches):
         step(xs[b])
         torch.cuda.synchronize(dev)
         n_active.append(int(buf.active[0].item()))
         assert L.moe_read_status(buf.ws) == 0
     for i in range(W):
         flush.fill_(i & 0xFF)
-        step(xs[i % N_BATCHES])
+        step(xs[i % n_batches])
     torch.cuda.synchronize(dev)
 
     # The timed steps replay CUDA graphs of the C-ABI calls, one graph per stage and batch:
@@ -257,7 +265,7 @@ def run_ours(args, ws, rank, local):
 
     cap = torch.cuda.Stream(dev)
     graphs = []
-    for b in range(N_BATCHES):
+    for b in range(n_batches):
         gs = []
         for seg in (seg_route, seg_ffn, seg_comb):
             g = torch.cuda.CUDAGraph()
@@ -267,7 +275,7 @@ def run_ours(args, ws, rank, local):
         graphs.append(gs)
     for i in range(W):
         flush.fill_(i & 0xFF)
-        for g in graphs[i % N_BATCHES]:
+        for g in graphs[i % n_batches]:
             g.replay()
     torch.cuda.synchronize(dev)
 
@@ -280,7 +288,7 @@ def run_ours(args, ws, rank, local):
     t_wall = time.perf_counter()
     for i in range(K):
         flush.fill_(i & 0xFF)
-        g_route, g_ffn, g_comb = graphs[i % N_BATCHES]
+        g_route, g_ffn, g_comb = graphs[i % n_batches]
         e0, e1, e2, e3 = ev[i]
         e0.record(stream)
         g_route.replay()
@@ -305,8 +313,21 @@ def run_ours(args, ws, rank, local):
     # activation rows read, the y_perm rows written (fp32); scratch (h) is not counted
     rows = w.P + w.T * w.n_shared
     small = w.T * w.d * 2 + rows * w.d * 4
-    ffn_bytes = [(n_active[i % N_BATCHES] + w.n_shared) * w.record_bytes + small for i in range(K)]
+    ffn_bytes = [(n_active[i % n_batches] + w.n_shared) * w.record_bytes + small for i in range(K)]
     achieved = sum(ffn_bytes) / (sum(ffn_ms) / 1e3) / 1e9
+    if prefill:
+        # tensor-bound: algorithmic FLOPs of the expert FFN (gate, up and down over every row)
+        ffn_flops = 2.0 * rows * 3 * w.d * w.f
+        tflops = ffn_flops / (sum(ffn_ms) / 1e3 / K) / 1e12
+        roofline = {"kernel": "moe_expert_ffn (grouped GEMM: gate/up + SwiGLU, down)", "bound": "tensor",
+                    "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tflops / bf16_peak,
+                    "peak_kind": f"{peak_kind} dense bf16 (the f16 dense rate is the same)", "traffic": None,
+                    "flops_per_launch": ffn_flops, "ms_per_launch": sum(ffn_ms) / K}
+    else:
+        roofline = {"kernel": "moe_expert_ffn (gate/up + SwiGLU, down)", "bound": "hbm", "achieved": achieved,
+                    "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                    "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                    "bytes_per_launch": float(np.mean(ffn_bytes)), "ms_per_launch": sum(ffn_ms) / K}
     router_bytes = w.d * w.E * 4
     step_bytes = [b + router_bytes for b in ffn_bytes]
     step_gbs = sum(step_bytes) / (sum(step_ms) / 1e3) / 1e9
@@ -320,7 +341,7 @@ def run_ours(args, ws, rank, local):
         flush.fill_(i & 0xFF)
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        x_dev.copy_(x_host[i % N_BATCHES], non_blocking=True)
+        x_dev.copy_(x_host[i % n_batches], non_blocking=True)
         step(x_dev)
         out_host.copy_(buf.out, non_blocking=True)
         torch.cuda.synchronize(dev)
@@ -334,7 +355,8 @@ def run_ours(args, ws, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         tps, steps, el, cores = time_oracle(w, prepare_oracle(w, list(range(4))), budget_s=args.cpu_seconds)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{steps} oracle layer passes ({el:.1f} s) over 4 rotating batches of T={w.T}"}
+               "sample": f"{steps} oracle layer passes ({el:.1f} s) over 4 rotating batches of "
+                         f"{min(w.T, ORACLE_MAX_TOKENS)} tokens of T={w.T}"}
 
     if rank != 0:
         return
@@ -344,13 +366,10 @@ def run_ours(args, ws, rank, local):
         "dtype": "f32", "data": "synthetic (seeded)",
         "config": {"workload": w.describe(), "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
                    "activations": "bf16", "l2": "512 MiB buffer written between timed steps (outside events)",
-                   "batches": N_BATCHES, "mean_active_experts": float(np.mean(n_active)),
+                   "batches": n_batches, "mean_active_experts": float(np.mean(n_active)),
                    "launch": "CUDA graphs per stage (route+permute, expert FFN, combine), replayed each step",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": {"kernel": "moe_expert_ffn (gate/up + SwiGLU, down)", "bound": "hbm",
-                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
-                     "bytes_per_launch": float(np.mean(ffn_bytes)), "ms_per_launch": sum(ffn_ms) / K},
+        "roofline": roofline,
         "stages_ms": {"route_permute": sum(route_ms) / K, "expert_ffn": sum(ffn_ms) / K,
                       "combine": sum(comb_ms) / K},
         "step_hbm_gbs": step_gbs,
