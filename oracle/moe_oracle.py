@@ -23,6 +23,10 @@ Readings taken where the pages are silent (each also listed in the design notes)
 * The gate is the softmax over all E logits, restricted to the selected k and renormalised.
 * Output is out[t] = sum_j w[t, j] y_{e_j}(x_t) + sum_s y_shared_s(x_t) (+ x_t as a residual
   when asked), rounded once at the end to bf16 (or kept in float64 for the fp32 debug mode).
+* In a stack of layers each layer is a pre-norm residual block: x_{l+1} = x_l + MoE_l(n(x_l))
+  with n the RMS normalisation without a learned gain, n(x) = x / sqrt(mean(x^2) + eps),
+  eps = 1e-6. With no normalisation the residual stream of N(0, 0.02) SwiGLU experts grows
+  without bound (SwiGLU is quadratic for large inputs) and overflows within a few dozen layers.
 
 Parity status: each function here is pinned by tests/test_oracle_pins.py against brute
 force, closed forms, hand-computed examples or invariants.
@@ -49,6 +53,19 @@ def dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     assert s.shape == (R, C // BLOCK)
     scale = np.repeat(s.astype(np.float64), BLOCK, axis=1)
     return q.astype(np.float64) * scale
+
+
+# ---------------------------------------------------------------------------------------
+# RMS normalisation of a layer's input (pre-norm residual block of a layer stack)
+# ---------------------------------------------------------------------------------------
+
+RMS_EPS = 1e-6
+
+
+def rms_norm(x: np.ndarray, eps: float = RMS_EPS) -> np.ndarray:
+    """n(x)[t] = x[t] / sqrt(mean_i x[t, i]^2 + eps), per row, in float64 (no learned gain)."""
+    x = x.astype(np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + eps)
 
 
 # ---------------------------------------------------------------------------------------

@@ -37,7 +37,7 @@ assert int(np.float32(ZSCALE).view(np.uint32)) == 0x37DDB3D7
 BLOCK = 32  # elements per quantisation block along the reduction dimension
 
 # stream tags (the first component of every stream key)
-TAG_GATE, TAG_UP, TAG_DOWN, TAG_X, TAG_ROUTER, TAG_PERM, TAG_ZIPF_MC = 1, 2, 3, 4, 5, 6, 7
+TAG_GATE, TAG_UP, TAG_DOWN, TAG_X, TAG_ROUTER, TAG_PERM, TAG_ZIPF_MC, TAG_DRIFT = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 def mix64_int(z: int) -> int:
@@ -216,6 +216,30 @@ def expert_rank_permutation(seed: int, layer: int, E: int) -> np.ndarray:
     return np.argsort(r, kind="stable").astype(np.int64)
 
 
+DRIFT_EVERY = 10      # steps between two drift epochs of the hot set
+DRIFT_SWAPS = 5       # adjacent-rank transpositions per epoch
+
+
+def drift_rank_permutation(perm: np.ndarray, seed: int, layer: int, epoch: int) -> np.ndarray:
+    """One drift epoch of a layer's popularity ranking: DRIFT_SWAPS transpositions of
+    adjacent ranks (r, r + 1), r drawn uniformly from 0 .. E-2 by the counter generator
+    keyed (seed, layer, epoch). Returns the new rank -> expert permutation (a copy)."""
+    E = perm.size
+    out = perm.copy()
+    r = draws_u64(stream_key(seed, TAG_DRIFT, layer, epoch), 0, DRIFT_SWAPS) % np.uint64(E - 1)
+    for j in r.astype(np.int64):
+        out[j], out[j + 1] = out[j + 1], out[j]
+    return out
+
+
+def router_column_scales(perm: np.ndarray, E: int, k: int, s: float, seed: int = 0) -> np.ndarray:
+    """fp32 [E]: the Zipf scale of each expert's column under the ranking perm."""
+    c, _ = zipf_column_scales(E, k, s, seed)
+    col = np.empty(E, dtype=np.float32)
+    col[perm] = c
+    return col
+
+
 @functools.lru_cache(maxsize=None)
 def zipf_column_scales(E: int, k: int, s: float, seed: int = 0, n_mc: int = 4096,
                        iters: int = 60) -> tuple[np.ndarray, np.ndarray]:
@@ -256,8 +280,10 @@ def router_weights(seed: int, layer: int, d: int, E: int, sigma: float,
     w = normal_f32(stream_key(seed, TAG_ROUTER, layer, 0), 0, d * E, sigma).reshape(d, E)
     if zipf_s is None:
         return w
-    c, _ = zipf_column_scales(E, k, zipf_s, seed)
-    perm = expert_rank_permutation(seed, layer, E)
-    col = np.empty(E, dtype=np.float32)
-    col[perm] = c
+    col = router_column_scales(expert_rank_permutation(seed, layer, E), E, k, zipf_s, seed)
     return (w * col[None, :]).astype(np.float32)
+
+
+def router_weights_unscaled(seed: int, layer: int, d: int, E: int, sigma: float) -> np.ndarray:
+    """The N(0, sigma) draws of router_weights before the Zipf column scales."""
+    return normal_f32(stream_key(seed, TAG_ROUTER, layer, 0), 0, d * E, sigma).reshape(d, E)

@@ -297,3 +297,31 @@ def test_logit_gap():
     l = np.array([[5.0, 1.0, 3.0, 2.5]], dtype=np.float32)
     assert O.logit_gap(l, 2)[0] == 0.5
     assert O.logit_gap(l, 4)[0] == np.inf
+
+
+# ---------------------------------------------------------------------------------------
+# RMS normalisation (pre-norm residual block of a layer stack)
+# ---------------------------------------------------------------------------------------
+
+def test_rms_norm_hand_example():
+    # [3, 4]: mean of squares 12.5, so the row is divided by sqrt(12.5 + eps)
+    out = O.rms_norm(np.array([[3.0, 4.0]]), eps=0.0)
+    assert np.allclose(out, [[3 / math.sqrt(12.5), 4 / math.sqrt(12.5)]], rtol=0, atol=1e-15)
+    assert abs(out[0, 0] - 0.848528137423857) < 1e-14
+
+
+def test_rms_norm_eps_sits_under_the_root():
+    # a constant row c with c^2 == eps: c / sqrt(2 eps) = 1/sqrt(2); a zero row stays zero
+    c = 1e-3
+    out = O.rms_norm(np.full((1, 64), c), eps=1e-6)
+    assert np.allclose(out, 1 / math.sqrt(2), rtol=1e-12)
+    assert np.array_equal(O.rms_norm(np.zeros((1, 32))), np.zeros((1, 32)))
+
+
+def test_rms_norm_is_per_row_and_scale_free():
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=(3, 256)) * np.array([[0.5], [7.0], [300.0]])
+    out = O.rms_norm(x, eps=0.0)
+    assert np.allclose(np.sqrt(np.mean(out * out, axis=1)), 1.0, rtol=1e-12)
+    assert np.allclose(O.rms_norm(x * 19.0, eps=0.0), out, rtol=1e-12)
+    assert np.all(np.sign(out) == np.sign(x))
