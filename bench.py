@@ -190,14 +190,17 @@ def run_reference(args, ws, rank):
     # early once 150 s have passed so that the run stays within a few minutes
     time_oracle(w, prep, budget_s=1e9, max_steps=max(W, 1))
     tps, steps, el, cores = time_oracle(w, prep, budget_s=150.0, max_steps=K)
+    sample = (f"{steps} oracle layer passes over {len(batches)} rotating batches of "
+              f"{min(w.T, ORACLE_MAX_TOKENS)} tokens of T={w.T}")
+    if w.layers > 1:
+        tps /= w.layers
+        sample += f" (layer 0); tokens/s divided by the {w.layers} layers of a step"
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps,
-        "warmup": W, "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
+        "warmup": W, "ms_per_step": 1e3 * el / steps * w.layers, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": w.describe(), "tokens_per_step": w.T},
-        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{steps} oracle layer passes over {len(batches)} rotating batches of "
-                                   f"{min(w.T, ORACLE_MAX_TOKENS)} tokens of T={w.T}"},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -264,7 +267,7 @@ def run_ours(args, ws, rank, local):
         L.moe_combine(s, buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, None)
 
     cap = torch.cuda.Stream(dev)
-    graphs = []
+    graphs, layer_graphs = [], []
     for b in range(n_batches):
         gs = []
         for seg in (seg_route, seg_ffn, seg_comb):
@@ -273,19 +276,42 @@ def run_ours(args, ws, rank, local):
                 seg(xs[b])
             gs.append(g)
         graphs.append(gs)
+        g = torch.cuda.CUDAGraph()  # the whole layer: the four calls in one graph
+        with torch.cuda.graph(g, stream=cap):
+            seg_route(xs[b])
+            seg_ffn(xs[b])
+            seg_comb(xs[b])
+        layer_graphs.append(g)
     for i in range(W):
         flush.fill_(i & 0xFF)
         for g in graphs[i % n_batches]:
             g.replay()
+        layer_graphs[i % n_batches].replay()
     torch.cuda.synchronize(dev)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # timed region 1 (the headline): one whole-layer graph per step
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(local)
     barrier(ws)
     torch.cuda.synchronize(dev)
     clocks.start()
     t_wall = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        a, b = ev_step[i]
+        a.record(stream)
+        layer_graphs[i % n_batches].replay()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+
+    # timed region 2 (the breakdown and the expert-FFN roofline): one graph per stage, events between
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize(dev)
     for i in range(K):
         flush.fill_(i & 0xFF)
         g_route, g_ffn, g_comb = graphs[i % n_batches]
@@ -298,11 +324,8 @@ def run_ours(args, ws, rank, local):
         g_comb.replay()
         e3.record(stream)
     torch.cuda.synchronize(dev)
-    barrier(ws)
-    wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
     assert L.moe_read_status(buf.ws) == 0, "a kernel reported an error during the timed steps"
-    step_ms = [a.elapsed_time(d) for a, _, _, d in ev]
+    staged_ms = [a.elapsed_time(d) for a, _, _, d in ev]
     ffn_ms = [b.elapsed_time(c) for _, b, c, _ in ev]
     route_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
     comb_ms = [c.elapsed_time(d) for _, _, c, d in ev]
@@ -367,16 +390,278 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": w.describe(), "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
                    "activations": "bf16", "l2": "512 MiB buffer written between timed steps (outside events)",
                    "batches": n_batches, "mean_active_experts": float(np.mean(n_active)),
-                   "launch": "CUDA graphs per stage (route+permute, expert FFN, combine), replayed each step",
+                   "launch": "one CUDA graph of the four C-ABI calls per step (stages_ms: one graph per stage, events between)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roofline,
         "stages_ms": {"route_permute": sum(route_ms) / K, "expert_ffn": sum(ffn_ms) / K,
-                      "combine": sum(comb_ms) / K},
+                      "combine": sum(comb_ms) / K, "step_as_three_graphs": sum(staged_ms) / K},
         "step_hbm_gbs": step_gbs,
         "wall_s": wall,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": 7 * K,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ multi-layer workloads ---
+
+def stack_cpu_baseline(w, rank, args):
+    """The oracle on one layer (layer 0's router and experts) at T tokens, extrapolated to the
+    L-layer step by dividing its tokens/s by L."""
+    if rank != 0 or args.no_cpu_baseline:
+        return None
+    tps, steps, el, cores = time_oracle(w, prepare_oracle(w, list(range(4))), budget_s=args.cpu_seconds)
+    return {"value": tps / w.layers, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{steps} oracle passes ({el:.1f} s) of one layer (layer 0) over 4 rotating batches of "
+                      f"T={w.T}; tokens/s divided by the {w.layers} layers of a step"}
+
+
+def run_stack(args, ws, rank, local, w):
+    """L resident layers on a residual stream; one CUDA graph of the whole L-layer step."""
+    import torch
+    from routed_expert_ffn_bucketing_b300 import _lib as L
+    from routed_expert_ffn_bucketing_b300.stack import DecodeStack, LayerWeights
+    from synth.device import DeviceLayer
+
+    dev = torch.device("cuda", local)
+    K, W = args.steps, args.warmup
+    hbm_peak, _, peak_kind = peaks()
+    need = w.layers * (w.E + w.n_shared) * w.record_bytes
+    free, _ = torch.cuda.mem_get_info(dev)
+    if need > free - (4 << 30):
+        raise SystemExit(f"stack workload needs {need / 1e9:.1f} GB of device memory, {free / 1e9:.1f} GB free")
+    dls = [DeviceLayer(w, layer=l, device=str(dev)) for l in range(w.layers)]
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    st = DecodeStack(s, [LayerWeights(dl.router, L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of,
+                                                                dl.shared_ptr)) for dl in dls], device=dev)
+    n_batches = 4
+    xs = [dls[0].x(b) for b in range(n_batches)]
+    stream = torch.cuda.current_stream(dev)
+    # experts per layer and batch (for the algorithmic bytes), from untimed eager passes
+    n_active = []
+    for b in range(n_batches):
+        keep = []
+        st.forward(xs[b], keep=keep)
+        torch.cuda.synchronize(dev)
+        assert L.moe_read_status(st.buf.ws) == 0
+        n_active.append([int(np.unique(r[1].cpu().numpy()).size) for r in keep if r[0] == "idx"])
+    cap = torch.cuda.Stream(dev)
+    graphs = []
+    for b in range(n_batches):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            st.forward(xs[b])
+        graphs.append(g)
+    for i in range(W):
+        graphs[i % n_batches].replay()
+    torch.cuda.synchronize(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    for i in range(K):
+        a, b = ev[i]
+        a.record(stream)
+        graphs[i % n_batches].replay()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.stop()
+    assert L.moe_read_status(st.buf.ws) == 0, "a kernel reported an error during the timed steps"
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = dist_max(sum(step_ms) / 1e3, ws, dev)
+    value = ws * w.T * K / total_s
+    small = w.T * w.d * 2 + (w.P + w.T * w.n_shared) * w.d * 4
+    layer_bytes = [[(n + w.n_shared) * w.record_bytes + w.d * w.E * 4 + small for n in na] for na in n_active]
+    step_bytes = [sum(layer_bytes[i % n_batches]) for i in range(K)]
+    achieved = sum(step_bytes) / (sum(step_ms) / 1e3) / 1e9
+
+    # end to end: pinned x in, the eager stack through the public API, bf16 out back
+    x_host = [x.cpu().pin_memory() for x in xs]
+    out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(xs[0])
+    K_e2e = min(K, 50)
+    e2e_s = 0.0
+    for i in range(W + K_e2e):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        x_dev.copy_(x_host[i % n_batches], non_blocking=True)
+        out_host.copy_(st.forward(x_dev), non_blocking=True)
+        torch.cuda.synchronize(dev)
+        if i >= W:
+            e2e_s += time.perf_counter() - t0
+    e2e_s = dist_max(e2e_s, ws, dev)
+    cpu = stack_cpu_baseline(w, rank, args)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": sum(step_ms) / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": w.describe(), "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
+                   "resident_gb": need / 1e9, "activations": "bf16 residual stream",
+                   "l2": "inputs larger than L2 (each step reads every layer's selected experts, ~10 GB)",
+                   "batches": n_batches, "mean_active_experts_per_layer": float(np.mean(n_active)),
+                   "launch": f"one CUDA graph of the {5 * w.layers} C-ABI calls of a step (norm, route, permute, "
+                             "expert FFN, combine per layer)",
+                   "block": "pre-norm residual: x + MoE(rms_norm(x)), eps 1e-6, no gain",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"kernel": f"whole {w.layers}-layer step (route, permute, expert FFN, combine per layer)",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                     "bytes_per_step": float(np.mean(step_bytes)), "ms_per_step": sum(step_ms) / K},
+        "e2e": {"value": ws * w.T * K_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
+                "d2h_bytes_per_step": w.T * w.d * 2, "steps": K_e2e, "launch": "eager C-ABI calls"},
+        "cpu_baseline": cpu,
+        "gpu_launches": 8 * w.layers * K,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _host_images(w, n_img: int, dev):
+    """Pinned host records of the first n_img experts in (layer, expert) order, made on the
+    device by the seeded generator and copied back in chunks."""
+    import torch
+    from synth.gpu import fill_expert_records
+    rb = w.record_bytes
+    host = torch.empty((n_img, rb), dtype=torch.uint8, pin_memory=True)
+    chunk = 256
+    tmp = torch.empty((chunk, rb), dtype=torch.uint8, device=dev)
+    i = 0
+    while i < n_img:
+        l, e = divmod(i, w.E)
+        n = min(chunk, n_img - i, w.E - e)
+        fill_expert_records(w.seed, l, e, n, w.d, w.f, tmp.data_ptr(), rb, w.expert_sigma)
+        host[i:i + n].copy_(tmp[:n])
+        i += n
+    torch.cuda.synchronize(dev)
+    return host
+
+
+def run_tiered(args, ws, rank, local, w):
+    """L layers, experts in pinned host memory, a device pool of w.slots slots; Zipf routing
+    whose hot set drifts every few steps. Wall-clock tokens/s, hit rate and H2D GB/s."""
+    import torch
+    import synth
+    from routed_expert_ffn_bucketing_b300 import _lib as L
+    from routed_expert_ffn_bucketing_b300.stack import TieredStack
+    from synth.gpu import fill_expert_records
+
+    dev = torch.device("cuda", local)
+    K, W = args.steps, args.warmup
+    rb = w.record_bytes
+    n_all = w.layers * w.E
+    with open("/proc/meminfo") as f:
+        avail = next(int(l.split()[1]) * 1024 for l in f if l.startswith("MemAvailable"))
+    n_img = int(min(n_all, args.host_gb * 1e9 // rb, 0.5 * avail // rb))
+    host = _host_images(w, n_img, dev)
+    h_records = [host[i % n_img].data_ptr() for i in range(n_all)]
+    shared = []
+    for l in range(w.layers):
+        t = torch.empty(max(w.n_shared, 1) * rb, dtype=torch.uint8, device=dev)
+        if w.n_shared:
+            fill_expert_records(w.seed, l, w.E, w.n_shared, w.d, w.f, t.data_ptr(), rb, w.expert_sigma)
+        shared.append(t)
+    base = [torch.from_numpy(synth.router_weights_unscaled(w.seed, l, w.d, w.E, w.router_sigma)).to(dev)
+            for l in range(w.layers)]
+    perms = [synth.expert_rank_permutation(w.seed, l, w.E) for l in range(w.layers)]
+    routers = [torch.empty_like(b) for b in base]
+
+    def set_routers():
+        for l in range(w.layers):
+            col = synth.router_column_scales(perms[l], w.E, w.k, w.zipf_s, w.seed)
+            torch.mul(base[l], torch.from_numpy(col).to(dev)[None, :], out=routers[l])
+
+    set_routers()
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    ts = TieredStack(s, w.layers, routers, h_records, w.slots, rb, shared, device=dev)
+    n_batches = 16
+    x_host = [torch.from_numpy(w.x_bits(b).astype(np.int16)).view(torch.bfloat16).pin_memory()
+              for b in range(n_batches)]
+    x_dev = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=dev)
+    out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+
+    # H2D copy rate of this host's pinned memory: one 2 GB copy after a warm one
+    probe = host[:max(1, min(n_img, (2 << 30) // rb))]
+    pd = torch.empty_like(probe, device=dev)
+    pcie = 0.0
+    for _ in range(2):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        pd.copy_(probe, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize(dev)
+        pcie = probe.numel() / (a.elapsed_time(b) / 1e3) / 1e9
+    del pd
+
+    launches = [0]
+
+    def run(step0, n, e2e):
+        wall = 0.0
+        for i in range(step0, step0 + n):
+            if i and i % synth.DRIFT_EVERY == 0:
+                for l in range(w.layers):
+                    perms[l] = synth.drift_rank_permutation(perms[l], w.seed, l, i // synth.DRIFT_EVERY)
+                set_routers()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            x_dev.copy_(x_host[i % n_batches], non_blocking=True)
+            y = ts.forward(x_dev)
+            if e2e:
+                out_host.copy_(y, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            wall += time.perf_counter() - t0
+            # per layer: norm 1, route 2, permute 1, expert FFN 3 (+3 for the missed experts), combine 1
+            launches[0] += sum(8 + 3 * (m > 0) for m in ts.layer_misses)
+        return wall
+
+    try:
+        run(0, W, False)
+        launches[0] = 0
+        s0 = L.slot_table_stats(ts.table)
+        clocks = ClockSampler(local)
+        barrier(ws)
+        clocks.start()
+        wall = run(W, K, True)
+        barrier(ws)
+        clk = clocks.stop()
+        s1 = L.slot_table_stats(ts.table)
+        assert L.moe_read_status(ts.buf.ws) == 0, "a kernel reported an error during the timed steps"
+    finally:
+        ts.close()
+    wall = dist_max(wall, ws, dev)
+    hits, misses = s1.hits - s0.hits, s1.misses - s0.misses
+    h2d = s1.bytes_h2d - s0.bytes_h2d
+    value = ws * w.T * K / wall
+    cpu = stack_cpu_baseline(w, rank, args)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": 1e3 * wall / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": w.describe() + f", {w.slots} device slots, drift every {synth.DRIFT_EVERY} steps",
+                   "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
+                   "pool_gb": w.slots * rb / 1e9, "host_images": n_img,
+                   "host_mapping": "(l*E + e) mod host_images" if n_img < n_all else "one image per expert",
+                   "timing": "wall clock per step (the host reads each layer's active list), x copied in and "
+                             "the output copied out inside every step",
+                   "parallelism": f"replicas x{ws}"},
+        "slot_pool": {"hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
+                      "evictions": s1.evictions - s0.evictions, "h2d_gbs": h2d / wall / 1e9,
+                      "h2d_bytes_per_step": h2d / K, "cold_start_misses": s0.misses},
+        "roofline": {"kernel": "miss copies (pinned host to device slots)", "bound": "pcie",
+                     "achieved": h2d / wall / 1e9, "peak": pcie, "unit": "GB/s", "frac": h2d / wall / 1e9 / pcie,
+                     "peak_kind": "measured 2 GB pinned H2D copy on this box", "traffic": None},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2 + h2d / K,
+                "d2h_bytes_per_step": w.T * w.d * 2},
+        "cpu_baseline": cpu,
+        "gpu_launches": launches[0],
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -391,6 +676,7 @@ def main():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-gb", type=float, default=24.0, help="pinned host memory for expert images (tiered)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -398,7 +684,16 @@ def main():
     if args.impl == "reference":
         run_reference(args, ws, rank)
     else:
-        run_ours(args, ws, rank, local)
+        from synth.workloads import WORKLOADS
+        w = WORKLOADS[args.workload]
+        if w.layers > 1:
+            import torch
+            if not torch.cuda.is_available():
+                raise SystemExit("bench.py needs a CUDA device")
+            torch.cuda.set_device(local)
+            (run_tiered if w.slots else run_stack)(args, ws, rank, local, w)
+        else:
+            run_ours(args, ws, rank, local)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -8,6 +8,7 @@
  *   moe_expert_ffn  each selected expert's SwiGLU FFN over int8 block-32 weights, looked up
  *                   through the resident slot table, plus the always-on shared experts
  *   moe_combine     weighted sum of the expert outputs per token (unpermute)
+ *   moe_rms_norm    (stacks of layers) the normalised input of a pre-norm residual block
  *   slot_table_*    host-side slot pool for experts that do not all fit on the device: a miss
  *                   is copied from pinned host memory on a side stream
  *
@@ -190,6 +191,18 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
 moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt,
                        const int32_t* inv_pos, const float* topk_w, const void* residual_opt,
                        void* out, moe_dtype odt, moe_stream_t stream);
+
+/* RMS normalisation of each token's row, the input of one layer of a stack. The pages run
+ * the layers of a transformer but leave the residual block open; the reading taken here is
+ * the pre-norm block x_{l+1} = x_l + MoE_l(n(x_l)), with n given by
+ *   out[t][i] = x[t][i] / sqrt(mean_j x[t][j]^2 + eps)      (no learned gain)
+ * The mean of squares is an fp32 sum in a fixed order (deterministic); out is rounded once
+ * to odt. Only shape->T and shape->d are used.
+ *  x    [T][d] in xdt's type; out [T][d] in odt's type; both 16-byte aligned. out may be x
+ *       when xdt == odt.
+ *  eps  finite and >= 0 (MOE_EINVAL otherwise). */
+moe_status moe_rms_norm(const moe_shape* shape, const void* x, moe_dtype xdt, void* out,
+                        moe_dtype odt, float eps, moe_stream_t stream);
 
 /* Waits for `stream`, then returns the device status word of workspace `ws` in *h_status.
  * MOE_OK if it is zero, MOE_EDEVICE if not, MOE_ECUDA if the copy failed. */

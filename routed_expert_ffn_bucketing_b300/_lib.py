@@ -59,6 +59,7 @@ _SIGS = {
     "moe_expert_ffn": (C.c_int, [C.POINTER(moe_shape), C.c_int, _P, C.c_int, C.POINTER(moe_expert_table), _P, _P, _P,
                                  _P, C.c_int, _P, C.c_size_t, _P]),
     "moe_combine": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, C.c_int, _P]),
+    "moe_rms_norm": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, C.c_int, C.c_float, _P]),
     "moe_read_status": (C.c_int, [_P, _P, C.POINTER(C.c_int32)]),
     "moe_last_error_string": (C.c_char_p, []),
     "slot_table_create": (C.c_int, [C.POINTER(_P), C.c_int32, C.c_int32, C.c_int32, C.c_uint64, _P, _P, _P,
@@ -160,6 +161,11 @@ def moe_expert_ffn(s, mode, x, xdt, table: moe_expert_table, offsets, sorted_pai
 def moe_combine(s, y_perm, ydt, inv_pos, topk_w, residual_opt, out, odt, stream=None) -> int:
     return _check(lib().moe_combine(C.byref(s), ptr(y_perm), ydt, ptr(inv_pos), ptr(topk_w), ptr(residual_opt),
                                     ptr(out), odt, stream_handle(stream)), "moe_combine")
+
+
+def moe_rms_norm(s, x, xdt, out, odt, eps: float, stream=None) -> int:
+    return _check(lib().moe_rms_norm(C.byref(s), ptr(x), xdt, ptr(out), odt, C.c_float(eps), stream_handle(stream)),
+                  "moe_rms_norm")
 
 
 def moe_read_status(ws, stream=None) -> int:

@@ -77,6 +77,12 @@ WsLayout ws_layout(const moe_shape& s) {
   o = align256(o + sizeof(int32_t) * T);
   L.tiles = o;
   o = align256(o + sizeof(int32_t) * 2 * ((P + T * s.n_shared) / 128 + P_items(s) + s.n_shared + 2));
+  // stream-K scratch of the decode kernels (T <= 8): tasks per kernel at most items * max(f/8, d/16)
+  const size_t sk_tasks = s.T <= 8 ? (P_items(s) + s.n_shared) * (s.f / 8 > s.d / 16 ? s.f / 8 : s.d / 16) : 0;
+  L.part = o;
+  o = align256(o + sizeof(float) * 2 * sk_tasks * 2 * 128);
+  L.task_cnt = o;
+  o = align256(o + sizeof(int32_t) * 2 * sk_tasks);
   L.cx = o;
   o = align256(o + sizeof(float) * T * (s.d / 32));
   L.ch = o;
@@ -314,10 +320,15 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
     return fail(MOE_EUNSUPPORTED, "moe_expert_ffn: PREFILL needs bf16 x, d a multiple of 256 and f of 128");
   } else if (xdt == MOE_BF16 && stream_supported(a)) {
     const size_t items_max = (P_items(*shape)) + shape->n_shared;
-    const StreamAux aux{at<__half>(ws, L.x16),    at<float>(ws, L.xunscale), at<uint32_t>(ws, L.hmax),
+    StreamAux aux{at<__half>(ws, L.x16),    at<float>(ws, L.xunscale), at<uint32_t>(ws, L.hmax),
                         at<ItemRec>(ws, L.items), at<int32_t>(ws, L.row_tok), at<__half>(ws, L.h16),
                         at<int32_t>(ws, L.hexp),  at<int32_t>(ws, L.item_cnt), at<float>(ws, L.cx),
-                        at<float>(ws, L.ch),      at<int32_t>(ws, L.item_cnt) + items_max};
+                        at<float>(ws, L.ch),      at<int32_t>(ws, L.item_cnt) + items_max,
+                        at<float>(ws, L.part),    at<int32_t>(ws, L.task_cnt),
+                        0, 0};
+    const size_t sk_tasks = shape->T <= 8 ? items_max * (shape->f / 8 > shape->d / 16 ? shape->f / 8 : shape->d / 16) : 0;
+    aux.part_stride = sk_tasks * 2 * 128;
+    aux.cnt_stride = sk_tasks;
     e = launch_ffn_stream(a, aux, device_sm_count(), cs);
   } else {
     e = launch_ffn_decode(a, cs);
@@ -341,6 +352,22 @@ moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt
   cudaError_t e = launch_combine(*shape, y_perm, ydt, inv_pos, topk_w, residual_opt, out, odt,
                                  reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "moe_combine: launch");
+  return MOE_OK;
+}
+
+moe_status moe_rms_norm(const moe_shape* shape, const void* x, moe_dtype xdt, void* out, moe_dtype odt, float eps,
+                        moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_dtype(xdt, "x")) != MOE_OK) return st;
+  if ((st = check_dtype(odt, "out")) != MOE_OK) return st;
+  if (!(eps >= 0.0f) || !isfinite(eps)) return fail(MOE_EINVAL, "moe_rms_norm: eps must be finite and >= 0");
+  if (shape->T == 0) return MOE_OK;
+  if (!x || !out) return fail(MOE_EINVAL, "moe_rms_norm: NULL argument");
+  if (!aligned(x, 16) || !aligned(out, 16)) return fail(MOE_EINVAL, "moe_rms_norm: misaligned x or out");
+  if (x == out && xdt != odt) return fail(MOE_EINVAL, "moe_rms_norm: in place needs xdt == odt");
+  cudaError_t e = launch_rms_norm(*shape, x, xdt, out, odt, eps, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_rms_norm: launch");
   return MOE_OK;
 }
 

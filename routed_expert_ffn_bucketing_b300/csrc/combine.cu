@@ -63,4 +63,55 @@ cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int
   return cudaGetLastError();
 }
 
+// RMS normalisation of each token's row, the input of a pre-norm residual block:
+//   out[t] = x[t] / sqrt(mean_i x[t][i]^2 + eps)   (no learned gain)
+// One CTA per token. Each thread sums the squares of its columns (4 at a time, in column
+// order), the warps reduce by a fixed butterfly and warp 0 adds the 8 warp sums in order, so
+// the result is deterministic. x and out may be the same buffer.
+__global__ void __launch_bounds__(256) rms_norm_kernel(const void* x, int xdt, void* out, int odt, int d,
+                                                       float eps) {
+  __shared__ float wsum[8];
+  __shared__ float inv_s;
+  const int t = blockIdx.x;
+  const size_t row = (size_t)t * d;
+  float ss = 0.0f;
+  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
+    const float4 v = load4(x, xdt, row + c);
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += wsum[w];
+    inv_s = 1.0f / sqrtf(tot / (float)d + eps);
+  }
+  __syncthreads();
+  const float inv = inv_s;
+  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
+    float4 v = load4(x, xdt, row + c);
+    v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
+    if (odt == 1) {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + row + c) = v;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + row + c) = u;
+    }
+  }
+}
+
+cudaError_t launch_rms_norm(const moe_shape& s, const void* x, int xdt, void* out, int odt, float eps,
+                            cudaStream_t st) {
+  rms_norm_kernel<<<s.T, 256, 0, st>>>(x, xdt, out, odt, s.d, eps);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

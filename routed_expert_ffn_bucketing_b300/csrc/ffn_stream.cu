@@ -65,11 +65,13 @@ __device__ __forceinline__ uint32_t codes02(uint32_t w) {
 // activations of token g (xv: pairs (0,2), (1,3), (4,6), (5,7)), as two MMAs. C is -1152 times
 // the block sums of the activations of columns 2c, 2c+1 (c0, c1).
 __device__ __forceinline__ void block_mma(float* d, uint2 w_lo, uint2 w_hi, const uint4& xv, float c0, float c1) {
-  d[0] = c0;
-  d[1] = c1;
-  d[2] = c0;
-  d[3] = c1;
-  mma_f16_16816(d, codes02(w_lo.x), codes02(w_hi.x), codes02(w_lo.x >> 8), codes02(w_hi.x >> 8), xv.x, xv.y);
+  // first MMA: accumulator input (c0, c1, c0, c1) read straight from c0 / c1; second: chained
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%10,%11};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(codes02(w_lo.x)), "r"(codes02(w_hi.x)), "r"(codes02(w_lo.x >> 8)), "r"(codes02(w_hi.x >> 8)), "r"(xv.x),
+        "r"(xv.y), "f"(c0), "f"(c1));
   mma_f16_16816(d, codes02(w_lo.y), codes02(w_hi.y), codes02(w_lo.y >> 8), codes02(w_hi.y >> 8), xv.z, xv.w);
 }
 
@@ -133,6 +135,8 @@ __global__ void __launch_bounds__(256) ffn_prepare_kernel(FfnArgs A, StreamAux X
     }
     if (threadIdx.x < 2) X.sched[threadIdx.x] = 0;
   }
+  if (A.T <= kPassTok)  // stream-K cut-task counters of both kernels
+    for (int i = t * blockDim.x + threadIdx.x; i < 2 * X.cnt_stride; i += gridDim.x * blockDim.x) X.task_cnt[i] = 0;
   const int d = A.d, nb = d / kQBlock;
   float m = 0.0f;
   for (int i = threadIdx.x; i < d; i += blockDim.x) m = fmaxf(m, fabsf(load_act(A.x, A.xdt, (size_t)t * d + i)));
@@ -195,22 +199,22 @@ struct ScaleVec {
 };
 
 // One warp computes the dot products of 16 M rows (lo: rows g, hi: rows g + 8 of the MMA) of
-// one expert with up to 8 token columns, over K = 32 nb elements (nb a multiple of D). wlo / whi
-// point at byte c*8 of the rows' codes, slo / shi at their f16 scale rows, xrow at the lane's
-// activation row (byte c*8 of it, permuted f16), cs0 / cs1 at the accumulator-input rows of
-// columns 2c, 2c+1. Weights are loaded D blocks ahead of their use; scales and accumulator
-// inputs are loaded once per group of D blocks with vector loads.
+// one expert with up to 8 token columns, over blocks [b_lo, b_hi) of K (both multiples of D).
+// wlo / whi point at byte c*8 of the rows' codes, slo / shi at their f16 scale rows, xrow at the
+// lane's activation row (byte c*8 of it, permuted f16), cs0 / cs1 at the accumulator-input rows
+// of columns 2c, 2c+1. Weights are loaded D blocks ahead of their use; scales and accumulator
+// inputs are loaded with vector loads.
 template <int D>
 __device__ __forceinline__ void rows_dot(const uint8_t* wlo, const uint8_t* whi, const __half* slo,
                                          const __half* shi, const __half* xrow, bool has, const float* cs0,
-                                         const float* cs1, int nb, float (&acc)[4]) {
+                                         const float* cs1, int b_lo, int b_hi, float (&acc)[4]) {
   uint2 ql[D], qh[D];
 #pragma unroll
   for (int j = 0; j < D; ++j) {
-    ql[j] = ld_codes(wlo + j * kQBlock);
-    qh[j] = ld_codes(whi + j * kQBlock);
+    ql[j] = ld_codes(wlo + (b_lo + j) * kQBlock);
+    qh[j] = ld_codes(whi + (b_lo + j) * kQBlock);
   }
-  for (int b0 = 0; b0 < nb; b0 += D) {
+  for (int b0 = b_lo; b0 < b_hi; b0 += D) {
     ScaleVec<D> sl, sh;
     sl.load(slo + b0);
     sh.load(shi + b0);
@@ -228,7 +232,7 @@ __device__ __forceinline__ void rows_dot(const uint8_t* wlo, const uint8_t* whi,
       const float cb = jj == 0 ? c1.x : jj == 1 ? c1.y : jj == 2 ? c1.z : c1.w;
       float dd[4];
       block_mma(dd, ql[j], qh[j], xv, ca, cb);
-      if (b + D < nb) {
+      if (b + D < b_hi) {
         ql[j] = ld_codes(wlo + (b + D) * kQBlock);
         qh[j] = ld_codes(whi + (b + D) * kQBlock);
       }
@@ -241,138 +245,215 @@ __device__ __forceinline__ void rows_dot(const uint8_t* wlo, const uint8_t* whi,
   }
 }
 
-// The streaming kernel. A task is (item, 16 M rows): for gate/up, 8 rows of f taken from both
-// the gate and the up matrix (M rows 0..7 and 8..15); for down, 16 rows of d. Warps take tasks
-// from a counter until none are left; a task's results depend only on the task, so the order
-// in which warps take them does not change any output.
+// Where a task's operands are, for one pass of up to 8 tokens starting at token `base`.
+struct TaskOps {
+  ItemRec it;
+  int item, row_lo, row_hi, base, ng;
+  const uint8_t *wlo, *whi;
+  const __half *slo, *shi, *xrow;
+  const float *cs0, *cs1;
+  bool has;
+};
+
 template <int KIND>
+__device__ __forceinline__ bool task_rows(const FfnArgs& A, const StreamAux& X, int t, int tpi, int nb, int g,
+                                          int c, TaskOps* o) {
+  const int item = t / tpi, mt = t % tpi;
+  o->it = X.items[item];
+  o->item = item;
+  if (o->it.rec == nullptr || o->it.ntok <= 0) return false;
+  const uint8_t* rec = o->it.rec;
+  const int d = A.d, f = A.f;
+  if (KIND == kGateUp) {
+    o->row_lo = o->row_hi = mt * 8 + g;  // gate row and up row of the same f index
+    o->wlo = rec + A.o_gate_q + (size_t)o->row_lo * d + c * 8;
+    o->whi = rec + A.o_up_q + (size_t)o->row_hi * d + c * 8;
+    o->slo = reinterpret_cast<const __half*>(rec + A.o_gate_s) + (size_t)o->row_lo * nb;
+    o->shi = reinterpret_cast<const __half*>(rec + A.o_up_s) + (size_t)o->row_hi * nb;
+  } else {
+    o->row_lo = mt * 16 + g;
+    o->row_hi = o->row_lo + 8;
+    o->wlo = rec + A.o_down_q + (size_t)o->row_lo * f + c * 8;
+    o->whi = rec + A.o_down_q + (size_t)o->row_hi * f + c * 8;
+    o->slo = reinterpret_cast<const __half*>(rec + A.o_down_s) + (size_t)o->row_lo * nb;
+    o->shi = reinterpret_cast<const __half*>(rec + A.o_down_s) + (size_t)o->row_hi * nb;
+  }
+  return true;
+}
+
+// B operand (activation row of token column g) and C operand rows (columns 2c and 2c + 1) of
+// the pass starting at token `base`.
+template <int KIND>
+__device__ __forceinline__ void task_pass(const FfnArgs& A, const StreamAux& X, int base, int nb, int g, int c,
+                                          TaskOps* o) {
+  const ItemRec& it = o->it;
+  o->base = base;
+  o->ng = min(kPassTok, it.ntok - base);
+  o->has = g < o->ng;
+  const int rg_ = it.row0 + base + (o->has ? g : 0);
+  const int r0 = it.row0 + base + (2 * c < o->ng ? 2 * c : 0);
+  const int r1 = it.row0 + base + (2 * c + 1 < o->ng ? 2 * c + 1 : 0);
+  if (KIND == kGateUp) {
+    o->xrow = X.x16 + (size_t)X.row_tok[rg_] * A.d + c * 8;
+    o->cs0 = X.cx + (size_t)X.row_tok[r0] * nb;
+    o->cs1 = X.cx + (size_t)X.row_tok[r1] * nb;
+  } else {
+    o->xrow = X.h16 + (size_t)rg_ * A.f + c * 8;
+    o->cs0 = X.ch + (size_t)r0 * nb;
+    o->cs1 = X.ch + (size_t)r1 * nb;
+  }
+}
+
+// Epilogue of one pass: lane (g, c) holds rows row_lo (q = 0, 1) / row_hi (q = 2, 3) for tokens
+// 2c, 2c + 1 of the pass.
+template <int KIND>
+__device__ __forceinline__ void task_epilogue(const FfnArgs& A, const StreamAux& X, const TaskOps& o, int g, int c,
+                                              const float (&acc)[4]) {
+  const ItemRec& it = o.it;
+  const int ng = o.ng, base = o.base;
+  if (KIND == kGateUp) {
+    float m[2] = {0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int tcol = 2 * c + q;
+      if (tcol < ng) {
+        const int r = it.row0 + base + tcol;
+        const float xs = X.xunscale[X.row_tok[r]];
+        const float hv = silu(acc[q] * xs) * (acc[2 + q] * xs);
+        A.h[(size_t)r * A.f + o.row_lo] = hv;
+        m[q] = fabsf(hv);
+      }
+    }
+#pragma unroll
+    for (int s = 4; s < 32; s <<= 1) {
+      m[0] = fmaxf(m[0], __shfl_xor_sync(0xFFFFFFFFu, m[0], s));
+      m[1] = fmaxf(m[1], __shfl_xor_sync(0xFFFFFFFFu, m[1], s));
+    }
+    if (g == 0) {
+      const int r = it.row0 + base + 2 * c;
+      if (2 * c < ng) atomicMax(X.hmax + r, __float_as_uint(m[0]));
+      if (2 * c + 1 < ng) atomicMax(X.hmax + r + 1, __float_as_uint(m[1]));
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int tcol = 2 * c + q;
+      if (tcol < ng) {
+        const int r = it.row0 + base + tcol;
+        const float up = pow2f(X.hexp[r]);
+        const float v_lo = acc[q] * up, v_hi = acc[2 + q] * up;
+        const size_t off = (size_t)r * A.d;
+        if (A.ydt == 1) {
+          static_cast<float*>(A.y)[off + o.row_lo] = v_lo;
+          static_cast<float*>(A.y)[off + o.row_hi] = v_hi;
+        } else {
+          static_cast<__nv_bfloat16*>(A.y)[off + o.row_lo] = __float2bfloat16_rn(v_lo);
+          static_cast<__nv_bfloat16*>(A.y)[off + o.row_hi] = __float2bfloat16_rn(v_hi);
+        }
+      }
+    }
+  }
+}
+
+// After a gate/up task's epilogue: the last task of its item to finish turns the item's h rows
+// into f16 for the down kernel. The warp fences its h and hmax writes before counting the task,
+// so the counter reaches tpi only after all of the item's writes are visible.
+__device__ __forceinline__ void gateup_task_done(const FfnArgs& A, const StreamAux& X, const TaskOps& o, int tpi,
+                                                 int lane) {
+  __threadfence();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(X.item_cnt + o.item, 1) == tpi - 1;
+  if (!__shfl_sync(0xFFFFFFFFu, last, 0)) return;
+  __threadfence();
+  const int f = A.f, nbf = f / kQBlock;
+  const ItemRec& it = o.it;
+  for (int i = lane; i < it.ntok * nbf; i += 32) {
+    const int r = it.row0 + i / nbf, b = i % nbf;
+    const int e = f16_exp_for(__uint_as_float(__ldcg(X.hmax + r)));
+    const float down = pow2f(-e);
+    float v[kQBlock];
+    const float4* src = reinterpret_cast<const float4*>(A.h + (size_t)r * f + b * kQBlock);
+#pragma unroll
+    for (int q = 0; q < kQBlock / 4; ++q) {
+      const float4 w4 = __ldcg(src + q);
+      v[4 * q] = w4.x * down;
+      v[4 * q + 1] = w4.y * down;
+      v[4 * q + 2] = w4.z * down;
+      v[4 * q + 3] = w4.w * down;
+    }
+    X.ch[(size_t)r * nbf + b] = store_block_f16(X.h16 + (size_t)r * f + b * kQBlock, v);
+    if (b == 0) X.hexp[r] = e;
+  }
+}
+
+// The streaming kernel. A task is (item, 16 M rows): for gate/up, 8 rows of f taken from both
+// the gate and the up matrix (M rows 0..7 and 8..15); for down, 16 rows of d.
+//
+// When every item has at most 8 tokens (T <= 8: one pass per task), the work is split
+// stream-K: the (task, group of D blocks) sequence is cut into one contiguous range per warp,
+// equal to within one group, so all warps stream the same number of bytes. A task cut between
+// two warps (never more: a range is at least one task long) is finished by the second of them
+// to arrive: it adds the partial sums as part 0 + part 1 (a fixed order) and runs the epilogue.
+// Otherwise warps take whole tasks, pass by pass, from an atomic counter.
+template <int KIND, int D>
 __global__ void __launch_bounds__(kThreads) ffn_stream_kernel(FfnArgs A, StreamAux X) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int d = A.d, f = A.f;
-  const int K = KIND == kGateUp ? d : f;
+  const int K = KIND == kGateUp ? A.d : A.f;
   const int nb = K / kQBlock;
-  const int tpi = KIND == kGateUp ? f / 8 : d / 16;  // tasks per item
+  const int tpi = KIND == kGateUp ? A.f / 8 : A.d / 16;  // tasks per item
   const int n_tasks = n_items(A) * tpi;
-  int* counter = X.sched + KIND;
-  (void)warp;
-  for (int t = grab_task(counter, lane); t < n_tasks; t = grab_task(counter, lane)) {
-    const int item = t / tpi, mt = t % tpi;
-    const ItemRec it = X.items[item];
-    if (it.rec == nullptr || it.ntok <= 0) continue;
-    int row_lo, row_hi;
-    const uint8_t *wlo, *whi;
-    const __half *slo, *shi;
-    if (KIND == kGateUp) {
-      row_lo = row_hi = mt * 8 + g;  // gate row and up row of the same f index
-      wlo = it.rec + A.o_gate_q + (size_t)row_lo * d + c * 8;
-      whi = it.rec + A.o_up_q + (size_t)row_hi * d + c * 8;
-      slo = reinterpret_cast<const __half*>(it.rec + A.o_gate_s) + (size_t)row_lo * nb;
-      shi = reinterpret_cast<const __half*>(it.rec + A.o_up_s) + (size_t)row_hi * nb;
-    } else {
-      row_lo = mt * 16 + g;
-      row_hi = row_lo + 8;
-      wlo = it.rec + A.o_down_q + (size_t)row_lo * f + c * 8;
-      whi = it.rec + A.o_down_q + (size_t)row_hi * f + c * 8;
-      slo = reinterpret_cast<const __half*>(it.rec + A.o_down_s) + (size_t)row_lo * nb;
-      shi = reinterpret_cast<const __half*>(it.rec + A.o_down_s) + (size_t)row_hi * nb;
-    }
-    for (int base = 0; base < it.ntok; base += kPassTok) {
-      const int ng = min(kPassTok, it.ntok - base);
-      // B operand: activation row of token column g; C operand: columns 2c and 2c + 1
-      const bool has = g < ng;
-      const int rg_ = it.row0 + base + (has ? g : 0);
-      const int r0 = it.row0 + base + (2 * c < ng ? 2 * c : 0);
-      const int r1 = it.row0 + base + (2 * c + 1 < ng ? 2 * c + 1 : 0);
-      const __half* xrow;
-      const float *cs0, *cs1;
-      if (KIND == kGateUp) {
-        xrow = X.x16 + (size_t)X.row_tok[rg_] * d + c * 8;
-        cs0 = X.cx + (size_t)X.row_tok[r0] * nb;
-        cs1 = X.cx + (size_t)X.row_tok[r1] * nb;
-      } else {
-        xrow = X.h16 + (size_t)rg_ * f + c * 8;
-        cs0 = X.ch + (size_t)r0 * nb;
-        cs1 = X.ch + (size_t)r1 * nb;
-      }
+  if (A.T <= kPassTok) {
+    const int gpt = nb / D;  // groups of D blocks per task
+    const long long total = (long long)n_tasks * gpt;
+    const int nw = min(gridDim.x * kWarps, n_tasks);  // each range at least one task long
+    const int wid = blockIdx.x * kWarps + warp;
+    if (wid >= nw) return;
+    float* part = X.part + (size_t)KIND * X.part_stride;
+    int* cnt = X.task_cnt + (size_t)KIND * X.cnt_stride;
+    const long long G1 = (long long)(wid + 1) * total / nw;
+    for (long long G = (long long)wid * total / nw; G < G1;) {
+      const int t = (int)(G / gpt), gs = (int)(G % gpt);
+      const int ge = (int)min((long long)gpt, gs + (G1 - G));
+      G += ge - gs;
+      TaskOps o;
+      if (!task_rows<KIND>(A, X, t, tpi, nb, g, c, &o)) continue;
+      task_pass<KIND>(A, X, 0, nb, g, c, &o);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (nb % kDepth == 0) rows_dot<kDepth>(wlo, whi, slo, shi, xrow, has, cs0, cs1, nb, acc);
-      else rows_dot<4>(wlo, whi, slo, shi, xrow, has, cs0, cs1, nb, acc);
-
-      // epilogue: lane (g, c) holds rows row_lo (q = 0, 1) / row_hi (q = 2, 3), tokens 2c, 2c+1
-      if (KIND == kGateUp) {
-        float m[2] = {0.f, 0.f};
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int tcol = 2 * c + q;
-          if (tcol < ng) {
-            const int r = it.row0 + base + tcol;
-            const float xs = X.xunscale[X.row_tok[r]];
-            const float hv = silu(acc[q] * xs) * (acc[2 + q] * xs);
-            A.h[(size_t)r * f + row_lo] = hv;
-            m[q] = fabsf(hv);
-          }
-        }
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          m[0] = fmaxf(m[0], __shfl_xor_sync(0xFFFFFFFFu, m[0], o));
-          m[1] = fmaxf(m[1], __shfl_xor_sync(0xFFFFFFFFu, m[1], o));
-        }
-        if (g == 0) {
-          const int r = it.row0 + base + 2 * c;
-          if (2 * c < ng) atomicMax(X.hmax + r, __float_as_uint(m[0]));
-          if (2 * c + 1 < ng) atomicMax(X.hmax + r + 1, __float_as_uint(m[1]));
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int tcol = 2 * c + q;
-          if (tcol < ng) {
-            const int r = it.row0 + base + tcol;
-            const float up = pow2f(X.hexp[r]);
-            const float v_lo = acc[q] * up, v_hi = acc[2 + q] * up;
-            const size_t off = (size_t)r * d;
-            if (A.ydt == 1) {
-              static_cast<float*>(A.y)[off + row_lo] = v_lo;
-              static_cast<float*>(A.y)[off + row_hi] = v_hi;
-            } else {
-              static_cast<__nv_bfloat16*>(A.y)[off + row_lo] = __float2bfloat16_rn(v_lo);
-              static_cast<__nv_bfloat16*>(A.y)[off + row_hi] = __float2bfloat16_rn(v_hi);
-            }
-          }
-        }
-      }
-    }
-
-    if (KIND == kGateUp) {
-      // The last task of this item to finish turns the item's h rows into f16 for the down
-      // kernel. The warp fences its h and hmax writes before counting the task, so the
-      // counter reaches tpi only after all of the item's writes are visible.
-      __threadfence();
-      int last = 0;
-      if (lane == 0) last = atomicAdd(X.item_cnt + item, 1) == tpi - 1;
-      if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+      rows_dot<D>(o.wlo, o.whi, o.slo, o.shi, o.xrow, o.has, o.cs0, o.cs1, gs * D, ge * D, acc);
+      if (gs != 0 || ge != gpt) {
+        // a cut task: publish this part, and the second part to arrive finishes the task
+        const int my = gs == 0 ? 0 : 1;
+        float4* slot = reinterpret_cast<float4*>(part + ((size_t)t * 2 + my) * 128);
+        slot[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         __threadfence();
-        const int nbf = f / kQBlock;
-        for (int i = lane; i < it.ntok * nbf; i += 32) {
-          const int r = it.row0 + i / nbf, b = i % nbf;
-          const int e = f16_exp_for(__uint_as_float(__ldcg(X.hmax + r)));
-          const float down = pow2f(-e);
-          float v[kQBlock];
-          const float4* src = reinterpret_cast<const float4*>(A.h + (size_t)r * f + b * kQBlock);
-#pragma unroll
-          for (int q = 0; q < kQBlock / 4; ++q) {
-            const float4 w4 = __ldcg(src + q);
-            v[4 * q] = w4.x * down;
-            v[4 * q + 1] = w4.y * down;
-            v[4 * q + 2] = w4.z * down;
-            v[4 * q + 3] = w4.w * down;
-          }
-          X.ch[(size_t)r * nbf + b] = store_block_f16(X.h16 + (size_t)r * f + b * kQBlock, v);
-          if (b == 0) X.hexp[r] = e;
-        }
+        int second = 0;
+        if (lane == 0) second = atomicAdd(cnt + t, 1) == 1;
+        if (!__shfl_sync(0xFFFFFFFFu, second, 0)) continue;
+        __threadfence();
+        const float4 p0 = __ldcg(reinterpret_cast<const float4*>(part + (size_t)t * 2 * 128) + lane);
+        const float4 p1 = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)t * 2 + 1) * 128) + lane);
+        acc[0] = p0.x + p1.x;
+        acc[1] = p0.y + p1.y;
+        acc[2] = p0.z + p1.z;
+        acc[3] = p0.w + p1.w;
       }
+      task_epilogue<KIND>(A, X, o, g, c, acc);
+      if (KIND == kGateUp) gateup_task_done(A, X, o, tpi, lane);
     }
+    return;
+  }
+  int* counter = X.sched + KIND;
+  for (int t = grab_task(counter, lane); t < n_tasks; t = grab_task(counter, lane)) {
+    TaskOps o;
+    if (!task_rows<KIND>(A, X, t, tpi, nb, g, c, &o)) continue;
+    for (int base = 0; base < o.it.ntok; base += kPassTok) {
+      task_pass<KIND>(A, X, base, nb, g, c, &o);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      rows_dot<D>(o.wlo, o.whi, o.slo, o.shi, o.xrow, o.has, o.cs0, o.cs1, 0, nb, acc);
+      task_epilogue<KIND>(A, X, o, g, c, acc);
+    }
+    if (KIND == kGateUp) gateup_task_done(A, X, o, tpi, lane);
   }
 }
 
@@ -389,9 +470,12 @@ cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, int sm_count
     const int warps = tasks < sm_count * kWarps ? tasks : sm_count * kWarps;
     return (warps + kWarps - 1) / kWarps;
   };
-  ffn_stream_kernel<kGateUp><<<grid(gu_tasks), kThreads, 0, st>>>(a, x);
+  // D = 8 blocks in flight where the block count allows it (K a multiple of 256), else 4
+  if ((a.d / kQBlock) % 8 == 0) ffn_stream_kernel<kGateUp, 8><<<grid(gu_tasks), kThreads, 0, st>>>(a, x);
+  else ffn_stream_kernel<kGateUp, 4><<<grid(gu_tasks), kThreads, 0, st>>>(a, x);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  ffn_stream_kernel<kDown><<<grid(dn_tasks), kThreads, 0, st>>>(a, x);
+  if ((a.f / kQBlock) % 8 == 0) ffn_stream_kernel<kDown, 8><<<grid(dn_tasks), kThreads, 0, st>>>(a, x);
+  else ffn_stream_kernel<kDown, 4><<<grid(dn_tasks), kThreads, 0, st>>>(a, x);
   return cudaGetLastError();
 }
 

@@ -42,6 +42,8 @@ struct WsLayout {
   size_t xp16;           // f16 [P + T*n_shared][d]: prefill activations gathered by row, rescaled per token
   size_t xexp;           // int32 [T]: the exponent of each token's rescale (prefill)
   size_t tiles;          // int2 [P/128 + items + 2]: prefill M tiles (item, first row), then the count
+  size_t part;           // fp32 [2][tasks][2][128]: stream-K partial sums (T <= 8 only)
+  size_t task_cnt;       // int32 [2][tasks]: stream-K parts finished per task (T <= 8 only)
   size_t cx;             // fp32 [T][d/32]: MMA accumulator inputs of the x16 blocks
   size_t ch;             // fp32 [P + T*n_shared][f/32]: MMA accumulator inputs of the h16 blocks
   size_t total;
@@ -103,6 +105,9 @@ struct StreamAux {
   float* cx;  // [T][d/32]: -1152 * (sum of each block of x16), the MMA accumulator input
   float* ch;  // [P + T*n_shared][f/32]: the same for h16
   int32_t* sched;  // [2]: next task of the gate/up and of the down kernel
+  float* part;         // [2][part_stride]: stream-K partial sums (128 floats per part, 2 parts per task)
+  int32_t* task_cnt;   // [2][cnt_stride]: stream-K parts finished per task
+  size_t part_stride, cnt_stride;
 };
 
 
@@ -142,5 +147,7 @@ bool prefill_supported(const FfnArgs& a);
 int device_sm_count();
 cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,
                            const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st);
+cudaError_t launch_rms_norm(const moe_shape& s, const void* x, int xdt, void* out, int odt, float eps,
+                            cudaStream_t st);
 
 }  // namespace moe

@@ -1,0 +1,151 @@
+"""Multi-layer drivers over the C-ABI: a decode stack with every expert resident, and a tiered
+stack whose experts live in pinned host memory and are cached in a device slot pool.
+
+Both only order the library's calls and hold buffers in torch tensors; every step of every
+layer runs in the library's kernels. Each layer is a pre-norm residual block,
+x_{l+1} = x_l + MoE_l(n(x_l)) with n the RMS normalisation (no gain, eps 1e-6): moe_rms_norm
+writes n(x_l), the layer routes and runs its experts on it, and the combine adds the residual
+x_l in fp32 and rounds once to bf16, in place.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib as L
+from . import layer as lay
+
+RMS_EPS = 1e-6
+
+
+@dataclass
+class LayerWeights:
+    """Device weights of one layer: router fp32 [d][E], and the expert table the FFN reads."""
+    router: torch.Tensor
+    table: L.moe_expert_table
+
+
+class DecodeStack:
+    """L MoE layers run one after another on a residual stream of T tokens."""
+
+    def __init__(self, shape: L.moe_shape, layers: list[LayerWeights], device="cuda"):
+        self.shape, self.layers = shape, layers
+        self.buf = lay.alloc_buffers(shape, device=device, ydt=L.MOE_F32, odt=L.MOE_BF16, keep_logits=False)
+        self.resid = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=device)
+        self.xn = torch.empty_like(self.resid)
+
+    def forward(self, x: torch.Tensor, stream=None, keep: list | None = None) -> torch.Tensor:
+        """Runs every layer on x (bf16 [T][d], left unchanged); returns the residual stream after
+        the last layer. With keep (a list), appends a copy of each layer's input and output."""
+        self.resid.copy_(x)
+        s, b = self.shape, self.buf
+        for lw in self.layers:
+            if keep is not None:
+                keep.append(("in", self.resid.clone()))
+            L.moe_rms_norm(s, self.resid, L.MOE_BF16, self.xn, L.MOE_BF16, RMS_EPS, stream)
+            L.moe_route(s, self.xn, L.MOE_BF16, lw.router, b.topk_idx, b.topk_w, None, b.ws, b.ws_bytes, stream)
+            L.moe_permute(s, b.topk_idx, b.counts, b.offsets, b.sorted_pair, b.inv_pos, b.active, b.ws, b.ws_bytes,
+                          stream)
+            L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, lw.table, b.offsets, b.sorted_pair, b.active,
+                             b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
+            # out aliases the residual: resid <- resid + MoE(resid)
+            L.moe_combine(s, b.y_perm, b.ydt, b.inv_pos, b.topk_w, self.resid, self.resid, L.MOE_BF16, stream)
+            if keep is not None:
+                keep.append(("idx", b.topk_idx.clone()))
+                keep.append(("out", self.resid.clone()))
+        return self.resid
+
+
+class TieredStack:
+    """L layers whose E routed experts per layer live in pinned host memory; a pool of n_slots
+    device slots caches them (the library's slot table: LRU over slots, misses copied on a side
+    stream). Shared experts stay resident.
+
+    Per layer: route and bucket on the compute stream; read the active list on the host; update
+    the slot table (miss copies on the copy stream, `ready` recorded after them). With overlap
+    (the default) the expert FFN then runs in two calls: the hit experts and the shared expert
+    first, while the copies are in flight, and the missed experts after the compute stream has
+    waited on `ready`. Without overlap one FFN call runs after the wait. Then the combine."""
+
+    def __init__(self, shape: L.moe_shape, n_layers: int, routers: list[torch.Tensor], h_records: list[int],
+                 n_slots: int, slot_bytes: int, shared: list[torch.Tensor], device="cuda"):
+        self.shape, self.L, self.routers = shape, n_layers, routers
+        self.shape_routed = L.shape(shape.T, shape.d, shape.f, shape.E, shape.k, 0)
+        self.n_slots, self.slot_bytes = n_slots, slot_bytes
+        self.pool = torch.empty(n_slots * slot_bytes, dtype=torch.uint8, device=device)
+        self.slot_of = torch.full((n_layers, shape.E), -1, dtype=torch.int32, device=device)
+        self.shared = shared  # per layer: n_shared records (device, uint8)
+        self.table = L.slot_table_create(n_layers, shape.E, n_slots, slot_bytes, self.pool, self.slot_of, h_records)
+        self.buf = lay.alloc_buffers(shape, device=device, ydt=L.MOE_F32, odt=L.MOE_BF16, keep_logits=False)
+        self.resid = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=device)
+        self.xn = torch.empty_like(self.resid)
+        self.copy_stream = torch.cuda.Stream(device)
+        self.ready = torch.cuda.Event()
+        self.done = torch.cuda.Event()
+        # torch creates an event on its first record; the library records `ready` by handle
+        self.ready.record(self.copy_stream)
+        self.done.record()
+        cap = min(shape.E, shape.T * shape.k)
+        # pinned lists in the library's active-list form: [count, ids...]
+        self.h_active = torch.empty(1 + cap, dtype=torch.int32).pin_memory()
+        self.h_hits = torch.zeros(1 + cap, dtype=torch.int32).pin_memory()
+        self.h_misses = torch.zeros(1 + cap, dtype=torch.int32).pin_memory()
+        self.d_hits = torch.zeros(1 + cap, dtype=torch.int32, device=device)
+        self.d_misses = torch.zeros(1 + cap, dtype=torch.int32, device=device)
+        self.stats = L.moe_slot_stats()
+        self.layer_misses: list[int] = []
+
+    def close(self):
+        if self.table:
+            L.slot_table_destroy(self.table)
+            self.table = None
+
+    def forward(self, x: torch.Tensor, keep: list | None = None, overlap: bool = True) -> torch.Tensor:
+        s, b = self.shape, self.buf
+        stream = torch.cuda.current_stream()
+        self.resid.copy_(x)
+        self.layer_misses = []
+        for l in range(self.L):
+            if keep is not None:
+                keep.append(("in", self.resid.clone()))
+            L.moe_rms_norm(s, self.resid, L.MOE_BF16, self.xn, L.MOE_BF16, RMS_EPS, stream)
+            L.moe_route(s, self.xn, L.MOE_BF16, self.routers[l], b.topk_idx, b.topk_w, None, b.ws, b.ws_bytes,
+                        stream)
+            L.moe_permute(s, b.topk_idx, b.counts, b.offsets, b.sorted_pair, b.inv_pos, b.active, b.ws, b.ws_bytes,
+                          stream)
+            self.h_active.copy_(b.active, non_blocking=True)
+            # the host needs the active list, and the previous layer's FFN must be done with the
+            # slots before any of them is overwritten: one event wait per layer
+            self.done.record(stream)
+            self.done.synchronize()
+            n = int(self.h_active[0])
+            hp, mp = self.h_hits.data_ptr(), self.h_misses.data_ptr()
+            st = L.slot_table_update(self.table, l, self.h_active.data_ptr() + 4, n, self.copy_stream.cuda_stream,
+                                     self.ready.cuda_event, hp + 4, hp, mp + 4, mp, self.stats)
+            if st != L.MOE_OK:
+                raise L.MoeError(st, "slot_table_update", "")
+            n_miss = int(self.h_misses[0])
+            self.layer_misses.append(n_miss)
+            table = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l],
+                                   self.shared[l] if s.n_shared else None)
+            if overlap:
+                self.d_hits.copy_(self.h_hits, non_blocking=True)
+                L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
+                                 self.d_hits, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
+                stream.wait_event(self.ready)
+                if n_miss:
+                    self.d_misses.copy_(self.h_misses, non_blocking=True)
+                    routed = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l], None)
+                    L.moe_expert_ffn(self.shape_routed, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, routed, b.offsets,
+                                     b.sorted_pair, self.d_misses, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
+            else:
+                stream.wait_event(self.ready)
+                L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
+                                 b.active, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
+            L.moe_combine(s, b.y_perm, b.ydt, b.inv_pos, b.topk_w, self.resid, self.resid, L.MOE_BF16, stream)
+            if keep is not None:
+                keep.append(("idx", b.topk_idx.clone()))
+                keep.append(("out", self.resid.clone()))
+        return self.resid

@@ -1,0 +1,130 @@
+"""Multi-layer runs through the C-ABI: a decode stack with every expert resident (pre-norm
+residual blocks, Zipf(1.1) routing), and a tiered stack whose experts are cached in a device
+slot pool smaller than the set of experts, filled from pinned host memory. Every layer is
+compared with the oracle given that layer's actual (bf16) input and the GPU's routing. The
+RMS normalisation call is checked on its own against the oracle."""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import moe_oracle as O
+from routed_expert_ffn_bucketing_b300 import _lib as L
+from routed_expert_ffn_bucketing_b300.stack import DecodeStack, LayerWeights, TieredStack
+from synth.device import DeviceLayer
+from synth.workloads import custom
+
+from gpu_util import TOL_BF16, cached_expert
+
+pytestmark = pytest.mark.gpu
+
+
+def check_layers(w, keep, layers):
+    """keep: the ('in', x), ('idx', topk), ('out', y) records of a stack run. Each layer is
+    x + MoE(n(x)) with n the oracle's RMS normalisation."""
+    recs = [keep[i:i + 3] for i in range(0, len(keep), 3)]
+    assert len(recs) == len(layers)
+    for l, (a, b, c) in zip(layers, recs):
+        assert a[0] == "in" and b[0] == "idx" and c[0] == "out"
+        x_np = a[1].float().cpu().numpy().astype(np.float64)
+        idx = b[1].cpu().numpy()
+        shared = [cached_expert(w, l, w.E + s) for s in range(w.n_shared)]
+        moe = O.moe_layer(O.rms_norm(x_np), w.router(l), w.k, lambda e: cached_expert(w, l, e), shared,
+                          forced_idx=idx)
+        ref = x_np + moe.out
+        out = c[1].float().cpu().numpy().astype(np.float64)
+        err, r = np.max(np.abs(out - ref)), O.rms(ref)
+        assert err <= TOL_BF16 * r, (l, err, r)
+
+
+@pytest.mark.parametrize("T,d", [(1, 32), (5, 2080), (4, 2048), (3, 4096)])
+@pytest.mark.parametrize("xdt,odt", [(L.MOE_BF16, L.MOE_BF16), (L.MOE_F32, L.MOE_F32), (L.MOE_BF16, L.MOE_F32)])
+def test_rms_norm_matches_oracle(T, d, xdt, odt):
+    g = torch.Generator().manual_seed(T * 7919 + d)
+    x = torch.randn((T, d), generator=g) * torch.logspace(-3, 3, T)[:, None]
+    x = x.to(torch.bfloat16 if xdt == L.MOE_BF16 else torch.float32)
+    xd = x.cuda()
+    out = torch.empty((T, d), dtype=torch.bfloat16 if odt == L.MOE_BF16 else torch.float32, device="cuda")
+    s = L.shape(T, d, 32, 4, 1, 0)
+    L.moe_rms_norm(s, xd, xdt, out, odt, 1e-6)
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref = O.rms_norm(x.float().numpy().astype(np.float64), eps=1e-6)
+    if odt == L.MOE_F32:
+        assert np.max(np.abs(got - ref)) <= 1e-5 * np.max(np.abs(ref))
+    else:
+        # one bf16 rounding of an fp32 value within 1e-6 of the exact one: at most one bf16 step
+        assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) * 1.001)
+    # in place
+    if xdt == odt:
+        y = xd.clone()
+        L.moe_rms_norm(s, y, xdt, y, odt, 1e-6)
+        assert torch.equal(y, out)
+
+
+def test_rms_norm_argument_errors():
+    s = L.shape(2, 64, 32, 4, 1, 0)
+    x = torch.zeros((2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(L.MoeError):
+        L.moe_rms_norm(s, x, L.MOE_BF16, x, L.MOE_BF16, -1.0)
+    with pytest.raises(L.MoeError):
+        L.moe_rms_norm(s, x, L.MOE_BF16, x, L.MOE_F32, 1e-6)
+    L.moe_rms_norm(L.shape(0, 64, 32, 4, 1, 0), None, L.MOE_BF16, None, L.MOE_BF16, 1e-6)  # T == 0: nothing to do
+    z = torch.zeros((2, 64), dtype=torch.float32, device="cuda")
+    L.moe_rms_norm(s, z, L.MOE_F32, z, L.MOE_F32, 1e-6)
+    assert torch.equal(z, torch.zeros_like(z))
+
+
+def test_decode_stack_layer_by_layer():
+    w = custom("stack", d=256, f=128, E=32, k=4, layers=3)
+    dls = [DeviceLayer(w, layer=l) for l in range(w.layers)]
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    layers = [LayerWeights(dl.router, L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr))
+              for dl in dls]
+    st = DecodeStack(s, layers)
+    keep = []
+    st.forward(dls[0].x(0), keep=keep)
+    assert L.moe_read_status(st.buf.ws) == 0
+    torch.cuda.synchronize()
+    check_layers(w, keep, range(w.layers))
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+def test_tiered_stack_misses_evictions_and_parity(overlap):
+    # 2 layers x 32 experts, but only 24 device slots: every step evicts and copies
+    w = custom("stack", d=256, f=128, E=32, k=6, layers=2, T=4)
+    n_slots = 24
+    rb = w.record_bytes
+    host = torch.empty((w.layers * w.E, rb), dtype=torch.uint8).pin_memory()
+    for l in range(w.layers):
+        for e in range(w.E):
+            host[l * w.E + e].copy_(torch.from_numpy(synth.pack_record(cached_expert(w, l, e))))
+    h_records = [host[i].data_ptr() for i in range(w.layers * w.E)]
+    dls = [DeviceLayer(w, layer=l) for l in range(w.layers)]  # routers and resident shared experts
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    shared = [dl.pool[w.E * rb:(w.E + w.n_shared) * rb] for dl in dls]
+    ts = TieredStack(s, w.layers, [dl.router for dl in dls], h_records, n_slots, rb, shared)
+    lookups = 0
+    try:
+        for step in range(3):
+            keep = []
+            ts.forward(dls[0].x(step), keep=keep, overlap=overlap)
+            assert L.moe_read_status(ts.buf.ws) == 0
+            torch.cuda.synchronize()
+            check_layers(w, keep, range(w.layers))
+            lookups += sum(np.unique(rec[1].cpu().numpy()).size for rec in keep if rec[0] == "idx")
+        st = L.slot_table_stats(ts.table)
+        assert st.misses > 0 and st.evictions > 0
+        assert st.hits + st.misses == lookups
+        assert st.bytes_h2d == st.misses * rb
+        # every resident expert's slot holds that expert's record
+        snap = np.zeros(w.layers * w.E, dtype=np.int32)
+        L.slot_table_snapshot(ts.table, snap.ctypes.data)
+        assert np.array_equal(snap.reshape(w.layers, w.E), ts.slot_of.cpu().numpy())
+        pool = ts.pool.cpu().numpy()
+        for i in np.nonzero(snap >= 0)[0][:12]:
+            slot = int(snap[i])
+            assert np.array_equal(pool[slot * rb:(slot + 1) * rb], host[i].numpy())
+    finally:
+        ts.close()
