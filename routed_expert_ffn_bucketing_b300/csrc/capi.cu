@@ -59,8 +59,16 @@ WsLayout ws_layout(const moe_shape& s) {
   o = align256(o + sizeof(uint16_t) * T * s.d);
   L.xunscale = o;
   o = align256(o + sizeof(float) * T);
+  // stream-K scratch of the decode kernels (T <= 8): tasks per kernel at most items * max(f/8, d/16)
+  const size_t sk_tasks = s.T <= 8 ? (P_items(s) + s.n_shared) * (s.f / 8 > s.d / 16 ? s.f / 8 : s.d / 16) : 0;
+  L.zero = o;
+  L.item_done = o;
+  o = align256(o + sizeof(int32_t) * (P_items(s) + s.n_shared));
   L.hmax = o;
   o = align256(o + sizeof(uint32_t) * (P + T * s.n_shared));
+  L.task_cnt = o;
+  o = align256(o + sizeof(int32_t) * 2 * sk_tasks);
+  L.zero_end = o;
   L.items = o;
   o = align256(o + sizeof(ItemRec) * ((P < (size_t)s.E ? P : (size_t)s.E) + s.n_shared));
   L.row_tok = o;
@@ -77,12 +85,8 @@ WsLayout ws_layout(const moe_shape& s) {
   o = align256(o + sizeof(int32_t) * T);
   L.tiles = o;
   o = align256(o + sizeof(int32_t) * 2 * ((P + T * s.n_shared) / 128 + P_items(s) + s.n_shared + 2));
-  // stream-K scratch of the decode kernels (T <= 8): tasks per kernel at most items * max(f/8, d/16)
-  const size_t sk_tasks = s.T <= 8 ? (P_items(s) + s.n_shared) * (s.f / 8 > s.d / 16 ? s.f / 8 : s.d / 16) : 0;
   L.part = o;
   o = align256(o + sizeof(float) * 2 * sk_tasks * 2 * 128);
-  L.task_cnt = o;
-  o = align256(o + sizeof(int32_t) * 2 * sk_tasks);
   L.cx = o;
   o = align256(o + sizeof(float) * T * (s.d / 32));
   L.ch = o;
@@ -318,6 +322,13 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
                            device_sm_count(), cs);
   } else if (mode == MOE_MODE_PREFILL) {
     return fail(MOE_EUNSUPPORTED, "moe_expert_ffn: PREFILL needs bf16 x, d a multiple of 256 and f of 128");
+  } else if (xdt == MOE_BF16 && persist_supported(a, device_sm_count())) {
+    const size_t items_max = (P_items(*shape)) + shape->n_shared;
+    const size_t sk_tasks = items_max * (shape->f / 8 > shape->d / 16 ? shape->f / 8 : shape->d / 16);
+    const PersistAux px{at<float>(ws, L.part),   at<int32_t>(ws, L.task_cnt), at<uint32_t>(ws, L.hmax),
+                        at<int32_t>(ws, L.item_done), sk_tasks * 2 * 128,     sk_tasks,
+                        at<uint8_t>(ws, L.zero), L.zero_end - L.zero};
+    e = launch_ffn_persist(a, px, device_sm_count(), cs);
   } else if (xdt == MOE_BF16 && stream_supported(a)) {
     const size_t items_max = (P_items(*shape)) + shape->n_shared;
     StreamAux aux{at<__half>(ws, L.x16),    at<float>(ws, L.xunscale), at<uint32_t>(ws, L.hmax),

@@ -16,8 +16,10 @@
 // A warp computes a whole task over all of K. Its lanes load the MMA fragments of the codes
 // directly from global memory (8 bytes of one row per lane and block, every 32-byte sector
 // used whole), eight blocks ahead of their use, so each SM keeps ~64 KB of loads in flight.
-// Warps take tasks from an atomic counter: load balance to within one task. There is no
-// shared memory, no barrier and no wait in these kernels.
+// Where they fit (decode sizes), each CTA first copies the activations the kernel reads (f16
+// rows and their block sums) into shared memory, so the per-block activation fragment of the
+// MMA is a shared-memory load instead of a cache access on the critical path. That copy ends
+// in the kernels' only barrier; they have no wait.
 //
 // Conversion. One lop3 turns two int8 codes (bytes 0 and 2 of a word, or 1 and 3 after a
 // shift) into the f16 pair 1152 + q, exactly (0x64 in the high byte, q + 128 in the low byte).
@@ -35,76 +37,11 @@
 // columns 2c, 2c + 1 of the result; in MMA half hf (0, 1) of a block its k slots {2c, 2c+1,
 // 2c+8, 2c+9} hold elements c*8 + hf*4 + {0, 2, 1, 3}, and the activation fragment of token g
 // uses the same order, so the k permutation cancels in the sum.
-#include "moe_common.cuh"
+#include "decode_mma.cuh"
 
 namespace moe {
 
 constexpr int kPassTok = 8;          // tokens per pass over a task (the 8 columns of an MMA)
-constexpr float kOffset = 1152.0f;   // f16 code of a weight = 1152 + q
-
-// ------------------------------------------------------------------ small helpers --------
-
-__device__ __forceinline__ void mma_f16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// f16 pair (1152 + q(byte 0), 1152 + q(byte 2)) of a word of int8 codes: the low bytes xor 0x80
-// under the mask, 0x64 in the high bytes (lop3 function b ? a ^ c : c).
-__device__ __forceinline__ uint32_t codes02(uint32_t w) {
-  uint32_t r;
-  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(w), "r"(0x00FF00FFu), "r"(0x64806480u));
-  return r;
-}
-
-// d = C + block product of M rows g, g+8 (8 codes each: w_lo, w_hi) with this lane's 8
-// activations of token g (xv: pairs (0,2), (1,3), (4,6), (5,7)), as two MMAs. C is -1152 times
-// the block sums of the activations of columns 2c, 2c+1 (c0, c1).
-__device__ __forceinline__ void block_mma(float* d, uint2 w_lo, uint2 w_hi, const uint4& xv, float c0, float c1) {
-  // first MMA: accumulator input (c0, c1, c0, c1) read straight from c0 / c1; second: chained
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%11,%10,%11};\n"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(codes02(w_lo.x)), "r"(codes02(w_hi.x)), "r"(codes02(w_lo.x >> 8)), "r"(codes02(w_hi.x >> 8)), "r"(xv.x),
-        "r"(xv.y), "f"(c0), "f"(c1));
-  mma_f16_16816(d, codes02(w_lo.y), codes02(w_hi.y), codes02(w_lo.y >> 8), codes02(w_hi.y >> 8), xv.z, xv.w);
-}
-
-__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
-
-// e with m * 2^-e in [2^14, 2^15) for a normal m > 0 (clamped to [-100, 100]); 0 for m == 0.
-// Scaling a row by 2^-e puts its largest magnitude near the top of the f16 range, so values
-// down to 2^-28 of that maximum stay normal f16 numbers.
-__device__ __forceinline__ int f16_exp_for(float m) {
-  if (!(m > 0.0f)) return 0;
-  const int e = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127 - 14;
-  return e < -100 ? -100 : (e > 100 ? 100 : e);
-}
-
-
-__device__ __forceinline__ int n_items(const FfnArgs& A) { return A.active[0] + A.n_shared; }
-
-// Element i of a row is stored at perm_pos(i): within each group of 4, order (0, 2, 1, 3).
-__device__ __forceinline__ int perm_pos(int i) { return (i & ~3) | ((i & 1) << 1) | ((i >> 1) & 1); }
-
-// Writes the 32 values v (one block, row order) to dst in the permuted order as f16 and
-// returns -1152 * (sum of the f16 values), the MMA accumulator input of that block.
-__device__ __forceinline__ float store_block_f16(__half* dst, const float* v) {
-  float s = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kQBlock; ++i) {
-    const __half q = __float2half_rn(v[i]);
-    dst[perm_pos(i)] = q;
-    s += __half2float(q);
-  }
-  return -kOffset * s;
-}
-
 // ------------------------------------------------------------------ prepare --------------
 
 // CTA t: x16[t] = f16(x[t] * 2^-e_t) (permuted), xunscale[t] = 2^e_t, cx[t][b] the MMA input of
@@ -165,18 +102,18 @@ constexpr int kWarps = 16;                // warps per CTA
 constexpr int kThreads = 32 * kWarps;
 constexpr int kDepth = 8;                 // weight blocks in flight per warp (kDepth x 512 bytes)
 
-// 8 int8 codes of one row at p (8-byte aligned), streamed once: no L1 allocation.
-__device__ __forceinline__ uint2 ld_codes(const uint8_t* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
-}
-
 // Next task of this warp from the kernel's task counter (one atomic per task, lane 0).
 __device__ __forceinline__ int grab_task(int* counter, int lane) {
   int t = 0;
   if (lane == 0) t = atomicAdd(counter, 1);
   return __shfl_sync(0xFFFFFFFFu, t, 0);
+}
+
+// An activation-side vector: from shared memory when staged (S), else a read-only global load.
+template <bool S, typename V>
+__device__ __forceinline__ V ld_act(const V* p) {
+  if (S) return *p;
+  return __ldg(p);
 }
 
 // D f16 scales (D = 4 or 8) of one row, loaded with one vector load.
@@ -204,7 +141,7 @@ struct ScaleVec {
 // lane's activation row (byte c*8 of it, permuted f16), cs0 / cs1 at the accumulator-input rows
 // of columns 2c, 2c+1. Weights are loaded D blocks ahead of their use; scales and accumulator
 // inputs are loaded with vector loads.
-template <int D>
+template <int D, bool S>
 __device__ __forceinline__ void rows_dot(const uint8_t* wlo, const uint8_t* whi, const __half* slo,
                                          const __half* shi, const __half* xrow, bool has, const float* cs0,
                                          const float* cs1, int b_lo, int b_hi, float (&acc)[4]) {
@@ -223,10 +160,10 @@ __device__ __forceinline__ void rows_dot(const uint8_t* wlo, const uint8_t* whi,
     for (int j = 0; j < D; ++j) {
       const int b = b0 + j;
       if ((j & 3) == 0) {
-        c0 = __ldg(reinterpret_cast<const float4*>(cs0 + b));
-        c1 = __ldg(reinterpret_cast<const float4*>(cs1 + b));
+        c0 = ld_act<S>(reinterpret_cast<const float4*>(cs0 + b));
+        c1 = ld_act<S>(reinterpret_cast<const float4*>(cs1 + b));
       }
-      const uint4 xv = has ? __ldg(reinterpret_cast<const uint4*>(xrow + b * kQBlock)) : make_uint4(0, 0, 0, 0);
+      const uint4 xv = has ? ld_act<S>(reinterpret_cast<const uint4*>(xrow + b * kQBlock)) : make_uint4(0, 0, 0, 0);
       const int jj = j & 3;
       const float ca = jj == 0 ? c0.x : jj == 1 ? c0.y : jj == 2 ? c0.z : c0.w;
       const float cb = jj == 0 ? c1.x : jj == 1 ? c1.y : jj == 2 ? c1.z : c1.w;
@@ -282,10 +219,11 @@ __device__ __forceinline__ bool task_rows(const FfnArgs& A, const StreamAux& X, 
 }
 
 // B operand (activation row of token column g) and C operand rows (columns 2c and 2c + 1) of
-// the pass starting at token `base`.
+// the pass starting at token `base`. xb / cb: the activation rows and their block sums (x16 and
+// cx for gate/up, h16 and ch for down), in global or shared memory.
 template <int KIND>
 __device__ __forceinline__ void task_pass(const FfnArgs& A, const StreamAux& X, int base, int nb, int g, int c,
-                                          TaskOps* o) {
+                                          TaskOps* o, const __half* xb, const float* cb) {
   const ItemRec& it = o->it;
   o->base = base;
   o->ng = min(kPassTok, it.ntok - base);
@@ -294,13 +232,13 @@ __device__ __forceinline__ void task_pass(const FfnArgs& A, const StreamAux& X, 
   const int r0 = it.row0 + base + (2 * c < o->ng ? 2 * c : 0);
   const int r1 = it.row0 + base + (2 * c + 1 < o->ng ? 2 * c + 1 : 0);
   if (KIND == kGateUp) {
-    o->xrow = X.x16 + (size_t)X.row_tok[rg_] * A.d + c * 8;
-    o->cs0 = X.cx + (size_t)X.row_tok[r0] * nb;
-    o->cs1 = X.cx + (size_t)X.row_tok[r1] * nb;
+    o->xrow = xb + (size_t)X.row_tok[rg_] * A.d + c * 8;
+    o->cs0 = cb + (size_t)X.row_tok[r0] * nb;
+    o->cs1 = cb + (size_t)X.row_tok[r1] * nb;
   } else {
-    o->xrow = X.h16 + (size_t)rg_ * A.f + c * 8;
-    o->cs0 = X.ch + (size_t)r0 * nb;
-    o->cs1 = X.ch + (size_t)r1 * nb;
+    o->xrow = xb + (size_t)rg_ * A.f + c * 8;
+    o->cs0 = cb + (size_t)r0 * nb;
+    o->cs1 = cb + (size_t)r1 * nb;
   }
 }
 
@@ -395,7 +333,7 @@ __device__ __forceinline__ void gateup_task_done(const FfnArgs& A, const StreamA
 // two warps (never more: a range is at least one task long) is finished by the second of them
 // to arrive: it adds the partial sums as part 0 + part 1 (a fixed order) and runs the epilogue.
 // Otherwise warps take whole tasks, pass by pass, from an atomic counter.
-template <int KIND, int D>
+template <int KIND, int D, bool S>
 __global__ void __launch_bounds__(kThreads) ffn_stream_kernel(FfnArgs A, StreamAux X) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -403,6 +341,23 @@ __global__ void __launch_bounds__(kThreads) ffn_stream_kernel(FfnArgs A, StreamA
   const int nb = K / kQBlock;
   const int tpi = KIND == kGateUp ? A.f / 8 : A.d / 16;  // tasks per item
   const int n_tasks = n_items(A) * tpi;
+  // activation rows: the T tokens' x for gate/up, every output row's h for down
+  const __half* xb = KIND == kGateUp ? X.x16 : X.h16;
+  const float* cb = KIND == kGateUp ? X.cx : X.ch;
+  if (S) {
+    extern __shared__ __align__(16) uint8_t act_smem[];
+    const int rows = KIND == kGateUp ? A.T : A.P + A.T * A.n_shared;
+    __half* sx = reinterpret_cast<__half*>(act_smem);
+    float* sc = reinterpret_cast<float*>(act_smem + (size_t)rows * K * sizeof(__half));
+    const int nx = rows * K / 8, nc = rows * nb / 4;  // uint4 / float4 counts
+    for (int i = threadIdx.x; i < nx; i += blockDim.x)
+      reinterpret_cast<uint4*>(sx)[i] = __ldcg(reinterpret_cast<const uint4*>(xb) + i);
+    for (int i = threadIdx.x; i < nc; i += blockDim.x)
+      reinterpret_cast<float4*>(sc)[i] = __ldcg(reinterpret_cast<const float4*>(cb) + i);
+    __syncthreads();
+    xb = sx;
+    cb = sc;
+  }
   if (A.T <= kPassTok) {
     const int gpt = nb / D;  // groups of D blocks per task
     const long long total = (long long)n_tasks * gpt;
@@ -418,9 +373,9 @@ __global__ void __launch_bounds__(kThreads) ffn_stream_kernel(FfnArgs A, StreamA
       G += ge - gs;
       TaskOps o;
       if (!task_rows<KIND>(A, X, t, tpi, nb, g, c, &o)) continue;
-      task_pass<KIND>(A, X, 0, nb, g, c, &o);
+      task_pass<KIND>(A, X, 0, nb, g, c, &o, xb, cb);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      rows_dot<D>(o.wlo, o.whi, o.slo, o.shi, o.xrow, o.has, o.cs0, o.cs1, gs * D, ge * D, acc);
+      rows_dot<D, S>(o.wlo, o.whi, o.slo, o.shi, o.xrow, o.has, o.cs0, o.cs1, gs * D, ge * D, acc);
       if (gs != 0 || ge != gpt) {
         // a cut task: publish this part, and the second part to arrive finishes the task
         const int my = gs == 0 ? 0 : 1;
@@ -448,9 +403,9 @@ __global__ void __launch_bounds__(kThreads) ffn_stream_kernel(FfnArgs A, StreamA
     TaskOps o;
     if (!task_rows<KIND>(A, X, t, tpi, nb, g, c, &o)) continue;
     for (int base = 0; base < o.it.ntok; base += kPassTok) {
-      task_pass<KIND>(A, X, base, nb, g, c, &o);
+      task_pass<KIND>(A, X, base, nb, g, c, &o, xb, cb);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      rows_dot<D>(o.wlo, o.whi, o.slo, o.shi, o.xrow, o.has, o.cs0, o.cs1, 0, nb, acc);
+      rows_dot<D, S>(o.wlo, o.whi, o.slo, o.shi, o.xrow, o.has, o.cs0, o.cs1, 0, nb, acc);
       task_epilogue<KIND>(A, X, o, g, c, acc);
     }
     if (KIND == kGateUp) gateup_task_done(A, X, o, tpi, lane);
@@ -458,6 +413,27 @@ __global__ void __launch_bounds__(kThreads) ffn_stream_kernel(FfnArgs A, StreamA
 }
 
 bool stream_supported(const FfnArgs& a) { return a.d % 128 == 0 && a.f % 128 == 0; }
+
+constexpr size_t kStageMax = 160 * 1024;  // largest activation copy kept in shared memory
+
+template <int KIND, int D>
+static cudaError_t launch_stream_d(const FfnArgs& a, const StreamAux& x, int grid, size_t smem, cudaStream_t st) {
+  if (smem <= kStageMax) {
+    const cudaError_t e = ensure_dynamic_smem((const void*)ffn_stream_kernel<KIND, D, true>, smem);
+    if (e != cudaSuccess) return e;
+    ffn_stream_kernel<KIND, D, true><<<grid, kThreads, smem, st>>>(a, x);
+  } else {
+    ffn_stream_kernel<KIND, D, false><<<grid, kThreads, 0, st>>>(a, x);
+  }
+  return cudaGetLastError();
+}
+
+template <int KIND>
+static cudaError_t launch_stream(const FfnArgs& a, const StreamAux& x, int grid, int K, size_t smem,
+                                 cudaStream_t st) {
+  return (K / kQBlock) % 8 == 0 ? launch_stream_d<KIND, 8>(a, x, grid, smem, st)
+                                : launch_stream_d<KIND, 4>(a, x, grid, smem, st);
+}
 
 cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, int sm_count, cudaStream_t st) {
   const int items_max = (a.P < a.E ? a.P : a.E) + a.n_shared;
@@ -470,13 +446,13 @@ cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, int sm_count
     const int warps = tasks < sm_count * kWarps ? tasks : sm_count * kWarps;
     return (warps + kWarps - 1) / kWarps;
   };
-  // D = 8 blocks in flight where the block count allows it (K a multiple of 256), else 4
-  if ((a.d / kQBlock) % 8 == 0) ffn_stream_kernel<kGateUp, 8><<<grid(gu_tasks), kThreads, 0, st>>>(a, x);
-  else ffn_stream_kernel<kGateUp, 4><<<grid(gu_tasks), kThreads, 0, st>>>(a, x);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((a.f / kQBlock) % 8 == 0) ffn_stream_kernel<kDown, 8><<<grid(dn_tasks), kThreads, 0, st>>>(a, x);
-  else ffn_stream_kernel<kDown, 4><<<grid(dn_tasks), kThreads, 0, st>>>(a, x);
-  return cudaGetLastError();
+  // D = 8 blocks in flight where the block count allows it (K a multiple of 256), else 4;
+  // activations staged in shared memory where they fit
+  const size_t rows = (size_t)a.P + (size_t)a.T * a.n_shared;
+  const size_t sm_gu = (size_t)a.T * a.d * sizeof(__half) + (size_t)a.T * (a.d / kQBlock) * sizeof(float);
+  const size_t sm_dn = rows * a.f * sizeof(__half) + rows * (a.f / kQBlock) * sizeof(float);
+  if ((e = launch_stream<kGateUp>(a, x, grid(gu_tasks), a.d, sm_gu, st)) != cudaSuccess) return e;
+  return launch_stream<kDown>(a, x, grid(dn_tasks), a.f, sm_dn, st);
 }
 
 }  // namespace moe

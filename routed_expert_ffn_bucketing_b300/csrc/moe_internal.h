@@ -32,7 +32,11 @@ struct WsLayout {
   size_t h;              // [P + T*n_shared][f] fp32: SwiGLU activations between the FFN kernels
   size_t x16;            // f16 [T][d]: activations rescaled per token by a power of two (permuted)
   size_t xunscale;       // fp32 [T]: the power of two that undoes that rescale
-  size_t hmax;           // uint32 [P + T*n_shared]: bits of max |h| per h row
+  size_t zero;           // start of the block the decode launcher zeroes with one memset:
+  size_t item_done;      //   int32 [min(E, P) + n_shared]: gate/up tasks finished per work item
+  size_t hmax;           //   uint32 [P + T*n_shared]: bits of max |h| per h row
+  size_t task_cnt;       //   int32 [2][tasks]: stream-K parts finished per task (T <= 8 only)
+  size_t zero_end;       // end of that block
   size_t items;          // ItemRec [min(E, P) + n_shared]: work items of the expert FFN
   size_t row_tok;        // int32 [P + T*n_shared]: token of each y_perm / h row
   size_t h16;            // f16 [P + T*n_shared][f]: h rescaled per row by a power of two (permuted)
@@ -43,7 +47,6 @@ struct WsLayout {
   size_t xexp;           // int32 [T]: the exponent of each token's rescale (prefill)
   size_t tiles;          // int2 [P/128 + items + 2]: prefill M tiles (item, first row), then the count
   size_t part;           // fp32 [2][tasks][2][128]: stream-K partial sums (T <= 8 only)
-  size_t task_cnt;       // int32 [2][tasks]: stream-K parts finished per task (T <= 8 only)
   size_t cx;             // fp32 [T][d/32]: MMA accumulator inputs of the x16 blocks
   size_t ch;             // fp32 [P + T*n_shared][f/32]: MMA accumulator inputs of the h16 blocks
   size_t total;
@@ -111,6 +114,18 @@ struct StreamAux {
 };
 
 
+// Workspace buffers of the persistent decode expert FFN. [zero, zero + zero_bytes) holds
+// item_done, hmax and task_cnt and is cleared by the launcher before the kernel.
+struct PersistAux {
+  float* part;         // [2][part_stride]
+  int32_t* task_cnt;   // [2][cnt_stride]
+  uint32_t* hmax;      // [P + T*n_shared]
+  int32_t* item_done;  // [min(E, P) + n_shared]
+  size_t part_stride, cnt_stride;
+  void* zero;
+  size_t zero_bytes;
+};
+
 // Workspace buffers of the prefill (tensor-core GEMM) expert FFN.
 struct PrefillAux {
   __half* xp16;       // [P + T*n_shared][d]: activation rows in expert order, f16, rescaled per token
@@ -139,6 +154,10 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);  // fp32 SIMT 
 // Streaming tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
 cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, int sm_count, cudaStream_t st);
 bool stream_supported(const FfnArgs& a);
+// One persistent cooperative kernel for T <= 8 (bf16 x); persist_supported() says whether the
+// shape fits (its shared-memory copy of the activations included).
+cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st);
+bool persist_supported(const FfnArgs& a, int sm_count);
 // Tensor-core grouped GEMM for many tokens per expert (bf16 x); prefill_supported() says whether
 // the shape fits (d a multiple of 256, f of 128).
 cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, const void* pool, const void* shared,
