@@ -447,7 +447,18 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   const uint16_t* sring_p = reinterpret_cast<const uint16_t*>(psm + Lo.sring) + (size_t)warp * 2 * 16 * dmax;
   const int nbd = d / kQBlock, nbf = f / kQBlock;
 
-  // ---- phase 0: work items (row span kept even for an expert with no slot), row tokens ----
+  // ---- phase 0 --------------------------------------------------------------------------
+  // x blocks first: each thread loads one (token, block) of x and keeps it in registers, so
+  // these loads are not queued behind the weight loads issued below. (CTAs start at different
+  // blocks, so they do not all read the same lines at once.)
+  const int rot = (int)((blockIdx.x * 7u) % (uint32_t)nbd);
+  const bool xmine = tid < T * nbd;
+  const int xb = (tid / T + rot) % nbd, xt = tid % T;
+  float xv[kQBlock];
+  if (xmine) load_bf16_block(static_cast<const uint16_t*>(A.x) + (size_t)xt * d + xb * kQBlock, xv);
+  for (int b = tid; b < nbd; b += kPThreads) bmax[b] = 0u;
+
+  // work items (row span kept even for an expert with no slot), row tokens
   const int n_active = A.active[0];
   const int n_items = n_active + A.n_shared;
   for (int i = tid; i < items_max; i += kPThreads) {
@@ -472,8 +483,13 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
     items[i] = rec;
   }
   for (int r = tid; r < rows; r += kPThreads) rowtok[r] = r < A.P ? A.sorted_pair[r] / A.k : (r - A.P) % T;
-  for (int b = tid; b < nbd; b += kPThreads) bmax[b] = 0u;
   __syncthreads();
+  if (xmine) {
+    float m = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kQBlock; ++q) m = fmaxf(m, fabsf(xv[q]));
+    atomicMax(bmax + xb, __float_as_uint(m));
+  }
 
   const int n_warps = gridDim.x * kPW, wid = blockIdx.x * kPW + warp;
   const uint32_t o_sx = Lo.act, o_scx = Lo.act + (uint32_t)T * act_stride(d);
@@ -488,30 +504,16 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   }
   cp_async_commit();
 
-  // ---- x to f16 in shared memory: one power of two per block over all tokens ------------
-  // (CTAs start at different blocks, so they do not all read the same lines at once)
-  const int rot = (int)((blockIdx.x * 7u) % (uint32_t)nbd);
-  for (int i = tid; i < T * nbd; i += kPThreads) {
-    const int b = (i / T + rot) % nbd, t = i % T;
-    float v[kQBlock];
-    load_bf16_block(static_cast<const uint16_t*>(A.x) + (size_t)t * d + b * kQBlock, v);
-    float m = 0.0f;
-#pragma unroll
-    for (int q = 0; q < kQBlock; ++q) m = fmaxf(m, fabsf(v[q]));
-    atomicMax(bmax + b, __float_as_uint(m));
-  }
+  // x to f16 in shared memory: one power of two per block over all tokens
   __syncthreads();
-  for (int i = tid; i < T * nbd; i += kPThreads) {
-    const int b = (i / T + rot) % nbd, t = i % T;
-    const int e = f16_exp_for(__uint_as_float(bmax[b]));
+  if (xmine) {
+    const int e = f16_exp_for(__uint_as_float(bmax[xb]));
     const float down = pow2f(-e);
-    float v[kQBlock];
-    load_bf16_block(static_cast<const uint16_t*>(A.x) + (size_t)t * d + b * kQBlock, v);
 #pragma unroll
-    for (int q = 0; q < kQBlock; ++q) v[q] *= down;
-    *reinterpret_cast<float*>(psm + o_scx + (size_t)t * sum_stride(d) + b * 4) =
-        stage_block_f16(psm + o_sx + (size_t)t * act_stride(d), b, v);
-    if (t == 0) xe[b] = pow2f(e);
+    for (int q = 0; q < kQBlock; ++q) xv[q] *= down;
+    *reinterpret_cast<float*>(psm + o_scx + (size_t)xt * sum_stride(d) + xb * 4) =
+        stage_block_f16(psm + o_sx + (size_t)xt * act_stride(d), xb, xv);
+    if (xt == 0) xe[xb] = pow2f(e);
   }
   __syncthreads();
 
@@ -639,7 +641,7 @@ size_t persist_smem_bytes(const FfnArgs& a, int sm_count) {
 
 bool persist_supported(const FfnArgs& a, int sm_count) {
   return a.xdt == 0 && a.T >= 1 && a.T <= 8 && a.d % 128 == 0 && a.f % 128 == 0 &&
-         persist_smem_bytes(a, sm_count) <= 200 * 1024;
+         a.T * (a.d / kQBlock) <= kPThreads && persist_smem_bytes(a, sm_count) <= 200 * 1024;
 }
 
 cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st) {
