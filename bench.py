@@ -399,7 +399,9 @@ def run_ours(args, ws, rank, local):
         "wall_s": wall,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": 7 * K,
+        # kernels per step: decode 4 (router GEMV with top-k, bucketing, persistent expert FFN,
+        # combine); prefill 11 (router GEMM, top-k, 3 bucketing, 5 expert FFN, combine)
+        "gpu_launches": (11 if prefill else 4) * K,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -517,7 +519,7 @@ def run_stack(args, ws, rank, local, w):
         "e2e": {"value": ws * w.T * K_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
                 "d2h_bytes_per_step": w.T * w.d * 2, "steps": K_e2e, "launch": "eager C-ABI calls"},
         "cpu_baseline": cpu,
-        "gpu_launches": 8 * w.layers * K,
+        "gpu_launches": 5 * w.layers * K,  # per layer: norm, router+top-k, bucketing, expert FFN, combine
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -616,8 +618,8 @@ def run_tiered(args, ws, rank, local, w):
                 out_host.copy_(y, non_blocking=True)
             torch.cuda.synchronize(dev)
             wall += time.perf_counter() - t0
-            # per layer: norm 1, route 2, permute 1, expert FFN 3 (+3 for the missed experts), combine 1
-            launches[0] += sum(8 + 3 * (m > 0) for m in ts.layer_misses)
+            # per layer: norm, router+top-k, bucketing, expert FFN (+1 for the missed experts), combine
+            launches[0] += sum(5 + (m > 0) for m in ts.layer_misses)
         return wall
 
     try:

@@ -224,11 +224,11 @@ moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const
     float* partial = at<float>(ws, L.route_partial);
     e = launch_route_gemv(*shape, x, xdt, w_router, partial, s);
     if (e == cudaSuccess)
-      e = launch_topk(*shape, partial, route_splits(shape->d), topk_idx, topk_w, logits_opt, status, s);
+      e = launch_topk_split(*shape, partial, route_splits(shape->d), topk_idx, topk_w, logits_opt, status, s);
   } else {
     float* logits = logits_opt ? logits_opt : at<float>(ws, L.logits);
     e = launch_route_gemm(*shape, x, xdt, w_router, logits, s);
-    if (e == cudaSuccess) e = launch_topk(*shape, logits, 1, topk_idx, topk_w, nullptr, status, s);
+    if (e == cudaSuccess) e = launch_topk(*shape, logits, topk_idx, topk_w, status, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "moe_route: launch");
   return MOE_OK;

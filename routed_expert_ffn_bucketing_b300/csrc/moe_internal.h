@@ -17,7 +17,7 @@ constexpr int MOE_DEV_TIMEOUT_BIT = MOE_DEV_TIMEOUT;
 constexpr int MOE_DEV_BAD_SLOT_BIT = MOE_DEV_BAD_SLOT;
 
 constexpr int kRouteGemvMaxT = 16;   // tokens up to which the router runs as a split-d GEMV
-constexpr int kRouteRowsPerSplit = 64;
+constexpr int kRouteRowsPerSplit = 128;
 constexpr int kPermChunk = 1024;     // pairs per bucketing chunk (one CTA)
 constexpr int kDecodeMaxT = 16;      // AUTO picks the decode kernels up to this many tokens
 constexpr int kDecodeTokGroup = 4;   // decode kernels stream weights once per group of tokens
@@ -143,10 +143,14 @@ struct PrefillAux {
 // Launchers; each returns cudaSuccess or the launch error.
 cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
                               cudaStream_t st);
+// Top-k from the router GEMV's split partial sums [splits][T][E]: one CTA per token.
+cudaError_t launch_topk_split(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
+                              float* logits_out, int* status, cudaStream_t st);
 cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const float* w, float* logits,
                               cudaStream_t st);
-cudaError_t launch_topk(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
-                        float* logits_out, int* status, cudaStream_t st);
+// Top-k of logits already summed (after the router GEMM): one warp per token.
+cudaError_t launch_topk(const moe_shape& s, const float* logits, int32_t* idx, float* wts, int* status,
+                        cudaStream_t st);
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
                            uint32_t* keys, int* status, cudaStream_t st);

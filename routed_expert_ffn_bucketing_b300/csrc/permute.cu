@@ -11,7 +11,9 @@
 // bitonic network. The keys are unique, so the sort is stable by construction. Run
 // lengths give the chunk's per-expert counts, a column scan over chunks gives every
 // (chunk, expert) its base, and the scatter writes sorted_pair / inv_pos. When all pairs fit in
-// one chunk (decode), one CTA does all of it in a single launch.
+// one chunk (decode), one CTA does all of it in a single launch; up to 256 pairs it counts
+// instead of sorting: each pair's rank is the number of earlier pairs of its expert, and the
+// last pair of each expert writes that expert's count (one writer per expert, no atomics).
 #include "moe_common.cuh"
 
 namespace moe {
@@ -122,6 +124,62 @@ __global__ void __launch_bounds__(CH) bucket_single_kernel(const int32_t* __rest
   }
 }
 
+// At most 256 pairs in one CTA of n >= max(P, E) threads (a multiple of 32): ranks, counts,
+// one scan for the offsets and one for the active list, scatter.
+__global__ void __launch_bounds__(1024) bucket_count_kernel(const int32_t* __restrict__ topk_idx, int P, int E,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ sorted_pair,
+                                                          int32_t* __restrict__ inv_pos,
+                                                          int32_t* __restrict__ active, int* status) {
+  __shared__ int ex[256];
+  __shared__ int cs[1024];
+  __shared__ int warp_sums[33];
+  const int i = threadIdx.x;
+  int e = 0;
+  if (i < P) {
+    e = topk_idx[i];
+    if (e < 0 || e >= E) {
+      flag_status(status, MOE_DEV_BAD_EXPERT_BIT);
+      e = e < 0 ? 0 : E - 1;  // keep every later write in bounds
+    }
+    ex[i] = e;
+  }
+  if (i < E) cs[i] = 0;
+  __syncthreads();
+  int rank = 0;
+  if (i < P) {
+    bool last = true;
+    for (int q = 0; q < P; ++q) {
+      const bool same = ex[q] == e;
+      rank += (q < i && same) ? 1 : 0;
+      last = last && !(q > i && same);
+    }
+    if (last) cs[e] = rank + 1;
+  }
+  __syncthreads();
+  const int v = i < E ? cs[i] : 0;
+  int total = 0, n_act = 0;
+  const int off = block_exclusive_scan(v, warp_sums, &total);
+  const int ar = block_exclusive_scan(v > 0 ? 1 : 0, warp_sums, &n_act);
+  if (i < E) {
+    counts[i] = v;
+    offsets[i] = off;
+    if (v > 0) active[1 + ar] = i;
+    cs[i] = off;
+  }
+  if (i == 0) {
+    offsets[E] = total;
+    active[0] = n_act;
+  }
+  __syncthreads();
+  if (i < P) {
+    const int pos = cs[e] + rank;
+    sorted_pair[pos] = i;
+    inv_pos[i] = pos;
+  }
+}
+
 // Multi-chunk, step 1: sort each chunk; write its keys and its per-expert counts cnt[c][e].
 __global__ void __launch_bounds__(CH) bucket_chunk_kernel(const int32_t* __restrict__ topk_idx, int P, int E,
                                                           uint32_t* __restrict__ chunk_keys,
@@ -207,6 +265,12 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
                            int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
                            uint32_t* keys, int* status, cudaStream_t st) {
   const int P = s.T * s.k;
+  if (P <= 256) {
+    const int need = P > s.E ? P : s.E;
+    const int n = (need + 31) / 32 * 32;
+    bucket_count_kernel<<<1, n, 0, st>>>(topk_idx, P, s.E, counts, offsets, sorted_pair, inv_pos, active, status);
+    return cudaGetLastError();
+  }
   if (P <= CH) {
     int n = 32;
     while (n < P) n <<= 1;

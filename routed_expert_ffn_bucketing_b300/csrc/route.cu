@@ -6,21 +6,107 @@
 // "三级存储分工"). Logits are fp32 with a fixed summation order, so results are deterministic.
 //
 //  * T <= 16 (decode, spec-verify): the router is a GEMV that streams w_router [d][E] once.
-//    The d rows are split into chunks of 64 so that the whole matrix is in flight at
-//    once (one CTA per 64 rows x 128 experts). Each chunk writes a partial sum, and the top-k
-//    kernel adds the chunks in ascending order.
+//    The d rows are split into chunks of 128 so that the whole matrix is in flight at
+//    once (one CTA per 128 rows x 128 experts). Each chunk writes a partial sum; the top-k
+//    kernel (one CTA per token) copies the token's partial sums to shared memory at once and
+//    adds them in a fixed order.
 //  * T > 16 (prefill): a tiled fp32 GEMM, 128 x 128 outputs per CTA. Each output sums its
 //    32-long k-blocks separately before adding them up, which keeps the fp32 error of a
 //    2048-long dot product near that of a tree sum.
 //  * top-k: one warp per token selects. Each lane holds E/32 logits as order-preserving
 //    integer keys, and k rounds of warp max (redux.sync) pick the experts. A tie goes to the
-//    lowest index. After the GEMV, one CTA per token first adds the split partial sums with
-//    all loads independent (a warp adding them one after another waited for each load in turn).
+//    lowest index.
 #include "moe_common.cuh"
 
 namespace moe {
 
+// ------------------------------------------------------------------ top-k helpers ---------
+
+// Order-preserving key of an fp32 logit: larger float, larger key. -0.0 maps like +0.0 and
+// NaN maps to 0, below every number (-inf has key 0x007FFFFF).
+__device__ __forceinline__ uint32_t logit_key(float v, bool* nan) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
+  if (v != v) {
+    *nan = true;
+    return 0u;
+  }
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
+// Selection of the k largest keys among the E logits held as PER keys per lane (logit e in
+// lane e % 32, slot e / 32), then the renormalised gate weights; one warp, one token.
+template <int PER>
+__device__ __forceinline__ void select_topk_warp(uint32_t (&key)[PER], int E, int k, int t, int32_t* idx,
+                                                 float* wts) {
+  const int lane = threadIdx.x & 31;
+  uint32_t taken = 0u;
+  int my_e = 0;
+  uint32_t my_key = 0u;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u;
+    int be = 0x7FFFFFFF;
+    bool found = false;
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const bool free_ = !((taken >> p) & 1u) && (lane + 32 * p) < E;
+      if (free_ && (!found || key[p] > bk)) {
+        bk = key[p];
+        be = lane + 32 * p;
+        found = true;
+      }
+    }
+    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const uint32_t cand = (found && bk == mk) ? (uint32_t)be : 0x7FFFFFFFu;
+    const int sel = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
+    if (lane == (sel & 31)) taken |= 1u << (sel >> 5);
+    if (lane == j) {
+      my_e = sel;
+      my_key = mk;
+    }
+  }
+  const float v = key_logit(my_key);
+  const float m = __shfl_sync(0xFFFFFFFFu, v, 0);
+  const float ex = lane < k ? expf(v - m) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_e;
+    wts[(size_t)t * k + lane] = ex / sum;
+  }
+}
+
 // ------------------------------------------------------------------ split-d GEMV ----------
+
+
+// Adds the S split partial sums held at slab[sp * stride] in four interleaved chains, then the
+// chains (a fixed order).
+__device__ __forceinline__ float sum_splits(const float* slab, int S, int stride) {
+  float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+  int sp = 0;
+  for (; sp + 4 <= S; sp += 4) {
+    c0 += slab[(sp + 0) * stride];
+    c1 += slab[(sp + 1) * stride];
+    c2 += slab[(sp + 2) * stride];
+    c3 += slab[(sp + 3) * stride];
+  }
+  for (; sp < S; ++sp) c0 += slab[sp * stride];
+  return (c0 + c1) + (c2 + c3);
+}
+
+__device__ __forceinline__ void cp_async_f4(float* dst, const float* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_f1(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
 
 template <int TT, int VEC>
 __global__ void __launch_bounds__(256) router_gemv_kernel(const void* __restrict__ x, int xdt,
@@ -86,6 +172,7 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const void* __restrict
     const int e = blockIdx.x * COLS + c;
     if (t < T && e < E) partial[((size_t)blockIdx.y * T + t) * E + e] = s;
   }
+
 }
 
 template <int TT, int VEC>
@@ -215,65 +302,6 @@ cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const 
 
 // ------------------------------------------------------------------ top-k ------------------
 
-// Order-preserving key of an fp32 logit: larger float, larger key. -0.0 maps like +0.0 and
-// NaN maps to 0, below every number (-inf has key 0x007FFFFF).
-__device__ __forceinline__ uint32_t logit_key(float v, bool* nan) {
-  uint32_t u = __float_as_uint(v);
-  if (u == 0x80000000u) u = 0u;
-  if (v != v) {
-    *nan = true;
-    return 0u;
-  }
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_logit(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
-}
-
-// Selection of the k largest keys among the E logits held as PER keys per lane (logit e in
-// lane e % 32, slot e / 32), then the renormalised gate weights; one warp, one token.
-template <int PER>
-__device__ __forceinline__ void select_topk_warp(uint32_t (&key)[PER], int E, int k, int t, int32_t* idx,
-                                                 float* wts) {
-  const int lane = threadIdx.x & 31;
-  uint32_t taken = 0u;
-  int my_e = 0;
-  uint32_t my_key = 0u;
-  for (int j = 0; j < k; ++j) {
-    uint32_t bk = 0u;
-    int be = 0x7FFFFFFF;
-    bool found = false;
-#pragma unroll
-    for (int p = 0; p < PER; ++p) {
-      const bool free_ = !((taken >> p) & 1u) && (lane + 32 * p) < E;
-      if (free_ && (!found || key[p] > bk)) {
-        bk = key[p];
-        be = lane + 32 * p;
-        found = true;
-      }
-    }
-    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
-    const uint32_t cand = (found && bk == mk) ? (uint32_t)be : 0x7FFFFFFFu;
-    const int sel = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
-    if (lane == (sel & 31)) taken |= 1u << (sel >> 5);
-    if (lane == j) {
-      my_e = sel;
-      my_key = mk;
-    }
-  }
-  const float v = key_logit(my_key);
-  const float m = __shfl_sync(0xFFFFFFFFu, v, 0);
-  const float ex = lane < k ? expf(v - m) : 0.0f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-  if (lane < k) {
-    idx[(size_t)t * k + lane] = my_e;
-    wts[(size_t)t * k + lane] = ex / sum;
-  }
-}
-
 // Logits already summed (router GEMM): one warp per token.
 template <int PER>
 __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
@@ -293,30 +321,33 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ log
   if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) flag_status(status, MOE_DEV_NAN_LOGIT_BIT);
 }
 
-// Split-d partial sums (router GEMV): one CTA per token. Thread e adds expert e's S partial
-// sums in four interleaved chains, then adds the chains (a fixed order), with all loads
-// independent; warp 0 then selects from shared memory.
+// Split-d partial sums (router GEMV): one CTA per token. The token's S x E partials are copied
+// to shared memory with every copy in flight at once (cp.async), added in a fixed order (four
+// interleaved chains over the splits, then the chains), and warp 0 selects.
 template <int PER>
-__global__ void __launch_bounds__(1024) topk_split_kernel(const float* __restrict__ partial, int S, int T, int E,
-                                                          int k, int32_t* __restrict__ idx,
-                                                          float* __restrict__ wts, float* __restrict__ logits_out,
-                                                          int* status) {
-  __shared__ float lg[32 * PER];
+__global__ void __launch_bounds__(512) topk_split_kernel(const float* __restrict__ partial, int S, int T, int E,
+                                                         int k, int32_t* __restrict__ idx, float* __restrict__ wts,
+                                                         float* __restrict__ logits_out, int* status) {
+  extern __shared__ float slab[];  // [S][E], then the logits [E]
   __shared__ int nan_any;
   const int t = blockIdx.x;
+  float* lg = slab + (size_t)S * E;
   if (threadIdx.x == 0) nan_any = 0;
+  if (E % 4 == 0) {
+    for (int i = threadIdx.x; i < S * (E / 4); i += blockDim.x) {
+      const int c4 = i % (E / 4), sp = i / (E / 4);
+      cp_async_f4(slab + (size_t)sp * E + c4 * 4, partial + ((size_t)sp * T + t) * E + c4 * 4);
+    }
+  } else {
+    for (int i = threadIdx.x; i < S * E; i += blockDim.x) {
+      const int c = i % E, sp = i / E;
+      cp_async_f1(slab + (size_t)sp * E + c, partial + ((size_t)sp * T + t) * E + c);
+    }
+  }
+  asm volatile("cp.async.commit_group;\ncp.async.wait_all;" ::: "memory");
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-    int sp = 0;
-    for (; sp + 4 <= S; sp += 4) {
-      c0 += partial[((size_t)(sp + 0) * T + t) * E + e];
-      c1 += partial[((size_t)(sp + 1) * T + t) * E + e];
-      c2 += partial[((size_t)(sp + 2) * T + t) * E + e];
-      c3 += partial[((size_t)(sp + 3) * T + t) * E + e];
-    }
-    for (; sp < S; ++sp) c0 += partial[((size_t)sp * T + t) * E + e];
-    const float v = (c0 + c1) + (c2 + c3);
+    const float v = sum_splits(slab + e, S, E);
     lg[e] = v;
     if (logits_out) logits_out[(size_t)t * E + e] = v;
     if (v != v) nan_any = 1;
@@ -347,20 +378,27 @@ __global__ void __launch_bounds__(1024) topk_split_kernel(const float* __restric
     else LAUNCH(32);                 \
   } while (0)
 
-cudaError_t launch_topk(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
-                        float* logits_out, int* status, cudaStream_t st) {
-  if (splits > 1) {
-    const int threads = (s.E + 31) / 32 * 32;
-#define L_SPLIT(P) \
-  topk_split_kernel<P><<<s.T, threads, 0, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status)
-    MOE_TOPK_DISPATCH(L_SPLIT);
-#undef L_SPLIT
-  } else {
-    const dim3 grid((s.T + 3) / 4);
-#define L_ONE(P) topk_kernel<P><<<grid, 128, 0, st>>>(partial, s.T, s.E, s.k, idx, wts, status)
-    MOE_TOPK_DISPATCH(L_ONE);
+cudaError_t launch_topk(const moe_shape& s, const float* logits, int32_t* idx, float* wts, int* status,
+                        cudaStream_t st) {
+  const dim3 grid((s.T + 3) / 4);
+#define L_ONE(P) topk_kernel<P><<<grid, 128, 0, st>>>(logits, s.T, s.E, s.k, idx, wts, status)
+  MOE_TOPK_DISPATCH(L_ONE);
 #undef L_ONE
-  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_split(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
+                              float* logits_out, int* status, cudaStream_t st) {
+  const size_t smem = sizeof(float) * (size_t)(splits + 1) * s.E;
+  const int threads = s.E >= 512 ? 512 : (s.E + 31) / 32 * 32;
+#define L_SPLIT(P)                                                                                     \
+  do {                                                                                                 \
+    const cudaError_t e = ensure_dynamic_smem((const void*)topk_split_kernel<P>, smem);               \
+    if (e != cudaSuccess) return e;                                                                    \
+    topk_split_kernel<P><<<s.T, threads, smem, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status); \
+  } while (0)
+  MOE_TOPK_DISPATCH(L_SPLIT);
+#undef L_SPLIT
   return cudaGetLastError();
 }
 
