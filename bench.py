@@ -35,6 +35,17 @@ METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill int8 TOPS as % of B300 p
 N_BATCHES = 16
 FLUSH_BYTES = 512 << 20
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernel(s),
+# from one ncu capture of the current kernels (the summaries in profiles/ give the command). A
+# capture is of one launch, i.e. one batch: the decode FFN's algorithmic bytes vary by batch.
+TRAFFIC = {
+    "decode": {"bytes": 185_617_664 + 3_590_656, "kernel": "ffn_persist_kernel<8, 8>",
+               "capture": "profiles/ffn_persist_decode_T4.md (one launch)"},
+    "prefill": {"bytes": 2_086_545_000 + 247_990_784 + 996_182_000 + 322_808_064,
+                "kernel": "prefill_gemm_kernel<0> + prefill_gemm_kernel<1>",
+                "capture": "profiles/prefill_gemm_T8192.md (one launch each; gather and h conversion not included)"},
+}
+
 
 def peaks():
     try:
@@ -344,12 +355,14 @@ def run_ours(args, ws, rank, local):
         tflops = ffn_flops / (sum(ffn_ms) / 1e3 / K) / 1e12
         roofline = {"kernel": "moe_expert_ffn (grouped GEMM: gate/up + SwiGLU, down)", "bound": "tensor",
                     "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tflops / bf16_peak,
-                    "peak_kind": f"{peak_kind} dense bf16 (the f16 dense rate is the same)", "traffic": None,
+                    "peak_kind": f"{peak_kind} dense bf16 (the f16 dense rate is the same)",
+                    "traffic": TRAFFIC["prefill"]["bytes"], "traffic_source": TRAFFIC["prefill"],
                     "flops_per_launch": ffn_flops, "ms_per_launch": sum(ffn_ms) / K}
     else:
         roofline = {"kernel": "moe_expert_ffn (gate/up + SwiGLU, down)", "bound": "hbm", "achieved": achieved,
                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                    "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                    "peak_kind": f"{peak_kind} copy bandwidth",
+                    "traffic": TRAFFIC["decode"]["bytes"], "traffic_source": TRAFFIC["decode"],
                     "bytes_per_launch": float(np.mean(ffn_bytes)), "ms_per_launch": sum(ffn_ms) / K}
     router_bytes = w.d * w.E * 4
     step_bytes = [b + router_bytes for b in ffn_bytes]

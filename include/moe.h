@@ -76,6 +76,17 @@ typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
  * (fp32 arithmetic on exactly dequantised weights). PREFILL is the tensor-core grouped
  * GEMM (bf16 operands after shared-memory dequantisation, fp32 accumulation); it
  * requires bf16 x. */
+/* Which expert-FFN kernels run (moe_expert_ffn). All give the same result within the bf16
+ * tolerance; each is deterministic.
+ *  DECODE   few tokens per expert: the int8 codes stream from HBM straight into f16
+ *           tensor-core fragments (weights exact, x and h rounded once to f16 after a
+ *           power-of-two rescale). T <= 8: one persistent cooperative kernel; 8 < T <= 16 (or
+ *           shapes whose shared-memory staging does not fit): three kernels. xdt = MOE_F32
+ *           selects the fp32 SIMT debug kernels instead.
+ *  PREFILL  many tokens per expert: a tcgen05 grouped GEMM (TMA operands, int8 weights
+ *           converted to f16 in shared memory, fp32 accumulators in tensor memory). Needs
+ *           xdt = MOE_BF16, d a multiple of 256 and f of 128 (else MOE_EUNSUPPORTED).
+ *  AUTO     PREFILL when T > 16 and xdt = MOE_BF16, else DECODE. */
 typedef enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL = 2 } moe_mode;
 
 /* Problem shape. T tokens, model width d, expert hidden width f, E routed experts,
@@ -175,8 +186,9 @@ moe_status moe_permute_static(const moe_shape* shape, const int32_t* topk_idx, i
  *  y_perm      out [P + T*n_shared][d] (ydt): row offsets[e] + i holds expert e's output for
  *              pair sorted_pair[offsets[e] + i]; row P + s*T + t holds shared expert s for token t
  *  ydt         MOE_F32 or MOE_BF16 (a bf16 y_perm halves the combine's reads)
- * PREFILL mode needs xdt = MOE_BF16. A routed expert with slot_of[e] < 0 sets
- * MOE_DEV_MISSING_SLOT and its rows are not written. */
+ * mode: see moe_mode. A routed expert with slot_of[e] < 0 sets MOE_DEV_MISSING_SLOT and its
+ * rows are not written. The call may run a memset and a cooperative launch on `stream`; a
+ * bounded wait inside a kernel that runs out sets MOE_DEV_TIMEOUT (outputs incomplete). */
 moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, moe_dtype xdt,
                           const moe_expert_table* experts, const int32_t* offsets,
                           const int32_t* sorted_pair, const int32_t* active, void* y_perm,
