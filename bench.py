@@ -248,7 +248,7 @@ def run_ours(args, ws, rank, local):
     xdt = L.MOE_BF16
 
     def step(x):
-        lay.forward(buf, x, dl.router, table, L.MOE_MODE_AUTO, stream=stream)
+        lay.forward(buf, x, dl.router, table, L.MOE_MODE_AUTO, stream=stream, fused=True)
 
     # active experts per batch (for the algorithmic byte count), from untimed passes
     n_active = []
@@ -263,25 +263,24 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize(dev)
 
     # The timed steps replay CUDA graphs of the C-ABI calls, one graph per stage and batch:
-    # (route + permute), expert FFN, combine. The kernels and their arguments are those of
-    # the eager calls; the graphs only take the host's launch cost out of the device time.
+    # (route + permute), expert FFN with the combine (moe_expert_ffn_combine). The kernels
+    # and their arguments are those of the eager calls; the graphs only take the host's launch
+    # cost out of the device time.
     def seg_route(x):
         L.moe_route(s, x, xdt, dl.router, buf.topk_idx, buf.topk_w, None, buf.ws, buf.ws_bytes, None)
         L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
                       buf.ws_bytes, None)
 
     def seg_ffn(x):
-        L.moe_expert_ffn(s, L.MOE_MODE_AUTO, x, xdt, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm,
-                         buf.ydt, buf.ws, buf.ws_bytes, None)
-
-    def seg_comb(x):
-        L.moe_combine(s, buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, None)
+        L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, x, xdt, table, buf.offsets, buf.sorted_pair, buf.active,
+                                 buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, buf.ws,
+                                 buf.ws_bytes, None)
 
     cap = torch.cuda.Stream(dev)
     graphs, layer_graphs = [], []
     for b in range(n_batches):
         gs = []
-        for seg in (seg_route, seg_ffn, seg_comb):
+        for seg in (seg_route, seg_ffn):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
                 seg(xs[b])
@@ -291,7 +290,6 @@ def run_ours(args, ws, rank, local):
         with torch.cuda.graph(g, stream=cap):
             seg_route(xs[b])
             seg_ffn(xs[b])
-            seg_comb(xs[b])
         layer_graphs.append(g)
     for i in range(W):
         flush.fill_(i & 0xFF)
@@ -321,45 +319,45 @@ def run_ours(args, ws, rank, local):
 
     # timed region 2 (the breakdown and the expert-FFN roofline): one graph per stage, events between
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     torch.cuda.synchronize(dev)
     for i in range(K):
         flush.fill_(i & 0xFF)
-        g_route, g_ffn, g_comb = graphs[i % n_batches]
-        e0, e1, e2, e3 = ev[i]
+        g_route, g_ffn = graphs[i % n_batches]
+        e0, e1, e2 = ev[i]
         e0.record(stream)
         g_route.replay()
         e1.record(stream)
         g_ffn.replay()
         e2.record(stream)
-        g_comb.replay()
-        e3.record(stream)
     torch.cuda.synchronize(dev)
     assert L.moe_read_status(buf.ws) == 0, "a kernel reported an error during the timed steps"
-    staged_ms = [a.elapsed_time(d) for a, _, _, d in ev]
-    ffn_ms = [b.elapsed_time(c) for _, b, c, _ in ev]
-    route_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
-    comb_ms = [c.elapsed_time(d) for _, _, c, d in ev]
+    staged_ms = [a.elapsed_time(c) for a, _, c in ev]
+    ffn_ms = [b.elapsed_time(c) for _, b, c in ev]
+    route_ms = [a.elapsed_time(b) for a, b, _ in ev]
     total_s = dist_max(sum(step_ms) / 1e3, ws, dev)
     value = ws * w.T * K / total_s
 
-    # algorithmic bytes of the expert-FFN call: each selected expert's record once, the T
-    # activation rows read, the y_perm rows written (fp32); scratch (h) is not counted
+    # algorithmic bytes of the expert-FFN call (with its combine): each selected expert's
+    # record once, the T activation rows read, the y_perm rows written (fp32) and the T output
+    # rows; scratch (h) is not counted
     rows = w.P + w.T * w.n_shared
-    small = w.T * w.d * 2 + rows * w.d * 4
+    small = w.T * w.d * 2 + rows * w.d * 4 + w.T * w.d * 2
     ffn_bytes = [(n_active[i % n_batches] + w.n_shared) * w.record_bytes + small for i in range(K)]
     achieved = sum(ffn_bytes) / (sum(ffn_ms) / 1e3) / 1e9
     if prefill:
         # tensor-bound: algorithmic FLOPs of the expert FFN (gate, up and down over every row)
         ffn_flops = 2.0 * rows * 3 * w.d * w.f
         tflops = ffn_flops / (sum(ffn_ms) / 1e3 / K) / 1e12
-        roofline = {"kernel": "moe_expert_ffn (grouped GEMM: gate/up + SwiGLU, down)", "bound": "tensor",
+        roofline = {"kernel": "moe_expert_ffn_combine (grouped GEMM: gate/up + SwiGLU, down; then the combine)",
+                    "bound": "tensor",
                     "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tflops / bf16_peak,
                     "peak_kind": f"{peak_kind} dense bf16 (the f16 dense rate is the same)",
                     "traffic": TRAFFIC["prefill"]["bytes"], "traffic_source": TRAFFIC["prefill"],
                     "flops_per_launch": ffn_flops, "ms_per_launch": sum(ffn_ms) / K}
     else:
-        roofline = {"kernel": "moe_expert_ffn (gate/up + SwiGLU, down)", "bound": "hbm", "achieved": achieved,
+        roofline = {"kernel": "moe_expert_ffn_combine (persistent kernel: gate/up + SwiGLU, down, combine)",
+                    "bound": "hbm", "achieved": achieved,
                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                     "peak_kind": f"{peak_kind} copy bandwidth",
                     "traffic": TRAFFIC["decode"]["bytes"], "traffic_source": TRAFFIC["decode"],
@@ -403,17 +401,18 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": w.describe(), "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
                    "activations": "bf16", "l2": "512 MiB buffer written between timed steps (outside events)",
                    "batches": n_batches, "mean_active_experts": float(np.mean(n_active)),
-                   "launch": "one CUDA graph of the four C-ABI calls per step (stages_ms: one graph per stage, events between)",
+                   "launch": "one CUDA graph of the three C-ABI calls per step: moe_route, moe_permute, "
+                             "moe_expert_ffn_combine (stages_ms: one graph per stage, events between)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roofline,
-        "stages_ms": {"route_permute": sum(route_ms) / K, "expert_ffn": sum(ffn_ms) / K,
-                      "combine": sum(comb_ms) / K, "step_as_three_graphs": sum(staged_ms) / K},
+        "stages_ms": {"route_permute": sum(route_ms) / K, "expert_ffn_combine": sum(ffn_ms) / K,
+                      "step_as_two_graphs": sum(staged_ms) / K},
         "step_hbm_gbs": step_gbs,
         "wall_s": wall,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        # kernels per step: decode 4 (router GEMV with top-k, bucketing, persistent expert FFN,
-        # combine); prefill 11 (router GEMM, top-k, 3 bucketing, 5 expert FFN, combine)
+        # kernels per step: decode 4 (router GEMV, top-k, bucketing, persistent expert FFN with
+        # the combine); prefill 11 (router GEMM, top-k, 3 bucketing, 5 expert FFN, combine)
         "gpu_launches": (11 if prefill else 4) * K,
         "clocks": clk,
     }
@@ -521,8 +520,8 @@ def run_stack(args, ws, rank, local, w):
                    "resident_gb": need / 1e9, "activations": "bf16 residual stream",
                    "l2": "inputs larger than L2 (each step reads every layer's selected experts, ~10 GB)",
                    "batches": n_batches, "mean_active_experts_per_layer": float(np.mean(n_active)),
-                   "launch": f"one CUDA graph of the {5 * w.layers} C-ABI calls of a step (norm, route, permute, "
-                             "expert FFN, combine per layer)",
+                   "launch": f"one CUDA graph of the {4 * w.layers} C-ABI calls of a step (norm, route, permute, "
+                             "expert FFN with the combine, per layer)",
                    "block": "pre-norm residual: x + MoE(rms_norm(x)), eps 1e-6, no gain",
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"kernel": f"whole {w.layers}-layer step (route, permute, expert FFN, combine per layer)",
@@ -532,7 +531,7 @@ def run_stack(args, ws, rank, local, w):
         "e2e": {"value": ws * w.T * K_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
                 "d2h_bytes_per_step": w.T * w.d * 2, "steps": K_e2e, "launch": "eager C-ABI calls"},
         "cpu_baseline": cpu,
-        "gpu_launches": 5 * w.layers * K,  # per layer: norm, router+top-k, bucketing, expert FFN, combine
+        "gpu_launches": 5 * w.layers * K,  # per layer: norm, router GEMV, top-k, bucketing, expert FFN + combine
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -631,8 +630,9 @@ def run_tiered(args, ws, rank, local, w):
                 out_host.copy_(y, non_blocking=True)
             torch.cuda.synchronize(dev)
             wall += time.perf_counter() - t0
-            # per layer: norm, router+top-k, bucketing, expert FFN (+1 for the missed experts), combine
-            launches[0] += sum(5 + (m > 0) for m in ts.layer_misses)
+            # per layer: norm, router GEMV, top-k, bucketing, expert FFN with the combine; with misses
+            # one more FFN call and a separate combine
+            launches[0] += sum(5 + 2 * (m > 0) for m in ts.layer_misses)
         return wall
 
     try:

@@ -8,6 +8,7 @@
  *   moe_expert_ffn  each selected expert's SwiGLU FFN over int8 block-32 weights, looked up
  *                   through the resident slot table, plus the always-on shared experts
  *   moe_combine     weighted sum of the expert outputs per token (unpermute)
+ *   moe_expert_ffn_combine  the last two in one call
  *   moe_rms_norm    (stacks of layers) the normalised input of a pre-norm residual block
  *   slot_table_*    host-side slot pool for experts that do not all fit on the device: a miss
  *                   is copied from pinned host memory on a side stream
@@ -193,6 +194,16 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
                           const moe_expert_table* experts, const int32_t* offsets,
                           const int32_t* sorted_pair, const int32_t* active, void* y_perm,
                           moe_dtype ydt, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Expert FFN followed by the combine, in one call: moe_expert_ffn and then moe_combine with
+ * these arguments, launched one after the other on `stream` (the same results, bit for bit).
+ * Arguments as in moe_expert_ffn and moe_combine; out may alias residual_opt. */
+moe_status moe_expert_ffn_combine(const moe_shape* shape, moe_mode mode, const void* x, moe_dtype xdt,
+                                  const moe_expert_table* experts, const int32_t* offsets,
+                                  const int32_t* sorted_pair, const int32_t* active, void* y_perm,
+                                  moe_dtype ydt, const int32_t* inv_pos, const float* topk_w,
+                                  const void* residual_opt, void* out, moe_dtype odt, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream);
 
 /* Combine / unpermute ([P5]: the token's output is the gated mixture of its selected
  * experts; [P2] "三级存储分工": the shared expert applies to every token):

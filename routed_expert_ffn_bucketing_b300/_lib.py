@@ -59,6 +59,8 @@ _SIGS = {
     "moe_expert_ffn": (C.c_int, [C.POINTER(moe_shape), C.c_int, _P, C.c_int, C.POINTER(moe_expert_table), _P, _P, _P,
                                  _P, C.c_int, _P, C.c_size_t, _P]),
     "moe_combine": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, C.c_int, _P]),
+    "moe_expert_ffn_combine": (C.c_int, [C.POINTER(moe_shape), C.c_int, _P, C.c_int, C.POINTER(moe_expert_table), _P,
+                                         _P, _P, _P, C.c_int, _P, _P, _P, _P, C.c_int, _P, C.c_size_t, _P]),
     "moe_rms_norm": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, C.c_int, C.c_float, _P]),
     "moe_read_status": (C.c_int, [_P, _P, C.POINTER(C.c_int32)]),
     "moe_last_error_string": (C.c_char_p, []),
@@ -156,6 +158,14 @@ def moe_expert_ffn(s, mode, x, xdt, table: moe_expert_table, offsets, sorted_pai
     return _check(lib().moe_expert_ffn(C.byref(s), mode, ptr(x), xdt, C.byref(table), ptr(offsets),
                                        ptr(sorted_pair), ptr(active), ptr(y_perm), ydt, ptr(ws), ws_bytes,
                                        stream_handle(stream)), "moe_expert_ffn")
+
+
+def moe_expert_ffn_combine(s, mode, x, xdt, table: moe_expert_table, offsets, sorted_pair, active, y_perm, ydt,
+                           inv_pos, topk_w, residual_opt, out, odt, ws, ws_bytes, stream=None) -> int:
+    return _check(lib().moe_expert_ffn_combine(C.byref(s), mode, ptr(x), xdt, C.byref(table), ptr(offsets),
+                                               ptr(sorted_pair), ptr(active), ptr(y_perm), ydt, ptr(inv_pos),
+                                               ptr(topk_w), ptr(residual_opt), ptr(out), odt, ptr(ws), ws_bytes,
+                                               stream_handle(stream)), "moe_expert_ffn_combine")
 
 
 def moe_combine(s, y_perm, ydt, inv_pos, topk_w, residual_opt, out, odt, stream=None) -> int:

@@ -250,10 +250,24 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t*
   return MOE_OK;
 }
 
-moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, moe_dtype xdt,
-                          const moe_expert_table* experts, const int32_t* offsets, const int32_t* sorted_pair,
-                          const int32_t* active, void* y_perm, moe_dtype ydt, void* ws, size_t ws_bytes,
-                          moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The combine that moe_expert_ffn_combine asks the expert FFN to fuse (already validated).
+struct CombineReq {
+  const int32_t* inv_pos;
+  const float* topk_w;
+  const void* residual;
+  void* out;
+  moe_dtype odt;
+};
+
+// moe_expert_ffn, and with `cmb` the combine launched after it on the same stream.
+moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x, moe_dtype xdt,
+                           const moe_expert_table* experts, const int32_t* offsets, const int32_t* sorted_pair,
+                           const int32_t* active, void* y_perm, moe_dtype ydt, void* ws, size_t ws_bytes,
+                           moe_stream_t stream, const CombineReq* cmb) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   if ((st = check_dtype(xdt, "x")) != MOE_OK) return st;
@@ -345,7 +359,41 @@ moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, 
     e = launch_ffn_decode(a, cs);
   }
   if (e != cudaSuccess) return cuda_fail(e, "moe_expert_ffn: launch");
+  if (cmb) {
+    e = launch_combine(*shape, y_perm, ydt, cmb->inv_pos, cmb->topk_w, cmb->residual, cmb->out, cmb->odt, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_expert_ffn_combine: combine launch");
+  }
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_expert_ffn(const moe_shape* shape, moe_mode mode, const void* x, moe_dtype xdt,
+                          const moe_expert_table* experts, const int32_t* offsets, const int32_t* sorted_pair,
+                          const int32_t* active, void* y_perm, moe_dtype ydt, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  return expert_ffn_impl(shape, mode, x, xdt, experts, offsets, sorted_pair, active, y_perm, ydt, ws, ws_bytes,
+                         stream, nullptr);
+}
+
+moe_status moe_expert_ffn_combine(const moe_shape* shape, moe_mode mode, const void* x, moe_dtype xdt,
+                                  const moe_expert_table* experts, const int32_t* offsets,
+                                  const int32_t* sorted_pair, const int32_t* active, void* y_perm, moe_dtype ydt,
+                                  const int32_t* inv_pos, const float* topk_w, const void* residual_opt, void* out,
+                                  moe_dtype odt, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_dtype(odt, "out")) != MOE_OK) return st;
+  if (shape->T > 0) {
+    if (!inv_pos || !topk_w || !out) return fail(MOE_EINVAL, "moe_expert_ffn_combine: NULL argument");
+    if (!aligned(out, 16) || (residual_opt && !aligned(residual_opt, 16)))
+      return fail(MOE_EINVAL, "moe_expert_ffn_combine: misaligned out or residual");
+  }
+  const CombineReq cmb{inv_pos, topk_w, residual_opt, out, odt};
+  return expert_ffn_impl(shape, mode, x, xdt, experts, offsets, sorted_pair, active, y_perm, ydt, ws, ws_bytes,
+                         stream, &cmb);
 }
 
 moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt, const int32_t* inv_pos,

@@ -12,7 +12,9 @@
 //   1. gate/up: a task is (item, 8 rows of f); M rows 0..7 of the MMA are gate rows and 8..15
 //      the same up rows, so each lane holds g and u of one (row, token) and writes
 //      h = silu(g) * u (fp32) and the row's max |h| (an order-free atomic max); the task then
-//      counts itself done for its item;
+//      counts itself done for its item in shared memory. When all its warps are through, the
+//      CTA fences once and adds its counts to the per-item counters in global memory (a fence
+//      per task would wait for the warp's next weight loads already in flight);
 //   2. each warp issues the first weight loads of its down work. The CTA waits (bounded) until
 //      every gate/up task of the items its down work covers is done, and converts those
 //      items' h rows to f16 in shared memory (power-of-two rescale from each row's max);
@@ -74,7 +76,7 @@ __host__ __device__ inline int p_rows_cap(int T, int d, int items_max, int rows,
 
 // Shared-memory layout of one CTA (byte offsets), the same on host and device.
 struct PLayout {
-  uint32_t items, rowtok, hexp, xe, bmax, sring, act, total;
+  uint32_t items, done, rowtok, hexp, xe, bmax, sring, act, total;
 };
 
 template <int DG, int DD>
@@ -83,6 +85,8 @@ __host__ __device__ inline PLayout p_layout(int T, int d, int f, int items_max, 
   uint32_t o = 0;
   L.items = o;
   o = align16(o + (uint32_t)items_max * (uint32_t)sizeof(ItemRec));
+  L.done = o;  // int32 [items]: gate/up tasks this CTA finished per item
+  o = align16(o + 4u * items_max);
   L.rowtok = o;
   o = align16(o + 4u * rows);
   L.hexp = o;
@@ -241,7 +245,7 @@ __device__ __forceinline__ void load_bf16_block(const uint16_t* p, float* v) {
 // columns 2c, 2c + 1 of the task's item.
 template <int KIND>
 __device__ __forceinline__ void p_epilogue(const FfnArgs& A, const PAux& X, const PTask& p, const int* hexp, int lane,
-                                           const float (&acc)[4]) {
+                                           const float (&acc)[4], int* s_done) {
   const int g = lane >> 2, c = lane & 3;
   if (KIND == kGU) {
     float m[2] = {0.f, 0.f};
@@ -264,10 +268,8 @@ __device__ __forceinline__ void p_epilogue(const FfnArgs& A, const PAux& X, cons
       if (2 * c < p.ntok) atomicMax(X.hmax + p.row0 + 2 * c, __float_as_uint(m[0]));
       if (2 * c + 1 < p.ntok) atomicMax(X.hmax + p.row0 + 2 * c + 1, __float_as_uint(m[1]));
     }
-    // the task is done: its h values and row maxima become visible before it is counted
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) atomicAdd(X.item_done + p.item, 1);
+    // the task is done: counted for its item in this CTA (published after the phase)
+    if (lane == 0) atomicAdd(s_done + p.item, 1);
   } else {
     const int row_lo = p.mt * 16 + g, row_hi = row_lo + 8;
 #pragma unroll
@@ -309,7 +311,7 @@ template <int KIND, int D>
 __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const uint8_t* psm, const ItemRec* items,
                                          const int* rowtok, uint32_t sx, uint32_t sc, uint32_t xe, const int* hexp,
                                          uint32_t sring_w, const uint16_t* sring_p, long long G0, long long G1,
-                                         int gpt, Ring<D>& ring, int& slot, int lane) {
+                                         int gpt, Ring<D>& ring, int& slot, int lane, int* s_done) {
   if (G0 >= G1) return;
   const int g = lane >> 2;
   const long long dhi = hi_delta<KIND>(A);
@@ -417,7 +419,7 @@ __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const 
             acc[3] = p0.w + p1.w;
           }
         }
-        if (finish) p_epilogue<KIND>(A, X, cur, hexp, lane, acc);
+        if (finish) p_epilogue<KIND>(A, X, cur, hexp, lane, acc, s_done);
       }
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     }
@@ -438,6 +440,7 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   const int items_max = (A.P < A.E ? A.P : A.E) + A.n_shared;
   const PLayout Lo = p_layout<DG, DD>(T, d, f, items_max, rows, X.rows_cap);
   ItemRec* items = reinterpret_cast<ItemRec*>(psm + Lo.items);
+  int* s_done = reinterpret_cast<int*>(psm + Lo.done);
   int* rowtok = reinterpret_cast<int*>(psm + Lo.rowtok);
   int* hexp = reinterpret_cast<int*>(psm + Lo.hexp);
   float* xe = reinterpret_cast<float*>(psm + Lo.xe);
@@ -481,6 +484,7 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
       rec.shared = 1;
     }
     items[i] = rec;
+    s_done[i] = 0;
   }
   for (int r = tid; r < rows; r += kPThreads) rowtok[r] = r < A.P ? A.sorted_pair[r] / A.k : (r - A.P) % T;
   __syncthreads();
@@ -519,9 +523,15 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
 
   // ---- phase 1: gate/up ----------------------------------------------------------------
   p_stream<kGU, DG>(A, X, psm, items, rowtok, o_sx, o_scx, Lo.xe, hexp, sring_w, sring_p, G0, G1, gpt_gu, rg, slot,
-                    lane);
+                    lane, s_done);
 
-  // ---- phase 2: first down loads; wait for this CTA's items; their h rows to f16 ----------
+  // ---- phase 2: publish this CTA's gate/up work; first down loads; wait for this CTA's
+  // items; their h rows to f16 -------------------------------------------------------------
+  // (every thread fences its own h writes and row maxima; no weight load is in flight now)
+  __threadfence();
+  __syncthreads();
+  for (int i = tid; i < items_max; i += kPThreads)
+    if (s_done[i] > 0) atomicAdd(X.item_done + i, s_done[i]);
   const int gpt_dn = nbf / DD;
   const int n_dn = n_items * (d / 16);
   warp_range(n_dn, gpt_dn, wid, n_warps, &G0, &G1);
@@ -594,7 +604,7 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
 
   // ---- phase 3: down -------------------------------------------------------------------
   p_stream<kDN, DD>(A, X, psm, items, rowtok, o_sh, o_sch, 0u, hexp, sring_w, sring_p, G0, G1, gpt_dn, rd, slot,
-                    lane);
+                    lane, s_done);
   cp_async_wait_all();
 }
 

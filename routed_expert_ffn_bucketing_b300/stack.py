@@ -48,10 +48,10 @@ class DecodeStack:
             L.moe_route(s, self.xn, L.MOE_BF16, lw.router, b.topk_idx, b.topk_w, None, b.ws, b.ws_bytes, stream)
             L.moe_permute(s, b.topk_idx, b.counts, b.offsets, b.sorted_pair, b.inv_pos, b.active, b.ws, b.ws_bytes,
                           stream)
-            L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, lw.table, b.offsets, b.sorted_pair, b.active,
-                             b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
-            # out aliases the residual: resid <- resid + MoE(resid)
-            L.moe_combine(s, b.y_perm, b.ydt, b.inv_pos, b.topk_w, self.resid, self.resid, L.MOE_BF16, stream)
+            # expert FFN and combine in one call; out aliases the residual: resid <- resid + MoE(n(resid))
+            L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, lw.table, b.offsets, b.sorted_pair,
+                                     b.active, b.y_perm, b.ydt, b.inv_pos, b.topk_w, self.resid, self.resid,
+                                     L.MOE_BF16, b.ws, b.ws_bytes, stream)
             if keep is not None:
                 keep.append(("idx", b.topk_idx.clone()))
                 keep.append(("out", self.resid.clone()))
@@ -130,21 +130,31 @@ class TieredStack:
             self.layer_misses.append(n_miss)
             table = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l],
                                    self.shared[l] if s.n_shared else None)
+            # resid <- resid + MoE(n(resid)): the combine is fused into the expert-FFN call where the
+            # layer makes only one
+            comb = (b.inv_pos, b.topk_w, self.resid, self.resid, L.MOE_BF16)
             if overlap:
                 self.d_hits.copy_(self.h_hits, non_blocking=True)
-                L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
-                                 self.d_hits, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
-                stream.wait_event(self.ready)
                 if n_miss:
+                    L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
+                                     self.d_hits, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
+                    stream.wait_event(self.ready)
                     self.d_misses.copy_(self.h_misses, non_blocking=True)
                     routed = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l], None)
+                    # the missed experts only (a shape without the shared expert, already done), then
+                    # the combine of the full layer
                     L.moe_expert_ffn(self.shape_routed, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, routed, b.offsets,
                                      b.sorted_pair, self.d_misses, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
+                    L.moe_combine(s, b.y_perm, b.ydt, *comb, stream)
+                else:
+                    stream.wait_event(self.ready)
+                    L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets,
+                                             b.sorted_pair, self.d_hits, b.y_perm, b.ydt, *comb, b.ws, b.ws_bytes,
+                                             stream)
             else:
                 stream.wait_event(self.ready)
-                L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
-                                 b.active, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
-            L.moe_combine(s, b.y_perm, b.ydt, b.inv_pos, b.topk_w, self.resid, self.resid, L.MOE_BF16, stream)
+                L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
+                                         b.active, b.y_perm, b.ydt, *comb, b.ws, b.ws_bytes, stream)
             if keep is not None:
                 keep.append(("idx", b.topk_idx.clone()))
                 keep.append(("out", self.resid.clone()))

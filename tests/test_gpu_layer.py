@@ -208,3 +208,49 @@ def test_prefill_layer_full_size():
     assert n_checked >= w.T - 8
     check_bucketing(run, w)
     check_output(run, w, tokens=np.array([0, 1, 77, 1023, 3333, 4096, 5000, 8191]))
+
+
+@pytest.mark.parametrize("wl,mode,residual,odt,ydt", [
+    ("decode", L.MOE_MODE_AUTO, False, L.MOE_BF16, L.MOE_F32),
+    ("decode", L.MOE_MODE_AUTO, True, L.MOE_BF16, L.MOE_F32),
+    ("decode", L.MOE_MODE_AUTO, True, L.MOE_F32, L.MOE_BF16),
+    ("tiny", L.MOE_MODE_AUTO, True, L.MOE_BF16, L.MOE_F32),      # T = 16: separate launches
+    ("tiny", L.MOE_MODE_PREFILL, False, L.MOE_BF16, L.MOE_BF16),
+])
+def test_fused_combine_is_bit_identical(wl, mode, residual, odt, ydt):
+    # moe_expert_ffn_combine against moe_expert_ffn followed by moe_combine: the same bits
+    from routed_expert_ffn_bucketing_b300 import layer as lay
+    w = WORKLOADS[wl] if wl != "decode" else custom("decode", T=4)
+    dl = DeviceLayer(w)
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    x = dl.x(3)
+    table = L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr)
+    outs = []
+    for fused in (False, True):
+        buf = lay.alloc_buffers(s, ydt=ydt, odt=odt, keep_logits=False)
+        res = x.float().to(torch.float32 if odt == L.MOE_F32 else torch.bfloat16).contiguous() if residual else None
+        L.moe_route(s, x, L.MOE_BF16, dl.router, buf.topk_idx, buf.topk_w, None, buf.ws, buf.ws_bytes)
+        L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
+                      buf.ws_bytes)
+        if fused:
+            L.moe_expert_ffn_combine(s, mode, x, L.MOE_BF16, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm,
+                                     buf.ydt, buf.inv_pos, buf.topk_w, res, buf.out, buf.odt, buf.ws, buf.ws_bytes)
+        else:
+            L.moe_expert_ffn(s, mode, x, L.MOE_BF16, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm,
+                             buf.ydt, buf.ws, buf.ws_bytes)
+            L.moe_combine(s, buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, res, buf.out, buf.odt)
+        assert L.moe_read_status(buf.ws) == 0
+        torch.cuda.synchronize()
+        outs.append(buf.out.clone())
+    assert torch.equal(outs[0], outs[1])
+    # and in place (out aliases the residual), as the stacks use it
+    if residual:
+        buf = lay.alloc_buffers(s, ydt=ydt, odt=odt, keep_logits=False)
+        r = x.float().to(torch.float32 if odt == L.MOE_F32 else torch.bfloat16).contiguous()
+        L.moe_route(s, x, L.MOE_BF16, dl.router, buf.topk_idx, buf.topk_w, None, buf.ws, buf.ws_bytes)
+        L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
+                      buf.ws_bytes)
+        L.moe_expert_ffn_combine(s, mode, x, L.MOE_BF16, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm,
+                                 buf.ydt, buf.inv_pos, buf.topk_w, r, r, buf.odt, buf.ws, buf.ws_bytes)
+        torch.cuda.synchronize()
+        assert torch.equal(r, outs[1])
