@@ -99,7 +99,12 @@ typedef struct {
 /* Byte offsets of one expert record. Each section starts on a 256-byte boundary:
  *   gate_q [f][d] int8, up_q [f][d] int8, down_q [d][f] int8,
  *   gate_s [f][d/32] fp16, up_s [f][d/32] fp16, down_s [d][f/32] fp16.
- * Weight W[r][i] = q[r][i] * s[r][i/32]; blocks run along the reduction dimension. */
+ * Weight W[r][i] = q[r][i] * s[r][i/32]; blocks run along the reduction dimension.
+ * Stored order of a code row of K codes: in each 64-code span (blocks 2p and 2p + 1) the
+ * 16-byte chunk c holds codes 8c..8c+7 of block 2p and then codes 8c..8c+7 of block 2p + 1,
+ * i.e. code i of the row sits at byte 64*(i/64) + 16*((i/8)%4) + 8*((i/32)%2) + i%8; a trailing
+ * block without a partner (K not a multiple of 64) is stored in order. One 16-byte load then
+ * gives a lane the same 8 codes of two blocks. Scales are stored in order. */
 typedef struct {
   uint64_t gate_q, up_q, down_q, gate_s, up_s, down_s, record_bytes;
 } moe_expert_layout;

@@ -1,6 +1,10 @@
 // Device helpers of the decode expert-FFN kernels: int8 codes to f16 MMA fragments, the
 // warp-level f16 MMA of one 32-element block, and the power-of-two rescale of activations.
 //
+// Codes are stored in pairs of blocks (code_pos): a lane's 16-byte chunk c of a 64-code span
+// holds codes 8c..8c+7 of both blocks, so each lane of an m16n8k16 MMA pair finds its 8 codes of
+// a block at one 8-byte half of its chunk.
+//
 // Conversion. One lop3 turns two int8 codes (bytes 0 and 2 of a word, or 1 and 3 after a
 // shift) into the f16 pair 1152 + q, exactly (0x64 in the high byte, q + 128 in the low byte).
 // The MMA's accumulator input is set to -1152 * (sum of the block's activations), so the MMA
@@ -86,6 +90,15 @@ __device__ __forceinline__ float store_block_f16(__half* dst, const float* v) {
 __device__ __forceinline__ uint2 ld_codes(const uint8_t* p) {
   uint2 r;
   asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+// 16 int8 codes at p (16-byte aligned), streamed once: no L1 allocation.
+__device__ __forceinline__ uint4 ld_codes16(const uint8_t* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
   return r;
 }
 

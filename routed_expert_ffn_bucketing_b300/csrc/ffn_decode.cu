@@ -27,7 +27,8 @@ constexpr int kDownRowsPerCta = 32;
 
 // Shared-memory layout of staged vectors: a length-n vector is n/16 chunks of four float4;
 // float4 j of chunk c of vector t sits at index (t * 4 + j) * (n / 16) + c. Lanes that read
-// consecutive chunks then read consecutive float4s (no bank conflicts).
+// consecutive chunks then read consecutive float4s (no bank conflicts). Vectors are staged in
+// the stored order of the code rows (code_pos), so chunk c of a vector meets chunk c of a row.
 __device__ __forceinline__ int il_index(int t, int j, int c, int nch) { return (t * 4 + j) * nch + c; }
 
 // Stage activations of tokens [g0, g0 + ng) of item `it` into xs (fp32, interleaved layout).
@@ -39,7 +40,8 @@ __device__ __forceinline__ void stage_x(const FfnArgs& A, const FfnItem& it, int
       const uint16_t* src = static_cast<const uint16_t*>(A.x) + (size_t)tok * A.d;
       for (int i = threadIdx.x * 8; i < A.d; i += kThreads * 8) {  // d % 32 == 0: 16-byte loads
         const uint4 v = *reinterpret_cast<const uint4*>(src + i);
-        const int c = i >> 4, j = (i & 15) >> 2;
+        const int pk = code_pos(i, A.d);  // the 8 elements stay together
+        const int c = pk >> 4, j = (pk & 15) >> 2;
         xs[il_index(t, j, c, nch)] = make_float4(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16),
                                                  bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16));
         xs[il_index(t, j + 1, c, nch)] = make_float4(bf16_bits_to_f32(v.z & 0xFFFFu), bf16_bits_to_f32(v.z >> 16),
@@ -47,8 +49,10 @@ __device__ __forceinline__ void stage_x(const FfnArgs& A, const FfnItem& it, int
       }
     } else {
       const float* src = static_cast<const float*>(A.x) + (size_t)tok * A.d;
-      for (int i = threadIdx.x * 4; i < A.d; i += kThreads * 4)
-        xs[il_index(t, (i & 15) >> 2, i >> 4, nch)] = *reinterpret_cast<const float4*>(src + i);
+      for (int i = threadIdx.x * 4; i < A.d; i += kThreads * 4) {
+        const int pk = code_pos(i & ~7, A.d) + (i & 7);
+        xs[il_index(t, (pk & 15) >> 2, pk >> 4, nch)] = *reinterpret_cast<const float4*>(src + i);
+      }
     }
   }
 }
@@ -58,15 +62,28 @@ __device__ __forceinline__ void stage_h(const float* h, int f, int ng, float4* h
   const int nch = f / 16;
   for (int i = threadIdx.x * 4; i < ng * f; i += kThreads * 4) {
     const int t = i / f, e = i % f;
-    hs[il_index(t, (e & 15) >> 2, e >> 4, nch)] = *reinterpret_cast<const float4*>(h + i);
+    const int pk = code_pos(e & ~7, f) + (e & 7);
+    hs[il_index(t, (pk & 15) >> 2, pk >> 4, nch)] = *reinterpret_cast<const float4*>(h + i);
   }
 }
 
-// acc[t] += scale * dot(q[0..16), chunk c of staged vector t) for t < ng <= NT. One 32-bit
-// word (four codes) at a time, so that few values are live at once. `ng` is the same for the
-// whole CTA, so the token guards do not diverge.
+// The scales of the two 8-code halves of stored chunk c of a row with K codes (scales: the
+// row's block scales): a paired chunk holds 8 codes of blocks 2p and 2p + 1, a chunk of a
+// trailing unpaired block 16 codes of that block.
+__device__ __forceinline__ void chunk_scales(const __half* scales, int c, int K, float* s0, float* s1) {
+  if (c < (K >> 6) * 4) {
+    *s0 = __half2float(scales[(c >> 2) * 2]);
+    *s1 = __half2float(scales[(c >> 2) * 2 + 1]);
+  } else {
+    *s0 = *s1 = __half2float(scales[c >> 1]);
+  }
+}
+
+// acc[t] += s0 * dot(q[0..8), ...) + s1 * dot(q[8..16), ...) with chunk c of staged vector t,
+// for t < ng <= NT. One 32-bit word (four codes) at a time, so that few values are live at
+// once. `ng` is the same for the whole CTA, so the token guards do not diverge.
 template <int NT>
-__device__ __forceinline__ void dot16(const uint4& w, float scale, const float4* vs, int c, int nch, int ng,
+__device__ __forceinline__ void dot16(const uint4& w, float s0, float s1, const float4* vs, int c, int nch, int ng,
                                       float* acc) {
   float s[NT];
   const uint32_t words[4] = {w.x, w.y, w.z, w.w};
@@ -78,16 +95,18 @@ __device__ __forceinline__ void dot16(const uint4& w, float scale, const float4*
     for (int t = 0; t < NT; ++t) {
       if (t < ng) {
         const float4 v = vs[il_index(t, j, c, nch)];
-        float p = (j == 0) ? q[0] * v.x : fmaf(q[0], v.x, s[t]);
+        float p = (j == 0 || j == 2) ? q[0] * v.x : fmaf(q[0], v.x, s[t]);
         p = fmaf(q[1], v.y, p);
         p = fmaf(q[2], v.z, p);
         s[t] = fmaf(q[3], v.w, p);
       }
     }
-  }
+    if (j == 1 || j == 3) {
 #pragma unroll
-  for (int t = 0; t < NT; ++t)
-    if (t < ng) acc[t] = fmaf(scale, s[t], acc[t]);
+      for (int t = 0; t < NT; ++t)
+        if (t < ng) acc[t] = fmaf(j == 1 ? s0 : s1, s[t], acc[t]);
+    }
+  }
 }
 
 template <int NT>
@@ -121,23 +140,23 @@ __device__ __forceinline__ void gateup_group(const FfnArgs& A, const FfnItem& it
     const uint8_t* urowp = uq + (size_t)r * d;
     for (int c0 = 0; c0 < nch; c0 += 32 * 4) {  // up to 4 chunks per lane in flight per matrix
       uint4 wg[4], wu[4];
-      float sg[4], su[4];
+      float sg0[4], sg1[4], su0[4], su1[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = c0 + u * 32 + lane;
         if (c < nch) {
           wg[u] = ld_stream16(growp + c * 16);
           wu[u] = ld_stream16(urowp + c * 16);
-          sg[u] = __half2float(gs[(size_t)r * nb + (c >> 1)]);
-          su[u] = __half2float(us[(size_t)r * nb + (c >> 1)]);
+          chunk_scales(gs + (size_t)r * nb, c, d, &sg0[u], &sg1[u]);
+          chunk_scales(us + (size_t)r * nb, c, d, &su0[u], &su1[u]);
         }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = c0 + u * 32 + lane;
         if (c < nch) {
-          dot16<NT>(wg[u], sg[u], xs, c, nch, ng, ag);
-          dot16<NT>(wu[u], su[u], xs, c, nch, ng, au);
+          dot16<NT>(wg[u], sg0[u], sg1[u], xs, c, nch, ng, ag);
+          dot16<NT>(wu[u], su0[u], su1[u], xs, c, nch, ng, au);
         }
       }
     }
@@ -192,19 +211,19 @@ __device__ __forceinline__ void down_group(const FfnArgs& A, const FfnItem& it, 
       const uint8_t* rowp = dq + (size_t)n * f;
       for (int c0 = 0; c0 < nch; c0 += LPR * 4) {
         uint4 w[4];
-        float sc[4];
+        float sc0[4], sc1[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int c = c0 + u * LPR + sl;
           if (c < nch) {
             w[u] = ld_stream16(rowp + c * 16);
-            sc[u] = __half2float(ds[(size_t)n * nb + (c >> 1)]);
+            chunk_scales(ds + (size_t)n * nb, c, f, &sc0[u], &sc1[u]);
           }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int c = c0 + u * LPR + sl;
-          if (c < nch) dot16<NT>(w[u], sc[u], hs, c, nch, ng, acc);
+          if (c < nch) dot16<NT>(w[u], sc0[u], sc1[u], hs, c, nch, ng, acc);
         }
       }
     }

@@ -21,8 +21,8 @@
 //   3. down: a task is (item, 16 rows of d); y_perm rows are written in fp32 or bf16.
 // Within a phase the (task, group of D blocks) sequence is cut into one contiguous range per
 // warp, equal to within one group (stream-K). A warp streams its range without a break: the
-// weights of the next group, and its scales, are requested while the current group is
-// multiplied, across task boundaries. A task cut between two warps is finished by the second
+// weights of the next group (one 16-byte load per lane, row and pair of blocks), and its
+// scales, are requested while the current group is multiplied, across task boundaries. A task cut between two warps is finished by the second
 // to arrive, which adds the two partial sums in a fixed order (part 0 + part 1). A warp's down
 // range covers about the same items as its gate/up range, so the waits of phase 2 are mostly on
 // work of the same or neighbouring CTAs.
@@ -118,7 +118,8 @@ struct PAux {
 // What one lane needs for one task: the addresses it loads codes and scales from, and where its
 // activation fragment and accumulator inputs are in shared memory.
 struct PTask {
-  const uint8_t* wlo;   // codes of M row g at byte c*8 (add 32 per block); row g + 8 is hi_delta(A) further
+  const uint8_t* wlo;   // codes of M row g at chunk c (byte c*16; add 64 per pair of blocks); row g + 8 is
+                        // hi_delta(A) further
   const uint8_t* ssrc;  // lanes 0..15: f16 scales of M row (lane) (add 2 per block); else unused
   uint32_t xrow;        // shared-memory offset of the activation row of token column g, element c*8
   uint32_t cs0, cs1;    // shared-memory offsets of the accumulator-input rows of columns 2c, 2c + 1
@@ -152,7 +153,7 @@ __device__ __forceinline__ PTask make_task(const FfnArgs& A, const ItemRec* item
   const int r0 = 2 * c < p.ntok ? 2 * c : 0, r1 = 2 * c + 1 < p.ntok ? 2 * c + 1 : 0;
   if (KIND == kGU) {
     const int d = A.d, nb = d / kQBlock;
-    p.wlo = rec + A.o_gate_q + (size_t)(p.mt * 8 + g) * d + c * 8;
+    p.wlo = rec + A.o_gate_q + (size_t)(p.mt * 8 + g) * d + c * 16;
     const int srow = p.mt * 8 + (lane & 7);
     p.ssrc = rec + (lane < 8 ? A.o_gate_s : A.o_up_s) + (size_t)srow * nb * 2;
     const int tg = p.valid ? rowtok[p.row0 + (p.has ? g : 0)] : 0;
@@ -161,7 +162,7 @@ __device__ __forceinline__ PTask make_task(const FfnArgs& A, const ItemRec* item
     p.cs1 = sc + (uint32_t)(p.valid ? rowtok[p.row0 + r1] : 0) * sum_stride(d);
   } else {
     const int f = A.f, nb = f / kQBlock;
-    p.wlo = rec + A.o_down_q + (size_t)(p.mt * 16 + g) * f + c * 8;
+    p.wlo = rec + A.o_down_q + (size_t)(p.mt * 16 + g) * f + c * 16;
     p.ssrc = rec + A.o_down_s + (size_t)(p.mt * 16 + (lane & 15)) * nb * 2;
     p.xrow = sx + (uint32_t)(p.row0 + (p.has ? g : 0)) * act_stride(f) + c * 16u;
     p.cs0 = sc + (uint32_t)(p.row0 + r0) * sum_stride(f);
@@ -182,9 +183,13 @@ __device__ __forceinline__ void issue_group(const PTask& p, long long dhi, int g
                                             int slot, int lane) {
   if (!p.valid) return;
 #pragma unroll
-  for (int j = 0; j < D; ++j) {
-    ring.lo[j] = ld_codes(p.wlo + (size_t)(gs * D + j) * kQBlock);
-    ring.hi[j] = ld_codes(p.wlo + dhi + (size_t)(gs * D + j) * kQBlock);
+  for (int j = 0; j < D; j += 2) {  // one 16-byte load: this lane's codes of blocks j and j + 1
+    const uint4 a = ld_codes16(p.wlo + (size_t)(gs * D + j) * kQBlock);
+    const uint4 b = ld_codes16(p.wlo + dhi + (size_t)(gs * D + j) * kQBlock);
+    ring.lo[j] = make_uint2(a.x, a.y);
+    ring.lo[j + 1] = make_uint2(a.z, a.w);
+    ring.hi[j] = make_uint2(b.x, b.y);
+    ring.hi[j + 1] = make_uint2(b.z, b.w);
   }
   if (lane < 16) {
     const uint32_t dst = sring_w + (uint32_t)(slot * 16 + lane) * (D * 2);
@@ -369,9 +374,13 @@ __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const 
         const float cb = jj == 0 ? c1.x : jj == 1 ? c1.y : jj == 2 ? c1.z : c1.w;
         float dd[4];
         block_mma(dd, ring.lo[j], ring.hi[j], xv, ca, cb);
-        if (more && src.valid) {
-          ring.lo[j] = ld_codes(src.wlo + (size_t)(gsn * D + j) * kQBlock);
-          ring.hi[j] = ld_codes(src.wlo + dhi + (size_t)(gsn * D + j) * kQBlock);
+        if (more && src.valid && (j & 1)) {  // blocks j - 1 and j are consumed: refill both
+          const uint4 a = ld_codes16(src.wlo + (size_t)(gsn * D + j - 1) * kQBlock);
+          const uint4 b = ld_codes16(src.wlo + dhi + (size_t)(gsn * D + j - 1) * kQBlock);
+          ring.lo[j - 1] = make_uint2(a.x, a.y);
+          ring.lo[j] = make_uint2(a.z, a.w);
+          ring.hi[j - 1] = make_uint2(b.x, b.y);
+          ring.hi[j] = make_uint2(b.z, b.w);
         }
         const uint32_t wl = slo[j >> 1], wh = shi[j >> 1];
         float s_lo = __half2float(__ushort_as_half((unsigned short)((j & 1) ? (wl >> 16) : (wl & 0xFFFFu))));
@@ -388,9 +397,13 @@ __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const 
       }
     } else if (more && src.valid) {
 #pragma unroll
-      for (int j = 0; j < D; ++j) {
-        ring.lo[j] = ld_codes(src.wlo + (size_t)(gsn * D + j) * kQBlock);
-        ring.hi[j] = ld_codes(src.wlo + dhi + (size_t)(gsn * D + j) * kQBlock);
+      for (int j = 0; j < D; j += 2) {
+        const uint4 a = ld_codes16(src.wlo + (size_t)(gsn * D + j) * kQBlock);
+        const uint4 b = ld_codes16(src.wlo + dhi + (size_t)(gsn * D + j) * kQBlock);
+        ring.lo[j] = make_uint2(a.x, a.y);
+        ring.lo[j + 1] = make_uint2(a.z, a.w);
+        ring.hi[j] = make_uint2(b.x, b.y);
+        ring.hi[j + 1] = make_uint2(b.z, b.w);
       }
     }
     slot ^= 1;

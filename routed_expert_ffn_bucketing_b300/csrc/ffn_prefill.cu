@@ -15,8 +15,10 @@
 //
 // The GEMM is persistent (one CTA per SM, a static stride over the work list) and warp
 // specialised:
-//   warp 0, lane 0: TMA. Per 64-element K step it loads the A tile (128 rows x 128 bytes of f16,
-//            128-byte swizzle) and the int8 codes of the 256 B rows (256 x 64 bytes).
+//   warp 0, lane 0: TMA. Per 64-element K step (one pair of 32-element blocks) it loads the A
+//            tile (128 rows x 128 bytes of f16, 128-byte swizzle) and the int8 codes of the 256 B
+//            rows (256 x 64 bytes, each row's pair of blocks in the stored order: 16-byte chunk c
+//            holds codes 8c..8c+7 of both blocks).
 //   warps 1..8: converters. Each thread turns 4 x 16 codes into f16 (q * s, one rounding; the
 //            fp16 scale s of the code's 32-element block) and writes them into the B tile in the
 //            128-byte-swizzled K-major layout the tensor core reads, then fences them into the
@@ -99,8 +101,9 @@ __host__ __device__ constexpr uint32_t f16_idesc(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// 16 int8 codes -> 16 f16 values q * s (s the f16 scale of their block): two 16-byte chunks.
-__device__ __forceinline__ void codes_to_f16(const uint4& q, __half2 s2, uint4* lo, uint4* hi) {
+// A lane's 16 stored codes (8 of each block of a pair) -> 16 f16 values q * s: codes 0..7 with
+// the first block's scale into lo, codes 8..15 with the second block's into hi.
+__device__ __forceinline__ void codes_to_f16(const uint4& q, __half2 s_lo, __half2 s_hi, uint4* lo, uint4* hi) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
   uint32_t o[8];
   const __half2 off = __half2half2(__ushort_as_half(0x6480));  // 1152
@@ -108,6 +111,7 @@ __device__ __forceinline__ void codes_to_f16(const uint4& q, __half2 s2, uint4* 
   for (int i = 0; i < 4; ++i) {
     const uint32_t u = w[i] ^ 0x80808080u;
     const uint32_t p01 = __byte_perm(u, 0x64646464u, 0x5140), p23 = __byte_perm(u, 0x64646464u, 0x5342);
+    const __half2 s2 = i < 2 ? s_lo : s_hi;
     const __half2 h01 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p01), off), s2);
     const __half2 h23 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p23), off), s2);
     o[2 * i] = *reinterpret_cast<const uint32_t*>(&h01);
@@ -361,10 +365,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
       }
       bool ok = true;
       for (int kc = 0; kc < KC; ++kc) {
-        const int blk = kc * 2 + (c >> 1);
-        __half s[4];
+        // this K step is one pair of blocks: 2 kc and 2 kc + 1
+        __half s0[4], s1[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s[i] = srow[i][blk];
+        for (int i = 0; i < 4; ++i) {
+          s0[i] = srow[i][kc * 2];
+          s1[i] = srow[i][kc * 2 + 1];
+        }
         const bool w1 = mbar_wait(&H.i_full[si], pi), w2 = mbar_wait(&H.ab_empty[sb], pb ^ 1u);
         if (!__all_sync(0xFFFFFFFFu, w1 && w2 && !p_aborted(H))) {
           if (lane == 0) p_set_abort(H, A.status);
@@ -376,11 +383,16 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = rb + 64 * i;
+          // stored chunk c: codes 8c..8c+7 of both blocks -> K-major chunks c and 4 + c
           const uint4 q = *reinterpret_cast<const uint4*>(src + r * kPK + c * 16);
           uint4 lo, hi;
-          codes_to_f16(q, __half2half2(s[i]), &lo, &hi);
-          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c) ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c + 1) ^ (r & 7)) << 4)) = hi;
+          codes_to_f16(q, __half2half2(s0[i]), __half2half2(s1[i]), &lo, &hi);
+          // odd rows write their high chunk first, so that the 8 lanes of a store phase (two
+          // rows) hit 8 distinct 16-byte bank groups
+          const bool odd = (r & 1) != 0;
+          const int ch_lo = c ^ (r & 7), ch_hi = (4 + c) ^ (r & 7);
+          *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_hi : ch_lo) << 4)) = odd ? hi : lo;
+          *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_lo : ch_hi) << 4)) = odd ? lo : hi;
         }
         fence_proxy_async_smem();
         __syncwarp();

@@ -109,6 +109,11 @@ __device__ __forceinline__ int grab_task(int* counter, int lane) {
   return __shfl_sync(0xFFFFFFFFu, t, 0);
 }
 
+// Byte offset, from a lane's chunk (c * 16) of a code row, of that lane's 8 codes of block b:
+// blocks come in pairs of 64 bytes, the second block's 8 codes right after the first's
+// (K is a multiple of 128 on this path, so every block has a partner).
+__device__ __forceinline__ int block_off(int b) { return (b >> 1) * 64 + (b & 1) * 8; }
+
 // An activation-side vector: from shared memory when staged (S), else a read-only global load.
 template <bool S, typename V>
 __device__ __forceinline__ V ld_act(const V* p) {
@@ -148,8 +153,8 @@ __device__ __forceinline__ void rows_dot(const uint8_t* wlo, const uint8_t* whi,
   uint2 ql[D], qh[D];
 #pragma unroll
   for (int j = 0; j < D; ++j) {
-    ql[j] = ld_codes(wlo + (b_lo + j) * kQBlock);
-    qh[j] = ld_codes(whi + (b_lo + j) * kQBlock);
+    ql[j] = ld_codes(wlo + block_off(b_lo + j));
+    qh[j] = ld_codes(whi + block_off(b_lo + j));
   }
   for (int b0 = b_lo; b0 < b_hi; b0 += D) {
     ScaleVec<D> sl, sh;
@@ -170,8 +175,8 @@ __device__ __forceinline__ void rows_dot(const uint8_t* wlo, const uint8_t* whi,
       float dd[4];
       block_mma(dd, ql[j], qh[j], xv, ca, cb);
       if (b + D < b_hi) {
-        ql[j] = ld_codes(wlo + (b + D) * kQBlock);
-        qh[j] = ld_codes(whi + (b + D) * kQBlock);
+        ql[j] = ld_codes(wlo + block_off(b + D));
+        qh[j] = ld_codes(whi + block_off(b + D));
       }
       const float s_lo = sl.at(j), s_hi = sh.at(j);
       acc[0] = fmaf(s_lo, dd[0], acc[0]);
@@ -203,15 +208,15 @@ __device__ __forceinline__ bool task_rows(const FfnArgs& A, const StreamAux& X, 
   const int d = A.d, f = A.f;
   if (KIND == kGateUp) {
     o->row_lo = o->row_hi = mt * 8 + g;  // gate row and up row of the same f index
-    o->wlo = rec + A.o_gate_q + (size_t)o->row_lo * d + c * 8;
-    o->whi = rec + A.o_up_q + (size_t)o->row_hi * d + c * 8;
+    o->wlo = rec + A.o_gate_q + (size_t)o->row_lo * d + c * 16;
+    o->whi = rec + A.o_up_q + (size_t)o->row_hi * d + c * 16;
     o->slo = reinterpret_cast<const __half*>(rec + A.o_gate_s) + (size_t)o->row_lo * nb;
     o->shi = reinterpret_cast<const __half*>(rec + A.o_up_s) + (size_t)o->row_hi * nb;
   } else {
     o->row_lo = mt * 16 + g;
     o->row_hi = o->row_lo + 8;
-    o->wlo = rec + A.o_down_q + (size_t)o->row_lo * f + c * 8;
-    o->whi = rec + A.o_down_q + (size_t)o->row_hi * f + c * 8;
+    o->wlo = rec + A.o_down_q + (size_t)o->row_lo * f + c * 16;
+    o->whi = rec + A.o_down_q + (size_t)o->row_hi * f + c * 16;
     o->slo = reinterpret_cast<const __half*>(rec + A.o_down_s) + (size_t)o->row_lo * nb;
     o->shi = reinterpret_cast<const __half*>(rec + A.o_down_s) + (size_t)o->row_hi * nb;
   }

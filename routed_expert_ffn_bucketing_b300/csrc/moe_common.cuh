@@ -11,6 +11,16 @@ namespace moe {
 
 constexpr int kQBlock = 32;  // elements per int8 quantisation block
 
+// Position of code k in a row of K int8 codes. Within each 64-code span (two blocks) the codes
+// are stored as four 16-byte chunks, chunk c holding codes 8c..8c+7 of the first block and then
+// 8c..8c+7 of the second: a lane that loads one 16-byte chunk gets the same 8 codes of both
+// blocks, the fragment the decode kernels multiply. A trailing block without a partner (K not a
+// multiple of 64) is stored as is.
+__host__ __device__ __forceinline__ int code_pos(int k, int K) {
+  if (k >= (K & ~63)) return k;
+  return (k & ~63) | (((k >> 3) & 3) << 4) | (((k >> 5) & 1) << 3) | (k & 7);
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // 128-bit streaming load of read-only data that is used once: no L1 allocation.

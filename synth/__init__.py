@@ -123,8 +123,8 @@ def _align256(n: int) -> int:
 @dataclass(frozen=True)
 class RecordLayout:
     """Byte offsets of one expert record: gate_q [f][d] i8, up_q [f][d] i8, down_q [d][f]
-    i8, gate_s [f][d/32] f16, up_s [f][d/32] f16, down_s [d][f/32] f16, each section
-    starting on a 256-byte boundary."""
+    i8 (each row in the stored order of interleave_codes), gate_s [f][d/32] f16, up_s [f][d/32]
+    f16, down_s [d][f/32] f16, each section starting on a 256-byte boundary."""
     d: int
     f: int
     gate_q: int
@@ -170,14 +170,36 @@ def expert_arrays(seed: int, layer: int, expert: int, d: int, f: int,
     return ExpertArrays(gq, gs, uq, us, dq, ds)
 
 
+def interleave_codes(q: np.ndarray) -> np.ndarray:
+    """Rows of int8 codes [R][K] in the stored order: in each 64-code span (two blocks of 32)
+    chunk c (16 bytes) holds codes 8c..8c+7 of the first block, then 8c..8c+7 of the second;
+    a trailing block without a partner stays as it is."""
+    R, K = q.shape
+    K64 = K // 64 * 64
+    out = q.copy()
+    out[:, :K64] = q[:, :K64].reshape(R, K64 // 64, 2, 4, 8).transpose(0, 1, 3, 2, 4).reshape(R, K64)
+    return out
+
+
+def deinterleave_codes(q: np.ndarray) -> np.ndarray:
+    """The inverse of interleave_codes."""
+    R, K = q.shape
+    K64 = K // 64 * 64
+    out = q.copy()
+    out[:, :K64] = q[:, :K64].reshape(R, K64 // 64, 4, 2, 8).transpose(0, 1, 3, 2, 4).reshape(R, K64)
+    return out
+
+
 def pack_record(a: ExpertArrays, slot_bytes: int | None = None) -> np.ndarray:
-    """Byte record (uint8) of one expert in the layout of record_layout; zero padding."""
+    """Byte record (uint8) of one expert in the layout of record_layout (codes in the stored
+    order of interleave_codes); zero padding."""
     f, d = a.gate_q.shape
     L = record_layout(d, f)
     n = L.record_bytes if slot_bytes is None else slot_bytes
     assert n >= L.record_bytes
     rec = np.zeros(n, dtype=np.uint8)
-    for off, arr in ((L.gate_q, a.gate_q), (L.up_q, a.up_q), (L.down_q, a.down_q),
+    for off, arr in ((L.gate_q, interleave_codes(a.gate_q)), (L.up_q, interleave_codes(a.up_q)),
+                     (L.down_q, interleave_codes(a.down_q)),
                      (L.gate_s, a.gate_s), (L.up_s, a.up_s), (L.down_s, a.down_s)):
         b = np.ascontiguousarray(arr).view(np.uint8).reshape(-1)
         rec[off:off + b.size] = b
@@ -191,9 +213,12 @@ def unpack_record(rec: np.ndarray, d: int, f: int) -> ExpertArrays:
     def take(off, n, dt, shape):
         return r[off:off + n * np.dtype(dt).itemsize].view(dt).reshape(shape).copy()
     nb_d, nb_f = d // BLOCK, f // BLOCK
-    return ExpertArrays(take(L.gate_q, f * d, np.int8, (f, d)), take(L.gate_s, f * nb_d, np.float16, (f, nb_d)),
-                        take(L.up_q, f * d, np.int8, (f, d)), take(L.up_s, f * nb_d, np.float16, (f, nb_d)),
-                        take(L.down_q, d * f, np.int8, (d, f)), take(L.down_s, d * nb_f, np.float16, (d, nb_f)))
+    return ExpertArrays(deinterleave_codes(take(L.gate_q, f * d, np.int8, (f, d))),
+                        take(L.gate_s, f * nb_d, np.float16, (f, nb_d)),
+                        deinterleave_codes(take(L.up_q, f * d, np.int8, (f, d))),
+                        take(L.up_s, f * nb_d, np.float16, (f, nb_d)),
+                        deinterleave_codes(take(L.down_q, d * f, np.int8, (d, f))),
+                        take(L.down_s, d * nb_f, np.float16, (d, nb_f)))
 
 
 # --------------------------------------------------------------------------------------

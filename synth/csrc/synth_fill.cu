@@ -69,7 +69,11 @@ __global__ void fill_records_kernel(FillArgs a) {
   float qf = 0.0f;
   if (sf != 0.0f) qf = fminf(fmaxf(rintf(__fdiv_rn(w, sf)), -127.0f), 127.0f);
   uint8_t* rec = a.dst + (uint64_t)ex * a.stride;
-  reinterpret_cast<int8_t*>(rec + s.q_off)[i] = (int8_t)(int)qf;
+  // stored order of a code row: in each 64-code span, chunk c (16 bytes) holds codes 8c..8c+7
+  // of the first block and then of the second; a trailing unpaired block stays as it is
+  const int k = (int)(bc * 32 + lane), K = s.cols;
+  const int pos = k >= (K & ~63) ? k : ((k & ~63) | (((k >> 3) & 3) << 4) | (((k >> 5) & 1) << 3) | (k & 7));
+  reinterpret_cast<int8_t*>(rec + s.q_off)[row * (uint64_t)s.cols + pos] = (int8_t)(int)qf;
   if (lane == 0) reinterpret_cast<__half*>(rec + s.s_off)[row * bpr + bc] = s16;
 }
 

@@ -94,3 +94,24 @@ def test_router_zipf_columns_follow_permutation():
     c, _ = synth.zipf_column_scales(32, 4, 1.1, 0)
     perm = synth.expert_rank_permutation(0, 5, 32)
     assert np.array_equal(w[:, perm[0]], (base[:, perm[0]] * c[0]).astype(np.float32))
+
+
+def test_interleaved_code_order():
+    # in each 64-code span, 16-byte chunk c holds codes 8c..8c+7 of the first block, then
+    # 8c..8c+7 of the second; a trailing unpaired block stays in place
+    K = 160  # two pairs and one unpaired block
+    q = np.arange(K, dtype=np.int64).reshape(1, K)
+    st = synth.interleave_codes(q)[0]
+    assert list(st[:16]) == list(range(0, 8)) + list(range(32, 40))
+    assert list(st[16:32]) == list(range(8, 16)) + list(range(40, 48))
+    assert list(st[48:64]) == list(range(24, 32)) + list(range(56, 64))
+    assert list(st[64:80]) == list(range(64, 72)) + list(range(96, 104))
+    assert list(st[128:]) == list(range(128, 160))
+    assert np.array_equal(synth.deinterleave_codes(synth.interleave_codes(q)), q)
+    # the device generator's position rule, written out here independently
+    def pos(k):
+        if k >= K // 64 * 64:
+            return k
+        p, h, c, i = k // 64, (k // 32) % 2, (k // 8) % 4, k % 8
+        return 64 * p + 16 * c + 8 * h + i
+    assert all(st[pos(k)] == k for k in range(K))
