@@ -39,9 +39,9 @@ FLUSH_BYTES = 512 << 20
 # from one ncu capture of the current kernels (the summaries in profiles/ give the command). A
 # capture is of one launch, i.e. one batch: the decode FFN's algorithmic bytes vary by batch.
 TRAFFIC = {
-    "decode": {"bytes": 185_617_664 + 3_590_656, "kernel": "ffn_persist_kernel<8, 8>",
+    "decode": {"bytes": 186_235_904 + 3_827_712, "kernel": "ffn_persist_kernel<8, 8>",
                "capture": "profiles/ffn_persist_decode_T4.md (one launch)"},
-    "prefill": {"bytes": 2_086_545_000 + 247_990_784 + 996_182_000 + 322_808_064,
+    "prefill": {"bytes": 2_086_812_000 + 247_447_296 + 996_140_000 + 323_280_640,
                 "kernel": "prefill_gemm_kernel<0> + prefill_gemm_kernel<1>",
                 "capture": "profiles/prefill_gemm_T8192.md (one launch each; gather and h conversion not included)"},
 }
@@ -271,16 +271,24 @@ def run_ours(args, ws, rank, local):
         L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
                       buf.ws_bytes, None)
 
-    def seg_ffn(x):
+    def seg_ffn_combine(x):
         L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, x, xdt, table, buf.offsets, buf.sorted_pair, buf.active,
                                  buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, buf.ws,
                                  buf.ws_bytes, None)
+
+    # for the breakdown: the same kernels as two calls
+    def seg_ffn(x):
+        L.moe_expert_ffn(s, L.MOE_MODE_AUTO, x, xdt, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm,
+                         buf.ydt, buf.ws, buf.ws_bytes, None)
+
+    def seg_comb(x):
+        L.moe_combine(s, buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, None)
 
     cap = torch.cuda.Stream(dev)
     graphs, layer_graphs = [], []
     for b in range(n_batches):
         gs = []
-        for seg in (seg_route, seg_ffn):
+        for seg in (seg_route, seg_ffn, seg_comb):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
                 seg(xs[b])
@@ -289,7 +297,7 @@ def run_ours(args, ws, rank, local):
         g = torch.cuda.CUDAGraph()  # the whole layer: the four calls in one graph
         with torch.cuda.graph(g, stream=cap):
             seg_route(xs[b])
-            seg_ffn(xs[b])
+            seg_ffn_combine(xs[b])
         layer_graphs.append(g)
     for i in range(W):
         flush.fill_(i & 0xFF)
@@ -319,45 +327,46 @@ def run_ours(args, ws, rank, local):
 
     # timed region 2 (the breakdown and the expert-FFN roofline): one graph per stage, events between
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     torch.cuda.synchronize(dev)
     for i in range(K):
         flush.fill_(i & 0xFF)
-        g_route, g_ffn = graphs[i % n_batches]
-        e0, e1, e2 = ev[i]
+        g_route, g_ffn, g_comb = graphs[i % n_batches]
+        e0, e1, e2, e3 = ev[i]
         e0.record(stream)
         g_route.replay()
         e1.record(stream)
         g_ffn.replay()
         e2.record(stream)
+        g_comb.replay()
+        e3.record(stream)
     torch.cuda.synchronize(dev)
     assert L.moe_read_status(buf.ws) == 0, "a kernel reported an error during the timed steps"
-    staged_ms = [a.elapsed_time(c) for a, _, c in ev]
-    ffn_ms = [b.elapsed_time(c) for _, b, c in ev]
-    route_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    staged_ms = [a.elapsed_time(d) for a, _, _, d in ev]
+    ffn_ms = [b.elapsed_time(c) for _, b, c, _ in ev]
+    route_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
+    comb_ms = [c.elapsed_time(d) for _, _, c, d in ev]
     total_s = dist_max(sum(step_ms) / 1e3, ws, dev)
     value = ws * w.T * K / total_s
 
-    # algorithmic bytes of the expert-FFN call (with its combine): each selected expert's
-    # record once, the T activation rows read, the y_perm rows written (fp32) and the T output
-    # rows; scratch (h) is not counted
+    # algorithmic bytes of the expert-FFN call: each selected expert's record once, the T
+    # activation rows read, the y_perm rows written (fp32); scratch (h) is not counted
     rows = w.P + w.T * w.n_shared
-    small = w.T * w.d * 2 + rows * w.d * 4 + w.T * w.d * 2
+    small = w.T * w.d * 2 + rows * w.d * 4
     ffn_bytes = [(n_active[i % n_batches] + w.n_shared) * w.record_bytes + small for i in range(K)]
     achieved = sum(ffn_bytes) / (sum(ffn_ms) / 1e3) / 1e9
     if prefill:
         # tensor-bound: algorithmic FLOPs of the expert FFN (gate, up and down over every row)
         ffn_flops = 2.0 * rows * 3 * w.d * w.f
         tflops = ffn_flops / (sum(ffn_ms) / 1e3 / K) / 1e12
-        roofline = {"kernel": "moe_expert_ffn_combine (grouped GEMM: gate/up + SwiGLU, down; then the combine)",
-                    "bound": "tensor",
+        roofline = {"kernel": "moe_expert_ffn (grouped GEMM: gate/up + SwiGLU, down)", "bound": "tensor",
                     "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tflops / bf16_peak,
                     "peak_kind": f"{peak_kind} dense bf16 (the f16 dense rate is the same)",
                     "traffic": TRAFFIC["prefill"]["bytes"], "traffic_source": TRAFFIC["prefill"],
                     "flops_per_launch": ffn_flops, "ms_per_launch": sum(ffn_ms) / K}
     else:
-        roofline = {"kernel": "moe_expert_ffn_combine (persistent kernel: gate/up + SwiGLU, down, combine)",
-                    "bound": "hbm", "achieved": achieved,
+        roofline = {"kernel": "moe_expert_ffn (persistent kernel: gate/up + SwiGLU, down)", "bound": "hbm",
+                    "achieved": achieved,
                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                     "peak_kind": f"{peak_kind} copy bandwidth",
                     "traffic": TRAFFIC["decode"]["bytes"], "traffic_source": TRAFFIC["decode"],
@@ -402,11 +411,12 @@ def run_ours(args, ws, rank, local):
                    "activations": "bf16", "l2": "512 MiB buffer written between timed steps (outside events)",
                    "batches": n_batches, "mean_active_experts": float(np.mean(n_active)),
                    "launch": "one CUDA graph of the three C-ABI calls per step: moe_route, moe_permute, "
-                             "moe_expert_ffn_combine (stages_ms: one graph per stage, events between)",
+                             "moe_expert_ffn_combine (stages_ms: the same kernels as moe_expert_ffn and "
+                             "moe_combine, one graph per stage, events between)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roofline,
-        "stages_ms": {"route_permute": sum(route_ms) / K, "expert_ffn_combine": sum(ffn_ms) / K,
-                      "step_as_two_graphs": sum(staged_ms) / K},
+        "stages_ms": {"route_permute": sum(route_ms) / K, "expert_ffn": sum(ffn_ms) / K,
+                      "combine": sum(comb_ms) / K, "step_as_three_graphs": sum(staged_ms) / K},
         "step_hbm_gbs": step_gbs,
         "wall_s": wall,
         "e2e": e2e,
