@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
                                                       int k, int n_shared) {
   const int t = blockIdx.y;
   const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  pdl_wait();  // y_perm from the expert FFN
   if (c >= d) return;
   const size_t P = (size_t)T * k;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -58,9 +59,8 @@ cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int
                            const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st) {
   const int threads = 256;
   dim3 grid((s.d / 4 + threads - 1) / threads, s.T);
-  combine_kernel<<<grid, threads, 0, st>>>(y, ydt, inv_pos, topk_w, residual, out, odt, s.T, s.d, s.k,
-                                           s.n_shared);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(threads), 0, st, y, ydt, inv_pos, topk_w, residual, out, odt, s.T, s.d,
+                    s.k, s.n_shared);
 }
 
 // RMS normalisation of each token's row, the input of a pre-norm residual block:

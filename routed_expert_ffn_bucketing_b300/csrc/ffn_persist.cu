@@ -448,6 +448,7 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   extern __shared__ __align__(16) uint8_t psm[];
   __shared__ int s_ok;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();  // the combine may launch; it waits for this grid before reading y_perm
   const int T = A.T, d = A.d, f = A.f;
   const int rows = A.P + T * A.n_shared;
   const int items_max = (A.P < A.E ? A.P : A.E) + A.n_shared;

@@ -52,6 +52,29 @@ __device__ __forceinline__ void i8x16_to_f32(const uint4& w, float* o) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Programmatic dependent launch. A kernel launched with launch_pdl may start while the kernel
+// before it on the stream is still running; pdl_wait() returns once that kernel has completed
+// and its memory writes are visible (at once when there is no such kernel), so it comes before
+// the first read of the predecessor's outputs. pdl_trigger() lets the next such kernel launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ void flag_status(int* status, int bit) {
   // error reporting only (rare path); bits from several threads must all survive
   atomicOr(status, bit);

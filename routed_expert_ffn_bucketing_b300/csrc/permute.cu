@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(1024) bucket_count_kernel(const int32_t* __res
   __shared__ int warp_sums[33];
   const int i = threadIdx.x;
   int e = 0;
+  pdl_wait();  // topk_idx from the router
   if (i < P) {
     e = topk_idx[i];
     if (e < 0 || e >= E) {
@@ -268,8 +269,8 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
   if (P <= 256) {
     const int need = P > s.E ? P : s.E;
     const int n = (need + 31) / 32 * 32;
-    bucket_count_kernel<<<1, n, 0, st>>>(topk_idx, P, s.E, counts, offsets, sorted_pair, inv_pos, active, status);
-    return cudaGetLastError();
+    return launch_pdl(bucket_count_kernel, dim3(1), dim3(n), 0, st, topk_idx, P, s.E, counts, offsets, sorted_pair,
+                      inv_pos, active, status);
   }
   if (P <= CH) {
     int n = 32;

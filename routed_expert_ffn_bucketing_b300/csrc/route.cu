@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const void* __restrict
                                                           float* __restrict__ partial, int T, int d,
                                                           int E) {
   constexpr int R = kRouteRowsPerSplit;  // rows of d per CTA
+  pdl_trigger();  // the top-k kernel may launch now; it waits for this grid before reading
   constexpr int COLS = 32 * VEC;         // experts per CTA
   extern __shared__ float sm[];
   float* xs = sm;            // [TT][R]
@@ -333,6 +334,8 @@ __global__ void __launch_bounds__(512) topk_split_kernel(const float* __restrict
   const int t = blockIdx.x;
   float* lg = slab + (size_t)S * E;
   if (threadIdx.x == 0) nan_any = 0;
+  pdl_trigger();
+  pdl_wait();  // the router GEMV's partial sums
   if (E % 4 == 0) {
     for (int i = threadIdx.x; i < S * (E / 4); i += blockDim.x) {
       const int c4 = i % (E / 4), sp = i / (E / 4);
@@ -395,7 +398,9 @@ cudaError_t launch_topk_split(const moe_shape& s, const float* partial, int spli
   do {                                                                                                 \
     const cudaError_t e = ensure_dynamic_smem((const void*)topk_split_kernel<P>, smem);               \
     if (e != cudaSuccess) return e;                                                                    \
-    topk_split_kernel<P><<<s.T, threads, smem, st>>>(partial, splits, s.T, s.E, s.k, idx, wts, logits_out, status); \
+    const cudaError_t e2 = launch_pdl(topk_split_kernel<P>, dim3(s.T), dim3(threads), smem, st, partial, splits, s.T, \
+                                      s.E, s.k, idx, wts, logits_out, status);                                     \
+    if (e2 != cudaSuccess) return e2;                                                                                 \
   } while (0)
   MOE_TOPK_DISPATCH(L_SPLIT);
 #undef L_SPLIT
