@@ -39,7 +39,7 @@ FLUSH_BYTES = 512 << 20
 # from one ncu capture of the current kernels (the summaries in profiles/ give the command). A
 # capture is of one launch, i.e. one batch: the decode FFN's algorithmic bytes vary by batch.
 TRAFFIC = {
-    "decode": {"bytes": 186_235_904 + 3_827_712, "kernel": "ffn_persist_kernel<8, 8>",
+    "decode": {"bytes": 186_220_288 + 3_603_200, "kernel": "ffn_persist_kernel<8, 8>",
                "capture": "profiles/ffn_persist_decode_T4.md (one launch)"},
     "prefill": {"bytes": 2_086_812_000 + 247_447_296 + 996_140_000 + 323_280_640,
                 "kernel": "prefill_gemm_kernel<0> + prefill_gemm_kernel<1>",
