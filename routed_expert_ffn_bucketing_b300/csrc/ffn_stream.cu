@@ -14,8 +14,10 @@
 //            f16 (rescaled per row by a power of two from max |h|) with their per-block sums;
 //   down:    a task is (item, 16 rows of d).
 // A warp computes a whole task over all of K. Its lanes load the MMA fragments of the codes
-// directly from global memory (8 bytes of one row per lane and block, every 32-byte sector
-// used whole), eight blocks ahead of their use, so each SM keeps ~64 KB of loads in flight.
+// directly from global memory (8 bytes of one row per lane and block; in the paired code layout
+// the loads of the two blocks of a pair together read each row's 64 bytes whole), eight blocks
+// ahead of their use, so each SM keeps ~64 KB of loads in flight. This path serves T up to 16
+// (two passes over a task for 8 < T <= 16) and shapes the persistent kernel cannot stage.
 // Where they fit (decode sizes), each CTA first copies the activations the kernel reads (f16
 // rows and their block sums) into shared memory, so the per-block activation fragment of the
 // MMA is a shared-memory load instead of a cache access on the critical path. That copy ends
