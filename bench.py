@@ -41,7 +41,7 @@ FLUSH_BYTES = 512 << 20
 TRAFFIC = {
     "decode": {"bytes": 186_220_288 + 3_603_200, "kernel": "ffn_persist_kernel<8, 8>",
                "capture": "profiles/ffn_persist_decode_T4.md (one launch)"},
-    "prefill": {"bytes": 2_086_812_000 + 247_447_296 + 996_140_000 + 323_280_640,
+    "prefill": {"bytes": 2_721_439_000 + 241_189_888 + 1_198_355_000 + 314_232_576,
                 "kernel": "prefill_gemm_kernel<0> + prefill_gemm_kernel<1>",
                 "capture": "profiles/prefill_gemm_T8192.md (one launch each; gather and h conversion not included)"},
 }

@@ -84,8 +84,8 @@ typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
  *           power-of-two rescale). T <= 8: one persistent cooperative kernel; 8 < T <= 16 (or
  *           shapes whose shared-memory staging does not fit): three kernels. xdt = MOE_F32
  *           selects the fp32 SIMT debug kernels instead.
- *  PREFILL  many tokens per expert: a tcgen05 grouped GEMM (TMA operands, int8 weights
- *           converted to f16 in shared memory, fp32 accumulators in tensor memory). Needs
+ *  PREFILL  many tokens per expert: a tcgen05 grouped GEMM (activations by TMA, int8 weights
+ *           converted to f16 into shared memory, fp32 accumulators in tensor memory). Needs
  *           xdt = MOE_BF16, d a multiple of 256 and f of 128 (else MOE_EUNSUPPORTED).
  *  AUTO     PREFILL when T > 16 and xdt = MOE_BF16, else DECODE. */
 typedef enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL = 2 } moe_mode;

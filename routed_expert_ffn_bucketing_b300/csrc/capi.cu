@@ -332,8 +332,7 @@ moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x,
                         at<__half>(ws, L.h16),      at<int32_t>(ws, L.hexp),   at<int2>(ws, L.tiles),
                         at<int32_t>(ws, L.tiles) + 2 * ((size_t)(shape->T * shape->k + shape->T * shape->n_shared) / 128 +
                                                         P_items(*shape) + shape->n_shared + 1)};
-    e = launch_ffn_prefill(a, px, experts->pool, experts->shared, experts->n_slots, experts->slot_bytes,
-                           device_sm_count(), cs);
+    e = launch_ffn_prefill(a, px, device_sm_count(), cs);
   } else if (mode == MOE_MODE_PREFILL) {
     return fail(MOE_EUNSUPPORTED, "moe_expert_ffn: PREFILL needs bf16 x, d a multiple of 256 and f of 128");
   } else if (xdt == MOE_BF16 && persist_supported(a, device_sm_count())) {

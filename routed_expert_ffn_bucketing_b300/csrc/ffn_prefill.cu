@@ -14,17 +14,22 @@
 //   gemm<DN>: for each (M tile, 256 rows of d): D[128][256] = h16[128][f] . Wd[256][f]^T.
 //
 // The GEMM is persistent (one CTA per SM, a static stride over the work list) and warp
-// specialised:
-//   warp 0, lane 0: TMA. Per 64-element K step (one pair of 32-element blocks) it loads the A
-//            tile (128 rows x 128 bytes of f16, 128-byte swizzle) and the int8 codes of the 256 B
-//            rows (256 x 64 bytes, each row's pair of blocks in the stored order: 16-byte chunk c
-//            holds codes 8c..8c+7 of both blocks).
-//   warps 1..8: converters. Each thread turns 4 x 16 codes into f16 (q * s, one rounding; the
-//            fp16 scale s of the code's 32-element block) and writes them into the B tile in the
-//            128-byte-swizzled K-major layout the tensor core reads, then fences them into the
-//            async proxy. The int8 codes stay exact until this single rounding.
+// specialised, with two shared-memory rings, each with its own full and empty barriers: A (4
+// stages of 16 KB, filled by TMA) and the converted f16 B tile (3 stages of 32 KB). The int8
+// codes never pass through shared memory: its bandwidth is what the tensor core's operand reads
+// (12 KB per M128 x N256 x K16 MMA), the TMA writes and the converters share, and an int8 stage
+// would cost a TMA write plus a converter read for every K step.
+//   warp 0, lane 0: TMA of the A tile of each 64-element K step (one pair of 32-element
+//            blocks): 128 rows x 128 bytes of f16 in the 128-byte swizzle; freed by the MMA.
+//   warps 1..8: converters. Each thread owns 4 B rows and one 16-byte chunk of each row's 64
+//            stored codes per K step (chunk c holds codes 8c..8c+7 of both blocks of the pair),
+//            loaded with the blocks' fp16 scales from the expert record two pairs of K steps
+//            ahead into registers. It turns them into f16 (q * s, one rounding) and writes them
+//            into the B tile in the 128-byte-swizzled K-major layout the tensor core reads,
+//            then fences them into the async proxy. The int8 codes stay exact until this single
+//            rounding.
 //   warp 9, lane 0: issues 4 tcgen05.mma (M = 128, N = 256, K = 16) per K step into one of two
-//            TMEM accumulators (2 x 256 columns) and commits each stage back to the producers.
+//            TMEM accumulators (2 x 256 columns) and commits each stage back to the A and B rings.
 //   warps 12..15: epilogue. TMEM lanes 32 q .. 32 q + 31 (q = warp % 4) hold rows of the tile;
 //            tcgen05.ld 16 columns at a time while the next tile accumulates in the other buffer.
 // Activations enter as f16 exactly (bf16 has 8 significant bits; each row is rescaled by a power
@@ -47,22 +52,21 @@ constexpr int kPN = 256;                     // UMMA N
 constexpr int kPK = 64;                      // K elements per stage (128 bytes of f16)
 constexpr int kPAStage = kPM * 128;          // 16 KB
 constexpr int kPBStage = kPN * 128;          // 32 KB
-constexpr int kPIStage = kPN * kPK;          // 16 KB of int8 codes
-constexpr int kPStages = 3;                  // A / B ring depth
-constexpr int kPIStages = 4;                 // int8 ring depth
+constexpr int kPAStages = 4;                 // A ring (TMA; freed by the MMA)
+constexpr int kPBStages = 3;                 // f16 B ring (converters; freed by the MMA)
 constexpr int kPConv = 8;                    // converter warps
 constexpr int kPThreads = 32 * 16;           // 0: TMA, 1..8: convert, 9: MMA, 12..15: epilogue
 constexpr int kPMmaWarp = 9;
 constexpr int kPEpiWarp0 = 12;
+constexpr int kPPairsAhead = 2;              // pairs of K steps a converter holds in registers
 
 enum { kPGateUp = 0, kPDown = 1 };
 
 struct PHead {
-  uint64_t a_full[kPStages];
-  uint64_t b_full[kPStages];
-  uint64_t ab_empty[kPStages];
-  uint64_t i_full[kPIStages];
-  uint64_t i_empty[kPIStages];
+  uint64_t a_full[kPAStages];
+  uint64_t a_empty[kPAStages];
+  uint64_t b_full[kPBStages];
+  uint64_t b_empty[kPBStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint32_t tmem;
@@ -70,7 +74,7 @@ struct PHead {
 };
 constexpr size_t kPHeadBytes = 1024;
 static_assert(sizeof(PHead) <= kPHeadBytes, "head too large");
-constexpr size_t kPSmem = kPHeadBytes + 1024 + (size_t)kPStages * (kPAStage + kPBStage) + (size_t)kPIStages * kPIStage;
+constexpr size_t kPSmem = kPHeadBytes + 1024 + (size_t)kPAStages * kPAStage + (size_t)kPBStages * kPBStage;
 
 __device__ __forceinline__ float p_pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
@@ -259,11 +263,77 @@ __device__ __forceinline__ bool work_at(const FfnArgs& A, const PrefillAux& X, i
   return true;
 }
 
+// Loads issued where they stand: the converters' prefetch only hides memory latency if the
+// compiler does not sink these loads down to the first use of their registers.
+__device__ __forceinline__ uint4 p_ld_codes(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint2 p_ld_scales(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+// What one converter thread needs of one pair of K steps (two 32-element blocks each): its
+// 16-byte chunk of the stored codes of each K step, and the four fp16 scales of the pair's four
+// blocks as one 8-byte word, for each of its four B rows.
+struct PPair {
+  uint4 q[2][4];  // [K step of the pair][row]
+  uint2 s[4];     // [row]
+};
+
+// A cursor over the CTA's sequence of (work item, pair of K steps), in the order the MMA consumes
+// them; it loads one thread's PPair straight from the expert record (global memory).
+template <int KIND>
+struct PCursor {
+  const uint8_t* qrow[4];
+  const __half* srow[4];
+  int w, kc;
+
+  __device__ __forceinline__ void seek(const FfnArgs& A, const PrefillAux& X, int w0, int nch, int n_work, int rb,
+                                       int c, int K) {
+    const int nb = K / kQBlock;
+    for (w = w0; w < n_work; w += gridDim.x) {
+      PWork wk;
+      if (!work_at<KIND>(A, X, w, nch, &wk)) continue;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = rb + 64 * i;
+        const int n = KIND == kPGateUp ? wk.n0 + (r & 127) : wk.n0 + r;
+        const uint64_t oq = KIND == kPGateUp ? (r < 128 ? A.o_gate_q : A.o_up_q) : A.o_down_q;
+        const uint64_t os = KIND == kPGateUp ? (r < 128 ? A.o_gate_s : A.o_up_s) : A.o_down_s;
+        qrow[i] = wk.rec + oq + (size_t)n * K + c * 16;
+        srow[i] = reinterpret_cast<const __half*>(wk.rec + os) + (size_t)n * nb;
+      }
+      kc = 0;
+      return;
+    }
+  }
+
+  // Loads the pair at the cursor and moves one pair forward; false past the CTA's last work.
+  __device__ __forceinline__ bool next(const FfnArgs& A, const PrefillAux& X, int nch, int n_work, int rb, int c,
+                                       int K, PPair& p) {
+    if (w >= n_work) return false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      p.q[0][i] = p_ld_codes(qrow[i] + kc * kPK);
+      p.q[1][i] = p_ld_codes(qrow[i] + kc * kPK + kPK);
+      p.s[i] = p_ld_scales(srow[i] + kc * 2);
+    }
+    kc += 2;
+    if (kc * kPK >= K) seek(A, X, w + gridDim.x, nch, n_work, rb, c, K);
+    return true;
+  }
+};
+
 template <int KIND>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, PrefillAux X,
-                                                                   const __grid_constant__ CUtensorMap tm_a,
-                                                                   const __grid_constant__ CUtensorMap tm_q_pool,
-                                                                   const __grid_constant__ CUtensorMap tm_q_shared) {
+                                                                   const __grid_constant__ CUtensorMap tm_a) {
   extern __shared__ __align__(1024) uint8_t dyn[];
   PHead& H = *reinterpret_cast<PHead*>(dyn);
   uint8_t* base = dyn + kPHeadBytes;
@@ -272,24 +342,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
     base += ((a + 1023u) & ~1023u) - a;
   }
   uint8_t* ringA = base;
-  uint8_t* ringB = ringA + kPStages * kPAStage;
-  uint8_t* ringI = ringB + kPStages * kPBStage;
+  uint8_t* ringB = ringA + kPAStages * kPAStage;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = KIND == kPGateUp ? A.d : A.f;
   const int KC = K / kPK;
   const int nch = KIND == kPGateUp ? A.f / 128 : A.d / kPN;
   const int n_work = X.n_tiles[0] * nch;
-  const int nb = K / kQBlock;  // scale blocks per B row
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPStages; ++s) {
+    for (int s = 0; s < kPAStages; ++s) {
       mbar_init(&H.a_full[s], 1);
-      mbar_init(&H.b_full[s], kPConv);
-      mbar_init(&H.ab_empty[s], 1);
+      mbar_init(&H.a_empty[s], 1);
     }
-    for (int s = 0; s < kPIStages; ++s) {
-      mbar_init(&H.i_full[s], 1);
-      mbar_init(&H.i_empty[s], kPConv);
+    for (int s = 0; s < kPBStages; ++s) {
+      mbar_init(&H.b_full[s], kPConv);
+      mbar_init(&H.b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&H.acc_full[b], 1);
@@ -298,8 +365,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
     H.abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_a);
-    prefetch_tmap(&tm_q_pool);
-    prefetch_tmap(&tm_q_shared);
   }
   if (warp == kPMmaWarp) {
     tmem_alloc(&H.tmem, 512);
@@ -311,106 +376,90 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
   const uint32_t tmem = H.tmem;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer of the A tiles ----------------
     if (lane == 0) {
-      int sa = 0, si = 0, issued = 0;
-      uint32_t pa = 0, pi = 0;
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
       for (int w = blockIdx.x; w < n_work && !p_aborted(H); w += gridDim.x) {
         PWork wk;
         if (!work_at<KIND>(A, X, w, nch, &wk)) continue;
-        const CUtensorMap* tq = wk.shared ? &tm_q_shared : &tm_q_pool;
         for (int kc = 0; kc < KC; ++kc) {
-          if (!mbar_wait(&H.ab_empty[sa], pa ^ 1u) || !mbar_wait(&H.i_empty[si], pi ^ 1u)) {
+          if (!mbar_wait(&H.a_empty[s], ph ^ 1u)) {
             p_set_abort(H, A.status);
             break;
           }
-          mbar_arrive_expect_tx(&H.a_full[sa], kPAStage);
-          tma_load_2d(ringA + (size_t)sa * kPAStage, &tm_a, kc * kPK, wk.rowA, &H.a_full[sa]);
-          mbar_arrive_expect_tx(&H.i_full[si], kPIStage);
-          if (KIND == kPGateUp)
-            tma_load_4d(ringI + (size_t)si * kPIStage, tq, kc * kPK, wk.n0, 0, wk.slot, &H.i_full[si]);
-          else
-            tma_load_3d(ringI + (size_t)si * kPIStage, tq, kc * kPK, wk.n0, wk.slot, &H.i_full[si]);
+          mbar_arrive_expect_tx(&H.a_full[s], kPAStage);
+          tma_load_2d(ringA + (size_t)s * kPAStage, &tm_a, kc * kPK, wk.rowA, &H.a_full[s]);
           ++issued;
-          if (++sa == kPStages) { sa = 0; pa ^= 1u; }
-          if (++si == kPIStages) { si = 0; pi ^= 1u; }
+          if (++s == kPAStages) { s = 0; ph ^= 1u; }
         }
       }
-      if (p_aborted(H)) {  // no copy may still be landing in shared memory when the CTA exits
-        for (int j = issued > kPStages ? issued - kPStages : 0; j < issued; ++j)
-          mbar_wait(&H.a_full[j % kPStages], (j / kPStages) & 1);
-        for (int j = issued > kPIStages ? issued - kPIStages : 0; j < issued; ++j)
-          mbar_wait(&H.i_full[j % kPIStages], (j / kPIStages) & 1);
-      }
+      if (p_aborted(H))  // no copy may still be landing in shared memory when the CTA exits
+        for (int j = issued > kPAStages ? issued - kPAStages : 0; j < issued; ++j)
+          mbar_wait(&H.a_full[j % kPAStages], (j / kPAStages) & 1);
     }
   } else if (warp >= 1 && warp <= kPConv) {
     // ---------------- converters ----------------
+    // Thread ct owns B rows rb + 64 i (i < 4) and 16-byte chunk c of each row's 64 stored codes
+    // per K step. Its codes and scales come straight from global memory, kPPairsAhead pairs of
+    // K steps ahead (crossing into the CTA's next work item), into registers: each slot of the
+    // register ring is consumed and then refilled in place, so no load is waited for early.
     const int ct = threadIdx.x - 32;  // 0..255
     const int rb = ct >> 2, c = ct & 3;
-    int sb = 0, si = 0;
-    uint32_t pb = 0, pi = 0;
-    for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
-      PWork wk;
-      if (!work_at<KIND>(A, X, w, nch, &wk)) continue;
-      // scale rows of this thread's four B rows rb + 64 i
-      const __half* srow[4];
+    int sb = 0;
+    uint32_t pb = 0;
+    PCursor<KIND> cur;
+    cur.seek(A, X, blockIdx.x, nch, n_work, rb, c, K);
+    PPair pp[kPPairsAhead];
+    bool have[kPPairsAhead];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = rb + 64 * i;
-        if (KIND == kPGateUp)
-          srow[i] = reinterpret_cast<const __half*>(wk.rec + (r < 128 ? A.o_gate_s : A.o_up_s)) +
-                    (size_t)(wk.n0 + (r & 127)) * nb;
-        else
-          srow[i] = reinterpret_cast<const __half*>(wk.rec + A.o_down_s) + (size_t)(wk.n0 + r) * nb;
+    for (int j = 0; j < kPPairsAhead; ++j) have[j] = cur.next(A, X, nch, n_work, rb, c, K, pp[j]);
+    bool ok = true;
+    while (ok && have[0]) {
+#pragma unroll
+      for (int j = 0; j < kPPairsAhead; ++j) {
+        if (!have[j]) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const bool w2 = mbar_wait(&H.b_empty[sb], pb ^ 1u);
+          if (!__all_sync(0xFFFFFFFFu, w2 && !p_aborted(H))) {
+            if (lane == 0) p_set_abort(H, A.status);
+            ok = false;
+            break;
+          }
+          uint8_t* dst = ringB + (size_t)sb * kPBStage;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = rb + 64 * i;
+            // this K step is one pair of blocks; their scales are the low and high half of one
+            // 32-bit word of the pair of K steps' scales
+            const uint32_t sw = h ? pp[j].s[i].y : pp[j].s[i].x;
+            const __half2 s01 = *reinterpret_cast<const __half2*>(&sw);
+            // stored chunk c: codes 8c..8c+7 of both blocks -> K-major chunks c and 4 + c
+            uint4 lo, hi;
+            codes_to_f16(pp[j].q[h][i], __low2half2(s01), __high2half2(s01), &lo, &hi);
+            // odd rows write their high chunk first, so that the 8 lanes of a store phase (two
+            // rows) hit 8 distinct 16-byte bank groups
+            const bool odd = (r & 1) != 0;
+            const int ch_lo = c ^ (r & 7), ch_hi = (4 + c) ^ (r & 7);
+            *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_hi : ch_lo) << 4)) = odd ? hi : lo;
+            *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_lo : ch_hi) << 4)) = odd ? lo : hi;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&H.b_full[sb]);
+          if (++sb == kPBStages) { sb = 0; pb ^= 1u; }
+        }
+        if (!ok) break;
+        have[j] = cur.next(A, X, nch, n_work, rb, c, K, pp[j]);
       }
-      bool ok = true;
-      for (int kc = 0; kc < KC; ++kc) {
-        // this K step is one pair of blocks: 2 kc and 2 kc + 1
-        __half s0[4], s1[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          s0[i] = srow[i][kc * 2];
-          s1[i] = srow[i][kc * 2 + 1];
-        }
-        const bool w1 = mbar_wait(&H.i_full[si], pi), w2 = mbar_wait(&H.ab_empty[sb], pb ^ 1u);
-        if (!__all_sync(0xFFFFFFFFu, w1 && w2 && !p_aborted(H))) {
-          if (lane == 0) p_set_abort(H, A.status);
-          ok = false;
-          break;
-        }
-        const uint8_t* src = ringI + (size_t)si * kPIStage;
-        uint8_t* dst = ringB + (size_t)sb * kPBStage;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = rb + 64 * i;
-          // stored chunk c: codes 8c..8c+7 of both blocks -> K-major chunks c and 4 + c
-          const uint4 q = *reinterpret_cast<const uint4*>(src + r * kPK + c * 16);
-          uint4 lo, hi;
-          codes_to_f16(q, __half2half2(s0[i]), __half2half2(s1[i]), &lo, &hi);
-          // odd rows write their high chunk first, so that the 8 lanes of a store phase (two
-          // rows) hit 8 distinct 16-byte bank groups
-          const bool odd = (r & 1) != 0;
-          const int ch_lo = c ^ (r & 7), ch_hi = (4 + c) ^ (r & 7);
-          *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_hi : ch_lo) << 4)) = odd ? hi : lo;
-          *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_lo : ch_hi) << 4)) = odd ? lo : hi;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&H.i_empty[si]);
-          mbar_arrive(&H.b_full[sb]);
-        }
-        if (++sb == kPStages) { sb = 0; pb ^= 1u; }
-        if (++si == kPIStages) { si = 0; pi ^= 1u; }
-      }
-      if (!ok) break;
     }
   } else if (warp == kPMmaWarp) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = f16_idesc(kPM, kPN);
-      int s = 0, lt = 0;
-      uint32_t p = 0;
+      int sa = 0, sb = 0, lt = 0;
+      uint32_t pa = 0, pb = 0;
       for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
         PWork wk;
         if (!work_at<KIND>(A, X, w, nch, &wk)) continue;
@@ -423,18 +472,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
         const uint32_t d_tmem = tmem + (uint32_t)(buf * kPN);
         bool ok = true;
         for (int kc = 0; kc < KC; ++kc) {
-          if (!mbar_wait(&H.a_full[s], p) || !mbar_wait(&H.b_full[s], p) || p_aborted(H)) {
+          if (!mbar_wait(&H.a_full[sa], pa) || !mbar_wait(&H.b_full[sb], pb) || p_aborted(H)) {
             p_set_abort(H, A.status);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(ringA + (size_t)s * kPAStage), b_addr = smem_u32(ringB + (size_t)s * kPBStage);
+          const uint32_t a_addr = smem_u32(ringA + (size_t)sa * kPAStage);
+          const uint32_t b_addr = smem_u32(ringB + (size_t)sb * kPBStage);
 #pragma unroll
           for (int k = 0; k < kPK / 16; ++k)
             umma_f16(d_tmem, sw128_desc(a_addr + k * 32), sw128_desc(b_addr + k * 32), idesc, (kc | k) != 0);
-          umma_commit(&H.ab_empty[s]);
-          if (++s == kPStages) { s = 0; p ^= 1u; }
+          umma_commit(&H.a_empty[sa]);
+          umma_commit(&H.b_empty[sb]);
+          if (++sa == kPAStages) { sa = 0; pa ^= 1u; }
+          if (++sb == kPBStages) { sb = 0; pb ^= 1u; }
         }
         if (!ok) break;
         umma_commit(&H.acc_full[buf]);
@@ -558,42 +610,17 @@ bool encode_a(CUtensorMap* m, const void* base, int K, int rows) {
   return p_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Codes of the gate/up matrices of n records: (K byte, row, gate|up, slot), boxes 64 x 128 x 2.
-bool encode_q_gu(CUtensorMap* m, const uint8_t* recs, uint64_t n, const FfnArgs& a, uint64_t slot_bytes) {
-  const cuuint64_t dims[4] = {(cuuint64_t)a.d, (cuuint64_t)a.f, 2, n};
-  const cuuint64_t strides[3] = {(cuuint64_t)a.d, (cuuint64_t)(a.o_up_q - a.o_gate_q), slot_bytes};
-  const cuuint32_t box[4] = {kPK, 128, 2, 1};
-  return p_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, recs + a.o_gate_q, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-// Codes of the down matrix of n records: (K byte, row, slot), boxes 64 x 256.
-bool encode_q_dn(CUtensorMap* m, const uint8_t* recs, uint64_t n, const FfnArgs& a, uint64_t slot_bytes) {
-  const cuuint64_t dims[3] = {(cuuint64_t)a.f, (cuuint64_t)a.d, n};
-  const cuuint64_t strides[2] = {(cuuint64_t)a.f, slot_bytes};
-  const cuuint32_t box[3] = {kPK, kPN, 1};
-  return p_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, recs + a.o_down_q, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
 }  // namespace
 
 bool prefill_supported(const FfnArgs& a) {
   return a.xdt == 0 && a.d % kPN == 0 && a.f % 128 == 0 && p_encode_fn() != nullptr;
 }
 
-cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, const void* pool, const void* shared,
-                               uint64_t n_slots, uint64_t slot_bytes, int sm_count, cudaStream_t st) {
+cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, int sm_count, cudaStream_t st) {
   const int rows = a.P + a.T * a.n_shared;
   if (rows == 0) return cudaSuccess;
-  CUtensorMap tm_x, tm_h, qgu_pool, qgu_sh, qdn_pool, qdn_sh;
-  const uint8_t* pl = static_cast<const uint8_t*>(pool);
-  const uint8_t* sh = a.n_shared > 0 ? static_cast<const uint8_t*>(shared) : pl;
-  const uint64_t nsh = a.n_shared > 0 ? (uint64_t)a.n_shared : 1;
-  if (!encode_a(&tm_x, x.xp16, a.d, rows) || !encode_a(&tm_h, x.h16, a.f, rows) ||
-      !encode_q_gu(&qgu_pool, pl, n_slots, a, slot_bytes) || !encode_q_gu(&qgu_sh, sh, nsh, a, slot_bytes) ||
-      !encode_q_dn(&qdn_pool, pl, n_slots, a, slot_bytes) || !encode_q_dn(&qdn_sh, sh, nsh, a, slot_bytes))
-    return cudaErrorInvalidValue;
+  CUtensorMap tm_x, tm_h;
+  if (!encode_a(&tm_x, x.xp16, a.d, rows) || !encode_a(&tm_h, x.h16, a.f, rows)) return cudaErrorInvalidValue;
   prefill_prepare_kernel<<<a.T, 256, 0, st>>>(a, x);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -604,11 +631,11 @@ cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, const void
   auto dn = prefill_gemm_kernel<kPDown>;
   if ((e = ensure_dynamic_smem(reinterpret_cast<const void*>(gu), kPSmem)) != cudaSuccess) return e;
   if ((e = ensure_dynamic_smem(reinterpret_cast<const void*>(dn), kPSmem)) != cudaSuccess) return e;
-  gu<<<sm_count, kPThreads, kPSmem, st>>>(a, x, tm_x, qgu_pool, qgu_sh);
+  gu<<<sm_count, kPThreads, kPSmem, st>>>(a, x, tm_x);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   prefill_convert_h_kernel<<<grid_rows, 256, 0, st>>>(a, x);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dn<<<sm_count, kPThreads, kPSmem, st>>>(a, x, tm_h, qdn_pool, qdn_sh);
+  dn<<<sm_count, kPThreads, kPSmem, st>>>(a, x, tm_h);
   return cudaGetLastError();
 }
 

@@ -164,8 +164,7 @@ cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_cou
 bool persist_supported(const FfnArgs& a, int sm_count);
 // Tensor-core grouped GEMM for many tokens per expert (bf16 x); prefill_supported() says whether
 // the shape fits (d a multiple of 256, f of 128).
-cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, const void* pool, const void* shared,
-                               uint64_t n_slots, uint64_t slot_bytes, int sm_count, cudaStream_t st);
+cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, int sm_count, cudaStream_t st);
 bool prefill_supported(const FfnArgs& a);
 int device_sm_count();
 cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,
