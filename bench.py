@@ -603,7 +603,17 @@ def run_tiered(args, ws, rank, local, w):
 
     set_routers()
     s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
-    ts = TieredStack(s, w.layers, routers, h_records, w.slots, rb, shared, device=dev)
+    policy = L.MOE_SLOT_FREQ if args.slot_policy == "freq" else L.MOE_SLOT_LRU
+    profile = None
+    if args.warm_profile:
+        # the usage profile a deployment would ship: each expert's inclusion frequency under the
+        # routing at step 0 (before any drift)
+        _, freq = synth.zipf_column_scales(w.E, w.k, w.zipf_s, w.seed)
+        profile = np.zeros(n_all, dtype=np.float32)
+        for l in range(w.layers):
+            profile[l * w.E + perms[l]] = freq
+    ts = TieredStack(s, w.layers, routers, h_records, w.slots, rb, shared, device=dev, policy=policy,
+                     half_life_steps=args.half_life_steps, profile=profile)
     n_batches = 16
     x_host = [torch.from_numpy(w.x_bits(b).astype(np.int16)).view(torch.bfloat16).pin_memory()
               for b in range(n_batches)]
@@ -677,7 +687,10 @@ def run_tiered(args, ws, rank, local, w):
                    "timing": "wall clock per step (the host reads each layer's active list), x copied in and "
                              "the output copied out inside every step",
                    "parallelism": f"replicas x{ws}"},
-        "slot_pool": {"hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
+        "slot_pool": {"policy": "LRU" if policy == L.MOE_SLOT_LRU else
+                      f"decayed use count (half-life {args.half_life_steps:g} steps)",
+                      "warm_profile": bool(args.warm_profile), "warm_loads": ts.n_warm,
+                      "hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
                       "evictions": s1.evictions - s0.evictions, "h2d_gbs": h2d / wall / 1e9,
                       "h2d_bytes_per_step": h2d / K, "cold_start_misses": s0.misses},
         "roofline": {"kernel": "miss copies (pinned host to device slots)", "bound": "pcie",
@@ -702,6 +715,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-gb", type=float, default=24.0, help="pinned host memory for expert images (tiered)")
+    ap.add_argument("--slot-policy", choices=["lru", "freq"], default="lru",
+                    help="tiered: replacement policy of the slot pool (LRU, or decayed use count)")
+    ap.add_argument("--half-life-steps", type=float, default=50.0, help="tiered, freq: half-life of the use counts")
+    ap.add_argument("--warm-profile", action="store_true",
+                    help="tiered: fill the pool from a usage profile before the first step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -243,15 +243,23 @@ const char* moe_last_error_string(void);
  * Slot table: an expert cache for experts that do not all fit in device memory
  * ([P2] "专家缓存" and "三级存储分工": the most used experts stay in VRAM, all experts
  * sit pinned in host RAM; [P2] "长文本": expert copies overlap with computation).
- * The table keeps, on the host, an LRU order over n_slots device slots and the owner
- * (layer, expert) of each slot. The device table d_slot_of [L][E] lives in caller memory.
- * Row `layer` of it is what moe_expert_ffn reads through moe_expert_table.slot_of.
+ * The table keeps, on the host, the owner (layer, expert) of each of n_slots device slots,
+ * their LRU order, and a decayed use count of every (layer, expert) ([P2] "专家缓存": the
+ * cache starts from a ranking of expert use and adapts to what the session uses most). The
+ * device table d_slot_of [L][E] lives in caller memory. Row `layer` of it is what
+ * moe_expert_ffn reads through moe_expert_table.slot_of.
  * ------------------------------------------------------------------------------------ */
 typedef struct moe_slot_table moe_slot_table;
 
 typedef struct {
   uint64_t hits, misses, evictions, bytes_h2d;
 } moe_slot_stats;
+
+/* Replacement policy (slot_table_set_policy). */
+typedef enum {
+  MOE_SLOT_LRU = 0,  /* evict the least recently used slot (the default) */
+  MOE_SLOT_FREQ = 1  /* evict the slot whose owner has the smallest decayed use count */
+} moe_slot_policy;
 
 /* Copies `bytes` from host `h_src` to device `d_dst` on `stream`; returns 0 on success.
  * The default copier is cudaMemcpyAsync. A caller can pass its own (e.g. to add tracing,
@@ -269,8 +277,12 @@ moe_status slot_table_create(moe_slot_table** out, int32_t L, int32_t E, int32_t
 
 /* Makes every expert of h_active[0..n_active) (host array) resident for `layer`:
  *  - a resident expert is a hit; it moves to the most-recently-used end;
- *  - a miss takes the least-recently-used slot whose owner is not in h_active (an empty
- *    slot first), is copied from h_records on copy_stream, and is marked most recent;
+ *  - every expert of h_active counts one use (see slot_table_set_policy);
+ *  - a miss takes, among the slots whose owner is not in h_active, an empty slot first, else
+ *    the policy's victim: the least recently used slot (MOE_SLOT_LRU) or the slot whose
+ *    owner has the smallest decayed use count, ties to the least recently used and then
+ *    the lowest slot index (MOE_SLOT_FREQ). It is copied from h_records on copy_stream and
+ *    marked most recent;
  *  - the changed entries of row `layer` of d_slot_of are then written on copy_stream, and
  *    `ready` (if not NULL) is recorded on copy_stream after all copies.
  * A compute stream that waits on `ready` sees the new row. Hits can run before `ready`.
@@ -283,6 +295,24 @@ moe_status slot_table_update(moe_slot_table* table, int32_t layer, const int32_t
                              int32_t n_active, moe_stream_t copy_stream, moe_event_t ready,
                              int32_t* h_hits, int32_t* n_hits, int32_t* h_misses,
                              int32_t* n_misses, moe_slot_stats* stats_opt);
+
+/* Sets the replacement policy (MOE_SLOT_LRU or MOE_SLOT_FREQ) and the half-life of the use
+ * counts, in slot_table_update calls (> 0, finite): a use made h calls ago weighs 2^(-h /
+ * half_life) of a use made now. Counts are kept under both policies (with no decay until a
+ * half-life is set), so the policy can change at any time. MOE_EINVAL otherwise. */
+moe_status slot_table_set_policy(moe_slot_table* table, int32_t policy, double half_life);
+
+/* Warm start from a usage profile ([P2] "专家缓存": a shipped ranking of expert use decides
+ * which experts start in VRAM). h_weight: host float [L*E] of use weights (>= 0, finite;
+ * one use = 1), added to the use counts. Then the empty slots, lowest index first, take the
+ * non-resident experts of positive weight in decreasing order of use count (ties: lower
+ * l*E + e first); their records are copied on copy_stream, the changed entries of d_slot_of
+ * written after them, and `ready` (if not NULL) recorded. Nothing is evicted. *n_loaded (if
+ * not NULL) receives the number of experts copied; bytes_h2d counts them, hits and misses do
+ * not. MOE_EINVAL for a NULL table or weights or a negative or non-finite weight (nothing
+ * changed); MOE_ECUDA if a copy fails (the experts copied before it stay resident). */
+moe_status slot_table_warm(moe_slot_table* table, const float* h_weight, moe_stream_t copy_stream,
+                           moe_event_t ready, int32_t* n_loaded);
 
 /* Cumulative counters since creation. */
 moe_status slot_table_stats(const moe_slot_table* table, moe_slot_stats* out);

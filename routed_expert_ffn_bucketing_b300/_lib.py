@@ -18,6 +18,7 @@ MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA, MOE_ENOSLOT, MOE_EDEVICE = 0, -
 MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_EXPERT, MOE_DEV_MISSING_SLOT, MOE_DEV_TIMEOUT, MOE_DEV_BAD_SLOT = 0x1, 0x2, 0x4, 0x8, 0x10
 MOE_BF16, MOE_F32 = 0, 1
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
+MOE_SLOT_LRU, MOE_SLOT_FREQ = 0, 1
 
 _STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_EUNSUPPORTED", -3: "MOE_ECUDA", -4: "MOE_ENOSLOT",
                  -5: "MOE_EDEVICE"}
@@ -68,6 +69,8 @@ _SIGS = {
                                     MOE_COPY_FN, _P]),
     "slot_table_update": (C.c_int, [_P, C.c_int32, _P, C.c_int32, _P, _P, _P, _P, _P, _P,
                                     C.POINTER(moe_slot_stats)]),
+    "slot_table_set_policy": (C.c_int, [_P, C.c_int32, C.c_double]),
+    "slot_table_warm": (C.c_int, [_P, _P, _P, _P, _P]),
     "slot_table_stats": (C.c_int, [_P, C.POINTER(moe_slot_stats)]),
     "slot_table_snapshot": (C.c_int, [_P, _P]),
     "slot_table_destroy": (C.c_int, [_P]),
@@ -214,6 +217,19 @@ def slot_table_update(table, layer, h_active, n_active, copy_stream, ready, h_hi
     if st < 0 and st != MOE_ENOSLOT:
         raise MoeError(st, "slot_table_update", "")
     return st
+
+
+def slot_table_set_policy(table, policy: int, half_life: float) -> None:
+    """policy: MOE_SLOT_LRU or MOE_SLOT_FREQ; half_life in slot_table_update calls."""
+    _check(lib().slot_table_set_policy(table, policy, half_life), "slot_table_set_policy")
+
+
+def slot_table_warm(table, h_weight, copy_stream=None, ready=None) -> int:
+    """h_weight: host address (int) of float32 [L*E] use weights. Returns the number of
+    experts copied into empty slots."""
+    n = C.c_int32()
+    _check(lib().slot_table_warm(table, h_weight, copy_stream, ready, C.byref(n)), "slot_table_warm")
+    return n.value
 
 
 def slot_table_stats(table) -> moe_slot_stats:

@@ -5,13 +5,27 @@
 // are cached one at a time, not one layer at a time. Section "长文本": expert copies over PCIe
 // overlap with computation.
 //
+// The same section says the cache starts from a shipped ranking of expert use and then learns
+// which experts the current session uses most. Two replacement policies:
+//   LRU  (default): a miss takes the least recently used slot that the current call does not
+//        need;
+//   FREQ: a miss takes the slot whose owner has the smallest use count decayed by half every
+//        `half_life` update calls (ties: least recently used, then the lowest slot index).
+// A profile of use weights can seed the counts and fill the empty slots (slot_table_warm).
+//
 // Host state: the owner (layer, expert) of each of n_slots device slots, an LRU list of
-// slots (head = least recently used), and a host mirror of the device table slot_of[L][E].
-// A miss takes the least recently used slot that the current call does not need. The
-// record is copied from pinned host memory on the caller's copy stream. Every table entry
-// that changed (the new owner, and the evicted owner in whatever layer it belonged to) is
-// then written to the device table on the same stream, so a compute stream that waits on
-// `ready` sees a table that matches the slot contents.
+// slots (head = least recently used), a min-heap of slots by decayed count, the decayed
+// count and last use of every (layer, expert), and a host mirror of the device table
+// slot_of[L][E]. The record of a miss is copied from pinned host memory on the caller's copy
+// stream. Every table entry that changed (the new owner, and the evicted owner in whatever
+// layer it belonged to) is then written to the device table on the same stream, so a compute
+// stream that waits on `ready` sees a table that matches the slot contents.
+//
+// Decay without touching every count: a use adds inc = g^c (g = 2^(1/half_life), c the
+// number of update calls so far) to the expert's count, which orders counts exactly as
+// decayed counts would. When inc passes 2^600 all counts and inc are multiplied by 2^-600
+// (exact in binary floating point; counts that underflow were last used hundreds of
+// half-lives ago).
 //
 // Protocol: call slot_table_update for a layer only after the computation that read the
 // slots of the previous update has completed (e.g. the host waited on an event recorded
@@ -19,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -42,6 +57,14 @@ struct moe_slot_table {
   std::vector<uint32_t> mark;  // [E] epoch marks: expert is in the current call's active set
   uint32_t epoch = 0;
   moe_slot_stats stats{};
+  // decayed use counts
+  int32_t policy = MOE_SLOT_LRU;
+  double g = 1.0, inc = 1.0;   // per-call growth of a use's weight, and the current weight
+  int64_t calls = 0;
+  std::vector<double> score;     // [L*E]
+  std::vector<int64_t> last_use; // [L*E]: call number of the last use, -1 never
+  std::vector<int32_t> heap, hpos;  // min-heap of slots by (count, last use, slot); hpos[slot]
+  std::vector<uint8_t> pinned;      // [n_slots]: owner is in the current call (never a victim)
 };
 
 namespace {
@@ -64,6 +87,68 @@ void lru_push_tail(moe_slot_table* t, int32_t s) {
   t->next[s] = -1;
   if (t->tail >= 0) t->next[t->tail] = s; else t->head = s;
   t->tail = s;
+}
+
+// Heap order of slots: pinned slots last, empty slots first, then by decayed count, last use
+// and slot index.
+bool slot_less(const moe_slot_table* t, int32_t a, int32_t b) {
+  if (t->pinned[a] != t->pinned[b]) return t->pinned[b];
+  if (t->pinned[a]) return a < b;
+  const int64_t oa = t->owner[a], ob = t->owner[b];
+  if ((oa < 0) != (ob < 0)) return oa < 0;
+  if (oa >= 0) {
+    if (t->score[oa] != t->score[ob]) return t->score[oa] < t->score[ob];
+    if (t->last_use[oa] != t->last_use[ob]) return t->last_use[oa] < t->last_use[ob];
+  }
+  return a < b;
+}
+
+void heap_swap(moe_slot_table* t, int32_t i, int32_t j) {
+  std::swap(t->heap[i], t->heap[j]);
+  t->hpos[t->heap[i]] = i;
+  t->hpos[t->heap[j]] = j;
+}
+
+void heap_sift_down(moe_slot_table* t, int32_t i) {
+  const int32_t n = (int32_t)t->heap.size();
+  for (;;) {
+    const int32_t l = 2 * i + 1, r = l + 1;
+    int32_t m = i;
+    if (l < n && slot_less(t, t->heap[l], t->heap[m])) m = l;
+    if (r < n && slot_less(t, t->heap[r], t->heap[m])) m = r;
+    if (m == i) break;
+    heap_swap(t, i, m);
+    i = m;
+  }
+}
+
+// Restores the heap order after the key of slot s changed. Only valid when no other key has
+// changed since the heap was last in order: each change is fixed before the next one.
+void heap_fix(moe_slot_table* t, int32_t s) {
+  int32_t i = t->hpos[s];
+  while (i > 0) {
+    const int32_t p = (i - 1) / 2;
+    if (!slot_less(t, t->heap[i], t->heap[p])) break;
+    heap_swap(t, i, p);
+    i = p;
+  }
+  heap_sift_down(t, i);
+}
+
+// Rebuilds the heap bottom-up after many keys changed at once.
+void heap_rebuild(moe_slot_table* t) {
+  for (int32_t i = (int32_t)t->heap.size() / 2 - 1; i >= 0; --i) heap_sift_down(t, i);
+}
+
+// Starts a new update call: the weight of a use grows by g, with the rescale described above.
+void advance_clock(moe_slot_table* t) {
+  ++t->calls;
+  t->inc *= t->g;
+  if (t->inc > 0x1p600) {
+    for (double& v : t->score) v *= 0x1p-600;
+    t->inc *= 0x1p-600;
+    heap_rebuild(t);  // counts that underflowed to equal values now tie
+  }
 }
 
 // Write the changed entries of the device table, one copy per run of adjacent keys.
@@ -122,6 +207,12 @@ moe_status slot_table_create(moe_slot_table** out, int32_t L, int32_t E, int32_t
   t->next.assign(n_slots, -1);
   for (int32_t s = 0; s < n_slots; ++s) lru_push_tail(t, s);
   t->mark.assign(E, 0);
+  t->score.assign((size_t)L * E, 0.0);
+  t->last_use.assign((size_t)L * E, -1);
+  t->pinned.assign(n_slots, 0);
+  t->heap.resize(n_slots);
+  t->hpos.resize(n_slots);
+  for (int32_t s = 0; s < n_slots; ++s) t->heap[s] = t->hpos[s] = s;
   if (d_slot_of) {
     if (t->default_copier) {
       if (cudaMemcpy(d_slot_of, t->mirror, mbytes, cudaMemcpyHostToDevice) != cudaSuccess) {
@@ -160,14 +251,23 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
     std::snprintf(g_slot_err, sizeof(g_slot_err), "%d misses, %d evictable slots", nm, t->n_slots - nh);
     return MOE_ENOSLOT;
   }
-  // hits first: most recently used, so that no miss evicts them
+  advance_clock(t);
+  // every expert of the call counts one use; hits first become most recently used and
+  // pinned, so that no miss evicts them (each slot's new key is fixed before the next change)
+  std::vector<int32_t> pins;
+  pins.reserve(n_active);
   nh = nm = 0;
   for (int32_t i = 0; i < n_active; ++i) {
     const int32_t e = h_active[i];
+    t->score[base + e] += t->inc;
+    t->last_use[base + e] = t->calls;
     const int32_t s = t->mirror[base + e];
     if (s >= 0) {
       lru_unlink(t, s);
       lru_push_tail(t, s);
+      t->pinned[s] = 1;
+      heap_fix(t, s);
+      pins.push_back(s);
       if (h_hits) h_hits[nh] = e;
       ++nh;
     }
@@ -177,7 +277,8 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
   for (int32_t i = 0; i < n_active; ++i) {
     const int32_t e = h_active[i];
     if (t->mirror[base + e] >= 0) continue;
-    const int32_t s = t->head;  // least recently used; never one of this call's experts
+    // LRU: the list's head; FREQ: the heap's root. Neither is one of this call's experts.
+    const int32_t s = t->policy == MOE_SLOT_FREQ ? t->heap[0] : t->head;
     const int64_t old = t->owner[s];
     if (old >= 0) {
       t->mirror[old] = -1;
@@ -187,6 +288,7 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
     t->owner[s] = -1;
     lru_unlink(t, s);
     lru_push_tail(t, s);
+    heap_fix(t, s);
     const int cr = t->copy_fn(t->d_pool + (uint64_t)s * t->slot_bytes, t->h_records[base + e], t->slot_bytes,
                               copy_stream, t->copy_user);
     if (cr != 0) {
@@ -196,11 +298,18 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
     }
     t->owner[s] = base + e;
     t->mirror[base + e] = s;
+    t->pinned[s] = 1;
+    heap_fix(t, s);
+    pins.push_back(s);
     changed.push_back(base + e);
     t->stats.misses++;
     t->stats.bytes_h2d += t->slot_bytes;
     if (h_misses) h_misses[nm] = e;
     ++nm;
+  }
+  for (const int32_t s : pins) {
+    t->pinned[s] = 0;
+    heap_fix(t, s);
   }
   t->stats.hits += nh;
   if (write_entries(t, changed, copy_stream) != 0 && rc == MOE_OK) rc = MOE_ECUDA;
@@ -210,6 +319,62 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
   if (n_hits) *n_hits = nh;
   if (n_misses) *n_misses = nm;
   if (stats_opt) *stats_opt = t->stats;
+  return rc;
+}
+
+moe_status slot_table_set_policy(moe_slot_table* t, int32_t policy, double half_life) {
+  if (!t || (policy != MOE_SLOT_LRU && policy != MOE_SLOT_FREQ) || !(half_life > 0.0) || !std::isfinite(half_life))
+    return MOE_EINVAL;
+  t->policy = policy;
+  t->g = std::pow(2.0, 1.0 / half_life);
+  return MOE_OK;
+}
+
+moe_status slot_table_warm(moe_slot_table* t, const float* h_weight, moe_stream_t copy_stream, moe_event_t ready,
+                           int32_t* n_loaded) {
+  if (!t || !h_weight) return MOE_EINVAL;
+  const int64_t n_keys = (int64_t)t->L * t->E;
+  for (int64_t i = 0; i < n_keys; ++i)
+    if (!(h_weight[i] >= 0.0f) || !std::isfinite(h_weight[i])) return MOE_EINVAL;
+  for (int64_t i = 0; i < n_keys; ++i) t->score[i] += (double)h_weight[i] * t->inc;
+  heap_rebuild(t);
+  // empty slots, lowest index first, take the best non-resident experts with a positive weight
+  std::vector<int32_t> empty;
+  for (int32_t s = 0; s < t->n_slots; ++s)
+    if (t->owner[s] < 0) empty.push_back(s);
+  std::vector<int64_t> cand;
+  for (int64_t i = 0; i < n_keys; ++i)
+    if (t->mirror[i] < 0 && h_weight[i] > 0.0f) cand.push_back(i);
+  const size_t n = std::min(empty.size(), cand.size());
+  std::partial_sort(cand.begin(), cand.begin() + n, cand.end(), [t](int64_t a, int64_t b) {
+    return t->score[a] != t->score[b] ? t->score[a] > t->score[b] : a < b;
+  });
+  std::vector<int64_t> changed;
+  moe_status rc = MOE_OK;
+  int32_t loaded = 0;
+  for (size_t j = 0; j < n; ++j) {
+    const int32_t s = empty[j];
+    const int64_t key = cand[j];
+    const int cr = t->copy_fn(t->d_pool + (uint64_t)s * t->slot_bytes, t->h_records[key], t->slot_bytes, copy_stream,
+                              t->copy_user);
+    if (cr != 0) {
+      std::snprintf(g_slot_err, sizeof(g_slot_err), "warm copy of layer %lld expert %lld failed (%d)",
+                    (long long)(key / t->E), (long long)(key % t->E), cr);
+      rc = MOE_ECUDA;
+      break;
+    }
+    t->owner[s] = key;
+    t->mirror[key] = s;
+    heap_fix(t, s);
+    changed.push_back(key);
+    t->stats.bytes_h2d += t->slot_bytes;
+    ++loaded;
+  }
+  if (write_entries(t, changed, copy_stream) != 0 && rc == MOE_OK) rc = MOE_ECUDA;
+  if (ready && cudaEventRecord(reinterpret_cast<cudaEvent_t>(ready), reinterpret_cast<cudaStream_t>(copy_stream)) !=
+                   cudaSuccess && rc == MOE_OK)
+    rc = MOE_ECUDA;
+  if (n_loaded) *n_loaded = loaded;
   return rc;
 }
 

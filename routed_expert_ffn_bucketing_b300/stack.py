@@ -12,6 +12,7 @@ from __future__ import annotations
 import ctypes as C
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 from . import _lib as L
@@ -60,8 +61,10 @@ class DecodeStack:
 
 class TieredStack:
     """L layers whose E routed experts per layer live in pinned host memory; a pool of n_slots
-    device slots caches them (the library's slot table: LRU over slots, misses copied on a side
-    stream). Shared experts stay resident.
+    device slots caches them (the library's slot table, misses copied on a side stream). Shared
+    experts stay resident. The replacement policy is LRU, or with policy=MOE_SLOT_FREQ the
+    decayed use count (half-life in steps, one step = one pass over the L layers); profile
+    (float32 [L*E] use weights) seeds the counts and fills the empty pool before the first step.
 
     Per layer: route and bucket on the compute stream; read the active list on the host; update
     the slot table (miss copies on the copy stream, `ready` recorded after them). With overlap
@@ -70,7 +73,8 @@ class TieredStack:
     waited on `ready`. Without overlap one FFN call runs after the wait. Then the combine."""
 
     def __init__(self, shape: L.moe_shape, n_layers: int, routers: list[torch.Tensor], h_records: list[int],
-                 n_slots: int, slot_bytes: int, shared: list[torch.Tensor], device="cuda"):
+                 n_slots: int, slot_bytes: int, shared: list[torch.Tensor], device="cuda",
+                 policy: int = L.MOE_SLOT_LRU, half_life_steps: float = 50.0, profile=None):
         self.shape, self.L, self.routers = shape, n_layers, routers
         self.shape_routed = L.shape(shape.T, shape.d, shape.f, shape.E, shape.k, 0)
         self.n_slots, self.slot_bytes = n_slots, slot_bytes
@@ -96,6 +100,15 @@ class TieredStack:
         self.d_misses = torch.zeros(1 + cap, dtype=torch.int32, device=device)
         self.stats = L.moe_slot_stats()
         self.layer_misses: list[int] = []
+        if policy != L.MOE_SLOT_LRU:
+            L.slot_table_set_policy(self.table, policy, half_life_steps * n_layers)
+        self.n_warm = 0
+        if profile is not None:
+            w = np.ascontiguousarray(profile, dtype=np.float32)
+            assert w.size == n_layers * shape.E
+            self.n_warm = L.slot_table_warm(self.table, w.ctypes.data, self.copy_stream.cuda_stream,
+                                            self.ready.cuda_event)
+            self.ready.synchronize()
 
     def close(self):
         if self.table:

@@ -224,3 +224,204 @@ def test_slot_table_copy_failure_is_reported_and_not_resident():
     st, hits, miss = _update(h, 0, [4, 5, 6])
     assert st == 0 and hits == [4] and miss == [5, 6]
     L.slot_table_destroy(h)
+
+
+# ---------------------------------------------------------------- decayed-frequency policy ----
+
+def _freq_table(Lyr, E, n_slots, half_life, policy=None):
+    h, cp, hrec = _make_table(Lyr, E, n_slots)
+    L.slot_table_set_policy(h, L.MOE_SLOT_FREQ if policy is None else policy, half_life)
+    return h, cp, hrec
+
+
+def _resident(h, Lyr, E):
+    snap = _snapshot(h, Lyr, E)
+    return {(l, e) for l in range(Lyr) for e in range(E) if snap[l, e] >= 0}
+
+
+def test_slot_table_freq_keeps_the_more_used_expert():
+    # pool of 2; expert 0 used twice, expert 1 once, then expert 2 misses
+    for policy, evicted in ((L.MOE_SLOT_FREQ, 1), (L.MOE_SLOT_LRU, 0)):
+        h, cp, _ = _freq_table(1, 8, 2, 1e9, policy)
+        for ids in ([0], [0], [1]):
+            _update(h, 0, ids)
+        st, hits, miss = _update(h, 0, [2])
+        assert st == 0 and miss == [2]
+        assert _resident(h, 1, 8) == {(0, 2), (0, 1 - evicted)}
+        L.slot_table_destroy(h)
+
+
+def test_slot_table_freq_counts_decay_with_the_half_life():
+    # expert 0 used at calls 1..3, expert 1 at call 4; at call 5 a miss needs a slot.
+    # half-life 1 call: 2^-4 + 2^-3 + 2^-2 = 0.4375 < 2^-1, so expert 0 goes;
+    # no decay: 3 uses against 1, so expert 1 goes.
+    for hl, keep in ((1.0, 1), (1e9, 0)):
+        h, cp, _ = _freq_table(1, 8, 2, hl)
+        for ids in ([0], [0], [0], [1]):
+            _update(h, 0, ids)
+        _update(h, 0, [5])
+        assert _resident(h, 1, 8) == {(0, 5), (0, keep)}
+        L.slot_table_destroy(h)
+
+
+def test_slot_table_freq_never_evicts_current_experts():
+    # expert 0 has the smallest count but is in the call, so the miss takes expert 1's slot
+    h, cp, _ = _freq_table(1, 8, 2, 1e9)
+    for ids in ([1], [1], [1], [0]):
+        _update(h, 0, ids)
+    st, hits, miss = _update(h, 0, [0, 2])
+    assert hits == [0] and miss == [2]
+    assert _resident(h, 1, 8) == {(0, 0), (0, 2)}
+    L.slot_table_destroy(h)
+
+
+class _FreqModel:
+    """The decayed-frequency rule as stated in include/moe.h, by brute force: a use made now
+    weighs inc (inc grows by 2^(1/half_life) per call, rescaled by 2^-600 past 2^600); a miss
+    takes an empty slot (lowest index) or the unpinned slot whose owner has the smallest
+    (count, last use), lowest slot index on ties."""
+
+    def __init__(self, Lyr, E, n, hl):
+        self.E, self.n, self.g, self.inc, self.calls = E, n, 2.0 ** (1.0 / hl), 1.0, 0
+        self.score, self.last = [0.0] * (Lyr * E), [-1] * (Lyr * E)
+        self.owner, self.slot_of = [-1] * n, {}
+
+    def update(self, layer, ids):
+        keys = [layer * self.E + e for e in ids]
+        nh = sum(k in self.slot_of for k in keys)
+        if len(keys) - nh > self.n - nh:
+            return None
+        self.calls += 1
+        self.inc *= self.g
+        if self.inc > 2.0 ** 600:
+            self.score = [v * 2.0 ** -600 for v in self.score]
+            self.inc *= 2.0 ** -600
+        for k in keys:
+            self.score[k] += self.inc
+            self.last[k] = self.calls
+        pinned = {self.slot_of[k] for k in keys if k in self.slot_of}
+        hits = [e for e, k in zip(ids, keys) if k in self.slot_of]
+        placed = []
+        for e, k in zip(ids, keys):
+            if k in self.slot_of:
+                continue
+
+            def order(s):
+                o = self.owner[s]
+                return (0, 0.0, 0, s) if o < 0 else (1, self.score[o], self.last[o], s)
+            v = min((s for s in range(self.n) if s not in pinned), key=order)
+            if self.owner[v] >= 0:
+                del self.slot_of[self.owner[v]]
+            self.owner[v], self.slot_of[k] = k, v
+            pinned.add(v)
+            placed.append((e, v))
+        return hits, placed
+
+
+@pytest.mark.parametrize("hl", [0.5, 2.5, 40.0])
+def test_slot_table_freq_matches_brute_force_model(hl):
+    # hl = 0.5 grows the use weight 4x per call: the 2^-600 rescale happens about every 300 calls
+    Lyr, E, n = 3, 16, 10
+    rng = np.random.default_rng(7)
+    h, cp, hrec = _freq_table(Lyr, E, n, hl)
+    model = _FreqModel(Lyr, E, n, hl)
+    for call in range(700):
+        layer = int(rng.integers(0, Lyr))
+        # skewed ids so that counts differ; sometimes more misses than free slots
+        size = int(rng.integers(1, 13 if call % 50 == 49 else 7))
+        p = 1.0 / np.arange(1, E + 1) ** 1.1
+        ids = [int(e) for e in rng.choice(E, size=size, replace=False, p=p / p.sum())]
+        n_rec = len(cp.records)
+        st, hits, miss = _update(h, layer, ids)
+        ref = model.update(layer, ids)
+        if ref is None:
+            assert st == L.MOE_ENOSLOT and len(cp.records) == n_rec
+            continue
+        assert st == 0 and hits == ref[0] and miss == [e for e, _ in ref[1]]
+        assert [s for s, _ in cp.records[n_rec:]] == [v for _, v in ref[1]]
+        assert [src for _, src in cp.records[n_rec:]] == [hrec[layer * E + e] for e, _ in ref[1]]
+        snap = _snapshot(h, Lyr, E).reshape(-1)
+        assert {k: int(snap[k]) for k in range(Lyr * E) if snap[k] >= 0} == model.slot_of
+    L.slot_table_destroy(h)
+
+
+def _zipf_trace(Lyr, E, k, n_calls, seed):
+    rng = np.random.default_rng(seed)
+    perms = [rng.permutation(E) for _ in range(Lyr)]
+    p = 1.0 / np.arange(1, E + 1) ** 1.1
+    p /= p.sum()
+    for c in range(n_calls):
+        l = c % Lyr
+        yield l, [int(perms[l][r]) for r in rng.choice(E, size=k, replace=False, p=p)]
+
+
+def test_slot_table_freq_beats_lru_on_zipf_routing():
+    # a stationary Zipf(1.1) popularity: counting uses keeps the hot experts that recency
+    # alone lets go between two calls of their layer
+    rates = {}
+    for policy in (L.MOE_SLOT_LRU, L.MOE_SLOT_FREQ):
+        h, cp, _ = _freq_table(4, 64, 48, 4000.0, policy)
+        hits = total = 0
+        for i, (l, ids) in enumerate(_zipf_trace(4, 64, 6, 4000, seed=3)):
+            st, hh, mm = _update(h, l, ids)
+            assert st == 0
+            if i >= 400:
+                hits, total = hits + len(hh), total + len(ids)
+        rates[policy] = hits / total
+        L.slot_table_destroy(h)
+    assert rates[L.MOE_SLOT_FREQ] > rates[L.MOE_SLOT_LRU] + 0.03, rates
+
+
+def test_slot_table_warm_fills_empty_slots_from_the_profile():
+    Lyr, E, n = 2, 8, 5
+    h, cp, hrec = _make_table(Lyr, E, n)
+    _update(h, 1, [7])                       # one slot already taken
+    w = np.zeros(Lyr * E, dtype=np.float32)
+    w[[3, 9, 12, 0, 5]] = [5.0, 4.0, 3.0, 2.0, 2.0]   # keys l*E + e; 0 and 5 tie
+    n_rec = len(cp.records)
+    assert L.slot_table_warm(h, w.ctypes.data) == 4
+    # empty slots 1..4 in order take keys 3, 9, 12, then 0 (the lower key of the tie)
+    assert cp.records[n_rec:] == [(1, hrec[3]), (2, hrec[9]), (3, hrec[12]), (4, hrec[0])]
+    assert _resident(h, Lyr, E) == {(1, 7), (0, 3), (1, 1), (1, 4), (0, 0)}
+    for key, slot in ((3, 1), (9, 2), (12, 3), (0, 4)):
+        assert cp.entries[key] == slot
+    s = L.slot_table_stats(h)
+    assert (s.hits, s.misses, s.bytes_h2d) == (0, 1, 5 * 256)
+    st, hits, miss = _update(h, 0, [0, 3])
+    assert hits == [0, 3] and miss == []
+    # a full pool: nothing more is loaded and nothing is evicted
+    assert L.slot_table_warm(h, w.ctypes.data) == 0
+    L.slot_table_destroy(h)
+
+
+def test_slot_table_warm_weights_seed_the_counts():
+    # under FREQ a profile weight counts like uses: expert 1 (weight 10) outlives expert 0
+    # (two real uses) when a miss needs a slot
+    h, cp, _ = _freq_table(1, 8, 2, 1e9)
+    w = np.zeros(8, dtype=np.float32)
+    w[1] = 10.0
+    assert L.slot_table_warm(h, w.ctypes.data) == 1
+    _update(h, 0, [0])
+    _update(h, 0, [0])
+    _update(h, 0, [4])
+    assert _resident(h, 1, 8) == {(0, 1), (0, 4)}
+    L.slot_table_destroy(h)
+
+
+def test_slot_table_policy_and_warm_reject_bad_arguments():
+    h, cp, _ = _make_table(1, 8, 2)
+    for policy, hl in ((2, 1.0), (-1, 1.0), (L.MOE_SLOT_FREQ, 0.0), (L.MOE_SLOT_FREQ, -3.0),
+                       (L.MOE_SLOT_FREQ, float("inf")), (L.MOE_SLOT_FREQ, float("nan"))):
+        with pytest.raises(L.MoeError) as e:
+            L.slot_table_set_policy(h, policy, hl)
+        assert e.value.status == L.MOE_EINVAL
+    for bad in (-1.0, float("nan"), float("inf")):
+        w = np.ones(8, dtype=np.float32)
+        w[3] = bad
+        with pytest.raises(L.MoeError) as e:
+            L.slot_table_warm(h, w.ctypes.data)
+        assert e.value.status == L.MOE_EINVAL
+    assert len(cp.records) == 0 and _resident(h, 1, 8) == set()
+    with pytest.raises(L.MoeError):
+        L.slot_table_warm(h, None)
+    L.slot_table_destroy(h)

@@ -90,9 +90,10 @@ def test_decode_stack_layer_by_layer():
     check_layers(w, keep, range(w.layers))
 
 
-@pytest.mark.parametrize("overlap", [True, False])
-def test_tiered_stack_misses_evictions_and_parity(overlap):
-    # 2 layers x 32 experts, but only 24 device slots: every step evicts and copies
+@pytest.mark.parametrize("overlap,freq", [(True, False), (False, False), (True, True)])
+def test_tiered_stack_misses_evictions_and_parity(overlap, freq):
+    # 2 layers x 32 experts, but only 24 device slots: every step evicts and copies. With freq:
+    # the decayed-use-count policy, and a usage profile that fills the pool before step 0
     w = custom("stack", d=256, f=128, E=32, k=6, layers=2, T=4)
     n_slots = 24
     rb = w.record_bytes
@@ -104,7 +105,10 @@ def test_tiered_stack_misses_evictions_and_parity(overlap):
     dls = [DeviceLayer(w, layer=l) for l in range(w.layers)]  # routers and resident shared experts
     s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
     shared = [dl.pool[w.E * rb:(w.E + w.n_shared) * rb] for dl in dls]
-    ts = TieredStack(s, w.layers, [dl.router for dl in dls], h_records, n_slots, rb, shared)
+    profile = np.random.default_rng(5).random(w.layers * w.E).astype(np.float32) if freq else None
+    ts = TieredStack(s, w.layers, [dl.router for dl in dls], h_records, n_slots, rb, shared,
+                     policy=L.MOE_SLOT_FREQ if freq else L.MOE_SLOT_LRU, half_life_steps=2.0, profile=profile)
+    assert ts.n_warm == (n_slots if freq else 0)
     lookups = 0
     try:
         for step in range(3):
@@ -117,7 +121,7 @@ def test_tiered_stack_misses_evictions_and_parity(overlap):
         st = L.slot_table_stats(ts.table)
         assert st.misses > 0 and st.evictions > 0
         assert st.hits + st.misses == lookups
-        assert st.bytes_h2d == st.misses * rb
+        assert st.bytes_h2d == (st.misses + ts.n_warm) * rb
         # every resident expert's slot holds that expert's record
         snap = np.zeros(w.layers * w.E, dtype=np.int32)
         L.slot_table_snapshot(ts.table, snap.ctypes.data)
