@@ -205,7 +205,7 @@ def slot_table_create(L, E, n_slots, slot_bytes, d_pool, d_slot_of, h_records, c
     st = lib().slot_table_create(C.byref(out), L, E, n_slots, slot_bytes, ptr(d_pool), ptr(d_slot_of), arr, fn,
                                  copy_user)
     if st < 0:
-        raise MoeError(st, "slot_table_create", "")
+        raise MoeError(st, "slot_table_create", moe_last_error_string())
     return out.value
 
 
@@ -215,7 +215,7 @@ def slot_table_update(table, layer, h_active, n_active, copy_stream, ready, h_hi
     st = lib().slot_table_update(table, layer, h_active, n_active, copy_stream, ready, h_hits, n_hits, h_misses,
                                  n_misses, C.byref(stats) if stats is not None else None)
     if st < 0 and st != MOE_ENOSLOT:
-        raise MoeError(st, "slot_table_update", "")
+        raise MoeError(st, "slot_table_update", moe_last_error_string())
     return st
 
 

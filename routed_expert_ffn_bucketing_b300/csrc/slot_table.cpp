@@ -34,12 +34,13 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <vector>
 
-#include "../../include/moe.h"
+#include "moe_internal.h"
 
 struct moe_slot_table {
   int32_t L = 0, E = 0, n_slots = 0;
@@ -69,7 +70,15 @@ struct moe_slot_table {
 
 namespace {
 
-thread_local char g_slot_err[256] = "";
+// Records a formatted message as this thread's moe_last_error_string() and returns st.
+moe_status slot_fail(moe_status st, const char* fmt, ...) {
+  char buf[256];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  return moe::report_error(st, buf);
+}
 
 int cuda_copy(void* dst, const void* src, size_t bytes, moe_stream_t stream, void*) {
   return (int)cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
@@ -176,11 +185,13 @@ extern "C" {
 moe_status slot_table_create(moe_slot_table** out, int32_t L, int32_t E, int32_t n_slots, uint64_t slot_bytes,
                              void* d_pool, int32_t* d_slot_of, const void* const* h_records, moe_copy_fn copy_fn,
                              void* copy_user) {
-  if (!out || L <= 0 || E <= 0 || n_slots <= 0 || slot_bytes == 0 || !h_records) return MOE_EINVAL;
-  if ((int64_t)L * E > (int64_t)1 << 30) return MOE_EUNSUPPORTED;
-  if (!copy_fn && (!d_pool || !d_slot_of)) return MOE_EINVAL;
+  if (!out || L <= 0 || E <= 0 || n_slots <= 0 || slot_bytes == 0 || !h_records)
+    return slot_fail(MOE_EINVAL, "slot_table_create: null pointer or L, E, n_slots, slot_bytes not > 0");
+  if ((int64_t)L * E > (int64_t)1 << 30) return slot_fail(MOE_EUNSUPPORTED, "slot_table_create: L*E above 2^30");
+  if (!copy_fn && (!d_pool || !d_slot_of))
+    return slot_fail(MOE_EINVAL, "slot_table_create: the default copier needs d_pool and d_slot_of");
   for (int64_t i = 0; i < (int64_t)L * E; ++i)
-    if (!h_records[i]) return MOE_EINVAL;
+    if (!h_records[i]) return slot_fail(MOE_EINVAL, "slot_table_create: h_records[%lld] is null", (long long)i);
   moe_slot_table* t = new moe_slot_table();
   t->L = L;
   t->E = E;
@@ -196,10 +207,14 @@ moe_status slot_table_create(moe_slot_table** out, int32_t L, int32_t E, int32_t
   if (t->default_copier) {
     if (cudaMallocHost(reinterpret_cast<void**>(&t->mirror), mbytes) != cudaSuccess) {
       delete t;
-      return MOE_ECUDA;
+      return slot_fail(MOE_ECUDA, "slot_table_create: cudaMallocHost of the table mirror failed");
     }
   } else {
     t->mirror = static_cast<int32_t*>(std::malloc(mbytes));
+    if (!t->mirror) {
+      delete t;
+      return slot_fail(MOE_EINVAL, "slot_table_create: no host memory for the table mirror");
+    }
   }
   for (size_t i = 0; i < (size_t)L * E; ++i) t->mirror[i] = -1;
   t->owner.assign(n_slots, -1);
@@ -218,12 +233,12 @@ moe_status slot_table_create(moe_slot_table** out, int32_t L, int32_t E, int32_t
       if (cudaMemcpy(d_slot_of, t->mirror, mbytes, cudaMemcpyHostToDevice) != cudaSuccess) {
         cudaFreeHost(t->mirror);
         delete t;
-        return MOE_ECUDA;
+        return slot_fail(MOE_ECUDA, "slot_table_create: clearing d_slot_of failed");
       }
     } else if (t->copy_fn(d_slot_of, t->mirror, mbytes, nullptr, t->copy_user) != 0) {
       std::free(t->mirror);
       delete t;
-      return MOE_ECUDA;
+      return slot_fail(MOE_ECUDA, "slot_table_create: clearing d_slot_of failed");
     }
   }
   *out = t;
@@ -233,7 +248,9 @@ moe_status slot_table_create(moe_slot_table** out, int32_t L, int32_t E, int32_t
 moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_active, int32_t n_active,
                              moe_stream_t copy_stream, moe_event_t ready, int32_t* h_hits, int32_t* n_hits,
                              int32_t* h_misses, int32_t* n_misses, moe_slot_stats* stats_opt) {
-  if (!t || layer < 0 || layer >= t->L || n_active < 0 || (n_active > 0 && !h_active)) return MOE_EINVAL;
+  if (!t || n_active < 0 || (n_active > 0 && !h_active))
+    return slot_fail(MOE_EINVAL, "slot_table_update: null table or active list, or n_active < 0");
+  if (layer < 0 || layer >= t->L) return slot_fail(MOE_EINVAL, "slot_table_update: layer %d not in [0, %d)", layer, t->L);
   // validate ids, reject repeats (epoch marks)
   if (++t->epoch == 0) {
     std::fill(t->mark.begin(), t->mark.end(), 0);
@@ -241,16 +258,16 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
   }
   for (int32_t i = 0; i < n_active; ++i) {
     const int32_t e = h_active[i];
-    if (e < 0 || e >= t->E || t->mark[e] == t->epoch) return MOE_EINVAL;
+    if (e < 0 || e >= t->E || t->mark[e] == t->epoch)
+      return slot_fail(MOE_EINVAL, "slot_table_update: expert id %d out of [0, %d) or repeated", e, t->E);
     t->mark[e] = t->epoch;
   }
   const int64_t base = (int64_t)layer * t->E;
   int32_t nh = 0, nm = 0;
   for (int32_t i = 0; i < n_active; ++i) (t->mirror[base + h_active[i]] >= 0 ? nh : nm)++;
-  if (nm > t->n_slots - nh) {
-    std::snprintf(g_slot_err, sizeof(g_slot_err), "%d misses, %d evictable slots", nm, t->n_slots - nh);
-    return MOE_ENOSLOT;
-  }
+  if (nm > t->n_slots - nh)
+    return slot_fail(MOE_ENOSLOT, "slot_table_update: %d misses but %d slots not needed by this call", nm,
+                     t->n_slots - nh);
   advance_clock(t);
   // every expert of the call counts one use; hits first become most recently used and
   // pinned, so that no miss evicts them (each slot's new key is fixed before the next change)
@@ -292,8 +309,7 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
     const int cr = t->copy_fn(t->d_pool + (uint64_t)s * t->slot_bytes, t->h_records[base + e], t->slot_bytes,
                               copy_stream, t->copy_user);
     if (cr != 0) {
-      std::snprintf(g_slot_err, sizeof(g_slot_err), "copy of expert %d failed (%d)", e, cr);
-      rc = MOE_ECUDA;
+      rc = slot_fail(MOE_ECUDA, "slot_table_update: copy of layer %d expert %d failed (%d)", layer, e, cr);
       break;
     }
     t->owner[s] = base + e;
@@ -312,10 +328,11 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
     heap_fix(t, s);
   }
   t->stats.hits += nh;
-  if (write_entries(t, changed, copy_stream) != 0 && rc == MOE_OK) rc = MOE_ECUDA;
+  if (write_entries(t, changed, copy_stream) != 0 && rc == MOE_OK)
+    rc = slot_fail(MOE_ECUDA, "slot_table: writing the device table failed");
   if (ready && cudaEventRecord(reinterpret_cast<cudaEvent_t>(ready), reinterpret_cast<cudaStream_t>(copy_stream)) !=
                    cudaSuccess && rc == MOE_OK)
-    rc = MOE_ECUDA;
+    rc = slot_fail(MOE_ECUDA, "slot_table: recording the ready event failed");
   if (n_hits) *n_hits = nh;
   if (n_misses) *n_misses = nm;
   if (stats_opt) *stats_opt = t->stats;
@@ -324,7 +341,7 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
 
 moe_status slot_table_set_policy(moe_slot_table* t, int32_t policy, double half_life) {
   if (!t || (policy != MOE_SLOT_LRU && policy != MOE_SLOT_FREQ) || !(half_life > 0.0) || !std::isfinite(half_life))
-    return MOE_EINVAL;
+    return slot_fail(MOE_EINVAL, "slot_table_set_policy: null table, unknown policy %d or half-life not > 0", policy);
   t->policy = policy;
   t->g = std::pow(2.0, 1.0 / half_life);
   return MOE_OK;
@@ -332,10 +349,11 @@ moe_status slot_table_set_policy(moe_slot_table* t, int32_t policy, double half_
 
 moe_status slot_table_warm(moe_slot_table* t, const float* h_weight, moe_stream_t copy_stream, moe_event_t ready,
                            int32_t* n_loaded) {
-  if (!t || !h_weight) return MOE_EINVAL;
+  if (!t || !h_weight) return slot_fail(MOE_EINVAL, "slot_table_warm: null table or weights");
   const int64_t n_keys = (int64_t)t->L * t->E;
   for (int64_t i = 0; i < n_keys; ++i)
-    if (!(h_weight[i] >= 0.0f) || !std::isfinite(h_weight[i])) return MOE_EINVAL;
+    if (!(h_weight[i] >= 0.0f) || !std::isfinite(h_weight[i]))
+      return slot_fail(MOE_EINVAL, "slot_table_warm: weight %lld is negative or not finite", (long long)i);
   for (int64_t i = 0; i < n_keys; ++i) t->score[i] += (double)h_weight[i] * t->inc;
   heap_rebuild(t);
   // empty slots, lowest index first, take the best non-resident experts with a positive weight
@@ -358,9 +376,8 @@ moe_status slot_table_warm(moe_slot_table* t, const float* h_weight, moe_stream_
     const int cr = t->copy_fn(t->d_pool + (uint64_t)s * t->slot_bytes, t->h_records[key], t->slot_bytes, copy_stream,
                               t->copy_user);
     if (cr != 0) {
-      std::snprintf(g_slot_err, sizeof(g_slot_err), "warm copy of layer %lld expert %lld failed (%d)",
-                    (long long)(key / t->E), (long long)(key % t->E), cr);
-      rc = MOE_ECUDA;
+      rc = slot_fail(MOE_ECUDA, "slot_table_warm: copy of layer %lld expert %lld failed (%d)",
+                     (long long)(key / t->E), (long long)(key % t->E), cr);
       break;
     }
     t->owner[s] = key;
@@ -370,10 +387,11 @@ moe_status slot_table_warm(moe_slot_table* t, const float* h_weight, moe_stream_
     t->stats.bytes_h2d += t->slot_bytes;
     ++loaded;
   }
-  if (write_entries(t, changed, copy_stream) != 0 && rc == MOE_OK) rc = MOE_ECUDA;
+  if (write_entries(t, changed, copy_stream) != 0 && rc == MOE_OK)
+    rc = slot_fail(MOE_ECUDA, "slot_table: writing the device table failed");
   if (ready && cudaEventRecord(reinterpret_cast<cudaEvent_t>(ready), reinterpret_cast<cudaStream_t>(copy_stream)) !=
                    cudaSuccess && rc == MOE_OK)
-    rc = MOE_ECUDA;
+    rc = slot_fail(MOE_ECUDA, "slot_table: recording the ready event failed");
   if (n_loaded) *n_loaded = loaded;
   return rc;
 }

@@ -138,7 +138,7 @@ class TieredStack:
             st = L.slot_table_update(self.table, l, self.h_active.data_ptr() + 4, n, self.copy_stream.cuda_stream,
                                      self.ready.cuda_event, hp + 4, hp, mp + 4, mp, self.stats)
             if st != L.MOE_OK:
-                raise L.MoeError(st, "slot_table_update", "")
+                raise L.MoeError(st, "slot_table_update", L.moe_last_error_string())
             n_miss = int(self.h_misses[0])
             self.layer_misses.append(n_miss)
             table = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l],

@@ -425,3 +425,20 @@ def test_slot_table_policy_and_warm_reject_bad_arguments():
     with pytest.raises(L.MoeError):
         L.slot_table_warm(h, None)
     L.slot_table_destroy(h)
+
+
+def test_slot_table_errors_carry_a_message():
+    h, cp, _ = _make_table(1, 16, 3)
+    _update(h, 0, [0, 1])
+    st, _, _ = _update(h, 0, [0, 1, 2, 3])
+    assert st == L.MOE_ENOSLOT and "2 misses but 1 slots" in L.moe_last_error_string()
+    a = (C.c_int32 * 2)(4, 4)
+    with pytest.raises(L.MoeError, match="repeated"):
+        L.slot_table_update(h, 0, C.addressof(a), 2, None, None)
+    with pytest.raises(L.MoeError, match="layer 3 not in"):
+        L.slot_table_update(h, 3, C.addressof(a), 1, None, None)
+    with pytest.raises(L.MoeError, match="half-life"):
+        L.slot_table_set_policy(h, L.MOE_SLOT_FREQ, 0.0)
+    L.slot_table_destroy(h)
+    with pytest.raises(L.MoeError, match="slot_table_create"):
+        L.slot_table_create(1, 4, 0, 256, 0, 0, [1, 2, 3, 4], FakeCopier(0, 0, 256, None).fn, None)
