@@ -2,26 +2,32 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload decode]
 
-A step is one whole pass (router + top-k, bucketing, slot-table lookup inside the expert
-FFN, SwiGLU experts, combine) over one batch of T tokens. Batches rotate over 16 seeded
-inputs, so each step routes to its own experts. A 512 MiB buffer (larger than the 126 MB
-L2) is written between timed steps, outside the timed events. Times are CUDA events on
-the launching stream, and the maximum is taken over ranks. One JSON line is printed by rank 0.
+A layer pass is the whole hot path (router + top-k, bucketing, slot-table lookup inside the
+expert FFN, SwiGLU experts, combine) over one batch of T tokens, replayed from a CUDA graph of
+the C-ABI calls. Pass i runs the weights of layer i % 4 (decode) on batch i % 16, so each pass
+reads its own experts (about 200 MB) and a layer's router and shared expert come back only
+after about 600 MB of other reads: the inputs are larger than L2 and nothing is flushed. A
+timed step is R consecutive passes, with R chosen so that the K timed steps last at least
+300 ms (clock samples every 100 ms fall inside them). Times are CUDA events on the launching
+stream, and the maximum is taken over ranks. One JSON line is printed by rank 0; with the
+default decode workload it also carries the prefill chunk's measurement (T = 8192) under
+"prefill".
 
 --impl reference times the CPU oracle on this host's cores instead, over the same
-workload and metric (one oracle layer pass per step).
+workload and metric: one oracle pass per worker process and step, one worker per core.
 """
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
 import sys
 import time
 
-# the CPU oracle is timed on one core: fix the BLAS thread count before numpy loads
+# the CPU oracle runs one numpy thread per process: fix the BLAS thread count before numpy loads
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -32,28 +38,33 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill int8 TOPS as % of B300 peak"
+DTYPE = "bf16 activations, int8 block-32 weights (fp16 scales) entering f16 tensor-core MMAs exactly, fp32 accumulation"
 N_BATCHES = 16
-FLUSH_BYTES = 512 << 20
+ROT_LAYERS = 4         # decode: layers whose weights rotate between passes
+MIN_TIMED_MS = 300.0   # the K timed steps last at least this long
+MAX_ORACLE_WORKERS = 32
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernel(s),
-# from one ncu capture of the current kernels (the summaries in profiles/ give the command). A
-# capture is of one launch, i.e. one batch: the decode FFN's algorithmic bytes vary by batch.
-TRAFFIC = {
-    "decode": {"bytes": 186_220_288 + 3_603_200, "kernel": "ffn_persist_kernel<8, 8>",
-               "capture": "profiles/ffn_persist_decode_T4.md (one launch)"},
-    "prefill": {"bytes": 2_721_439_000 + 241_189_888 + 1_198_355_000 + 314_232_576,
-                "kernel": "prefill_gemm_kernel<0> + prefill_gemm_kernel<1>",
-                "capture": "profiles/prefill_gemm_T8192.md (one launch each; gather and h conversion not included)"},
-}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernel,
+# from one ncu capture of the kernel as it is now built, or None when the kernel has changed
+# since its last capture.
+TRAFFIC = {"decode": None, "prefill": None}
 
 
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0.0)) or None,
+                "measured")
     except Exception:
-        return 6400.0, 1800.0, "fallback"
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def pcts(v) -> dict:
+    """Median and 10th / 90th percentiles of a list of per-pass times (ms)."""
+    a = np.asarray(v, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90)),
+            "n": int(a.size)}
 
 
 # ------------------------------------------------------------------ clocks ----------------
@@ -69,10 +80,11 @@ class ClockSampler:
 
     def start(self):
         try:
-            self.path = f"/tmp/moe_bench_clocks_{os.getpid()}.csv"
+            self.path = f"/tmp/moe_bench_clocks_{os.getpid()}_{time.monotonic_ns()}.csv"
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)  # nvidia-smi takes a moment to start sampling
         except Exception:
             self.proc = None
 
@@ -84,7 +96,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, mx, reasons = [], None, set()
+        sm, mx, power, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         try:
             for line in open(self.path):
@@ -94,6 +106,7 @@ class ClockSampler:
                 try:
                     sm.append(float(f[1]))
                     mx = float(f[2])
+                    power.append(float(f[3]))
                 except ValueError:
                     continue
                 for n, v in zip(names, f[5:9]):
@@ -104,7 +117,8 @@ class ClockSampler:
             pass
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "sm_mhz_min": min(sm), "power_w_max": max(power) if power else None}
 
 
 # ------------------------------------------------------------------ CPU oracle ------------
@@ -158,6 +172,81 @@ def time_oracle(w, prep, budget_s: float, max_steps: int | None = None):
     return xs[0].shape[0] * steps / el, steps, el, int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
 
 
+_BARRIER = None
+
+
+def _oracle_pool_init(barrier):
+    global _BARRIER
+    _BARRIER = barrier
+
+
+def _oracle_worker(job):
+    """One worker of the all-core oracle timing: its own batch, its experts made here; W warm-up
+    passes, a barrier, then `steps` timed passes (or until `budget_s`). One numpy thread."""
+    from oracle import moe_oracle as O
+    from synth.workloads import WORKLOADS
+    wname, batch, warm, steps, budget_s = job
+    w = WORKLOADS[wname]
+    router = w.router(0)
+    x = w.x_f64(batch)[:ORACLE_MAX_TOKENS]
+    need = set(O.select_topk(O.router_logits(x, router), w.k).reshape(-1).tolist())
+    ex = {e: w.expert(0, e) for e in sorted(need | {w.E + s for s in range(w.n_shared)})}
+    shared = [ex[w.E + s] for s in range(w.n_shared)]
+    _BARRIER.wait()
+    for _ in range(warm):
+        O.moe_layer(x, router, w.k, lambda e: ex[e], shared)
+    _BARRIER.wait()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        O.moe_layer(x, router, w.k, lambda e: ex[e], shared)
+        n += 1
+        el = time.perf_counter() - t0
+        if (steps is not None and n >= steps) or (budget_s is not None and el >= budget_s):
+            break
+    return x.shape[0] * n, n, el
+
+
+def oracle_workers() -> tuple[int, int]:
+    """(workers the all-core timing uses, logical CPUs this process may run on)."""
+    try:
+        avail = len(os.sched_getaffinity(0))
+    except Exception:
+        avail = os.cpu_count() or 1
+    return max(1, min(avail, MAX_ORACLE_WORKERS)), avail
+
+
+def time_oracle_all_cores(wname: str, warm: int = 1, steps: int | None = None, budget_s: float | None = None):
+    """The oracle as it stands, one single-threaded process per core, all timing at once (spawn
+    processes). Returns (tokens/s over all workers, passes, seconds, workers, cpus)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    n, avail = oracle_workers()
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(n)
+    jobs = [(wname, i % N_BATCHES, warm, steps, budget_s) for i in range(n)]
+    with cf.ProcessPoolExecutor(max_workers=n, mp_context=ctx, initializer=_oracle_pool_init,
+                                initargs=(barrier,)) as ex:
+        res = list(ex.map(_oracle_worker, jobs))
+    tokens = sum(r[0] for r in res)
+    passes = sum(r[1] for r in res)
+    el = max(r[2] for r in res)
+    return tokens / el, passes, el, n, avail
+
+
+def cpu_baseline_line(w, args) -> dict:
+    """The oracle timed on this host: all cores (one process per core, the headline value) and
+    one core."""
+    tps_all, passes, el, n, avail = time_oracle_all_cores(w.name, budget_s=args.cpu_seconds)
+    tps1, steps1, el1, _ = time_oracle(w, prepare_oracle(w, list(range(4))), budget_s=args.cpu_seconds)
+    lw = w.layers
+    return {"value": tps_all / lw, "unit": "tokens/s", "cores": n, "kind": "oracle", "nproc": avail,
+            "sample": f"{passes} oracle passes ({el:.1f} s) of T={min(w.T, ORACLE_MAX_TOKENS)} tokens, one process "
+                      f"per core on {n} of {avail} logical CPUs, each on its own batch"
+                      + (f" (layer 0; tokens/s divided by the {lw} layers of a step)" if lw > 1 else ""),
+            "single_core": {"value": tps1 / lw, "cores": 1,
+                            "sample": f"{steps1} oracle passes ({el1:.1f} s) over 4 rotating batches"}}
+
+
 # ------------------------------------------------------------------ distributed -----------
 
 def dist_setup():
@@ -195,14 +284,11 @@ def run_reference(args, ws, rank):
     from synth.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
-    batches = list(range(4))
-    prep = prepare_oracle(w, batches)
-    # W untimed oracle passes, then K timed ones (one batch of T tokens per step), stopping
-    # early once 150 s have passed so that the run stays within a few minutes
-    time_oracle(w, prep, budget_s=1e9, max_steps=max(W, 1))
-    tps, steps, el, cores = time_oracle(w, prep, budget_s=150.0, max_steps=K)
-    sample = (f"{steps} oracle layer passes over {len(batches)} rotating batches of "
-              f"{min(w.T, ORACLE_MAX_TOKENS)} tokens of T={w.T}")
+    # each step: one oracle pass per worker (one per core), all at once; stop early after 150 s
+    tps, passes, el, n, avail = time_oracle_all_cores(w.name, warm=W, steps=K, budget_s=150.0)
+    steps = max(1, passes // n)
+    sample = (f"{passes} oracle layer passes ({el:.1f} s) of T={min(w.T, ORACLE_MAX_TOKENS)} tokens, one process "
+              f"per core on {n} of {avail} logical CPUs, each on its own batch")
     if w.layers > 1:
         tps /= w.layers
         sample += f" (layer 0); tokens/s divided by the {w.layers} layers of a step"
@@ -210,20 +296,171 @@ def run_reference(args, ws, rank):
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps,
         "warmup": W, "ms_per_step": 1e3 * el / steps * w.layers, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": w.describe(), "tokens_per_step": w.T},
-        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "config": {"workload": w.describe(), "tokens_per_step": min(w.T, ORACLE_MAX_TOKENS) * n},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": sample,
+                         "nproc": avail},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-# ------------------------------------------------------------------ our arm ---------------
+# ------------------------------------------------------------------ one-layer workloads ----
 
-def run_ours(args, ws, rank, local):
+def time_layer(w, dev, K: int, W: int, rot_layers: int, n_batches: int, ydt: int, min_ms: float, ws: int,
+               e2e: bool) -> dict:
+    """Times layer passes of the one-layer workload w on `dev`: pass i runs layer i % rot_layers
+    on batch i % n_batches from a CUDA graph of the C-ABI calls. Region 1: K steps of R passes
+    each (R so that the region lasts >= min_ms), the clocks sampled meanwhile. Region 2: the same
+    passes as three graphs (route + bucketing, expert FFN, combine) with events between, for the
+    expert FFN's own time. With e2e, also the passes through the public API with host buffers."""
     import torch
     from routed_expert_ffn_bucketing_b300 import _lib as L
     from routed_expert_ffn_bucketing_b300 import layer as lay
     from synth.device import DeviceLayer
+
+    dls = [DeviceLayer(w, layer=l, device=str(dev)) for l in range(rot_layers)]
+    xs = [dls[0].x(b) for b in range(n_batches)]
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    buf = lay.alloc_buffers(s, device=dev, ydt=ydt, odt=L.MOE_BF16, keep_logits=False)
+    tables = [L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr) for dl in dls]
+    stream = torch.cuda.current_stream(dev)
+    xdt = L.MOE_BF16
+    n_combo = rot_layers * n_batches // math.gcd(rot_layers, n_batches)
+    combo = [(i % rot_layers, i % n_batches) for i in range(n_combo)]
+
+    def seg_route(l, x):
+        L.moe_route(s, x, xdt, dls[l].router, buf.topk_idx, buf.topk_w, None, buf.ws, buf.ws_bytes, None)
+        L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
+                      buf.ws_bytes, None)
+
+    def seg_ffn_combine(l, x):
+        L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, x, xdt, tables[l], buf.offsets, buf.sorted_pair, buf.active,
+                                 buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, buf.ws,
+                                 buf.ws_bytes, None)
+
+    def seg_ffn(l, x):
+        L.moe_expert_ffn(s, L.MOE_MODE_AUTO, x, xdt, tables[l], buf.offsets, buf.sorted_pair, buf.active,
+                         buf.y_perm, buf.ydt, buf.ws, buf.ws_bytes, None)
+
+    def seg_comb(l, x):
+        L.moe_combine(s, buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, None)
+
+    # active experts per pass (for the algorithmic byte count), from untimed eager passes
+    n_active = []
+    for l, b in combo:
+        seg_route(l, xs[b])
+        seg_ffn_combine(l, xs[b])
+        torch.cuda.synchronize(dev)
+        n_active.append(int(buf.active[0].item()))
+        assert L.moe_read_status(buf.ws) == 0
+    cap = torch.cuda.Stream(dev)
+    layer_graphs, stage_graphs = [], []
+    for l, b in combo:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            seg_route(l, xs[b])
+            seg_ffn_combine(l, xs[b])
+        layer_graphs.append(g)
+        gs = []
+        for seg in (seg_route, seg_ffn, seg_comb):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                seg(l, xs[b])
+            gs.append(g)
+        stage_graphs.append(gs)
+    for i in range(max(W, 3) * n_combo):
+        layer_graphs[i % n_combo].replay()
+    torch.cuda.synchronize(dev)
+    # passes per step: the K steps together last >= min_ms
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(4 * n_combo):
+        layer_graphs[i % n_combo].replay()
+    b_.record(stream)
+    torch.cuda.synchronize(dev)
+    est = a.elapsed_time(b_) / (4 * n_combo)
+    R = max(1, math.ceil(min_ms / (K * est)))
+
+    # ---- region 1: K steps of R passes
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(dev.index or 0)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_wall = time.perf_counter()
+    p = 0
+    for i in range(K):
+        ev[i][0].record(stream)
+        for _ in range(R):
+            layer_graphs[p % n_combo].replay()
+            p += 1
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    assert L.moe_read_status(buf.ws) == 0, "a kernel reported an error during the timed steps"
+    step_ms = [x.elapsed_time(y) for x, y in ev]
+    total_s = dist_max(sum(step_ms) / 1e3, ws, dev)
+
+    # ---- region 2: stages, for the expert FFN's own time
+    n2 = min(K * R, max(8 * n_combo, 256))
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n2)]
+    torch.cuda.synchronize(dev)
+    for i in range(n2):
+        e = ev2[i]
+        g_route, g_ffn, g_comb = stage_graphs[i % n_combo]
+        e[0].record(stream)
+        g_route.replay()
+        e[1].record(stream)
+        g_ffn.replay()
+        e[2].record(stream)
+        g_comb.replay()
+        e[3].record(stream)
+    torch.cuda.synchronize(dev)
+    route_ms = [e[0].elapsed_time(e[1]) for e in ev2]
+    ffn_ms = [e[1].elapsed_time(e[2]) for e in ev2]
+    comb_ms = [e[2].elapsed_time(e[3]) for e in ev2]
+    staged_ms = [e[0].elapsed_time(e[3]) for e in ev2]
+
+    res = {"R": R, "K": K, "step_ms": step_ms, "total_s": total_s, "wall": wall, "clocks": clk,
+           "pass_ms": [t / R for t in step_ms], "n_active": [n_active[i % n_combo] for i in range(n2)],
+           "n_active_mean": float(np.mean(n_active)), "route_ms": route_ms, "ffn_ms": ffn_ms, "comb_ms": comb_ms,
+           "staged_ms": staged_ms, "n_combo": n_combo}
+
+    if e2e:
+        # the same passes through the public API with host buffers: pinned x copied in, a graph of
+        # the C-ABI calls on the device copy, the bf16 output copied back and waited for, per pass
+        x_host = [x.cpu().pin_memory() for x in xs]
+        out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+        x_dev = torch.empty_like(xs[0])
+        e2e_graphs = []
+        for l in range(rot_layers):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                seg_route(l, x_dev)
+                seg_ffn_combine(l, x_dev)
+            e2e_graphs.append(g)
+        n_e2e = min(K * R, 4000)
+        e2e_s = 0.0
+        for i in range(W + n_e2e):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            x_dev.copy_(x_host[i % n_batches], non_blocking=True)
+            e2e_graphs[i % rot_layers].replay()
+            out_host.copy_(buf.out, non_blocking=True)
+            stream.synchronize()
+            if i >= W:
+                e2e_s += time.perf_counter() - t0
+        res["e2e_s"] = dist_max(e2e_s, ws, dev)
+        res["n_e2e"] = n_e2e
+    del layer_graphs, stage_graphs
+    return res
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    from routed_expert_ffn_bucketing_b300 import _lib as L
     from synth.workloads import WORKLOADS
 
     if not torch.cuda.is_available():
@@ -232,201 +469,102 @@ def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
-    hbm_peak, bf16_peak, peak_kind = peaks()
-
+    hbm_peak, bf16_peak, bf16_sus, peak_kind = peaks()
     prefill = w.T > 16
-    n_batches = 4 if prefill else N_BATCHES
-    dl = DeviceLayer(w, device=str(dev))
-    xs = [dl.x(b) for b in range(n_batches)]
-    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
-    # prefill writes y_perm in bf16 (half the combine's reads); decode keeps fp32
-    buf = lay.alloc_buffers(s, device=dev, ydt=L.MOE_BF16 if prefill else L.MOE_F32, odt=L.MOE_BF16,
-                            keep_logits=False)
-    table = L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    xdt = L.MOE_BF16
-
-    def step(x):
-        lay.forward(buf, x, dl.router, table, L.MOE_MODE_AUTO, stream=stream, fused=True)
-
-    # active experts per batch (for the algorithmic byte count), from untimed passes
-    n_active = []
-    for b in range(n_batches):
-        step(xs[b])
-        torch.cuda.synchronize(dev)
-        n_active.append(int(buf.active[0].item()))
-        assert L.moe_read_status(buf.ws) == 0
-    for i in range(W):
-        flush.fill_(i & 0xFF)
-        step(xs[i % n_batches])
-    torch.cuda.synchronize(dev)
-
-    # The timed steps replay CUDA graphs of the C-ABI calls, one graph per stage and batch:
-    # (route + permute), expert FFN with the combine (moe_expert_ffn_combine). The kernels
-    # and their arguments are those of the eager calls; the graphs only take the host's launch
-    # cost out of the device time.
-    def seg_route(x):
-        L.moe_route(s, x, xdt, dl.router, buf.topk_idx, buf.topk_w, None, buf.ws, buf.ws_bytes, None)
-        L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
-                      buf.ws_bytes, None)
-
-    def seg_ffn_combine(x):
-        L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, x, xdt, table, buf.offsets, buf.sorted_pair, buf.active,
-                                 buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, buf.ws,
-                                 buf.ws_bytes, None)
-
-    # for the breakdown: the same kernels as two calls
-    def seg_ffn(x):
-        L.moe_expert_ffn(s, L.MOE_MODE_AUTO, x, xdt, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm,
-                         buf.ydt, buf.ws, buf.ws_bytes, None)
-
-    def seg_comb(x):
-        L.moe_combine(s, buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, None)
-
-    cap = torch.cuda.Stream(dev)
-    graphs, layer_graphs = [], []
-    for b in range(n_batches):
-        gs = []
-        for seg in (seg_route, seg_ffn, seg_comb):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cap):
-                seg(xs[b])
-            gs.append(g)
-        graphs.append(gs)
-        g = torch.cuda.CUDAGraph()  # the whole layer: the four calls in one graph
-        with torch.cuda.graph(g, stream=cap):
-            seg_route(xs[b])
-            seg_ffn_combine(xs[b])
-        layer_graphs.append(g)
-    for i in range(W):
-        flush.fill_(i & 0xFF)
-        for g in graphs[i % n_batches]:
-            g.replay()
-        layer_graphs[i % n_batches].replay()
-    torch.cuda.synchronize(dev)
-
-    # timed region 1 (the headline): one whole-layer graph per step
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    clocks = ClockSampler(local)
-    barrier(ws)
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    t_wall = time.perf_counter()
-    for i in range(K):
-        flush.fill_(i & 0xFF)
-        a, b = ev_step[i]
-        a.record(stream)
-        layer_graphs[i % n_batches].replay()
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(ws)
-    wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev_step]
-
-    # timed region 2 (the breakdown and the expert-FFN roofline): one graph per stage, events between
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    torch.cuda.synchronize(dev)
-    for i in range(K):
-        flush.fill_(i & 0xFF)
-        g_route, g_ffn, g_comb = graphs[i % n_batches]
-        e0, e1, e2, e3 = ev[i]
-        e0.record(stream)
-        g_route.replay()
-        e1.record(stream)
-        g_ffn.replay()
-        e2.record(stream)
-        g_comb.replay()
-        e3.record(stream)
-    torch.cuda.synchronize(dev)
-    assert L.moe_read_status(buf.ws) == 0, "a kernel reported an error during the timed steps"
-    staged_ms = [a.elapsed_time(d) for a, _, _, d in ev]
-    ffn_ms = [b.elapsed_time(c) for _, b, c, _ in ev]
-    route_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
-    comb_ms = [c.elapsed_time(d) for _, _, c, d in ev]
-    total_s = dist_max(sum(step_ms) / 1e3, ws, dev)
-    value = ws * w.T * K / total_s
-
-    # algorithmic bytes of the expert-FFN call: each selected expert's record once, the T
-    # activation rows read, the y_perm rows written (fp32); scratch (h) is not counted
-    rows = w.P + w.T * w.n_shared
-    small = w.T * w.d * 2 + rows * w.d * 4
-    ffn_bytes = [(n_active[i % n_batches] + w.n_shared) * w.record_bytes + small for i in range(K)]
-    achieved = sum(ffn_bytes) / (sum(ffn_ms) / 1e3) / 1e9
-    if prefill:
-        # tensor-bound: algorithmic FLOPs of the expert FFN (gate, up and down over every row)
-        ffn_flops = 2.0 * rows * 3 * w.d * w.f
-        tflops = ffn_flops / (sum(ffn_ms) / 1e3 / K) / 1e12
-        roofline = {"kernel": "moe_expert_ffn (grouped GEMM: gate/up + SwiGLU, down)", "bound": "tensor",
-                    "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tflops / bf16_peak,
-                    "peak_kind": f"{peak_kind} dense bf16 (the f16 dense rate is the same)",
-                    "traffic": TRAFFIC["prefill"]["bytes"], "traffic_source": TRAFFIC["prefill"],
-                    "flops_per_launch": ffn_flops, "ms_per_launch": sum(ffn_ms) / K}
-    else:
-        roofline = {"kernel": "moe_expert_ffn (persistent kernel: gate/up + SwiGLU, down)", "bound": "hbm",
-                    "achieved": achieved,
-                    "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                    "peak_kind": f"{peak_kind} copy bandwidth",
-                    "traffic": TRAFFIC["decode"]["bytes"], "traffic_source": TRAFFIC["decode"],
-                    "bytes_per_launch": float(np.mean(ffn_bytes)), "ms_per_launch": sum(ffn_ms) / K}
-    router_bytes = w.d * w.E * 4
-    step_bytes = [b + router_bytes for b in ffn_bytes]
-    step_gbs = sum(step_bytes) / (sum(step_ms) / 1e3) / 1e9
-
-    # end to end through the public API with host buffers: pinned x in, bf16 out back, per step
-    x_host = [x.cpu().pin_memory() for x in xs]
-    out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(xs[0])
-    e2e_s = 0.0
-    for i in range(W + K):
-        flush.fill_(i & 0xFF)
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        x_dev.copy_(x_host[i % n_batches], non_blocking=True)
-        step(x_dev)
-        out_host.copy_(buf.out, non_blocking=True)
-        torch.cuda.synchronize(dev)
-        if i >= W:
-            e2e_s += time.perf_counter() - t0
-    e2e_s = dist_max(e2e_s, ws, dev)
-    e2e = {"value": ws * w.T * K / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
-           "d2h_bytes_per_step": w.T * w.d * 2}
-
+    r = time_layer(w, dev, K, W, rot_layers=1 if prefill else ROT_LAYERS, n_batches=4 if prefill else N_BATCHES,
+                   ydt=L.MOE_BF16 if prefill else L.MOE_F32, min_ms=MIN_TIMED_MS, ws=ws, e2e=True)
+    R = r["R"]
+    value = ws * w.T * K * R / r["total_s"]
+    line_roof, extra = layer_roofline(w, r, hbm_peak, bf16_peak, bf16_sus, peak_kind)
+    e2e = {"value": ws * w.T * r["n_e2e"] / r["e2e_s"], "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
+           "d2h_bytes_per_step": w.T * w.d * 2, "passes": r["n_e2e"],
+           "launch": "per pass: pinned x copied in, one CUDA graph of the C-ABI calls, bf16 output copied out, "
+                     "stream synchronised"}
+    nested = None
+    if not prefill and not args.no_prefill and args.workload == "decode":
+        torch.cuda.empty_cache()
+        wp = WORKLOADS["prefill"]
+        rp = time_layer(wp, dev, 10, 3, rot_layers=1, n_batches=4, ydt=L.MOE_BF16, min_ms=MIN_TIMED_MS, ws=ws,
+                        e2e=False)
+        roof_p, extra_p = layer_roofline(wp, rp, hbm_peak, bf16_peak, bf16_sus, peak_kind)
+        nested = {"workload": wp.describe(), "value": ws * wp.T * 10 * rp["R"] / rp["total_s"], "unit": "tokens/s",
+                  "steps": 10, "passes_per_step": rp["R"], "ms_per_pass": pcts(rp["pass_ms"]),
+                  "roofline": roof_p, **extra_p, "clocks": rp["clocks"],
+                  "gpu_launches": 11 * 10 * rp["R"]}
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tps, steps, el, cores = time_oracle(w, prepare_oracle(w, list(range(4))), budget_s=args.cpu_seconds)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{steps} oracle layer passes ({el:.1f} s) over 4 rotating batches of "
-                         f"{min(w.T, ORACLE_MAX_TOKENS)} tokens of T={w.T}"}
-
+        cpu = cpu_baseline_line(w, args)
     if rank != 0:
         return
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
-        "ms_per_step": sum(step_ms) / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded)",
-        "config": {"workload": w.describe(), "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
-                   "activations": "bf16", "l2": "512 MiB buffer written between timed steps (outside events)",
-                   "batches": n_batches, "mean_active_experts": float(np.mean(n_active)),
-                   "launch": "one CUDA graph of the three C-ABI calls per step: moe_route, moe_permute, "
+        "ms_per_step": sum(r["step_ms"]) / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": DTYPE, "data": "synthetic (seeded)",
+        "config": {"workload": w.describe(), "tokens_per_pass": w.T, "passes_per_step": R,
+                   "tokens_per_step": w.T * R, "weights": "int8 block-32 + fp16 scales", "activations": "bf16",
+                   "l2": ("inputs larger than L2: pass i runs layer i % 4's weights (4 x 2.57 GB resident) on batch "
+                          "i % 16, about 200 MB of experts per pass; no flush" if not prefill else
+                          "inputs larger than L2: each pass reads all 513 experts (2.57 GB); no flush"),
+                   "layers_rotated": 1 if prefill else ROT_LAYERS, "batches": 4 if prefill else N_BATCHES,
+                   "mean_active_experts": r["n_active_mean"],
+                   "launch": "one CUDA graph of the three C-ABI calls per pass: moe_route, moe_permute, "
                              "moe_expert_ffn_combine (stages_ms: the same kernels as moe_expert_ffn and "
                              "moe_combine, one graph per stage, events between)",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": roofline,
-        "stages_ms": {"route_permute": sum(route_ms) / K, "expert_ffn": sum(ffn_ms) / K,
-                      "combine": sum(comb_ms) / K, "step_as_three_graphs": sum(staged_ms) / K},
-        "step_hbm_gbs": step_gbs,
-        "wall_s": wall,
+        "ms_per_pass": pcts(r["pass_ms"]),
+        "roofline": line_roof,
+        **extra,
+        "wall_s": r["wall"],
         "e2e": e2e,
         "cpu_baseline": cpu,
-        # kernels per step: decode 4 (router GEMV, top-k, bucketing, persistent expert FFN with
-        # the combine); prefill 11 (router GEMM, top-k, 3 bucketing, 5 expert FFN, combine)
-        "gpu_launches": (11 if prefill else 4) * K,
-        "clocks": clk,
+        # kernels per pass: decode 5 (router GEMV, top-k, bucketing, persistent expert FFN, combine);
+        # prefill 11 (router GEMM, top-k, 3 bucketing, 5 expert FFN, combine)
+        "gpu_launches": (11 if prefill else 5) * K * R,
+        "clocks": r["clocks"],
     }
+    if nested is not None:
+        line["prefill"] = nested
     print(json.dumps(line), flush=True)
+
+
+def layer_roofline(w, r, hbm_peak, bf16_peak, bf16_sus, peak_kind):
+    """The expert FFN's roofline entry for a one-layer workload, from time_layer's region 2."""
+    ffn_ms = r["ffn_ms"]
+    n = len(ffn_ms)
+    rows = w.P + w.T * w.n_shared
+    stages = {"route_permute": pcts(r["route_ms"]), "expert_ffn": pcts(ffn_ms), "combine": pcts(r["comb_ms"]),
+              "pass_as_three_graphs": pcts(r["staged_ms"])}
+    if w.T > 16:
+        # tensor-bound: algorithmic FLOPs of the expert FFN (gate, up and down over every row)
+        flops = 2.0 * rows * 3 * w.d * w.f
+        tflops = flops / (sum(ffn_ms) / 1e3 / n) / 1e12
+        router_flops = 2.0 * w.T * w.d * w.E
+        roof = {"kernel": "moe_expert_ffn (tcgen05 grouped GEMM: gate/up + SwiGLU, down)", "bound": "tensor",
+                "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tflops / bf16_peak,
+                "peak_kind": f"{peak_kind} dense bf16 burst (f16 has the same dense rate)",
+                "frac_of_sustained": tflops / bf16_sus if bf16_sus else None,
+                "int8_peak": None,
+                "int8_note": "tcgen05.mma kind::i8 does not exist for sm_103a (ptxas: Feature '.kind::i8' not "
+                             "supported on .target 'sm_103a'); the int8 codes enter f16 MMAs exactly",
+                "traffic": TRAFFIC["prefill"], "flops_per_launch": flops, "ms_per_launch": sum(ffn_ms) / n}
+        extra = {"stages_ms": stages,
+                 "router": {"ms": pcts(r["route_ms"])["median"], "flops": router_flops,
+                            "tflops": router_flops / (np.median(r["route_ms"]) / 1e3) / 1e12,
+                            "note": "route_permute stage: router GEMM + top-k + bucketing"}}
+    else:
+        small = w.T * w.d * 2 + rows * w.d * 4
+        byts = [(na + w.n_shared) * w.record_bytes + small for na in r["n_active"]]
+        achieved = sum(byts) / (sum(ffn_ms) / 1e3) / 1e9
+        roof = {"kernel": "moe_expert_ffn (persistent kernel: gate/up + SwiGLU, down)", "bound": "hbm",
+                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "peak_kind": f"{peak_kind} copy bandwidth", "frac_of_8tbs": achieved / 8000.0,
+                "traffic": TRAFFIC["decode"], "bytes_per_launch": float(np.mean(byts)),
+                "ms_per_launch": sum(ffn_ms) / n}
+        router_bytes = w.d * w.E * 4
+        step_bytes = [(na + w.n_shared) * w.record_bytes + small + router_bytes for na in r["n_active"]]
+        extra = {"stages_ms": stages,
+                 "pass_hbm_gbs": float(np.mean(step_bytes)) / (np.mean(r["pass_ms"]) / 1e3) / 1e9}
+    return roof, extra
 
 
 # ------------------------------------------------------------------ multi-layer workloads ---
@@ -436,10 +574,7 @@ def stack_cpu_baseline(w, rank, args):
     L-layer step by dividing its tokens/s by L."""
     if rank != 0 or args.no_cpu_baseline:
         return None
-    tps, steps, el, cores = time_oracle(w, prepare_oracle(w, list(range(4))), budget_s=args.cpu_seconds)
-    return {"value": tps / w.layers, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{steps} oracle passes ({el:.1f} s) of one layer (layer 0) over 4 rotating batches of "
-                      f"T={w.T}; tokens/s divided by the {w.layers} layers of a step"}
+    return cpu_baseline_line(w, args)
 
 
 def run_stack(args, ws, rank, local, w):
@@ -525,7 +660,7 @@ def run_stack(args, ws, rank, local, w):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": sum(step_ms) / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded)",
+        "dtype": DTYPE, "data": "synthetic (seeded)",
         "config": {"workload": w.describe(), "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
                    "resident_gb": need / 1e9, "activations": "bf16 residual stream",
                    "l2": "inputs larger than L2 (each step reads every layer's selected experts, ~10 GB)",
@@ -541,7 +676,7 @@ def run_stack(args, ws, rank, local, w):
         "e2e": {"value": ws * w.T * K_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
                 "d2h_bytes_per_step": w.T * w.d * 2, "steps": K_e2e, "launch": "eager C-ABI calls"},
         "cpu_baseline": cpu,
-        "gpu_launches": 5 * w.layers * K,  # per layer: norm, router GEMV, top-k, bucketing, expert FFN + combine
+        "gpu_launches": 6 * w.layers * K,  # per layer: norm, router GEMV, top-k, bucketing, expert FFN, combine
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -650,9 +785,9 @@ def run_tiered(args, ws, rank, local, w):
                 out_host.copy_(y, non_blocking=True)
             torch.cuda.synchronize(dev)
             wall += time.perf_counter() - t0
-            # per layer: norm, router GEMV, top-k, bucketing, expert FFN with the combine; with misses
-            # one more FFN call and a separate combine
-            launches[0] += sum(5 + 2 * (m > 0) for m in ts.layer_misses)
+            # per layer: norm, router GEMV, top-k, bucketing, expert FFN, combine; with misses one more
+            # expert FFN (the missed experts after their copies)
+            launches[0] += sum(6 + (m > 0) for m in ts.layer_misses)
         return wall
 
     try:
@@ -666,7 +801,7 @@ def run_tiered(args, ws, rank, local, w):
         barrier(ws)
         clk = clocks.stop()
         s1 = L.slot_table_stats(ts.table)
-        assert L.moe_read_status(ts.buf.ws) == 0, "a kernel reported an error during the timed steps"
+        assert ts.status() == 0, "a kernel reported an error during the timed steps"
     finally:
         ts.close()
     wall = dist_max(wall, ws, dev)
@@ -679,7 +814,7 @@ def run_tiered(args, ws, rank, local, w):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": 1e3 * wall / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded)",
+        "dtype": DTYPE, "data": "synthetic (seeded)",
         "config": {"workload": w.describe() + f", {w.slots} device slots, drift every {synth.DRIFT_EVERY} steps",
                    "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
                    "pool_gb": w.slots * rb / 1e9, "host_images": n_img,
@@ -712,8 +847,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="decode: skip the nested prefill measurement")
     ap.add_argument("--host-gb", type=float, default=24.0, help="pinned host memory for expert images (tiered)")
     ap.add_argument("--slot-policy", choices=["lru", "freq"], default="lru",
                     help="tiered: replacement policy of the slot pool (LRU, or decayed use count)")

@@ -72,22 +72,22 @@ typedef enum {
 
 typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
 
-/* moe_expert_ffn kernel family. AUTO: DECODE when T <= 16 or x is fp32, else PREFILL.
- * DECODE streams each selected expert's int8 rows once per group of up to 8 of its tokens
- * (fp32 arithmetic on exactly dequantised weights). PREFILL is the tensor-core grouped
- * GEMM (bf16 operands after shared-memory dequantisation, fp32 accumulation); it
- * requires bf16 x. */
 /* Which expert-FFN kernels run (moe_expert_ffn). All give the same result within the bf16
  * tolerance; each is deterministic.
  *  DECODE   few tokens per expert: the int8 codes stream from HBM straight into f16
  *           tensor-core fragments (weights exact, x and h rounded once to f16 after a
  *           power-of-two rescale). T <= 8: one persistent cooperative kernel; 8 < T <= 16 (or
  *           shapes whose shared-memory staging does not fit): three kernels. xdt = MOE_F32
- *           selects the fp32 SIMT debug kernels instead.
+ *           (the fp32 debug mode), and DECODE asked for explicitly with T > 16, run the fp32
+ *           SIMT kernels instead: exact-weight fp32 arithmetic, far slower than either
+ *           tensor-core path.
  *  PREFILL  many tokens per expert: a tcgen05 grouped GEMM (activations by TMA, int8 weights
  *           converted to f16 into shared memory, fp32 accumulators in tensor memory). Needs
  *           xdt = MOE_BF16, d a multiple of 256 and f of 128 (else MOE_EUNSUPPORTED).
- *  AUTO     PREFILL when T > 16 and xdt = MOE_BF16, else DECODE. */
+ *  AUTO     xdt = MOE_F32: the fp32 SIMT kernels. xdt = MOE_BF16: DECODE for T <= 16 and
+ *           PREFILL for T > 16; a shape that PREFILL does not take with T > 16 returns
+ *           MOE_EUNSUPPORTED (nothing enqueued) rather than falling back to the SIMT kernels.
+ *           Ask for DECODE explicitly to run those. */
 typedef enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL = 2 } moe_mode;
 
 /* Problem shape. T tokens, model width d, expert hidden width f, E routed experts,
@@ -132,7 +132,12 @@ typedef struct {
 
 /* Bytes of workspace that moe_route / moe_permute / moe_expert_ffn need for this shape
  * (any mode, either dtype). One workspace serves one layer's calls from moe_route to
- * moe_combine. Its first 256 bytes hold the device status word. Host only. */
+ * moe_combine. Its first 256 bytes hold the device status word. Host only.
+ * The decode expert FFN keeps counters in the workspace that must read zero when it starts.
+ * moe_route clears them (and the status word) for its shape, and every moe_expert_ffn call
+ * leaves them at zero, even one whose wait ran out. So fill a new workspace with zeros before
+ * its first use (cudaMemset, torch.zeros), and again before using it with another shape, unless
+ * moe_route with that shape comes first. */
 moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes);
 
 /* Router and top-k ([P5] "MoE专家按需调度": the router picks the top-K experts per token).
@@ -183,7 +188,10 @@ moe_status moe_permute_static(const moe_shape* shape, const int32_t* topk_idx, i
                               int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos,
                               int32_t* active, int32_t* status, moe_stream_t stream);
 
-/* Expert FFN: for every expert in `active` (and every shared expert), for each of its rows
+/* Expert FFN ([P5] "MoE专家按需调度": only the experts the router picked compute for a token;
+ * [P2] "专家缓存": each is computed from its copy in the VRAM expert cache, found through the
+ * slot table; [P2] "三级存储分工": the resident shared expert applies to every token): for
+ * every expert in `active` (and every shared expert), for each of its rows
  * y = W_down (silu(W_gate x) * (W_up x)), silu(z) = z / (1 + e^-z), W = q * s per block of 32.
  * The expert's record is found through the slot table (experts->slot_of).
  *  x           [T][d] (xdt), the same activations given to moe_route
@@ -231,6 +239,16 @@ moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt
  *  eps  finite and >= 0 (MOE_EINVAL otherwise). */
 moe_status moe_rms_norm(const moe_shape* shape, const void* x, moe_dtype xdt, void* out,
                         moe_dtype odt, float eps, moe_stream_t stream);
+
+/* Limit of the bounded waits inside the expert-FFN kernels (a CTA waiting for work that other
+ * CTAs or its own warps publish), in nanoseconds, for every moe_expert_ffn /
+ * moe_expert_ffn_combine call made after this one in the process. 0 restores the default of
+ * 1 s, which no legitimate wait comes near. A wait that runs out sets MOE_DEV_TIMEOUT and the
+ * kernel abandons its remaining work; asynchronous copies and tensor-core operations already
+ * issued are still waited for (with the default limit) before the kernel exits. A short limit
+ * makes that failure path run on purpose, e.g. in a test, with no fault. MOE_EINVAL above
+ * 10 s. No counterpart on the pages: this is error handling of the kernels. */
+moe_status moe_set_wait_limit(uint64_t ns);
 
 /* Waits for `stream`, then returns the device status word of workspace `ws` in *h_status.
  * MOE_OK if it is zero, MOE_EDEVICE if not, MOE_ECUDA if the copy failed. */
@@ -307,7 +325,10 @@ moe_status slot_table_set_policy(moe_slot_table* table, int32_t policy, double h
  * one use = 1), added to the use counts. Then the empty slots, lowest index first, take the
  * non-resident experts of positive weight in decreasing order of use count (ties: lower
  * l*E + e first); their records are copied on copy_stream, the changed entries of d_slot_of
- * written after them, and `ready` (if not NULL) recorded. Nothing is evicted. *n_loaded (if
+ * written after them, and `ready` (if not NULL) recorded. Nothing is evicted. The loaded
+ * slots join the recency order after the slots still empty, in increasing order of use count
+ * (the highest count most recent), so that under MOE_SLOT_LRU the first evictions take the
+ * loaded experts the profile ranks lowest. *n_loaded (if
  * not NULL) receives the number of experts copied; bytes_h2d counts them, hits and misses do
  * not. MOE_EINVAL for a NULL table or weights or a negative or non-finite weight (nothing
  * changed); MOE_ECUDA if a copy fails (the experts copied before it stay resident). */

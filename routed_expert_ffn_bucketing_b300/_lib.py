@@ -64,6 +64,7 @@ _SIGS = {
                                          _P, _P, _P, C.c_int, _P, _P, _P, _P, C.c_int, _P, C.c_size_t, _P]),
     "moe_rms_norm": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, C.c_int, C.c_float, _P]),
     "moe_read_status": (C.c_int, [_P, _P, C.POINTER(C.c_int32)]),
+    "moe_set_wait_limit": (C.c_int, [C.c_uint64]),
     "moe_last_error_string": (C.c_char_p, []),
     "slot_table_create": (C.c_int, [C.POINTER(_P), C.c_int32, C.c_int32, C.c_int32, C.c_uint64, _P, _P, _P,
                                     MOE_COPY_FN, _P]),
@@ -188,6 +189,11 @@ def moe_read_status(ws, stream=None) -> int:
     if st not in (MOE_OK, MOE_EDEVICE):
         _check(st, "moe_read_status")
     return v.value
+
+
+def moe_set_wait_limit(ns: int) -> None:
+    """Limit (ns) of the expert-FFN kernels' bounded waits for later calls; 0 = the 1 s default."""
+    _check(lib().moe_set_wait_limit(ns), "moe_set_wait_limit")
 
 
 def moe_last_error_string() -> str:

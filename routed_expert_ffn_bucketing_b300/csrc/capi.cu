@@ -1,5 +1,6 @@
 // C-ABI entry points (include/moe.h): argument checks, workspace layout, kernel dispatch.
 // Every check happens on the host before any launch; a failed check enqueues nothing.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -28,6 +29,12 @@ static moe_status cuda_fail(cudaError_t e, const char* where) {
 }
 
 static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s
+constexpr uint64_t kMaxWaitNs = 10000000000ull;     // 10 s
+static std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 // Routed work items at most: experts with at least one pair.
 static size_t P_items(const moe_shape& s) {
@@ -62,8 +69,8 @@ WsLayout ws_layout(const moe_shape& s) {
   // stream-K scratch of the decode kernels (T <= 8): tasks per kernel at most items * max(f/8, d/16)
   const size_t sk_tasks = s.T <= 8 ? (P_items(s) + s.n_shared) * (s.f / 8 > s.d / 16 ? s.f / 8 : s.d / 16) : 0;
   L.zero = o;
-  L.item_done = o;
-  o = align256(o + sizeof(int32_t) * (P_items(s) + s.n_shared));
+  L.item_done = o;  // then the exit counter and the abort flag of the persistent kernel
+  o = align256(o + sizeof(int32_t) * (P_items(s) + s.n_shared + 2));
   L.hmax = o;
   o = align256(o + sizeof(uint32_t) * (P + T * s.n_shared));
   L.task_cnt = o;
@@ -217,17 +224,23 @@ moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(*shape);
   int* status = at<int>(ws, L.status);
-  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
-  if (e != cudaSuccess) return cuda_fail(e, "moe_route: clearing the status word");
-  if (shape->T == 0) return MOE_OK;
+  cudaError_t e;
+  if (shape->T == 0) {
+    e = cudaMemsetAsync(status, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_route: clearing the status word");
+    return MOE_OK;
+  }
+  // the router kernel clears the status word, and the counters the decode expert FFN keeps in
+  // this workspace, before anything reads them
   if (shape->T <= kRouteGemvMaxT) {
     float* partial = at<float>(ws, L.route_partial);
-    e = launch_route_gemv(*shape, x, xdt, w_router, partial, s);
+    e = launch_route_gemv(*shape, x, xdt, w_router, partial, status, at<uint8_t>(ws, L.zero), L.zero_end - L.zero,
+                          s);
     if (e == cudaSuccess)
       e = launch_topk_split(*shape, partial, route_splits(shape->d), topk_idx, topk_w, logits_opt, status, s);
   } else {
     float* logits = logits_opt ? logits_opt : at<float>(ws, L.logits);
-    e = launch_route_gemm(*shape, x, xdt, w_router, logits, s);
+    e = launch_route_gemm(*shape, x, xdt, w_router, logits, status, s);
     if (e == cudaSuccess) e = launch_topk(*shape, logits, topk_idx, topk_w, status, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "moe_route: launch");
@@ -308,6 +321,7 @@ moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x,
   a.ydt = ydt;
   a.h = at<float>(ws, L.h);
   a.status = at<int>(ws, L.status);
+  a.wait_ns = wait_limit_ns();
   a.T = shape->T;
   a.d = shape->d;
   a.f = shape->f;
@@ -335,12 +349,18 @@ moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x,
     e = launch_ffn_prefill(a, px, device_sm_count(), cs);
   } else if (mode == MOE_MODE_PREFILL) {
     return fail(MOE_EUNSUPPORTED, "moe_expert_ffn: PREFILL needs bf16 x, d a multiple of 256 and f of 128");
+  } else if (want_prefill) {
+    // AUTO never drops many tokens onto the SIMT kernels; DECODE asks for them explicitly
+    return fail(MOE_EUNSUPPORTED,
+                "moe_expert_ffn: AUTO with T=%d > %d needs the tensor-core GEMM (d a multiple of 256, f of 128; "
+                "here d=%d f=%d); pass MOE_MODE_DECODE to run the fp32 SIMT kernels",
+                shape->T, kDecodeMaxT, shape->d, shape->f);
   } else if (xdt == MOE_BF16 && persist_supported(a, device_sm_count())) {
     const size_t items_max = (P_items(*shape)) + shape->n_shared;
     const size_t sk_tasks = items_max * (shape->f / 8 > shape->d / 16 ? shape->f / 8 : shape->d / 16);
-    const PersistAux px{at<float>(ws, L.part),   at<int32_t>(ws, L.task_cnt), at<uint32_t>(ws, L.hmax),
-                        at<int32_t>(ws, L.item_done), sk_tasks * 2 * 128,     sk_tasks,
-                        at<uint8_t>(ws, L.zero), L.zero_end - L.zero};
+    const PersistAux px{at<float>(ws, L.part),       at<int32_t>(ws, L.task_cnt), at<uint32_t>(ws, L.hmax),
+                        at<int32_t>(ws, L.item_done), sk_tasks * 2 * 128,         sk_tasks,
+                        at<int32_t>(ws, L.item_done) + items_max};
     e = launch_ffn_persist(a, px, device_sm_count(), cs);
   } else if (xdt == MOE_BF16 && stream_supported(a)) {
     const size_t items_max = (P_items(*shape)) + shape->n_shared;
@@ -426,6 +446,12 @@ moe_status moe_rms_norm(const moe_shape* shape, const void* x, moe_dtype xdt, vo
   if (x == out && xdt != odt) return fail(MOE_EINVAL, "moe_rms_norm: in place needs xdt == odt");
   cudaError_t e = launch_rms_norm(*shape, x, xdt, out, odt, eps, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "moe_rms_norm: launch");
+  return MOE_OK;
+}
+
+moe_status moe_set_wait_limit(uint64_t ns) {
+  if (ns > kMaxWaitNs) return fail(MOE_EINVAL, "moe_set_wait_limit: %llu ns is above 10 s", (unsigned long long)ns);
+  g_wait_ns.store(ns ? ns : kDefaultWaitNs, std::memory_order_relaxed);
   return MOE_OK;
 }
 

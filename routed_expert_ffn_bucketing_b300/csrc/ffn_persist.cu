@@ -27,9 +27,11 @@
 // range covers about the same items as its gate/up range, so the waits of phase 2 are mostly on
 // work of the same or neighbouring CTAs.
 //
-// The counters (per-item tasks done, stream-K parts, row maxima) are zeroed by the launcher in
-// one memset before the kernel. Every wait is bounded: one that runs out sets MOE_DEV_TIMEOUT
-// and the CTA stops before its down work.
+// The counters (per-item tasks done, stream-K parts, row maxima) hold zeros at launch: moe_route
+// clears them, and every launch leaves them cleared (the finisher of a cut task resets its
+// counter; the last CTA out resets the rest), so no memset stands between the bucketing kernel
+// and this one and the kernel launches as its programmatic dependent. Every wait is bounded: one
+// that runs out sets MOE_DEV_TIMEOUT and the CTA stops before its down work.
 #include "decode_mma.cuh"
 #include "sm100_ptx.cuh"
 
@@ -108,11 +110,12 @@ __host__ __device__ inline PLayout p_layout(int T, int d, int f, int items_max, 
 
 struct PAux {
   float* part;         // [2][part_stride]: stream-K partial sums, 128 floats per part, 2 parts per task
-  int32_t* task_cnt;   // [2][cnt_stride]: stream-K parts finished per task (zeroed)
-  uint32_t* hmax;      // [rows]: bits of max |h| per h row (zeroed)
-  int32_t* item_done;  // [items]: gate/up tasks finished per item (zeroed)
+  int32_t* task_cnt;   // [2][cnt_stride]: stream-K parts finished per task (0 at launch)
+  uint32_t* hmax;      // [rows]: bits of max |h| per h row (0 at launch)
+  int32_t* item_done;  // [items]: gate/up tasks finished per item (0 at launch)
   size_t part_stride, cnt_stride;
   int rows_cap;
+  int32_t* exit;       // [2]: CTAs finished; abandoned work (0 at launch)
 };
 
 // What one lane needs for one task: the addresses it loads codes and scales from, and where its
@@ -420,7 +423,10 @@ __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const 
           __threadfence();
           __syncwarp();
           int second = 0;
-          if (lane == 0) second = atomicAdd(cnt + t, 1) == 1;
+          if (lane == 0) {
+            second = atomicAdd(cnt + t, 1) == 1;
+            if (second) cnt[t] = 0;  // both parts are in: the counter is free for the next launch
+          }
           finish = __shfl_sync(0xFFFFFFFFu, second, 0) != 0;
           if (finish) {
             __threadfence();
@@ -440,6 +446,31 @@ __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const 
       cur = nxt;
       t = tn;
     }
+  }
+}
+
+// End of every CTA: the last CTA to finish puts the counters back to zero for the next launch
+// (per-item tasks done, row maxima, the exit counter itself; all stream-K counters too if a
+// CTA abandoned its work, which leaves some of them unpaired). A stream-K counter is otherwise
+// reset by the warp that finishes its task.
+__device__ __forceinline__ void p_exit(const FfnArgs& A, const PAux& X, int rows, int items_max, int tid) {
+  __shared__ int s_last;
+  __syncthreads();  // every thread of this CTA is done with the counters
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(X.exit, 1) == (int)gridDim.x - 1;
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  for (int i = tid; i < items_max; i += kPThreads) X.item_done[i] = 0;
+  for (int r = tid; r < rows; r += kPThreads) X.hmax[r] = 0u;
+  if (__ldcg(X.exit + 1))
+    for (size_t i = tid; i < 2 * X.cnt_stride; i += kPThreads) X.task_cnt[i] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    X.exit[0] = 0;
+    X.exit[1] = 0;
   }
 }
 
@@ -465,15 +496,37 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   const int nbd = d / kQBlock, nbf = f / kQBlock;
 
   // ---- phase 0 --------------------------------------------------------------------------
-  // x blocks first: each thread loads one (token, block) of x and keeps it in registers, so
-  // these loads are not queued behind the weight loads issued below. (CTAs start at different
-  // blocks, so they do not all read the same lines at once.)
+  // Before the kernel's inputs from the bucketing kernel are complete (programmatic dependent
+  // launch: this grid may start while that kernel runs): x to f16 in shared memory, with one
+  // power of two per block over all tokens. x itself was written before the layer's first
+  // kernel started. (CTAs start at different blocks, so they do not all read the same lines.)
   const int rot = (int)((blockIdx.x * 7u) % (uint32_t)nbd);
   const bool xmine = tid < T * nbd;
   const int xb = (tid / T + rot) % nbd, xt = tid % T;
-  float xv[kQBlock];
-  if (xmine) load_bf16_block(static_cast<const uint16_t*>(A.x) + (size_t)xt * d + xb * kQBlock, xv);
-  for (int b = tid; b < nbd; b += kPThreads) bmax[b] = 0u;
+  const uint32_t o_sx = Lo.act, o_scx = Lo.act + (uint32_t)T * act_stride(d);
+  {
+    float xv[kQBlock];
+    if (xmine) load_bf16_block(static_cast<const uint16_t*>(A.x) + (size_t)xt * d + xb * kQBlock, xv);
+    for (int b = tid; b < nbd; b += kPThreads) bmax[b] = 0u;
+    __syncthreads();
+    if (xmine) {
+      float m = 0.0f;
+#pragma unroll
+      for (int q = 0; q < kQBlock; ++q) m = fmaxf(m, fabsf(xv[q]));
+      atomicMax(bmax + xb, __float_as_uint(m));
+    }
+    __syncthreads();
+    if (xmine) {
+      const int e = f16_exp_for(__uint_as_float(bmax[xb]));
+      const float down = pow2f(-e);
+#pragma unroll
+      for (int q = 0; q < kQBlock; ++q) xv[q] *= down;
+      *reinterpret_cast<float*>(psm + o_scx + (size_t)xt * sum_stride(d) + xb * 4) =
+          stage_block_f16(psm + o_sx + (size_t)xt * act_stride(d), xb, xv);
+      if (xt == 0) xe[xb] = pow2f(e);
+    }
+  }
+  pdl_wait();  // the active list, offsets and sorted pairs of this layer (and the slot table)
 
   // work items (row span kept even for an expert with no slot), row tokens
   const int n_active = A.active[0];
@@ -501,16 +554,9 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
     s_done[i] = 0;
   }
   for (int r = tid; r < rows; r += kPThreads) rowtok[r] = r < A.P ? A.sorted_pair[r] / A.k : (r - A.P) % T;
-  __syncthreads();
-  if (xmine) {
-    float m = 0.0f;
-#pragma unroll
-    for (int q = 0; q < kQBlock; ++q) m = fmaxf(m, fabsf(xv[q]));
-    atomicMax(bmax + xb, __float_as_uint(m));
-  }
+  __syncthreads();  // items, row tokens and the staged x are visible to every warp
 
   const int n_warps = gridDim.x * kPW, wid = blockIdx.x * kPW + warp;
-  const uint32_t o_sx = Lo.act, o_scx = Lo.act + (uint32_t)T * act_stride(d);
   long long G0, G1;
   const int gpt_gu = nbd / DG;
   warp_range(n_items * (f / 8), gpt_gu, wid, n_warps, &G0, &G1);
@@ -521,19 +567,6 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
     issue_group<DG>(p, hi_delta<kGU>(A), (int)(G0 % gpt_gu), rg, sring_w, slot, lane);
   }
   cp_async_commit();
-
-  // x to f16 in shared memory: one power of two per block over all tokens
-  __syncthreads();
-  if (xmine) {
-    const int e = f16_exp_for(__uint_as_float(bmax[xb]));
-    const float down = pow2f(-e);
-#pragma unroll
-    for (int q = 0; q < kQBlock; ++q) xv[q] *= down;
-    *reinterpret_cast<float*>(psm + o_scx + (size_t)xt * sum_stride(d) + xb * 4) =
-        stage_block_f16(psm + o_sx + (size_t)xt * act_stride(d), xb, xv);
-    if (xt == 0) xe[xb] = pow2f(e);
-  }
-  __syncthreads();
 
   // ---- phase 1: gate/up ----------------------------------------------------------------
   p_stream<kGU, DG>(A, X, psm, items, rowtok, o_sx, o_scx, Lo.xe, hexp, sring_w, sring_p, G0, G1, gpt_gu, rg, slot,
@@ -581,7 +614,7 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(X.item_done + i) : "memory");
         if (v >= need) break;
-        if ((k & 15u) == 15u && globaltimer_ns() - t0 > kWaitNs) {
+        if ((k & 15u) == 15u && globaltimer_ns() - t0 > A.wait_ns) {
           ok = 0;
           break;
         }
@@ -591,8 +624,12 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   }
   __syncthreads();  // also: every warp of this CTA is past gate/up, so the x rows may be overwritten
   if (!s_ok) {
-    if (tid == 0) flag_status(A.status, MOE_DEV_TIMEOUT_BIT);
+    if (tid == 0) {
+      flag_status(A.status, MOE_DEV_TIMEOUT_BIT);
+      atomicExch(X.exit + 1, 1);  // stream-K counters of this CTA's down tasks stay unpaired
+    }
     cp_async_wait_all();
+    p_exit(A, X, rows, items_max, tid);
     return;
   }
   for (int r = r_lo + tid; r < r_hi; r += kPThreads) hexp[r] = f16_exp_for(__uint_as_float(__ldcg(X.hmax + r)));
@@ -620,6 +657,7 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   p_stream<kDN, DD>(A, X, psm, items, rowtok, o_sh, o_sch, 0u, hexp, sring_w, sring_p, G0, G1, gpt_dn, rd, slot,
                     lane, s_done);
   cp_async_wait_all();
+  p_exit(A, X, rows, items_max, tid);
 }
 
 int persist_rows_cap(const FfnArgs& a, int sm_count) {
@@ -641,18 +679,12 @@ cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int sm_count
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_persist_kernel<DG, DD>, kPThreads, L.total);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  PAux px{x.part, x.task_cnt, x.hmax, x.item_done, x.part_stride, x.cnt_stride, rows_cap};
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sm_count);
-  cfg.blockDim = dim3(kPThreads);
-  cfg.dynamicSmemBytes = L.total;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, ffn_persist_kernel<DG, DD>, a, px);
+  PAux px{x.part, x.task_cnt, x.hmax, x.item_done, x.part_stride, x.cnt_stride, rows_cap, x.exit};
+  // One CTA per SM (the occupancy check above: a CTA takes every register of its SM), launched as
+  // a programmatic dependent of the bucketing kernel before it: the CTAs stage x while the
+  // bucketing runs and wait for its outputs (griddepcontrol.wait). Every CTA's waits for other
+  // CTAs are bounded, so the grid needs no cooperative launch to be safe.
+  return launch_pdl(ffn_persist_kernel<DG, DD>, dim3(sm_count), dim3(kPThreads), L.total, st, a, px);
 }
 
 }  // namespace
@@ -669,8 +701,6 @@ bool persist_supported(const FfnArgs& a, int sm_count) {
 }
 
 cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(x.zero, 0, x.zero_bytes, st);
-  if (e != cudaSuccess) return e;
   const bool g8 = (a.d / kQBlock) % 8 == 0, d8 = (a.f / kQBlock) % 8 == 0;
   if (g8 && d8) return launch_persist_d<8, 8>(a, x, sm_count, st);
   if (g8) return launch_persist_d<8, 4>(a, x, sm_count, st);

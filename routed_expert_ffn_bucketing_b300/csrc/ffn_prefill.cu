@@ -36,7 +36,9 @@
 // of two that puts its max |x| in [2^14, 2^15)), and h is rescaled per row the same way.
 //
 // Every wait is bounded. A wait that runs out sets MOE_DEV_TIMEOUT and the CTA stops its work;
-// every role still reaches the final barrier, so the TMEM columns are always freed.
+// every role still reaches the final barrier, so the TMEM columns are always freed. Before
+// that, the A producer waits for its TMA copies still in flight and the MMA thread for its
+// last tcgen05.mma (a final commit to the drain barrier), with the default limit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -69,6 +71,7 @@ struct PHead {
   uint64_t b_empty[kPBStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t drain;  // the MMA thread's last commit: every MMA it issued has completed
   uint32_t tmem;
   int abort;
 };
@@ -362,6 +365,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
       mbar_init(&H.acc_full[b], 1);
       mbar_init(&H.acc_empty[b], 4);
     }
+    mbar_init(&H.drain, 1);
     H.abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_a);
@@ -384,7 +388,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
         PWork wk;
         if (!work_at<KIND>(A, X, w, nch, &wk)) continue;
         for (int kc = 0; kc < KC; ++kc) {
-          if (!mbar_wait(&H.a_empty[s], ph ^ 1u)) {
+          if (!mbar_wait(&H.a_empty[s], ph ^ 1u, A.wait_ns)) {
             p_set_abort(H, A.status);
             break;
           }
@@ -396,7 +400,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
       }
       if (p_aborted(H))  // no copy may still be landing in shared memory when the CTA exits
         for (int j = issued > kPAStages ? issued - kPAStages : 0; j < issued; ++j)
-          mbar_wait(&H.a_full[j % kPAStages], (j / kPAStages) & 1);
+          mbar_wait(&H.a_full[j % kPAStages], (j / kPAStages) & 1);  // default limit
+
     }
   } else if (warp >= 1 && warp <= kPConv) {
     // ---------------- converters ----------------
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
         if (!have[j]) break;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const bool w2 = mbar_wait(&H.b_empty[sb], pb ^ 1u);
+          const bool w2 = mbar_wait(&H.b_empty[sb], pb ^ 1u, A.wait_ns);
           if (!__all_sync(0xFFFFFFFFu, w2 && !p_aborted(H))) {
             if (lane == 0) p_set_abort(H, A.status);
             ok = false;
@@ -464,7 +469,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
         PWork wk;
         if (!work_at<KIND>(A, X, w, nch, &wk)) continue;
         const int buf = lt & 1;
-        if (!mbar_wait(&H.acc_empty[buf], ((lt >> 1) & 1) ^ 1u)) {
+        if (!mbar_wait(&H.acc_empty[buf], ((lt >> 1) & 1) ^ 1u, A.wait_ns)) {
           p_set_abort(H, A.status);
           break;
         }
@@ -472,7 +477,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
         const uint32_t d_tmem = tmem + (uint32_t)(buf * kPN);
         bool ok = true;
         for (int kc = 0; kc < KC; ++kc) {
-          if (!mbar_wait(&H.a_full[sa], pa) || !mbar_wait(&H.b_full[sb], pb) || p_aborted(H)) {
+          if (!mbar_wait(&H.a_full[sa], pa, A.wait_ns) || !mbar_wait(&H.b_full[sb], pb, A.wait_ns) ||
+              p_aborted(H)) {
             p_set_abort(H, A.status);
             ok = false;
             break;
@@ -492,6 +498,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
         umma_commit(&H.acc_full[buf]);
         ++lt;
       }
+      // Drain: one more commit arrives once every MMA this thread issued has completed,
+      // including those left queued when a wait above ran out. TMEM and the rings are freed
+      // only after it (waited for with the default limit, not the caller's shorter one).
+      umma_commit(&H.drain);
+      mbar_wait(&H.drain, 0);
     }
   } else if (warp >= kPEpiWarp0) {
     // ---------------- epilogue ----------------
@@ -502,7 +513,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
       PWork wk;
       if (!work_at<KIND>(A, X, w, nch, &wk)) continue;
       const int buf = lt & 1;
-      const bool ok = mbar_wait(&H.acc_full[buf], (lt >> 1) & 1) && !p_aborted(H);
+      const bool ok = mbar_wait(&H.acc_full[buf], (lt >> 1) & 1, A.wait_ns) && !p_aborted(H);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         if (lane == 0) p_set_abort(H, A.status);
         break;
@@ -567,8 +578,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
       ++lt;
     }
   }
-  // Every role ends here. The MMA thread's last commit has been waited for by the epilogue, or
-  // the work was abandoned; wait (bounded) for the tensor core to finish before freeing TMEM.
+  // Every role ends here. The MMA thread has waited for its drain commit, so no MMA is still
+  // reading the rings or writing TMEM, and the A producer has waited for its copies in flight.
   tc_fence_before();
   __syncthreads();
   if (warp == kPMmaWarp) {

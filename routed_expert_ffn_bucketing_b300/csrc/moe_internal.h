@@ -79,6 +79,7 @@ struct FfnArgs {
   int ydt;
   float* h;  // fp32 [P + T*n_shared][f]
   int* status;
+  uint64_t wait_ns;  // limit of the kernels' bounded waits for other threads' work (moe_set_wait_limit)
   int T, d, f, E, k, n_shared, P;
   // record layout
   uint64_t o_gate_q, o_up_q, o_down_q, o_gate_s, o_up_s, o_down_s;
@@ -114,16 +115,15 @@ struct StreamAux {
 };
 
 
-// Workspace buffers of the persistent decode expert FFN. [zero, zero + zero_bytes) holds
-// item_done, hmax and task_cnt and is cleared by the launcher before the kernel.
+// Workspace buffers of the persistent decode expert FFN. item_done, hmax, task_cnt and exit
+// hold zeros when the kernel starts (moe_route clears them, and each launch leaves them so).
 struct PersistAux {
   float* part;         // [2][part_stride]
   int32_t* task_cnt;   // [2][cnt_stride]
   uint32_t* hmax;      // [P + T*n_shared]
   int32_t* item_done;  // [min(E, P) + n_shared]
   size_t part_stride, cnt_stride;
-  void* zero;
-  size_t zero_bytes;
+  int32_t* exit;       // [2]: CTAs finished, and 1 if one of them abandoned its work
 };
 
 // Workspace buffers of the prefill (tensor-core GEMM) expert FFN.
@@ -141,13 +141,15 @@ struct PrefillAux {
 };
 
 // Launchers; each returns cudaSuccess or the launch error.
+// The router GEMV also sets *status to 0 and clears zero[0, zero_bytes) (16-byte aligned, a
+// multiple of 16 bytes) before any other kernel of the layer reads them.
 cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
-                              cudaStream_t st);
+                              int* status, void* zero, size_t zero_bytes, cudaStream_t st);
 // Top-k from the router GEMV's split partial sums [splits][T][E]: one CTA per token.
 cudaError_t launch_topk_split(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
                               float* logits_out, int* status, cudaStream_t st);
 cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const float* w, float* logits,
-                              cudaStream_t st);
+                              int* status, cudaStream_t st);
 // Top-k of logits already summed (after the router GEMM): one warp per token.
 cudaError_t launch_topk(const moe_shape& s, const float* logits, int32_t* idx, float* wts, int* status,
                         cudaStream_t st);
@@ -167,6 +169,8 @@ bool persist_supported(const FfnArgs& a, int sm_count);
 cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, int sm_count, cudaStream_t st);
 bool prefill_supported(const FfnArgs& a);
 int device_sm_count();
+// The limit, in nanoseconds, that the next expert-FFN launches give their bounded waits.
+uint64_t wait_limit_ns();
 cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,
                            const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st);
 cudaError_t launch_rms_norm(const moe_shape& s, const void* x, int xdt, void* out, int odt, float eps,

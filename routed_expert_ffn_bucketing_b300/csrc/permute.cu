@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(1024) bucket_count_kernel(const int32_t* __res
   __shared__ int warp_sums[33];
   const int i = threadIdx.x;
   int e = 0;
+  pdl_trigger();  // the expert FFN may launch and stage its activations meanwhile
   pdl_wait();  // topk_idx from the router
   if (i < P) {
     e = topk_idx[i];

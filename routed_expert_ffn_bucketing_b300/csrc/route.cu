@@ -112,9 +112,16 @@ template <int TT, int VEC>
 __global__ void __launch_bounds__(256) router_gemv_kernel(const void* __restrict__ x, int xdt,
                                                           const float* __restrict__ w,
                                                           float* __restrict__ partial, int T, int d,
-                                                          int E) {
+                                                          int E, int* status, uint4* zero, int zero_n16) {
   constexpr int R = kRouteRowsPerSplit;  // rows of d per CTA
   pdl_trigger();  // the top-k kernel may launch now; it waits for this grid before reading
+  // this launch is ordered after every earlier kernel of the stream: clear the layer's status
+  // word and the expert FFN's counters here, so no memset precedes the pass
+  {
+    const int cta = blockIdx.y * gridDim.x + blockIdx.x, n_cta = gridDim.x * gridDim.y;
+    if (cta == 0 && threadIdx.x == 0) *status = 0;
+    for (int i = cta * blockDim.x + threadIdx.x; i < zero_n16; i += n_cta * blockDim.x) zero[i] = make_uint4(0, 0, 0, 0);
+  }
   constexpr int COLS = 32 * VEC;         // experts per CTA
   extern __shared__ float sm[];
   float* xs = sm;            // [TT][R]
@@ -178,31 +185,32 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const void* __restrict
 
 template <int TT, int VEC>
 static cudaError_t gemv_launch(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
-                               cudaStream_t st) {
+                               int* status, void* zero, size_t zero_bytes, cudaStream_t st) {
   constexpr int COLS = 32 * VEC;
   const size_t smem = sizeof(float) * (TT * kRouteRowsPerSplit + 8 * TT * COLS);
   auto kern = router_gemv_kernel<TT, VEC>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   dim3 grid((s.E + COLS - 1) / COLS, route_splits(s.d));
-  kern<<<grid, 256, smem, st>>>(x, xdt, w, partial, s.T, s.d, s.E);
+  kern<<<grid, 256, smem, st>>>(x, xdt, w, partial, s.T, s.d, s.E, status, static_cast<uint4*>(zero),
+                                (int)(zero_bytes / 16));
   return cudaGetLastError();
 }
 
 template <int VEC>
-static cudaError_t gemv_dispatch_t(const moe_shape& s, const void* x, int xdt, const float* w, float* p,
-                                   cudaStream_t st) {
-  if (s.T <= 1) return gemv_launch<1, VEC>(s, x, xdt, w, p, st);
-  if (s.T <= 2) return gemv_launch<2, VEC>(s, x, xdt, w, p, st);
-  if (s.T <= 4) return gemv_launch<4, VEC>(s, x, xdt, w, p, st);
-  if (s.T <= 8) return gemv_launch<8, VEC>(s, x, xdt, w, p, st);
-  return gemv_launch<16, VEC>(s, x, xdt, w, p, st);
+static cudaError_t gemv_dispatch_t(const moe_shape& s, const void* x, int xdt, const float* w, float* p, int* status,
+                                   void* z, size_t zb, cudaStream_t st) {
+  if (s.T <= 1) return gemv_launch<1, VEC>(s, x, xdt, w, p, status, z, zb, st);
+  if (s.T <= 2) return gemv_launch<2, VEC>(s, x, xdt, w, p, status, z, zb, st);
+  if (s.T <= 4) return gemv_launch<4, VEC>(s, x, xdt, w, p, status, z, zb, st);
+  if (s.T <= 8) return gemv_launch<8, VEC>(s, x, xdt, w, p, status, z, zb, st);
+  return gemv_launch<16, VEC>(s, x, xdt, w, p, status, z, zb, st);
 }
 
 cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
-                              cudaStream_t st) {
-  if (s.E % 4 == 0) return gemv_dispatch_t<4>(s, x, xdt, w, partial, st);
-  return gemv_dispatch_t<1>(s, x, xdt, w, partial, st);
+                              int* status, void* zero, size_t zero_bytes, cudaStream_t st) {
+  if (s.E % 4 == 0) return gemv_dispatch_t<4>(s, x, xdt, w, partial, status, zero, zero_bytes, st);
+  return gemv_dispatch_t<1>(s, x, xdt, w, partial, status, zero, zero_bytes, st);
 }
 
 // ------------------------------------------------------------------ tiled GEMM -------------
@@ -211,7 +219,10 @@ cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const 
 // Every 32 k the block sum is added to the running total (two-level accumulation).
 __global__ void __launch_bounds__(256) router_gemm_kernel(const void* __restrict__ x, int xdt,
                                                           const float* __restrict__ w,
-                                                          float* __restrict__ out, int T, int d, int E) {
+                                                          float* __restrict__ out, int T, int d, int E,
+                                                          int* status) {
+  // ordered after every earlier kernel of the stream, and before the top-k that flags NaNs
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
   __shared__ __align__(16) float As[2][8][128];  // [k][token]
   __shared__ __align__(16) float Bs[2][8][128];  // [k][expert]
   const int tid = threadIdx.x;
@@ -295,9 +306,9 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const void* __restrict
 }
 
 cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const float* w, float* logits,
-                              cudaStream_t st) {
+                              int* status, cudaStream_t st) {
   dim3 grid((s.E + 127) / 128, (s.T + 127) / 128);
-  router_gemm_kernel<<<grid, 256, 0, st>>>(x, xdt, w, logits, s.T, s.d, s.E);
+  router_gemm_kernel<<<grid, 256, 0, st>>>(x, xdt, w, logits, s.T, s.d, s.E, status);
   return cudaGetLastError();
 }
 

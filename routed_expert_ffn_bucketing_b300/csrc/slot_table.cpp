@@ -387,6 +387,13 @@ moe_status slot_table_warm(moe_slot_table* t, const float* h_weight, moe_stream_
     t->stats.bytes_h2d += t->slot_bytes;
     ++loaded;
   }
+  // LRU order of the loaded slots: the lowest weight least recent, the highest weight most
+  // recent, all after the slots still empty. Under LRU the first evictions then take the
+  // experts the profile ranks lowest, not the best ones.
+  for (int32_t j = loaded - 1; j >= 0; --j) {
+    lru_unlink(t, empty[j]);
+    lru_push_tail(t, empty[j]);
+  }
   if (write_entries(t, changed, copy_stream) != 0 && rc == MOE_OK)
     rc = slot_fail(MOE_ECUDA, "slot_table: writing the device table failed");
   if (ready && cudaEventRecord(reinterpret_cast<cudaEvent_t>(ready), reinterpret_cast<cudaStream_t>(copy_stream)) !=

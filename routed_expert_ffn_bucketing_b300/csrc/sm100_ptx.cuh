@@ -1,8 +1,9 @@
 // Inline-PTX helpers for the sm_103a kernels: mbarriers with time-bounded waits, bulk and
 // tensor (TMA) copies, and the tcgen05 tensor-core / tensor-memory instructions.
 //
-// Every wait here gives up after kWaitNs nanoseconds of the global timer and returns false,
-// so that a kernel whose copies or MMAs never complete reports an error instead of hanging.
+// Every wait here gives up after a limit in nanoseconds of the global timer (kWaitNs unless
+// the caller passes one) and returns false, so that a kernel whose copies or MMAs never
+// complete reports an error instead of hanging.
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -47,14 +48,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return done != 0;
 }
 
-// Waits for the completion of the phase with parity `parity`; false if kWaitNs ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Waits for the completion of the phase with parity `parity`; false if limit_ns ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((i & 15u) == 0 && globaltimer_ns() - t0 > kWaitNs) return false;
+    if ((i & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

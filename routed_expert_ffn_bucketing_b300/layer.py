@@ -57,7 +57,8 @@ def alloc_buffers(shape: L.moe_shape, device="cuda", ydt: int = L.MOE_F32, odt: 
         active=torch.empty(1 + min(E, max(P, 1)), **i32),
         y_perm=torch.empty((P + T * ns, d), dtype=_dt(ydt), device=device),
         out=torch.empty((T, d), dtype=_dt(odt), device=device),
-        ws=torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device),
+        # zero-filled once: the decode expert FFN keeps counters here that each call leaves at zero
+        ws=torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=device),
         ydt=ydt,
         odt=odt,
     )

@@ -83,6 +83,9 @@ class TieredStack:
         self.shared = shared  # per layer: n_shared records (device, uint8)
         self.table = L.slot_table_create(n_layers, shape.E, n_slots, slot_bytes, self.pool, self.slot_of, h_records)
         self.buf = lay.alloc_buffers(shape, device=device, ydt=L.MOE_F32, odt=L.MOE_BF16, keep_logits=False)
+        # the missed experts' FFN call has its own shape (no shared expert) and so its own
+        # workspace layout: it gets its own zero-filled workspace
+        self.ws_miss = torch.zeros(L.moe_workspace_size(self.shape_routed), dtype=torch.uint8, device=device)
         self.resid = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=device)
         self.xn = torch.empty_like(self.resid)
         self.copy_stream = torch.cuda.Stream(device)
@@ -109,6 +112,10 @@ class TieredStack:
             self.n_warm = L.slot_table_warm(self.table, w.ctypes.data, self.copy_stream.cuda_stream,
                                             self.ready.cuda_event)
             self.ready.synchronize()
+
+    def status(self) -> int:
+        """The device status words of both workspaces, OR-ed (waits for the current stream)."""
+        return L.moe_read_status(self.buf.ws) | L.moe_read_status(self.ws_miss)
 
     def close(self):
         if self.table:
@@ -157,7 +164,8 @@ class TieredStack:
                     # the missed experts only (a shape without the shared expert, already done), then
                     # the combine of the full layer
                     L.moe_expert_ffn(self.shape_routed, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, routed, b.offsets,
-                                     b.sorted_pair, self.d_misses, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
+                                     b.sorted_pair, self.d_misses, b.y_perm, b.ydt, self.ws_miss,
+                                     self.ws_miss.numel(), stream)
                     L.moe_combine(s, b.y_perm, b.ydt, *comb, stream)
                 else:
                     stream.wait_event(self.ready)

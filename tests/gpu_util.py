@@ -105,6 +105,38 @@ def check_bucketing(run: GpuRun, w: Workload):
     assert act[0] == b.active.size and np.array_equal(act[1:1 + act[0]], b.active)
 
 
+def check_expert_rows(run: GpuRun, w: Workload, experts, layer: int = 0, tol: float = TOL_BF16,
+                      rows: dict | None = None):
+    """Whole experts' y_perm rows against the oracle's SwiGLU FFN of the same tokens: for a
+    routed expert e < E its rows offsets[e]..offsets[e+1] (tokens sorted_pair // k), for shared
+    expert s = e - E its T rows (token order). rows[e] may name a sub-range of an expert's
+    rows (relative to its first row). max |y - y_oracle| <= tol * rms(y_oracle) per expert.
+    Returns {e: (n_rows, err / rms)}."""
+    offs = run.buf.offsets.cpu().numpy()
+    sp = run.buf.sorted_pair.cpu().numpy()
+    out = {}
+    for e in experts:
+        e = int(e)
+        if e < w.E:
+            r0, r1 = int(offs[e]), int(offs[e + 1])
+            toks = sp[r0:r1] // w.k
+        else:
+            r0 = w.P + (e - w.E) * w.T
+            r1 = r0 + w.T
+            toks = np.arange(w.T)
+        if rows and e in rows:
+            a, b = rows[e]
+            toks = toks[a:b]
+            r0, r1 = r0 + a, r0 + b
+        assert r1 > r0, (e, r0, r1)
+        y = run.buf.y_perm[r0:r1].float().cpu().numpy().astype(np.float64)
+        ref = O.swiglu_ffn(run.x_np[toks], O.dense_expert(cached_expert(w, layer, e)))
+        err, r = float(np.max(np.abs(y - ref))), O.rms(ref)
+        assert err <= tol * r, (e, r1 - r0, err, r)
+        out[e] = (r1 - r0, err / r)
+    return out
+
+
 def bf16_ulp(v: np.ndarray) -> np.ndarray:
     """Spacing of bf16 values at |v| (8 significant bits)."""
     _, e = np.frexp(np.abs(v))

@@ -394,6 +394,25 @@ def test_slot_table_warm_fills_empty_slots_from_the_profile():
     L.slot_table_destroy(h)
 
 
+def test_slot_table_warm_under_lru_evicts_the_lowest_weight_first():
+    # 4 slots, 3 warm experts: the empty slot goes first, then warm experts from the lowest
+    # weight up, the profile's best expert last
+    h, cp, hrec = _make_table(1, 16, 4)
+    w = np.zeros(16, dtype=np.float32)
+    w[[2, 9, 5]] = [1.0, 7.0, 3.0]
+    assert L.slot_table_warm(h, w.ctypes.data) == 3
+    assert _resident(h, 1, 16) == {(0, 2), (0, 9), (0, 5)}
+    _update(h, 0, [11])                      # takes the empty slot
+    assert _resident(h, 1, 16) == {(0, 2), (0, 9), (0, 5), (0, 11)}
+    _update(h, 0, [12])                      # evicts expert 2 (weight 1)
+    assert _resident(h, 1, 16) == {(0, 9), (0, 5), (0, 11), (0, 12)}
+    _update(h, 0, [13])                      # then expert 5 (weight 3)
+    assert _resident(h, 1, 16) == {(0, 9), (0, 11), (0, 12), (0, 13)}
+    _update(h, 0, [14])                      # then expert 9: warm loads are older than any use
+    assert _resident(h, 1, 16) == {(0, 11), (0, 12), (0, 13), (0, 14)}
+    L.slot_table_destroy(h)
+
+
 def test_slot_table_warm_weights_seed_the_counts():
     # under FREQ a profile weight counts like uses: expert 1 (weight 10) outlives expert 0
     # (two real uses) when a miss needs a slot
@@ -442,3 +461,12 @@ def test_slot_table_errors_carry_a_message():
     L.slot_table_destroy(h)
     with pytest.raises(L.MoeError, match="slot_table_create"):
         L.slot_table_create(1, 4, 0, 256, 0, 0, [1, 2, 3, 4], FakeCopier(0, 0, 256, None).fn, None)
+
+
+def test_wait_limit_argument_check():
+    # no CUDA call: the limit is host state that later launches copy into their arguments
+    with pytest.raises(L.MoeError) as e:
+        L.moe_set_wait_limit(11_000_000_000)
+    assert e.value.status == L.MOE_EINVAL and "10 s" in L.moe_last_error_string()
+    L.moe_set_wait_limit(5_000_000)
+    L.moe_set_wait_limit(0)

@@ -11,7 +11,7 @@ from routed_expert_ffn_bucketing_b300 import _lib as L
 from synth.device import DeviceLayer
 from synth.workloads import WORKLOADS, custom
 
-from gpu_util import check_bucketing, check_output, check_routing, run_layer
+from gpu_util import check_bucketing, check_expert_rows, check_output, check_routing, run_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -208,6 +208,25 @@ def test_prefill_layer_full_size():
     assert n_checked >= w.T - 8
     check_bucketing(run, w)
     check_output(run, w, tokens=np.array([0, 1, 77, 1023, 3333, 4096, 5000, 8191]))
+    # whole experts' rows of y_perm, chosen to cover the GEMM's tile walk at full size (6
+    # column tiles of gate/up at f = 768, 8 of down at d = 2048): the heaviest Zipf expert
+    # (every one of its 128-row M tiles, the partial last one included), a mid-rank expert, the
+    # three experts with the fewest rows (one partial M tile each), the last three experts of
+    # the tile list, and the shared expert's first and last M tiles
+    counts = run.buf.counts.cpu().numpy()
+    act = np.nonzero(counts)[0]
+    heavy = int(act[np.argmax(counts[act])])
+    assert counts[heavy] > 4 * 128 and counts[heavy] % 128, counts[heavy]
+    by_count = act[np.argsort(counts[act], kind="stable")]
+    mid = int(by_count[by_count.size // 2])
+    fewest = [int(e) for e in by_count[:3]]
+    last = [int(e) for e in act[-3:]]
+    assert max(counts[fewest]) < 128
+    shared = w.E
+    got = check_expert_rows(run, w, sorted({heavy, mid, *fewest, *last}) + [shared],
+                            rows={shared: (w.T - 128 - 64, w.T)})
+    got.update(check_expert_rows(run, w, [shared], rows={shared: (0, 128)}))
+    assert got[heavy][0] == counts[heavy]
 
 
 @pytest.mark.parametrize("wl,mode,residual,odt,ydt", [

@@ -23,7 +23,11 @@ pytestmark = pytest.mark.gpu
 
 def check_layers(w, keep, layers):
     """keep: the ('in', x), ('idx', topk), ('out', y) records of a stack run. Each layer is
-    x + MoE(n(x)) with n the oracle's RMS normalisation."""
+    x + MoE(bf16(n(x))) with n the oracle's RMS normalisation: the normalised input is a bf16
+    activation tensor like every layer input, so the oracle rounds it once to bf16 (its own
+    rounding, pinned on its own) before routing and the experts. Without that rounding the
+    gate weights alone differ by about 2^-9 of a logit's size (logits of tens), which moves
+    outputs by up to a few percent of their rms."""
     recs = [keep[i:i + 3] for i in range(0, len(keep), 3)]
     assert len(recs) == len(layers)
     for l, (a, b, c) in zip(layers, recs):
@@ -31,8 +35,8 @@ def check_layers(w, keep, layers):
         x_np = a[1].float().cpu().numpy().astype(np.float64)
         idx = b[1].cpu().numpy()
         shared = [cached_expert(w, l, w.E + s) for s in range(w.n_shared)]
-        moe = O.moe_layer(O.rms_norm(x_np), w.router(l), w.k, lambda e: cached_expert(w, l, e), shared,
-                          forced_idx=idx)
+        xn = O.round_to_bf16(O.rms_norm(x_np))
+        moe = O.moe_layer(xn, w.router(l), w.k, lambda e: cached_expert(w, l, e), shared, forced_idx=idx)
         ref = x_np + moe.out
         out = c[1].float().cpu().numpy().astype(np.float64)
         err, r = np.max(np.abs(out - ref)), O.rms(ref)
@@ -90,6 +94,56 @@ def test_decode_stack_layer_by_layer():
     check_layers(w, keep, range(w.layers))
 
 
+def test_decode_stack_full_shape_three_layers():
+    # three consecutive layers of the 48-layer stack at its real shape (d = 2048, f = 768,
+    # E = 512, top-10 + 1 shared, Zipf(1.1) routing), each against the oracle on its own input
+    w = custom("stack", layers=3)
+    dls = [DeviceLayer(w, layer=l) for l in range(w.layers)]
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    layers = [LayerWeights(dl.router, L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr))
+              for dl in dls]
+    st = DecodeStack(s, layers)
+    for batch in (0, 1):
+        keep = []
+        st.forward(dls[0].x(batch), keep=keep)
+        assert L.moe_read_status(st.buf.ws) == 0
+        torch.cuda.synchronize()
+        check_layers(w, keep, range(w.layers))
+
+
+def test_tiered_step_full_width():
+    # the tiered path at the full layer width (d = 2048, f = 768, top-10 + 1 shared): 2 layers of
+    # 64 experts in pinned host memory, 48 device slots, so a step's two layers (about 36
+    # experts each) cannot both stay resident: misses, evictions and copies every step
+    from synth.gpu import fill_expert_records
+    w = custom("stack", E=64, layers=2)
+    n_slots = 48
+    rb = w.record_bytes
+    n_all = w.layers * w.E
+    host = torch.empty((n_all, rb), dtype=torch.uint8).pin_memory()
+    tmp = torch.empty((w.E, rb), dtype=torch.uint8, device="cuda")
+    for l in range(w.layers):
+        fill_expert_records(w.seed, l, 0, w.E, w.d, w.f, tmp.data_ptr(), rb, w.expert_sigma)
+        host[l * w.E:(l + 1) * w.E].copy_(tmp)
+    torch.cuda.synchronize()
+    dls = [DeviceLayer(w, layer=l) for l in range(w.layers)]
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    shared = [dl.pool[w.E * rb:(w.E + w.n_shared) * rb] for dl in dls]
+    ts = TieredStack(s, w.layers, [dl.router for dl in dls], [host[i].data_ptr() for i in range(n_all)], n_slots,
+                     rb, shared)
+    try:
+        for step in range(2):
+            keep = []
+            ts.forward(dls[0].x(step), keep=keep)
+            assert ts.status() == 0
+            torch.cuda.synchronize()
+            check_layers(w, keep, range(w.layers))
+        st = L.slot_table_stats(ts.table)
+        assert st.misses > 0 and st.evictions > 0
+    finally:
+        ts.close()
+
+
 @pytest.mark.parametrize("overlap,freq", [(True, False), (False, False), (True, True)])
 def test_tiered_stack_misses_evictions_and_parity(overlap, freq):
     # 2 layers x 32 experts, but only 24 device slots: every step evicts and copies. With freq:
@@ -114,7 +168,7 @@ def test_tiered_stack_misses_evictions_and_parity(overlap, freq):
         for step in range(3):
             keep = []
             ts.forward(dls[0].x(step), keep=keep, overlap=overlap)
-            assert L.moe_read_status(ts.buf.ws) == 0
+            assert ts.status() == 0
             torch.cuda.synchronize()
             check_layers(w, keep, range(w.layers))
             lookups += sum(np.unique(rec[1].cpu().numpy()).size for rec in keep if rec[0] == "idx")
