@@ -329,9 +329,8 @@ def time_layer(w, dev, K: int, W: int, rot_layers: int, n_batches: int, ydt: int
     combo = [(i % rot_layers, i % n_batches) for i in range(n_combo)]
 
     def seg_route(l, x):
-        L.moe_route(s, x, xdt, dls[l].router, buf.topk_idx, buf.topk_w, None, buf.ws, buf.ws_bytes, None)
-        L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
-                      buf.ws_bytes, None)
+        L.moe_route_permute(s, x, xdt, dls[l].router, buf.topk_idx, buf.topk_w, None, buf.counts, buf.offsets,
+                            buf.sorted_pair, buf.inv_pos, buf.active, buf.ws, buf.ws_bytes, None)
 
     def seg_ffn_combine(l, x):
         L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, x, xdt, tables[l], buf.offsets, buf.sorted_pair, buf.active,
@@ -507,9 +506,9 @@ def run_ours(args, ws, rank, local):
                           "inputs larger than L2: each pass reads all 513 experts (2.57 GB); no flush"),
                    "layers_rotated": 1 if prefill else ROT_LAYERS, "batches": 4 if prefill else N_BATCHES,
                    "mean_active_experts": r["n_active_mean"],
-                   "launch": "one CUDA graph of the three C-ABI calls per pass: moe_route, moe_permute, "
-                             "moe_expert_ffn_combine (stages_ms: the same kernels as moe_expert_ffn and "
-                             "moe_combine, one graph per stage, events between)",
+                   "launch": "one CUDA graph of the two C-ABI calls per pass: moe_route_permute, "
+                             "moe_expert_ffn_combine (stages_ms: route_permute, then the same kernels as "
+                             "moe_expert_ffn and moe_combine; one graph per stage, events between)",
                    "parallelism": f"replicas x{ws}"},
         "ms_per_pass": pcts(r["pass_ms"]),
         "roofline": line_roof,
@@ -517,9 +516,9 @@ def run_ours(args, ws, rank, local):
         "wall_s": r["wall"],
         "e2e": e2e,
         "cpu_baseline": cpu,
-        # kernels per pass: decode 5 (router GEMV, top-k, bucketing, persistent expert FFN, combine);
-        # prefill 11 (router GEMM, top-k, 3 bucketing, 5 expert FFN, combine)
-        "gpu_launches": (11 if prefill else 5) * K * R,
+        # kernels per pass: decode 4 (router GEMV, top-k with bucketing, persistent expert FFN,
+        # combine); prefill 11 (router GEMM, top-k, 3 bucketing, 5 expert FFN, combine)
+        "gpu_launches": (11 if prefill else 4) * K * R,
         "clocks": r["clocks"],
     }
     if nested is not None:
@@ -676,7 +675,7 @@ def run_stack(args, ws, rank, local, w):
         "e2e": {"value": ws * w.T * K_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
                 "d2h_bytes_per_step": w.T * w.d * 2, "steps": K_e2e, "launch": "eager C-ABI calls"},
         "cpu_baseline": cpu,
-        "gpu_launches": 6 * w.layers * K,  # per layer: norm, router GEMV, top-k, bucketing, expert FFN, combine
+        "gpu_launches": 5 * w.layers * K,  # per layer: norm, router GEMV, top-k with bucketing, expert FFN, combine
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -785,9 +784,9 @@ def run_tiered(args, ws, rank, local, w):
                 out_host.copy_(y, non_blocking=True)
             torch.cuda.synchronize(dev)
             wall += time.perf_counter() - t0
-            # per layer: norm, router GEMV, top-k, bucketing, expert FFN, combine; with misses one more
-            # expert FFN (the missed experts after their copies)
-            launches[0] += sum(6 + (m > 0) for m in ts.layer_misses)
+            # per layer: norm, router GEMV, top-k with bucketing, expert FFN, combine; with misses one
+            # more expert FFN (the missed experts after their copies)
+            launches[0] += sum(5 + (m > 0) for m in ts.layer_misses)
         return wall
 
     try:

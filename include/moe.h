@@ -170,6 +170,17 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t*
                        int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int32_t* active,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_route followed by moe_permute, in one call: the same outputs, bit for bit, with the same
+ * arguments (see both). For few tokens the top-k and the bucketing run as one kernel, a cluster
+ * of T CTAs with one per token, which saves a launch and a round trip through global memory.
+ * That takes T <= 8, T*k <= 256, E <= 512 with E a multiple of 4, and one token's router split
+ * partial sums within 100 KB of shared memory; otherwise the two calls' kernels run one after
+ * the other. */
+moe_status moe_route_permute(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                             int32_t* topk_idx, float* topk_w, float* logits_opt, int32_t* counts,
+                             int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int32_t* active,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Bucketing without a workspace, for callers that cannot allocate device memory where they
  * bucket: for example an engine that sizes all device memory once at start-up and lets no
  * library add to it, or a serving path where a cudaMalloc could stall the device. The pages

@@ -56,6 +56,8 @@ _SIGS = {
     "moe_workspace_size": (C.c_int, [C.POINTER(moe_shape), C.POINTER(C.c_size_t)]),
     "moe_route": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "moe_permute": (C.c_int, [C.POINTER(moe_shape), _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
+    "moe_route_permute": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    C.c_size_t, _P]),
     "moe_permute_static": (C.c_int, [C.POINTER(moe_shape), _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (C.c_int, [C.POINTER(moe_shape), C.c_int, _P, C.c_int, C.POINTER(moe_expert_table), _P, _P, _P,
                                  _P, C.c_int, _P, C.c_size_t, _P]),
@@ -143,6 +145,14 @@ def moe_permute(s, topk_idx, counts, offsets, sorted_pair, inv_pos, active, ws, 
     return _check(lib().moe_permute(C.byref(s), ptr(topk_idx), ptr(counts), ptr(offsets), ptr(sorted_pair),
                                     ptr(inv_pos), ptr(active), ptr(ws), ws_bytes, stream_handle(stream)),
                   "moe_permute")
+
+
+def moe_route_permute(s, x, xdt, w_router, topk_idx, topk_w, logits_opt, counts, offsets, sorted_pair, inv_pos,
+                      active, ws, ws_bytes, stream=None) -> int:
+    return _check(lib().moe_route_permute(C.byref(s), ptr(x), xdt, ptr(w_router), ptr(topk_idx), ptr(topk_w),
+                                          ptr(logits_opt), ptr(counts), ptr(offsets), ptr(sorted_pair), ptr(inv_pos),
+                                          ptr(active), ptr(ws), ws_bytes, stream_handle(stream)),
+                  "moe_route_permute")
 
 
 def moe_permute_static(s, topk_idx, counts, offsets, sorted_pair, inv_pos, active, status, stream=None) -> int:

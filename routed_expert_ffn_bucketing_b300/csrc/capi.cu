@@ -263,6 +263,36 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t*
   return MOE_OK;
 }
 
+moe_status moe_route_permute(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                             int32_t* topk_idx, float* topk_w, float* logits_opt, int32_t* counts, int32_t* offsets,
+                             int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_dtype(xdt, "x")) != MOE_OK) return st;
+  if ((st = check_ws(shape, ws, ws_bytes)) != MOE_OK) return st;
+  if (shape->T == 0 || !route_tail_supported(*shape)) {
+    st = moe_route(shape, x, xdt, w_router, topk_idx, topk_w, logits_opt, ws, ws_bytes, stream);
+    if (st != MOE_OK) return st;
+    return moe_permute(shape, topk_idx, counts, offsets, sorted_pair, inv_pos, active, ws, ws_bytes, stream);
+  }
+  if (!x || !w_router || !topk_idx || !topk_w || !counts || !offsets || !sorted_pair || !inv_pos || !active)
+    return fail(MOE_EINVAL, "moe_route_permute: NULL argument");
+  if (!aligned(x, 16) || !aligned(w_router, 16))
+    return fail(MOE_EINVAL, "moe_route_permute: x and w_router must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(*shape);
+  int* status = at<int>(ws, L.status);
+  float* partial = at<float>(ws, L.route_partial);
+  cudaError_t e = launch_route_gemv(*shape, x, xdt, w_router, partial, status, at<uint8_t>(ws, L.zero),
+                                    L.zero_end - L.zero, s);
+  if (e == cudaSuccess)
+    e = launch_route_tail(*shape, partial, route_splits(shape->d), topk_idx, topk_w, logits_opt, counts, offsets,
+                          sorted_pair, inv_pos, active, status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_route_permute: launch");
+  return MOE_OK;
+}
+
 }  // extern "C"
 
 namespace {

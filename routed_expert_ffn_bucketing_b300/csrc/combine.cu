@@ -4,7 +4,9 @@
 // section "三级存储分工"):
 //   out[t] = sum_j w[t][j] * y_perm[inv_pos[t*k + j]] + sum_s y_perm[P + s*T + t] (+ residual[t])
 // The sum is fp32 in exactly that order (deterministic) and is rounded once to the output type.
-// One thread produces 4 consecutive columns of one token.
+// One thread produces 4 consecutive columns of one token. The token's k rows and weights are
+// read once per CTA into shared memory; each thread then requests all of its k rows before it
+// adds any of them, so the loads are in flight together instead of one after another.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -25,15 +27,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
                                                       const float* __restrict__ topk_w,
                                                       const void* residual, void* out, int odt, int T, int d,
                                                       int k, int n_shared) {
+  __shared__ int s_row[32];
+  __shared__ float s_w[32];
   const int t = blockIdx.y;
   const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   pdl_wait();  // y_perm from the expert FFN
+  if (threadIdx.x < k) {
+    s_row[threadIdx.x] = inv_pos[(size_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
   if (c >= d) return;
   const size_t P = (size_t)T * k;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    const int row = inv_pos[(size_t)t * k + j];
-    fma4(topk_w[(size_t)t * k + j], load4(y, ydt, (size_t)row * d + c), acc);
+  for (int j0 = 0; j0 < k; j0 += 8) {  // k <= 32: up to 8 rows requested before they are added
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (j0 + q < k) v[q] = load4(y, ydt, (size_t)s_row[j0 + q] * d + c);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (j0 + q < k) fma4(s_w[j0 + q], v[q], acc);
   }
   for (int s = 0; s < n_shared; ++s) {
     const float4 v = load4(y, ydt, (P + (size_t)s * T + t) * d + c);

@@ -148,6 +148,12 @@ cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const 
 // Top-k from the router GEMV's split partial sums [splits][T][E]: one CTA per token.
 cudaError_t launch_topk_split(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
                               float* logits_out, int* status, cudaStream_t st);
+// Decode routing tail: the top-k of the router GEMV's split partial sums and the bucketing of
+// the pairs, in one CTA (route_tail_supported says whether the shape fits).
+bool route_tail_supported(const moe_shape& s);
+cudaError_t launch_route_tail(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
+                              float* logits_out, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                              int32_t* inv_pos, int32_t* active, int* status, cudaStream_t st);
 cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const float* w, float* logits,
                               int* status, cudaStream_t st);
 // Top-k of logits already summed (after the router GEMM): one warp per token.

@@ -14,7 +14,7 @@
 // one chunk (decode), one CTA does all of it in a single launch; up to 256 pairs it counts
 // instead of sorting: each pair's rank is the number of earlier pairs of its expert, and the
 // last pair of each expert writes that expert's count (one writer per expert, no atomics).
-#include "moe_common.cuh"
+#include "bucket.cuh"
 
 namespace moe {
 
@@ -48,36 +48,6 @@ __device__ __forceinline__ int lower_bound_u32(const uint32_t* keys, int n, uint
     else hi = mid;
   }
   return lo;
-}
-
-// Block-wide exclusive scan of one int per thread (a multiple of 32 threads, at most 1024);
-// returns the total in *total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-      if (lane >= o) wi += n;
-    }
-    warp_sums[lane] = wi - w;  // exclusive over warps
-    if (lane == 31) warp_sums[32] = wi;
-  }
-  __syncthreads();
-  const int r = warp_sums[warp] + incl - v;
-  *total = warp_sums[32];
-  __syncthreads();
-  return r;
 }
 
 __device__ __forceinline__ uint32_t load_pair_key(const int32_t* topk_idx, int p, int local, int P, int E,
@@ -124,8 +94,8 @@ __global__ void __launch_bounds__(CH) bucket_single_kernel(const int32_t* __rest
   }
 }
 
-// At most 256 pairs in one CTA of n >= max(P, E) threads (a multiple of 32): ranks, counts,
-// one scan for the offsets and one for the active list, scatter.
+// At most 256 pairs in one CTA of n >= max(P, E) threads (a multiple of 32): the experts of
+// the pairs are read into shared memory, then bucket_count_block.
 __global__ void __launch_bounds__(1024) bucket_count_kernel(const int32_t* __restrict__ topk_idx, int P, int E,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets,
@@ -136,50 +106,17 @@ __global__ void __launch_bounds__(1024) bucket_count_kernel(const int32_t* __res
   __shared__ int cs[1024];
   __shared__ int warp_sums[33];
   const int i = threadIdx.x;
-  int e = 0;
   pdl_trigger();  // the expert FFN may launch and stage its activations meanwhile
   pdl_wait();  // topk_idx from the router
   if (i < P) {
-    e = topk_idx[i];
+    int e = topk_idx[i];
     if (e < 0 || e >= E) {
       flag_status(status, MOE_DEV_BAD_EXPERT_BIT);
       e = e < 0 ? 0 : E - 1;  // keep every later write in bounds
     }
     ex[i] = e;
   }
-  if (i < E) cs[i] = 0;
-  __syncthreads();
-  int rank = 0;
-  if (i < P) {
-    bool last = true;
-    for (int q = 0; q < P; ++q) {
-      const bool same = ex[q] == e;
-      rank += (q < i && same) ? 1 : 0;
-      last = last && !(q > i && same);
-    }
-    if (last) cs[e] = rank + 1;
-  }
-  __syncthreads();
-  const int v = i < E ? cs[i] : 0;
-  int total = 0, n_act = 0;
-  const int off = block_exclusive_scan(v, warp_sums, &total);
-  const int ar = block_exclusive_scan(v > 0 ? 1 : 0, warp_sums, &n_act);
-  if (i < E) {
-    counts[i] = v;
-    offsets[i] = off;
-    if (v > 0) active[1 + ar] = i;
-    cs[i] = off;
-  }
-  if (i == 0) {
-    offsets[E] = total;
-    active[0] = n_act;
-  }
-  __syncthreads();
-  if (i < P) {
-    const int pos = cs[e] + rank;
-    sorted_pair[pos] = i;
-    inv_pos[i] = pos;
-  }
+  bucket_count_block(ex, P, E, cs, warp_sums, counts, offsets, sorted_pair, inv_pos, active);
 }
 
 // Multi-chunk, step 1: sort each chunk; write its keys and its per-expert counts cnt[c][e].

@@ -16,9 +16,14 @@
 //  * top-k: one warp per token selects. Each lane holds E/32 logits as order-preserving
 //    integer keys, and k rounds of warp max (redux.sync) pick the experts. A tie goes to the
 //    lowest index.
-#include "moe_common.cuh"
+#include <cooperative_groups.h>
+
+#include "bucket.cuh"
+#include "sm100_ptx.cuh"
 
 namespace moe {
+
+namespace cg = cooperative_groups;
 
 // ------------------------------------------------------------------ top-k helpers ---------
 
@@ -38,46 +43,71 @@ __device__ __forceinline__ float key_logit(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
 }
 
+// Descending bitonic sort of N (a power of two) values held in registers.
+template <int N>
+__device__ __forceinline__ void sort_desc_regs(uint64_t (&v)[N]) {
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;  // direction of this pair in the bitonic merge
+          const uint64_t a = v[i], b = v[j];
+          const bool swap = desc ? (a < b) : (a > b);
+          v[i] = swap ? b : a;
+          v[j] = swap ? a : b;
+        }
+      }
+}
+
 // Selection of the k largest keys among the E logits held as PER keys per lane (logit e in
-// lane e % 32, slot e / 32), then the renormalised gate weights; one warp, one token.
+// lane e % 32, slot e / 32), then the renormalised gate weights; one warp, one token. Each
+// candidate is the 64-bit value (key, ~e): a larger value is a larger logit, or an equal one
+// with a lower expert index. Each lane sorts its candidates once; a round then takes the
+// largest head over the lanes (two warp max reductions, on the key and then on ~e among the
+// lanes holding that key) and the winning lane pops its head. Experts >= E are 0 and never win
+// while a real candidate (NaN included, key 0 but ~e > 0) is left.
 template <int PER>
 __device__ __forceinline__ void select_topk_warp(uint32_t (&key)[PER], int E, int k, int t, int32_t* idx,
-                                                 float* wts) {
+                                                 float* wts, int* idx_smem = nullptr) {
   const int lane = threadIdx.x & 31;
-  uint32_t taken = 0u;
+  uint64_t v[PER];
+#pragma unroll
+  for (int p = 0; p < PER; ++p) {
+    const int e = lane + 32 * p;
+    v[p] = e < E ? ((uint64_t)key[p] << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
+  }
+  sort_desc_regs<PER>(v);
   int my_e = 0;
   uint32_t my_key = 0u;
   for (int j = 0; j < k; ++j) {
-    uint32_t bk = 0u;
-    int be = 0x7FFFFFFF;
-    bool found = false;
+    const uint32_t hk = (uint32_t)(v[0] >> 32);
+    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, hk);
+    const uint32_t lo = hk == mk ? (uint32_t)v[0] : 0u;
+    const uint32_t ml = __reduce_max_sync(0xFFFFFFFFu, lo);
+    if (hk == mk && (uint32_t)v[0] == ml) {  // the unique winner pops its head
 #pragma unroll
-    for (int p = 0; p < PER; ++p) {
-      const bool free_ = !((taken >> p) & 1u) && (lane + 32 * p) < E;
-      if (free_ && (!found || key[p] > bk)) {
-        bk = key[p];
-        be = lane + 32 * p;
-        found = true;
-      }
+      for (int p = 0; p + 1 < PER; ++p) v[p] = v[p + 1];
+      v[PER - 1] = 0ull;
     }
-    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
-    const uint32_t cand = (found && bk == mk) ? (uint32_t)be : 0x7FFFFFFFu;
-    const int sel = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
-    if (lane == (sel & 31)) taken |= 1u << (sel >> 5);
     if (lane == j) {
-      my_e = sel;
+      my_e = (int)(~ml);
       my_key = mk;
     }
   }
-  const float v = key_logit(my_key);
-  const float m = __shfl_sync(0xFFFFFFFFu, v, 0);
-  const float ex = lane < k ? expf(v - m) : 0.0f;
+  const float val = key_logit(my_key);
+  const float m = __shfl_sync(0xFFFFFFFFu, val, 0);
+  const float ex = lane < k ? expf(val - m) : 0.0f;
   float sum = ex;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
   if (lane < k) {
     idx[(size_t)t * k + lane] = my_e;
     wts[(size_t)t * k + lane] = ex / sum;
+    if (idx_smem) idx_smem[t * k + lane] = my_e;
   }
 }
 
@@ -381,6 +411,66 @@ __global__ void __launch_bounds__(512) topk_split_kernel(const float* __restrict
   }
 }
 
+// Decode routing tail as one cluster of T CTAs (T <= 8), CTA t for token t: bulk copies bring
+// the token's S split partial sums of the router GEMV, they are added in the fixed order of
+// topk_split_kernel, warp 0 selects the token's top k and writes the experts of its pairs into
+// CTA 0's shared memory (distributed shared memory); after the cluster barrier CTA 0 buckets
+// the T*k pairs with bucket_count_block. The outputs are those of topk_split_kernel followed by
+// bucket_count_kernel, bit for bit, from one launch instead of two.
+template <int PER>
+__global__ void __launch_bounds__(512) route_tail_kernel(const float* __restrict__ partial, int S, int T, int E,
+                                                          int k, int32_t* __restrict__ idx, float* __restrict__ wts,
+                                                          float* __restrict__ logits_out, int32_t* counts,
+                                                          int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos,
+                                                          int32_t* active, int* status) {
+  extern __shared__ __align__(16) float tail_sm[];  // [S][E] this token's partial sums, then [E] logits
+  __shared__ uint64_t bar;
+  __shared__ int ex[256];
+  __shared__ int cs[512];
+  __shared__ int warp_sums[33];
+  __shared__ int nan_any;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x, t = blockIdx.x;
+  float* lg = tail_sm + (size_t)S * E;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    nan_any = 0;
+  }
+  __syncthreads();
+  pdl_trigger();  // the expert FFN may launch and stage its activations meanwhile
+  pdl_wait();     // the router GEMV's partial sums
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, (uint32_t)(S * E * 4));
+    for (int sp = 0; sp < S; ++sp)
+      bulk_g2s(tail_sm + (size_t)sp * E, partial + ((size_t)sp * T + t) * E, (uint32_t)(E * 4), &bar);
+  }
+  // a copy that never lands cannot be waited out; it is flagged and the tail goes on (its
+  // outputs are then not to be trusted, as MOE_DEV_TIMEOUT says)
+  if (!mbar_wait(&bar, 0) && tid == 0) flag_status(status, MOE_DEV_TIMEOUT_BIT);
+  for (int e = tid; e < E; e += blockDim.x) {
+    const float v = sum_splits(tail_sm + e, S, E);
+    lg[e] = v;
+    if (logits_out) logits_out[(size_t)t * E + e] = v;
+    if (v != v) nan_any = 1;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    uint32_t key[PER];
+    bool nan = false;
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const int e = tid + 32 * p;
+      key[p] = e < E ? logit_key(lg[e], &nan) : 0u;
+    }
+    select_topk_warp<PER>(key, E, k, t, idx, wts, cluster.map_shared_rank(ex, 0));
+  }
+  if (tid == 0 && nan_any) flag_status(status, MOE_DEV_NAN_LOGIT_BIT);
+  cluster.sync();  // every token's experts are in CTA 0's ex[]
+  if (cluster.block_rank() == 0)
+    bucket_count_block(ex, T * k, E, cs, warp_sums, counts, offsets, sorted_pair, inv_pos, active);
+}
+
 #define MOE_TOPK_DISPATCH(LAUNCH)    \
   do {                               \
     const int per = (s.E + 31) / 32; \
@@ -415,6 +505,45 @@ cudaError_t launch_topk_split(const moe_shape& s, const float* partial, int spli
   } while (0)
   MOE_TOPK_DISPATCH(L_SPLIT);
 #undef L_SPLIT
+  return cudaGetLastError();
+}
+
+bool route_tail_supported(const moe_shape& s) {
+  const size_t smem = sizeof(float) * (size_t)(route_splits(s.d) + 1) * s.E;
+  return s.T >= 1 && s.T <= 8 && s.T * s.k <= 256 && s.E <= 512 && s.E % 4 == 0 && smem <= 100 * 1024;
+}
+
+cudaError_t launch_route_tail(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
+                              float* logits_out, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                              int32_t* inv_pos, int32_t* active, int* status, cudaStream_t st) {
+  const size_t smem = sizeof(float) * (size_t)(splits + 1) * s.E;
+  int n = s.T * s.k > s.E ? s.T * s.k : s.E;
+  n = (n + 31) / 32 * 32;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.T);
+  cfg.blockDim = dim3(n);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = s.T;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+#define L_TAIL(P)                                                                                          \
+  do {                                                                                                     \
+    const cudaError_t e = ensure_dynamic_smem((const void*)route_tail_kernel<P>, smem);                    \
+    if (e != cudaSuccess) return e;                                                                        \
+    const cudaError_t e2 = cudaLaunchKernelEx(&cfg, route_tail_kernel<P>, partial, splits, s.T, s.E, s.k, idx, \
+                                              wts, logits_out, counts, offsets, sorted_pair, inv_pos, active, \
+                                              status);                                                     \
+    if (e2 != cudaSuccess) return e2;                                                                      \
+  } while (0)
+  MOE_TOPK_DISPATCH(L_TAIL);
+#undef L_TAIL
   return cudaGetLastError();
 }
 

@@ -46,9 +46,8 @@ class DecodeStack:
             if keep is not None:
                 keep.append(("in", self.resid.clone()))
             L.moe_rms_norm(s, self.resid, L.MOE_BF16, self.xn, L.MOE_BF16, RMS_EPS, stream)
-            L.moe_route(s, self.xn, L.MOE_BF16, lw.router, b.topk_idx, b.topk_w, None, b.ws, b.ws_bytes, stream)
-            L.moe_permute(s, b.topk_idx, b.counts, b.offsets, b.sorted_pair, b.inv_pos, b.active, b.ws, b.ws_bytes,
-                          stream)
+            L.moe_route_permute(s, self.xn, L.MOE_BF16, lw.router, b.topk_idx, b.topk_w, None, b.counts, b.offsets,
+                                b.sorted_pair, b.inv_pos, b.active, b.ws, b.ws_bytes, stream)
             # expert FFN and combine in one call; out aliases the residual: resid <- resid + MoE(n(resid))
             L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, lw.table, b.offsets, b.sorted_pair,
                                      b.active, b.y_perm, b.ydt, b.inv_pos, b.topk_w, self.resid, self.resid,
@@ -131,10 +130,8 @@ class TieredStack:
             if keep is not None:
                 keep.append(("in", self.resid.clone()))
             L.moe_rms_norm(s, self.resid, L.MOE_BF16, self.xn, L.MOE_BF16, RMS_EPS, stream)
-            L.moe_route(s, self.xn, L.MOE_BF16, self.routers[l], b.topk_idx, b.topk_w, None, b.ws, b.ws_bytes,
-                        stream)
-            L.moe_permute(s, b.topk_idx, b.counts, b.offsets, b.sorted_pair, b.inv_pos, b.active, b.ws, b.ws_bytes,
-                          stream)
+            L.moe_route_permute(s, self.xn, L.MOE_BF16, self.routers[l], b.topk_idx, b.topk_w, None, b.counts,
+                                b.offsets, b.sorted_pair, b.inv_pos, b.active, b.ws, b.ws_bytes, stream)
             self.h_active.copy_(b.active, non_blocking=True)
             # the host needs the active list, and the previous layer's FFN must be done with the
             # slots before any of them is overwritten: one event wait per layer

@@ -273,3 +273,46 @@ def test_fused_combine_is_bit_identical(wl, mode, residual, odt, ydt):
                                  buf.ydt, buf.inv_pos, buf.topk_w, r, r, buf.odt, buf.ws, buf.ws_bytes)
         torch.cuda.synchronize()
         assert torch.equal(r, outs[1])
+
+
+@pytest.mark.parametrize("wl,T,E,k", [("decode", 4, 512, 10), ("decode", 1, 512, 10), ("decode", 16, 512, 10),
+                                      ("tiny", 16, 16, 2), ("tiny", 7, 40, 5), ("decode", 16, 1024, 32),
+                                      ("tiny", 300, 64, 10)])
+def test_route_permute_is_bit_identical(wl, T, E, k):
+    # moe_route_permute against moe_route followed by moe_permute: the same bits in every output,
+    # on shapes inside the one-kernel tail (T <= 16, T*k <= 256), at its edges and beyond it
+    from routed_expert_ffn_bucketing_b300 import layer as lay
+    w = custom(wl, T=T, E=E, k=k, n_shared=0, router_sigma=1.0)
+    dl = DeviceLayer(w, fill="host" if w.d * w.f * (w.E + w.n_shared) < (1 << 26) else "device")
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    x = dl.x(1)
+    outs = []
+    for fused in (False, True):
+        buf = lay.alloc_buffers(s)
+        if fused:
+            L.moe_route_permute(s, x, L.MOE_BF16, dl.router, buf.topk_idx, buf.topk_w, buf.logits, buf.counts,
+                                buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws, buf.ws_bytes)
+        else:
+            L.moe_route(s, x, L.MOE_BF16, dl.router, buf.topk_idx, buf.topk_w, buf.logits, buf.ws, buf.ws_bytes)
+            L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active,
+                          buf.ws, buf.ws_bytes)
+        assert L.moe_read_status(buf.ws) == 0
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in (buf.topk_idx, buf.topk_w, buf.logits, buf.counts, buf.offsets,
+                                         buf.sorted_pair, buf.inv_pos)] + [buf.active[:1 + int(buf.active[0])].clone()])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    run = GpuRunLike(outs[1], dl)
+    check_routing(run, w)
+    check_bucketing(run, w)
+
+
+class GpuRunLike:
+    """The fields of a GpuRun that check_routing and check_bucketing read."""
+
+    def __init__(self, o, dl):
+        from types import SimpleNamespace
+        self.buf = SimpleNamespace(topk_idx=o[0], topk_w=o[1], logits=o[2], counts=o[3], offsets=o[4],
+                                   sorted_pair=o[5], inv_pos=o[6], active=o[7])
+        self.x_np = dl.x(1).float().cpu().numpy().astype(np.float64)
+
