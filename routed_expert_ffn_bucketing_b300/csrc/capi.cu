@@ -55,6 +55,8 @@ WsLayout ws_layout(const moe_shape& s) {
   if (s.T <= kRouteGemvMaxT) o = align256(o + sizeof(float) * route_splits(s.d) * T * s.E);
   L.logits = o;
   if (s.T > kRouteGemvMaxT) o = align256(o + sizeof(float) * T * s.E);
+  L.wparts = o;
+  if (s.T > kRouteGemvMaxT) o = align256(o + sizeof(uint16_t) * 3 * (size_t)s.E * s.d);
   L.perm_cnt = o;
   const size_t C = P > (size_t)kPermChunk ? (size_t)perm_chunks((int)P) : 0;
   o = align256(o + sizeof(int32_t) * C * s.E);
@@ -240,7 +242,10 @@ moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const
       e = launch_topk_split(*shape, partial, route_splits(shape->d), topk_idx, topk_w, logits_opt, status, s);
   } else {
     float* logits = logits_opt ? logits_opt : at<float>(ws, L.logits);
-    e = launch_route_gemm(*shape, x, xdt, w_router, logits, status, s);
+    if (route_tc_supported(*shape, xdt))
+      e = launch_route_tc(*shape, x, w_router, at<uint8_t>(ws, L.wparts), logits, status, s);
+    else
+      e = launch_route_gemm(*shape, x, xdt, w_router, logits, status, s);
     if (e == cudaSuccess) e = launch_topk(*shape, logits, topk_idx, topk_w, status, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "moe_route: launch");

@@ -46,6 +46,7 @@
 
 #include "moe_common.cuh"
 #include "sm100_ptx.cuh"
+#include "tmap.h"
 
 namespace moe {
 
@@ -606,25 +607,29 @@ PFN_cuTensorMapEncodeTiled_v12000 p_encode_fn() {
   return fn;
 }
 
-bool p_encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
-  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return p_encode_fn()(m, dt, rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // A operand: rows x K f16, boxes of 64 x 128 in the 128-byte swizzle.
 bool encode_a(CUtensorMap* m, const void* base, int K, int rows) {
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {kPK, kPM};
-  return p_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  return tmap_encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, (uint64_t)K, (uint64_t)rows, (uint64_t)K * 2, kPK,
+                        kPM, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
 
+bool tmap_available() { return p_encode_fn() != nullptr; }
+
+bool tmap_encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  if (!p_encode_fn()) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return p_encode_fn()(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool prefill_supported(const FfnArgs& a) {
-  return a.xdt == 0 && a.d % kPN == 0 && a.f % 128 == 0 && p_encode_fn() != nullptr;
+  return a.xdt == 0 && a.d % kPN == 0 && a.f % 128 == 0 && tmap_available();
 }
 
 cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, int sm_count, cudaStream_t st) {

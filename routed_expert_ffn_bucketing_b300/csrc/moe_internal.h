@@ -27,6 +27,7 @@ struct WsLayout {
   size_t status;         // int32 device status word
   size_t route_partial;  // fp32 [S][T][E]: split-d router partial sums (T <= kRouteGemvMaxT)
   size_t logits;         // fp32 [T][E]: router GEMM output (T > kRouteGemvMaxT)
+  size_t wparts;         // bf16 [3][E][d]: the router weights split in three exact parts (T > kRouteGemvMaxT)
   size_t perm_cnt;       // int32 [C][E]: per-chunk counts, then per-chunk bases
   size_t perm_keys;      // uint32 [C * kPermChunk]: chunk-sorted (expert, pair) keys
   size_t h;              // [P + T*n_shared][f] fp32: SwiGLU activations between the FFN kernels
@@ -154,6 +155,13 @@ bool route_tail_supported(const moe_shape& s);
 cudaError_t launch_route_tail(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
                               float* logits_out, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
                               int32_t* inv_pos, int32_t* active, int* status, cudaStream_t st);
+// Router logits for T > 16 on the tensor cores (bf16 x; d a multiple of 256): the fp32 weights
+// split into three exact bf16 parts in `parts` (route_tc_parts_bytes), then a tcgen05 GEMM. Also
+// clears *status.
+bool route_tc_supported(const moe_shape& s, int xdt);
+size_t route_tc_parts_bytes(const moe_shape& s);
+cudaError_t launch_route_tc(const moe_shape& s, const void* x, const float* w, void* parts, float* logits, int* status,
+                            cudaStream_t st);
 cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const float* w, float* logits,
                               int* status, cudaStream_t st);
 // Top-k of logits already summed (after the router GEMM): one warp per token.

@@ -10,7 +10,7 @@ from routed_expert_ffn_bucketing_b300 import _lib as L
 from synth.device import DeviceLayer
 from synth.workloads import custom
 
-from gpu_util import check_output, run_layer
+from gpu_util import check_output, check_routing, run_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +49,7 @@ def test_auto_refuses_many_tokens_on_a_shape_without_the_gemm():
     assert e.value.status == L.MOE_EUNSUPPORTED and "MOE_MODE_DECODE" in str(e.value)
     run = run_layer(dl, 0, mode=L.MOE_MODE_DECODE)  # the explicit request runs the SIMT kernels
     assert run.status == 0
+    check_routing(run, w)  # d % 256 != 0: the router is the fp32 SIMT GEMM, not the tensor-core one
     check_output(run, w)
 
 
