@@ -322,7 +322,7 @@ def time_layer(w, dev, K: int, W: int, rot_layers: int, n_batches: int, ydt: int
     xs = [dls[0].x(b) for b in range(n_batches)]
     s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
     buf = lay.alloc_buffers(s, device=dev, ydt=ydt, odt=L.MOE_BF16, keep_logits=False)
-    tables = [L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr) for dl in dls]
+    tables = [L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr, fmt=w.fmt) for dl in dls]
     stream = torch.cuda.current_stream(dev)
     xdt = L.MOE_BF16
     n_combo = rot_layers * n_batches // math.gcd(rot_layers, n_batches)
@@ -490,6 +490,18 @@ def run_ours(args, ws, rank, local):
                   "steps": 10, "passes_per_step": rp["R"], "ms_per_pass": pcts(rp["pass_ms"]),
                   "roofline": roof_p, **extra_p, "clocks": rp["clocks"],
                   "gpu_launches": 11 * 10 * rp["R"]}
+    nested_q2 = None
+    if not prefill and not args.no_q2 and args.workload == "decode":
+        # the same decode pass on 2-bit expert records (2.5 bits per weight)
+        torch.cuda.empty_cache()
+        wq = WORKLOADS["decode_q2"]
+        rq = time_layer(wq, dev, K, W, rot_layers=ROT_LAYERS, n_batches=N_BATCHES, ydt=L.MOE_F32,
+                        min_ms=MIN_TIMED_MS, ws=ws, e2e=False)
+        roof_q, extra_q = layer_roofline(wq, rq, hbm_peak, bf16_peak, bf16_sus, peak_kind)
+        nested_q2 = {"workload": wq.describe(), "value": ws * wq.T * K * rq["R"] / rq["total_s"], "unit": "tokens/s",
+                     "record_bytes": wq.record_bytes, "steps": K, "passes_per_step": rq["R"],
+                     "ms_per_pass": pcts(rq["pass_ms"]), "roofline": roof_q, **extra_q, "clocks": rq["clocks"],
+                     "gpu_launches": 4 * K * rq["R"]}
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_line(w, args)
@@ -523,6 +535,8 @@ def run_ours(args, ws, rank, local):
     }
     if nested is not None:
         line["prefill"] = nested
+    if nested_q2 is not None:
+        line["decode_q2"] = nested_q2
     print(json.dumps(line), flush=True)
 
 
@@ -849,6 +863,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="decode: skip the nested prefill measurement")
+    ap.add_argument("--no-q2", action="store_true", help="decode: skip the nested 2-bit-format measurement")
     ap.add_argument("--host-gb", type=float, default=24.0, help="pinned host memory for expert images (tiered)")
     ap.add_argument("--slot-policy", choices=["lru", "freq"], default="lru",
                     help="tiered: replacement policy of the slot pool (LRU, or decayed use count)")

@@ -113,8 +113,30 @@ typedef struct {
  * multiple of 32 or out is NULL. */
 moe_status moe_get_expert_layout(int32_t d, int32_t f, moe_expert_layout* out);
 
+/* Expert record formats (moe_expert_table.format).
+ *  MOE_FMT_INT8  int8 codes and one fp16 scale per 32 weights (8.5 bits per weight), the layout
+ *                of moe_get_expert_layout.
+ *  MOE_FMT_Q2    the sub-4-bit format of the pages' ~2.4 bits-per-weight experts ("Strata 工作原理图解
+ *                GPU内存SSD三级存储如何让125B模型塞进消费级显卡", sections "专家缓存" and "实测速度": 2-bit
+ *                quantised experts, about 700 of them per GB): 2-bit codes c in 0..3 and one fp16
+ *                scale s per 32 weights along the reduction dimension, W = s * (c - 1.5), 2.5 bits
+ *                per weight. Sections as in MOE_FMT_INT8, the code sections a quarter of the size:
+ *                gate_q [f][d/4], up_q [f][d/4], down_q [d][f/4] bytes. In a code row, each group of
+ *                8 blocks (256 codes) is 64 bytes: 16-byte chunk q holds, for block b = 0..7, the
+ *                little-endian 16-bit word of codes 8q..8q+7 of block b, code j (0..7) at bits
+ *                2 * slot(j) with slot(0..7) = 0, 2, 1, 3, 4, 6, 5, 7. Needs d and f multiples of
+ *                256, and the decode expert FFN (bf16 x, T <= 8); other kernels return
+ *                MOE_EUNSUPPORTED for it. */
+#define MOE_FMT_INT8 0
+#define MOE_FMT_Q2 1
+
+/* Fills *out for (d, f) in record format `format`. Host only. MOE_EINVAL for a bad format, d or f
+ * not a positive multiple of 32 (of 256 for MOE_FMT_Q2), or out NULL. */
+moe_status moe_get_record_layout(int32_t d, int32_t f, int32_t format, moe_expert_layout* out);
+
 /* Where the experts of one layer live.
- *  pool       device: slot records, slot s at pool + s * slot_bytes, s < n_slots
+ *  pool       device: slot records, slot s at pool + s * slot_bytes, s < n_slots (records in
+ *             `format`; a zero-filled table means MOE_FMT_INT8)
  *  slot_bytes stride of the pool: >= record_bytes and a multiple of 256
  *  slot_of    device int32 [E]: slot of routed expert e, or -1 when it is not resident
  *             (the row of one layer of the slot table; [P2] "专家缓存")
@@ -128,6 +150,7 @@ typedef struct {
   const int32_t* slot_of;
   const void* shared;
   uint64_t n_slots;
+  uint32_t format; /* MOE_FMT_INT8 or MOE_FMT_Q2, for every record of the table */
 } moe_expert_table;
 
 /* Bytes of workspace that moe_route / moe_permute / moe_expert_ffn need for this shape

@@ -55,6 +55,17 @@ def dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return q.astype(np.float64) * scale
 
 
+def dequantize_q2(c: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Dense float64 weights of the sub-4-bit format: 2-bit codes c [R][C] (values 0..3) and
+    fp16 block scales s [R][C/32], W[r, i] = s[r, i // 32] * (c[r, i] - 1.5): four levels
+    symmetric about zero, 2.5 bits per weight with the scale. Exact in float64."""
+    R, C = c.shape
+    assert s.shape == (R, C // BLOCK)
+    assert np.all((c >= 0) & (c <= 3))
+    scale = np.repeat(s.astype(np.float64), BLOCK, axis=1)
+    return (c.astype(np.float64) - 1.5) * scale
+
+
 # ---------------------------------------------------------------------------------------
 # RMS normalisation of a layer's input (pre-norm residual block of a layer stack)
 # ---------------------------------------------------------------------------------------
@@ -117,9 +128,9 @@ class DenseExpert:
 
 def dense_expert(a) -> DenseExpert:
     """Dequantise the six arrays of one expert (any object with gate_q, gate_s, up_q, up_s,
-    down_q and down_s attributes)."""
-    return DenseExpert(dequantize(a.gate_q, a.gate_s), dequantize(a.up_q, a.up_s),
-                       dequantize(a.down_q, a.down_s))
+    down_q and down_s attributes; fmt "q2" for the 2-bit format, int8 codes otherwise)."""
+    deq = dequantize_q2 if getattr(a, "fmt", "int8") == "q2" else dequantize
+    return DenseExpert(deq(a.gate_q, a.gate_s), deq(a.up_q, a.up_s), deq(a.down_q, a.down_s))
 
 
 def silu(z: np.ndarray) -> np.ndarray:

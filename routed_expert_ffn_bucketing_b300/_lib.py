@@ -19,6 +19,7 @@ MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_EXPERT, MOE_DEV_MISSING_SLOT, MOE_DEV_TIMEOUT, MO
 MOE_BF16, MOE_F32 = 0, 1
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
 MOE_SLOT_LRU, MOE_SLOT_FREQ = 0, 1
+MOE_FMT_INT8, MOE_FMT_Q2 = 0, 1
 
 _STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_EUNSUPPORTED", -3: "MOE_ECUDA", -4: "MOE_ENOSLOT",
                  -5: "MOE_EDEVICE"}
@@ -41,7 +42,7 @@ class moe_expert_layout(C.Structure):
 
 class moe_expert_table(C.Structure):
     _fields_ = [("pool", C.c_void_p), ("slot_bytes", C.c_uint64), ("slot_of", C.c_void_p), ("shared", C.c_void_p),
-                ("n_slots", C.c_uint64)]
+                ("n_slots", C.c_uint64), ("format", C.c_uint32)]
 
 
 class moe_slot_stats(C.Structure):
@@ -53,6 +54,7 @@ MOE_COPY_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_
 _P = C.c_void_p
 _SIGS = {
     "moe_get_expert_layout": (C.c_int, [C.c_int32, C.c_int32, C.POINTER(moe_expert_layout)]),
+    "moe_get_record_layout": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.POINTER(moe_expert_layout)]),
     "moe_workspace_size": (C.c_int, [C.POINTER(moe_shape), C.POINTER(C.c_size_t)]),
     "moe_route": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "moe_permute": (C.c_int, [C.POINTER(moe_shape), _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
@@ -130,6 +132,12 @@ def moe_get_expert_layout(d: int, f: int) -> moe_expert_layout:
     return out
 
 
+def moe_get_record_layout(d: int, f: int, fmt: int) -> moe_expert_layout:
+    out = moe_expert_layout()
+    _check(lib().moe_get_record_layout(d, f, fmt, C.byref(out)), "moe_get_record_layout")
+    return out
+
+
 def moe_workspace_size(s: moe_shape) -> int:
     n = C.c_size_t()
     _check(lib().moe_workspace_size(C.byref(s), C.byref(n)), "moe_workspace_size")
@@ -163,8 +171,8 @@ def moe_permute_static(s, topk_idx, counts, offsets, sorted_pair, inv_pos, activ
                   "moe_permute_static")
 
 
-def expert_table(pool, slot_bytes: int, n_slots: int, slot_of, shared=None) -> moe_expert_table:
-    return moe_expert_table(ptr(pool), slot_bytes, ptr(slot_of), ptr(shared), n_slots)
+def expert_table(pool, slot_bytes: int, n_slots: int, slot_of, shared=None, fmt: int = MOE_FMT_INT8) -> moe_expert_table:
+    return moe_expert_table(ptr(pool), slot_bytes, ptr(slot_of), ptr(shared), n_slots, fmt)
 
 
 def moe_expert_ffn(s, mode, x, xdt, table: moe_expert_table, offsets, sorted_pair, active, y_perm, ydt, ws,

@@ -184,9 +184,17 @@ extern "C" {
 const char* moe_last_error_string(void) { return g_err; }
 
 moe_status moe_get_expert_layout(int32_t d, int32_t f, moe_expert_layout* out) {
+  return moe_get_record_layout(d, f, MOE_FMT_INT8, out);
+}
+
+moe_status moe_get_record_layout(int32_t d, int32_t f, int32_t format, moe_expert_layout* out) {
   if (!out) return fail(MOE_EINVAL, "out is NULL");
+  if (format != MOE_FMT_INT8 && format != MOE_FMT_Q2) return fail(MOE_EINVAL, "unknown record format %d", format);
   if (d <= 0 || f <= 0 || d % 32 || f % 32) return fail(MOE_EINVAL, "d=%d f=%d must be positive multiples of 32", d, f);
-  const uint64_t q = (uint64_t)d * f, sgu = (uint64_t)f * (d / 32) * 2, sd = (uint64_t)d * (f / 32) * 2;
+  if (format == MOE_FMT_Q2 && (d % 256 || f % 256))
+    return fail(MOE_EINVAL, "the 2-bit format needs d=%d and f=%d to be multiples of 256", d, f);
+  const uint64_t q = (uint64_t)d * f / (format == MOE_FMT_Q2 ? 4 : 1);
+  const uint64_t sgu = (uint64_t)f * (d / 32) * 2, sd = (uint64_t)d * (f / 32) * 2;
   uint64_t o = 0;
   auto take = [&](uint64_t n) {
     const uint64_t r = o;
@@ -331,8 +339,10 @@ moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x,
     return fail(MOE_EINVAL, "moe_expert_ffn: n_slots %llu must be in [1, 2^31]", (unsigned long long)experts->n_slots);
   if ((shape->n_shared > 0) != (experts->shared != nullptr))
     return fail(MOE_EINVAL, "moe_expert_ffn: shared must be non-NULL exactly when n_shared > 0");
+  if (experts->format != MOE_FMT_INT8 && experts->format != MOE_FMT_Q2)
+    return fail(MOE_EINVAL, "moe_expert_ffn: unknown record format %u", experts->format);
   moe_expert_layout lay;
-  moe_get_expert_layout(shape->d, shape->f, &lay);
+  if ((st = moe_get_record_layout(shape->d, shape->f, (int32_t)experts->format, &lay)) != MOE_OK) return st;
   if (experts->slot_bytes < lay.record_bytes || experts->slot_bytes % 256)
     return fail(MOE_EINVAL, "moe_expert_ffn: slot_bytes %llu must be >= %llu and a multiple of 256",
                 (unsigned long long)experts->slot_bytes, (unsigned long long)lay.record_bytes);
@@ -357,6 +367,7 @@ moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x,
   a.h = at<float>(ws, L.h);
   a.status = at<int>(ws, L.status);
   a.wait_ns = wait_limit_ns();
+  a.fmt = (int)experts->format;
   a.T = shape->T;
   a.d = shape->d;
   a.f = shape->f;
@@ -374,6 +385,9 @@ moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x,
   // tokens): streaming tensor-core kernels for bf16 x, fp32 SIMT kernels in the fp32 debug mode.
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (a.fmt == MOE_FMT_Q2 && !(xdt == MOE_BF16 && mode != MOE_MODE_PREFILL && persist_supported(a, device_sm_count())))
+    return fail(MOE_EUNSUPPORTED,
+                "moe_expert_ffn: 2-bit records run on the decode kernel only (bf16 x, T <= 8, d and f multiples of 256)");
   const bool want_prefill = mode == MOE_MODE_PREFILL || (mode == MOE_MODE_AUTO && shape->T > kDecodeMaxT && xdt == MOE_BF16);
   if (want_prefill && prefill_supported(a)) {
     const PrefillAux px{at<__half>(ws, L.xp16),    at<float>(ws, L.xunscale), at<int32_t>(ws, L.xexp),

@@ -56,6 +56,36 @@ __device__ __forceinline__ void block_mma(float* d, uint2 w_lo, uint2 w_hi, cons
   mma_f16_16816(d, codes02(w_lo.y), codes02(w_hi.y), codes02(w_lo.y >> 8), codes02(w_hi.y >> 8), xv.z, xv.w);
 }
 
+// The 2-bit format (w = s (c - 1.5)). A lane's 8 codes of one row of a block are one 16-bit word
+// u, code j at bits 2 * slot(j) with slot order (0, 2, 1, 3, 4, 6, 5, 7), so that the codes of
+// each MMA register pair sit at bits 4r and 4r + 2 of u, r = 0..3. With t = u | (u << 14) the two
+// codes of pair r are at bits 4r and 4r + 16 of t (the bits where the two copies of u overlap,
+// 14 and 15, are never read), and one lop3 of t >> 4r turns them into the f16 pair
+// (1024 + c_a, 1024 + c_b) exactly (0x64 in the high byte). The
+// accumulator input is -1025.5 times the block sum of the activations, so the MMA returns
+// sum_k (c_k - 1.5) x_k.
+constexpr float kOffsetQ2 = 1025.5f;
+
+__device__ __forceinline__ uint32_t q2pair(uint32_t t) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(t), "r"(0x00030003u), "r"(0x64006400u));  // (a & b) | c
+  return r;
+}
+
+// d = C + block product of M rows g, g+8 (16-bit code words u_lo, u_hi of the 2-bit format) with
+// this lane's 8 activations of token g, as two MMAs; C as in block_mma, with the offset 1025.5.
+__device__ __forceinline__ void block_mma_q2(float* d, uint32_t u_lo, uint32_t u_hi, const uint4& xv, float c0,
+                                             float c1) {
+  const uint32_t tl = u_lo | (u_lo << 14), th = u_hi | (u_hi << 14);
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%10,%11};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(q2pair(tl)), "r"(q2pair(th)), "r"(q2pair(tl >> 4)), "r"(q2pair(th >> 4)), "r"(xv.x), "r"(xv.y),
+        "f"(c0), "f"(c1));
+  mma_f16_16816(d, q2pair(tl >> 8), q2pair(th >> 8), q2pair(tl >> 12), q2pair(th >> 12), xv.z, xv.w);
+}
+
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
 // e with m * 2^-e in [2^14, 2^15) for a normal m > 0 (clamped to [-100, 100]); 0 for m == 0.

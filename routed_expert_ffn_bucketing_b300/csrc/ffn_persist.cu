@@ -51,6 +51,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// Waits until at most N of this thread's committed cp.async groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
@@ -81,7 +86,7 @@ struct PLayout {
   uint32_t items, done, rowtok, hexp, xe, bmax, sring, act, total;
 };
 
-template <int DG, int DD>
+template <int DG, int DD, int FMT>
 __host__ __device__ inline PLayout p_layout(int T, int d, int f, int items_max, int rows, int rows_cap) {
   PLayout L;
   uint32_t o = 0;
@@ -97,9 +102,9 @@ __host__ __device__ inline PLayout p_layout(int T, int d, int f, int items_max, 
   o = align16(o + 4u * (d / kQBlock));
   L.bmax = o;  // uint32 [d/32]: bits of max |x| over block b of every token
   o = align16(o + 4u * (d / kQBlock));
-  L.sring = o;  // per warp: 2 slots x 16 rows x D f16 scales
+  L.sring = o;  // per warp: 2 slots (int8) or 4 (2-bit format) x 16 rows x D f16 scales
   const int dmax = DG > DD ? DG : DD;
-  o = align16(o + (uint32_t)kPW * 2u * 16u * dmax * 2u);
+  o = align16(o + (uint32_t)kPW * (FMT == 1 ? 4u : 2u) * 16u * dmax * 2u);
   L.act = o;  // x rows for gate/up, then this CTA's h rows for down
   const uint32_t xb = (uint32_t)T * (act_stride(d) + sum_stride(d));
   const uint32_t hb = (uint32_t)rows_cap * (act_stride(f) + sum_stride(f));
@@ -132,14 +137,14 @@ struct PTask {
 
 // Distance from the codes of M row g to those of M row g + 8: the up matrix's row (gate/up) or
 // the down row 8 further (down).
-template <int KIND>
+template <int KIND, int FMT>
 __device__ __forceinline__ long long hi_delta(const FfnArgs& A) {
-  return KIND == 0 ? (long long)A.o_up_q - (long long)A.o_gate_q : 8LL * A.f;
+  return KIND == 0 ? (long long)A.o_up_q - (long long)A.o_gate_q : 8LL * A.f / (FMT == 1 ? 4 : 1);
 }
 
 // sx, sc: shared-memory offsets of the staged activation rows and of their accumulator inputs
 // (for down: of row 0, which may lie before the staged span; only staged rows are addressed).
-template <int KIND>
+template <int KIND, int FMT>
 __device__ __forceinline__ PTask make_task(const FfnArgs& A, const ItemRec* items, const int* rowtok, uint32_t sx,
                                            uint32_t sc, int t, int lane) {
   const int g = lane >> 2, c = lane & 3;
@@ -156,7 +161,7 @@ __device__ __forceinline__ PTask make_task(const FfnArgs& A, const ItemRec* item
   const int r0 = 2 * c < p.ntok ? 2 * c : 0, r1 = 2 * c + 1 < p.ntok ? 2 * c + 1 : 0;
   if (KIND == kGU) {
     const int d = A.d, nb = d / kQBlock;
-    p.wlo = rec + A.o_gate_q + (size_t)(p.mt * 8 + g) * d + c * 16;
+    p.wlo = rec + A.o_gate_q + (size_t)(p.mt * 8 + g) * (d / (FMT == 1 ? 4 : 1)) + c * 16;
     const int srow = p.mt * 8 + (lane & 7);
     p.ssrc = rec + (lane < 8 ? A.o_gate_s : A.o_up_s) + (size_t)srow * nb * 2;
     const int tg = p.valid ? rowtok[p.row0 + (p.has ? g : 0)] : 0;
@@ -165,7 +170,7 @@ __device__ __forceinline__ PTask make_task(const FfnArgs& A, const ItemRec* item
     p.cs1 = sc + (uint32_t)(p.valid ? rowtok[p.row0 + r1] : 0) * sum_stride(d);
   } else {
     const int f = A.f, nb = f / kQBlock;
-    p.wlo = rec + A.o_down_q + (size_t)(p.mt * 16 + g) * f + c * 16;
+    p.wlo = rec + A.o_down_q + (size_t)(p.mt * 16 + g) * (f / (FMT == 1 ? 4 : 1)) + c * 16;
     p.ssrc = rec + A.o_down_s + (size_t)(p.mt * 16 + (lane & 15)) * nb * 2;
     p.xrow = sx + (uint32_t)(p.row0 + (p.has ? g : 0)) * act_stride(f) + c * 16u;
     p.cs0 = sc + (uint32_t)(p.row0 + r0) * sum_stride(f);
@@ -174,25 +179,34 @@ __device__ __forceinline__ PTask make_task(const FfnArgs& A, const ItemRec* item
   return p;
 }
 
-template <int D>
+// The codes of the group being multiplied, in registers: int8, one 8-byte fragment per block and
+// row; 2-bit format (groups of 8 blocks), one 16-byte chunk per row.
+template <int D, int FMT>
 struct Ring {
   uint2 lo[D], hi[D];
+};
+constexpr int kQ2Ahead = 4;  // groups of 2-bit codes a warp has requested ahead of the one it multiplies
+template <>
+struct Ring<8, 1> {
+  uint4 lo[kQ2Ahead], hi[kQ2Ahead];  // [0]: the group being multiplied
 };
 
 // Requests group gs of task p: D blocks of both rows into the ring, and the 16 rows' D scales
 // into scale slot `slot` of this warp (lanes 0..15, one cp.async each).
-template <int D>
-__device__ __forceinline__ void issue_group(const PTask& p, long long dhi, int gs, Ring<D>& ring, uint32_t sring_w,
-                                            int slot, int lane) {
+template <int D, int FMT>
+__device__ __forceinline__ void issue_group(const PTask& p, long long dhi, int gs, Ring<D, FMT>& ring,
+                                            uint32_t sring_w, int slot, int lane) {
   if (!p.valid) return;
+  if constexpr (FMT == 0) {
 #pragma unroll
-  for (int j = 0; j < D; j += 2) {  // one 16-byte load: this lane's codes of blocks j and j + 1
-    const uint4 a = ld_codes16(p.wlo + (size_t)(gs * D + j) * kQBlock);
-    const uint4 b = ld_codes16(p.wlo + dhi + (size_t)(gs * D + j) * kQBlock);
-    ring.lo[j] = make_uint2(a.x, a.y);
-    ring.lo[j + 1] = make_uint2(a.z, a.w);
-    ring.hi[j] = make_uint2(b.x, b.y);
-    ring.hi[j + 1] = make_uint2(b.z, b.w);
+    for (int j = 0; j < D; j += 2) {  // one 16-byte load: this lane's codes of blocks j and j + 1
+      const uint4 a = ld_codes16(p.wlo + (size_t)(gs * D + j) * kQBlock);
+      const uint4 b = ld_codes16(p.wlo + dhi + (size_t)(gs * D + j) * kQBlock);
+      ring.lo[j] = make_uint2(a.x, a.y);
+      ring.lo[j + 1] = make_uint2(a.z, a.w);
+      ring.hi[j] = make_uint2(b.x, b.y);
+      ring.hi[j + 1] = make_uint2(b.z, b.w);
+    }
   }
   if (lane < 16) {
     const uint32_t dst = sring_w + (uint32_t)(slot * 16 + lane) * (D * 2);
@@ -202,10 +216,10 @@ __device__ __forceinline__ void issue_group(const PTask& p, long long dhi, int g
 }
 
 // Writes the 32 values v of block b (row order) as f16 in the permuted order to the staged row
-// at `row` (shared memory) and returns -1152 * (sum of the f16 values), the block's MMA
-// accumulator input. The block is written as four 16-byte chunks, chunk (q + b/2) % 4 at step
+// at `row` (shared memory) and returns -offset * (sum of the f16 values), the block's MMA
+// accumulator input (offset 1152 for int8 codes, 1025.5 for the 2-bit format). The block is written as four 16-byte chunks, chunk (q + b/2) % 4 at step
 // q, so that 8 threads storing blocks b..b+7 of a row hit 8 distinct 16-byte bank groups.
-__device__ __forceinline__ float stage_block_f16(uint8_t* row, int b, const float* v) {
+__device__ __forceinline__ float stage_block_f16(uint8_t* row, int b, const float* v, float offset) {
   uint32_t w[16];
   float s = 0.0f;
 #pragma unroll
@@ -231,7 +245,7 @@ __device__ __forceinline__ float stage_block_f16(uint8_t* row, int b, const floa
     u.w = k == 0 ? w[3] : k == 1 ? w[7] : k == 2 ? w[11] : w[15];
     dst[k] = u;
   }
-  return -kOffset * s;
+  return -offset * s;
 }
 
 // 32 bf16 values (64 bytes at p, 16-byte aligned) to fp32.
@@ -315,18 +329,19 @@ __device__ __forceinline__ void warp_range(int n_tasks, int gpt, int wid, int n_
 // (issue_group was called for it and its cp.async committed). On return `slot` is the slot the
 // next phase's first group goes to. xe: for gate/up, the shared-memory offset of the x block
 // unscales (each block's MMA result is multiplied by its own power of two).
-template <int KIND, int D>
+template <int KIND, int D, int FMT>
 __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const uint8_t* psm, const ItemRec* items,
                                          const int* rowtok, uint32_t sx, uint32_t sc, uint32_t xe, const int* hexp,
                                          uint32_t sring_w, const uint16_t* sring_p, long long G0, long long G1,
-                                         int gpt, Ring<D>& ring, int& slot, int lane, int* s_done) {
+                                         int gpt, Ring<D, FMT>& ring, int& slot, int lane, int* s_done) {
+  static_assert(FMT == 0, "the 2-bit format streams through p_stream_q2");
   if (G0 >= G1) return;
   const int g = lane >> 2;
-  const long long dhi = hi_delta<KIND>(A);
+  const long long dhi = hi_delta<KIND, FMT>(A);
   float* part = X.part + (size_t)KIND * X.part_stride;
   int* cnt = X.task_cnt + (size_t)KIND * X.cnt_stride;
   int t = (int)(G0 / gpt);
-  PTask cur = make_task<KIND>(A, items, rowtok, sx, sc, t, lane);
+  PTask cur = make_task<KIND, FMT>(A, items, rowtok, sx, sc, t, lane);
   PTask nxt = cur;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (long long G = G0; G < G1; ++G) {
@@ -334,7 +349,7 @@ __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const 
     const long long Gn = G + 1;
     const bool more = Gn < G1;
     const int tn = more ? (int)(Gn / gpt) : t;
-    if (more && tn != t) nxt = make_task<KIND>(A, items, rowtok, sx, sc, tn, lane);
+    if (more && tn != t) nxt = make_task<KIND, FMT>(A, items, rowtok, sx, sc, tn, lane);
     const int gsn = (int)(Gn - (long long)tn * gpt);
     const PTask& src = tn != t ? nxt : cur;
     __syncwarp();
@@ -377,13 +392,15 @@ __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const 
         const float cb = jj == 0 ? c1.x : jj == 1 ? c1.y : jj == 2 ? c1.z : c1.w;
         float dd[4];
         block_mma(dd, ring.lo[j], ring.hi[j], xv, ca, cb);
-        if (more && src.valid && (j & 1)) {  // blocks j - 1 and j are consumed: refill both
-          const uint4 a = ld_codes16(src.wlo + (size_t)(gsn * D + j - 1) * kQBlock);
-          const uint4 b = ld_codes16(src.wlo + dhi + (size_t)(gsn * D + j - 1) * kQBlock);
-          ring.lo[j - 1] = make_uint2(a.x, a.y);
-          ring.lo[j] = make_uint2(a.z, a.w);
-          ring.hi[j - 1] = make_uint2(b.x, b.y);
-          ring.hi[j] = make_uint2(b.z, b.w);
+        {
+          if (more && src.valid && (j & 1)) {  // blocks j - 1 and j are consumed: refill both
+            const uint4 a = ld_codes16(src.wlo + (size_t)(gsn * D + j - 1) * kQBlock);
+            const uint4 b = ld_codes16(src.wlo + dhi + (size_t)(gsn * D + j - 1) * kQBlock);
+            ring.lo[j - 1] = make_uint2(a.x, a.y);
+            ring.lo[j] = make_uint2(a.z, a.w);
+            ring.hi[j - 1] = make_uint2(b.x, b.y);
+            ring.hi[j] = make_uint2(b.z, b.w);
+          }
         }
         const uint32_t wl = slo[j >> 1], wh = shi[j >> 1];
         float s_lo = __half2float(__ushort_as_half((unsigned short)((j & 1) ? (wl >> 16) : (wl & 0xFFFFu))));
@@ -399,14 +416,16 @@ __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const 
         acc[3] = fmaf(s_hi, dd[3], acc[3]);
       }
     } else if (more && src.valid) {
+      {
 #pragma unroll
-      for (int j = 0; j < D; j += 2) {
-        const uint4 a = ld_codes16(src.wlo + (size_t)(gsn * D + j) * kQBlock);
-        const uint4 b = ld_codes16(src.wlo + dhi + (size_t)(gsn * D + j) * kQBlock);
-        ring.lo[j] = make_uint2(a.x, a.y);
-        ring.lo[j + 1] = make_uint2(a.z, a.w);
-        ring.hi[j] = make_uint2(b.x, b.y);
-        ring.hi[j + 1] = make_uint2(b.z, b.w);
+        for (int j = 0; j < D; j += 2) {
+          const uint4 a = ld_codes16(src.wlo + (size_t)(gsn * D + j) * kQBlock);
+          const uint4 b = ld_codes16(src.wlo + dhi + (size_t)(gsn * D + j) * kQBlock);
+          ring.lo[j] = make_uint2(a.x, a.y);
+          ring.lo[j + 1] = make_uint2(a.z, a.w);
+          ring.hi[j] = make_uint2(b.x, b.y);
+          ring.hi[j + 1] = make_uint2(b.z, b.w);
+        }
       }
     }
     slot ^= 1;
@@ -449,6 +468,167 @@ __device__ __forceinline__ void p_stream(const FfnArgs& A, const PAux& X, const 
   }
 }
 
+// ------------------------------------------------------------------ 2-bit format ---------
+// A group of the 2-bit format is 8 blocks: 64 bytes of codes per M row (one 16-byte chunk per
+// lane) and 16 bytes of fp16 scales per row. Bytes per group are a quarter of int8's, so with
+// one group in flight per warp the streaming would be bound by latency, not bandwidth: a warp
+// keeps kQ2Ahead groups requested ahead, the codes in a register queue (Ring<8, 1>) and the
+// scales in a cp.async ring of kQ2Ahead slots (one commit per group).
+
+// Requests group gs of task p: its codes into (lo, hi), its scales into scale slot `slot`;
+// commits one cp.async group in any case.
+__device__ __forceinline__ void q2_request(const PTask& p, long long dhi, int gs, uint4& lo, uint4& hi,
+                                           uint32_t sring_w, int slot, int lane) {
+  if (p.valid) {
+    lo = ld_codes16(p.wlo + (size_t)gs * 64);
+    hi = ld_codes16(p.wlo + dhi + (size_t)gs * 64);
+    if (lane < 16) cp_async16(sring_w + (uint32_t)(slot * 16 + lane) * 16u, p.ssrc + gs * 16);
+  }
+  cp_async_commit();
+}
+
+// Requests the first kQ2Ahead groups of the range [G0, G1) into queue positions 0..kQ2Ahead-1.
+template <int KIND>
+__device__ __forceinline__ void q2_prime(const FfnArgs& A, const ItemRec* items, const int* rowtok, uint32_t sx,
+                                         uint32_t sc, long long G0, long long G1, int gpt, Ring<8, 1>& ring,
+                                         uint32_t sring_w, int lane) {
+  const long long dhi = hi_delta<KIND, 1>(A);
+  int t = -1;
+  PTask p{};
+#pragma unroll
+  for (int i = 0; i < kQ2Ahead; ++i) {
+    const long long G = G0 + i;
+    if (G < G1) {
+      if ((int)(G / gpt) != t) {
+        t = (int)(G / gpt);
+        p = make_task<KIND, 1>(A, items, rowtok, sx, sc, t, lane);
+      }
+      q2_request(p, dhi, (int)(G - (long long)t * gpt), ring.lo[i], ring.hi[i], sring_w, (int)(G % kQ2Ahead), lane);
+    } else {
+      cp_async_commit();
+    }
+  }
+}
+
+// Streams groups [G0, G1) of one phase of the 2-bit format (primed by q2_prime). As p_stream,
+// with the group requested kQ2Ahead ahead instead of one.
+template <int KIND>
+__device__ __forceinline__ void p_stream_q2(const FfnArgs& A, const PAux& X, const uint8_t* psm,
+                                            const ItemRec* items, const int* rowtok, uint32_t sx, uint32_t sc,
+                                            uint32_t xe, const int* hexp, uint32_t sring_w, const uint16_t* sring_p,
+                                            long long G0, long long G1, int gpt, Ring<8, 1>& ring, int lane,
+                                            int* s_done) {
+  if (G0 >= G1) return;
+  const int g = lane >> 2;
+  const long long dhi = hi_delta<KIND, 1>(A);
+  float* part = X.part + (size_t)KIND * X.part_stride;
+  int* cnt = X.task_cnt + (size_t)KIND * X.cnt_stride;
+  int t = (int)(G0 / gpt);
+  PTask cur = make_task<KIND, 1>(A, items, rowtok, sx, sc, t, lane);
+  int tl = -1;  // task of the group requested ahead
+  PTask la = cur;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (long long G = G0; G < G1; ++G) {
+    const int gs = (int)(G - (long long)t * gpt);
+    cp_async_wait<kQ2Ahead - 1>();  // this group's scales have landed
+    __syncwarp();
+    if (cur.valid) {
+      const uint16_t* sp = sring_p + (size_t)((int)(G % kQ2Ahead) * 16) * 8;
+      const uint4 sa = *reinterpret_cast<const uint4*>(sp + g * 8);
+      const uint4 sb = *reinterpret_cast<const uint4*>(sp + (8 + g) * 8);
+      const uint32_t slo[4] = {sa.x, sa.y, sa.z, sa.w}, shi[4] = {sb.x, sb.y, sb.z, sb.w};
+      const uint32_t qlo[4] = {ring.lo[0].x, ring.lo[0].y, ring.lo[0].z, ring.lo[0].w};
+      const uint32_t qhi[4] = {ring.hi[0].x, ring.hi[0].y, ring.hi[0].z, ring.hi[0].w};
+      float4 c0, c1, xu;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int b = gs * 8 + j;
+        if ((j & 3) == 0) {
+          c0 = *reinterpret_cast<const float4*>(psm + cur.cs0 + b * 4);
+          c1 = *reinterpret_cast<const float4*>(psm + cur.cs1 + b * 4);
+          if (KIND == kGU) xu = *reinterpret_cast<const float4*>(psm + xe + b * 4);
+        }
+        const uint4 xv =
+            cur.has ? *reinterpret_cast<const uint4*>(psm + cur.xrow + b * kQBlock * 2) : make_uint4(0, 0, 0, 0);
+        const int jj = j & 3;
+        const float ca = jj == 0 ? c0.x : jj == 1 ? c0.y : jj == 2 ? c0.z : c0.w;
+        const float cb = jj == 0 ? c1.x : jj == 1 ? c1.y : jj == 2 ? c1.z : c1.w;
+        float dd[4];
+        const uint32_t wl = qlo[j >> 1], wh = qhi[j >> 1];
+        block_mma_q2(dd, (j & 1) ? (wl >> 16) : (wl & 0xFFFFu), (j & 1) ? (wh >> 16) : (wh & 0xFFFFu), xv, ca, cb);
+        const uint32_t sl = slo[j >> 1], sh = shi[j >> 1];
+        float s_lo = __half2float(__ushort_as_half((unsigned short)((j & 1) ? (sl >> 16) : (sl & 0xFFFFu))));
+        float s_hi = __half2float(__ushort_as_half((unsigned short)((j & 1) ? (sh >> 16) : (sh & 0xFFFFu))));
+        if (KIND == kGU) {
+          const float u = jj == 0 ? xu.x : jj == 1 ? xu.y : jj == 2 ? xu.z : xu.w;
+          s_lo *= u;
+          s_hi *= u;
+        }
+        acc[0] = fmaf(s_lo, dd[0], acc[0]);
+        acc[1] = fmaf(s_lo, dd[1], acc[1]);
+        acc[2] = fmaf(s_hi, dd[2], acc[2]);
+        acc[3] = fmaf(s_hi, dd[3], acc[3]);
+      }
+    }
+    // the queue moves one place; group G + kQ2Ahead goes to its end, its scales into the slot this
+    // group's scales occupied (every lane has read them)
+#pragma unroll
+    for (int i = 0; i + 1 < kQ2Ahead; ++i) {
+      ring.lo[i] = ring.lo[i + 1];
+      ring.hi[i] = ring.hi[i + 1];
+    }
+    __syncwarp();
+    const long long Gl = G + kQ2Ahead;
+    if (Gl < G1) {
+      const int tn = (int)(Gl / gpt);
+      if (tn != tl) {
+        tl = tn;
+        la = tl == t ? cur : make_task<KIND, 1>(A, items, rowtok, sx, sc, tl, lane);
+      }
+      q2_request(la, dhi, (int)(Gl - (long long)tl * gpt), ring.lo[kQ2Ahead - 1], ring.hi[kQ2Ahead - 1], sring_w,
+                 (int)(Gl % kQ2Ahead), lane);
+    } else {
+      cp_async_commit();
+    }
+    if (gs == gpt - 1 || G + 1 == G1) {
+      // the task ends in this range: finish it, or publish this part of a cut task
+      if (cur.valid) {
+        const long long t0 = (long long)t * gpt;
+        const bool first = G0 <= t0, last = G1 >= t0 + gpt;
+        bool finish = true;
+        if (!(first && last)) {
+          const int my = first ? 0 : 1;
+          float4* slot_p = reinterpret_cast<float4*>(part + ((size_t)t * 2 + my) * 128);
+          slot_p[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+          __threadfence();
+          __syncwarp();
+          int second = 0;
+          if (lane == 0) {
+            second = atomicAdd(cnt + t, 1) == 1;
+            if (second) cnt[t] = 0;  // both parts are in: the counter is free for the next launch
+          }
+          finish = __shfl_sync(0xFFFFFFFFu, second, 0) != 0;
+          if (finish) {
+            __threadfence();
+            const float4 p0 = __ldcg(reinterpret_cast<const float4*>(part + (size_t)t * 2 * 128) + lane);
+            const float4 p1 = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)t * 2 + 1) * 128) + lane);
+            acc[0] = p0.x + p1.x;
+            acc[1] = p0.y + p1.y;
+            acc[2] = p0.z + p1.z;
+            acc[3] = p0.w + p1.w;
+          }
+        }
+        if (finish) p_epilogue<KIND>(A, X, cur, hexp, lane, acc, s_done);
+      }
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      if (G + 1 < G1) {
+        t = (int)((G + 1) / gpt);
+        cur = tl == t ? la : make_task<KIND, 1>(A, items, rowtok, sx, sc, t, lane);
+      }
+    }
+  }
+}
+
 // End of every CTA: the last CTA to finish puts the counters back to zero for the next launch
 // (per-item tasks done, row maxima, the exit counter itself; all stream-K counters too if a
 // CTA abandoned its work, which leaves some of them unpaired). A stream-K counter is otherwise
@@ -474,8 +654,9 @@ __device__ __forceinline__ void p_exit(const FfnArgs& A, const PAux& X, int rows
   }
 }
 
-template <int DG, int DD>
+template <int DG, int DD, int FMT>
 __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PAux X) {
+  constexpr float kOff = FMT == 1 ? kOffsetQ2 : kOffset;  // MMA offset of a code (1024 + c or 1152 + q)
   extern __shared__ __align__(16) uint8_t psm[];
   __shared__ int s_ok;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -483,7 +664,7 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   const int T = A.T, d = A.d, f = A.f;
   const int rows = A.P + T * A.n_shared;
   const int items_max = (A.P < A.E ? A.P : A.E) + A.n_shared;
-  const PLayout Lo = p_layout<DG, DD>(T, d, f, items_max, rows, X.rows_cap);
+  const PLayout Lo = p_layout<DG, DD, FMT>(T, d, f, items_max, rows, X.rows_cap);
   ItemRec* items = reinterpret_cast<ItemRec*>(psm + Lo.items);
   int* s_done = reinterpret_cast<int*>(psm + Lo.done);
   int* rowtok = reinterpret_cast<int*>(psm + Lo.rowtok);
@@ -491,8 +672,9 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   float* xe = reinterpret_cast<float*>(psm + Lo.xe);
   uint32_t* bmax = reinterpret_cast<uint32_t*>(psm + Lo.bmax);
   const int dmax = DG > DD ? DG : DD;
-  const uint32_t sring_w = smem_u32(psm + Lo.sring) + (uint32_t)warp * 2u * 16u * dmax * 2u;
-  const uint16_t* sring_p = reinterpret_cast<const uint16_t*>(psm + Lo.sring) + (size_t)warp * 2 * 16 * dmax;
+  const int n_sslot = FMT == 1 ? 4 : 2;  // scale slots per warp
+  const uint32_t sring_w = smem_u32(psm + Lo.sring) + (uint32_t)warp * n_sslot * 16u * dmax * 2u;
+  const uint16_t* sring_p = reinterpret_cast<const uint16_t*>(psm + Lo.sring) + (size_t)warp * n_sslot * 16 * dmax;
   const int nbd = d / kQBlock, nbf = f / kQBlock;
 
   // ---- phase 0 --------------------------------------------------------------------------
@@ -522,7 +704,7 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
 #pragma unroll
       for (int q = 0; q < kQBlock; ++q) xv[q] *= down;
       *reinterpret_cast<float*>(psm + o_scx + (size_t)xt * sum_stride(d) + xb * 4) =
-          stage_block_f16(psm + o_sx + (size_t)xt * act_stride(d), xb, xv);
+          stage_block_f16(psm + o_sx + (size_t)xt * act_stride(d), xb, xv, kOff);
       if (xt == 0) xe[xb] = pow2f(e);
     }
   }
@@ -560,17 +742,25 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   long long G0, G1;
   const int gpt_gu = nbd / DG;
   warp_range(n_items * (f / 8), gpt_gu, wid, n_warps, &G0, &G1);
-  Ring<DG> rg;
+  Ring<DG, FMT> rg;
   int slot = 0;
-  if (G0 < G1) {
-    const PTask p = make_task<kGU>(A, items, rowtok, o_sx, o_scx, (int)(G0 / gpt_gu), lane);
-    issue_group<DG>(p, hi_delta<kGU>(A), (int)(G0 % gpt_gu), rg, sring_w, slot, lane);
+  if constexpr (FMT == 1) {
+    q2_prime<kGU>(A, items, rowtok, o_sx, o_scx, G0, G1, gpt_gu, rg, sring_w, lane);
+  } else {
+    if (G0 < G1) {
+      const PTask p = make_task<kGU, FMT>(A, items, rowtok, o_sx, o_scx, (int)(G0 / gpt_gu), lane);
+      issue_group<DG, FMT>(p, hi_delta<kGU, FMT>(A), (int)(G0 % gpt_gu), rg, sring_w, slot, lane);
+    }
+    cp_async_commit();
   }
-  cp_async_commit();
 
   // ---- phase 1: gate/up ----------------------------------------------------------------
-  p_stream<kGU, DG>(A, X, psm, items, rowtok, o_sx, o_scx, Lo.xe, hexp, sring_w, sring_p, G0, G1, gpt_gu, rg, slot,
-                    lane, s_done);
+  if constexpr (FMT == 1)
+    p_stream_q2<kGU>(A, X, psm, items, rowtok, o_sx, o_scx, Lo.xe, hexp, sring_w, sring_p, G0, G1, gpt_gu, rg, lane,
+                     s_done);
+  else
+    p_stream<kGU, DG, FMT>(A, X, psm, items, rowtok, o_sx, o_scx, Lo.xe, hexp, sring_w, sring_p, G0, G1, gpt_gu, rg,
+                           slot, lane, s_done);
 
   // ---- phase 2: publish this CTA's gate/up work; first down loads; wait for this CTA's
   // items; their h rows to f16 -------------------------------------------------------------
@@ -597,13 +787,17 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   const int r_hi = cta_dn ? items[i_hi].row0 + items[i_hi].ntok : 0;
   const uint32_t o_sh = Lo.act - (uint32_t)r_lo * act_stride(f);
   const uint32_t o_sch = Lo.act + (uint32_t)X.rows_cap * act_stride(f) - (uint32_t)r_lo * sum_stride(f);
-  Ring<DD> rd;
+  Ring<DD, FMT> rd;
   __syncwarp();
-  if (G0 < G1) {
-    const PTask p = make_task<kDN>(A, items, rowtok, o_sh, o_sch, (int)(G0 / gpt_dn), lane);
-    issue_group<DD>(p, hi_delta<kDN>(A), (int)(G0 % gpt_dn), rd, sring_w, slot, lane);
+  if constexpr (FMT == 1) {
+    q2_prime<kDN>(A, items, rowtok, o_sh, o_sch, G0, G1, gpt_dn, rd, sring_w, lane);
+  } else {
+    if (G0 < G1) {
+      const PTask p = make_task<kDN, FMT>(A, items, rowtok, o_sh, o_sch, (int)(G0 / gpt_dn), lane);
+      issue_group<DD, FMT>(p, hi_delta<kDN, FMT>(A), (int)(G0 % gpt_dn), rd, sring_w, slot, lane);
+    }
+    cp_async_commit();
   }
-  cp_async_commit();
   if (tid == 0) {
     int ok = r_hi - r_lo <= X.rows_cap;
     const uint64_t t0 = globaltimer_ns();
@@ -649,13 +843,17 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
     }
     // staged row r sits at (o_sh + r * stride) mod 2^32, i.e. (r - r_lo) strides into the region
     *reinterpret_cast<float*>(psm + (uint32_t)(o_sch + (uint32_t)r * sum_stride(f)) + b * 4) =
-        stage_block_f16(psm + (uint32_t)(o_sh + (uint32_t)r * act_stride(f)), b, v);
+        stage_block_f16(psm + (uint32_t)(o_sh + (uint32_t)r * act_stride(f)), b, v, kOff);
   }
   __syncthreads();
 
   // ---- phase 3: down -------------------------------------------------------------------
-  p_stream<kDN, DD>(A, X, psm, items, rowtok, o_sh, o_sch, 0u, hexp, sring_w, sring_p, G0, G1, gpt_dn, rd, slot,
-                    lane, s_done);
+  if constexpr (FMT == 1)
+    p_stream_q2<kDN>(A, X, psm, items, rowtok, o_sh, o_sch, 0u, hexp, sring_w, sring_p, G0, G1, gpt_dn, rd, lane,
+                     s_done);
+  else
+    p_stream<kDN, DD, FMT>(A, X, psm, items, rowtok, o_sh, o_sch, 0u, hexp, sring_w, sring_p, G0, G1, gpt_dn, rd,
+                           slot, lane, s_done);
   cp_async_wait_all();
   p_exit(A, X, rows, items_max, tid);
 }
@@ -666,17 +864,17 @@ int persist_rows_cap(const FfnArgs& a, int sm_count) {
   return p_rows_cap(a.T, a.d, items_max, rows, sm_count * kPW);
 }
 
-template <int DG, int DD>
+template <int DG, int DD, int FMT>
 cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st) {
   const int rows = a.P + a.T * a.n_shared;
   const int items_max = (a.P < a.E ? a.P : a.E) + a.n_shared;
   const int rows_cap = persist_rows_cap(a, sm_count);
-  const PLayout L = p_layout<DG, DD>(a.T, a.d, a.f, items_max, rows, rows_cap);
-  const void* fn = (const void*)ffn_persist_kernel<DG, DD>;
+  const PLayout L = p_layout<DG, DD, FMT>(a.T, a.d, a.f, items_max, rows, rows_cap);
+  const void* fn = (const void*)ffn_persist_kernel<DG, DD, FMT>;
   cudaError_t e = ensure_dynamic_smem(fn, L.total);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_persist_kernel<DG, DD>, kPThreads, L.total);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_persist_kernel<DG, DD, FMT>, kPThreads, L.total);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   PAux px{x.part, x.task_cnt, x.hmax, x.item_done, x.part_stride, x.cnt_stride, rows_cap, x.exit};
@@ -684,7 +882,7 @@ cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int sm_count
   // a programmatic dependent of the bucketing kernel before it: the CTAs stage x while the
   // bucketing runs and wait for its outputs (griddepcontrol.wait). Every CTA's waits for other
   // CTAs are bounded, so the grid needs no cooperative launch to be safe.
-  return launch_pdl(ffn_persist_kernel<DG, DD>, dim3(sm_count), dim3(kPThreads), L.total, st, a, px);
+  return launch_pdl(ffn_persist_kernel<DG, DD, FMT>, dim3(sm_count), dim3(kPThreads), L.total, st, a, px);
 }
 
 }  // namespace
@@ -692,20 +890,24 @@ cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int sm_count
 size_t persist_smem_bytes(const FfnArgs& a, int sm_count) {
   const int rows = a.P + a.T * a.n_shared;
   const int items_max = (a.P < a.E ? a.P : a.E) + a.n_shared;
-  return p_layout<8, 8>(a.T, a.d, a.f, items_max, rows, persist_rows_cap(a, sm_count)).total;
+  const int cap = persist_rows_cap(a, sm_count);
+  return a.fmt == 1 ? p_layout<8, 8, 1>(a.T, a.d, a.f, items_max, rows, cap).total
+                    : p_layout<8, 8, 0>(a.T, a.d, a.f, items_max, rows, cap).total;
 }
 
 bool persist_supported(const FfnArgs& a, int sm_count) {
   return a.xdt == 0 && a.T >= 1 && a.T <= 8 && a.d % 128 == 0 && a.f % 128 == 0 &&
+         (a.fmt == 0 || (a.d % 256 == 0 && a.f % 256 == 0)) &&
          a.T * (a.d / kQBlock) <= kPThreads && persist_smem_bytes(a, sm_count) <= 200 * 1024;
 }
 
 cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st) {
+  if (a.fmt == 1) return launch_persist_d<8, 8, 1>(a, x, sm_count, st);  // d and f multiples of 256
   const bool g8 = (a.d / kQBlock) % 8 == 0, d8 = (a.f / kQBlock) % 8 == 0;
-  if (g8 && d8) return launch_persist_d<8, 8>(a, x, sm_count, st);
-  if (g8) return launch_persist_d<8, 4>(a, x, sm_count, st);
-  if (d8) return launch_persist_d<4, 8>(a, x, sm_count, st);
-  return launch_persist_d<4, 4>(a, x, sm_count, st);
+  if (g8 && d8) return launch_persist_d<8, 8, 0>(a, x, sm_count, st);
+  if (g8) return launch_persist_d<8, 4, 0>(a, x, sm_count, st);
+  if (d8) return launch_persist_d<4, 8, 0>(a, x, sm_count, st);
+  return launch_persist_d<4, 4, 0>(a, x, sm_count, st);
 }
 
 }  // namespace moe

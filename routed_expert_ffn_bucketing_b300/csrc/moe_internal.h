@@ -81,6 +81,7 @@ struct FfnArgs {
   float* h;  // fp32 [P + T*n_shared][f]
   int* status;
   uint64_t wait_ns;  // limit of the kernels' bounded waits for other threads' work (moe_set_wait_limit)
+  int fmt;           // expert record format: 0 int8 codes, 1 the 2-bit format (MOE_FMT_Q2)
   int T, d, f, E, k, n_shared, P;
   // record layout
   uint64_t o_gate_q, o_up_q, o_down_q, o_gate_s, o_up_s, o_down_s;

@@ -10,7 +10,9 @@ This module prepares inputs and nothing else. It holds:
   a CUDA implementation of the same draw (synth/csrc/synth_fill.cu) is bit-identical;
 * the block-32 weight quantiser that turns N(0, sigma) weights into int8 codes plus one
   fp16 scale per 32 consecutive elements of the reduction dimension (the weight format
-  of the workloads: s = fp16_rne(amax / 127), q = clamp(rint(w / s), -127, 127));
+  of the workloads: s = fp16_rne(amax / 127), q = clamp(rint(w / s), -127, 127)), and the
+  2.5-bit one of the sub-4-bit format (2-bit codes c with w = s (c - 1.5): s = fp16_rne(amax /
+  1.5), c = clamp(rint(w / s + 1.5), 0, 3));
 * the packing of one expert's six arrays into its byte record;
 * the router columns' Zipf(s) popularity recipe.
 
@@ -100,6 +102,24 @@ def quantize_block32(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return q, s16
 
 
+def quantize_q2_block32(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """2-bit codes (uint8, 0..3) and fp16 scales of fp32 w [R][C] in blocks of 32 along C, for
+    the format w = s * (c - 1.5): s = fp16_rne(amax / 1.5) (fp32 division), c = clamp(rint(w / s
+    + 1.5), 0, 3) with the division and the addition in fp32 and round-half-even; a block whose
+    scale is 0 gets c = 0."""
+    R, C = w.shape
+    assert C % BLOCK == 0
+    wb = w.astype(np.float32).reshape(R, C // BLOCK, BLOCK)
+    amax = np.abs(wb).max(axis=2)
+    s16 = (amax / np.float32(1.5)).astype(np.float32).astype(np.float16)
+    sf = s16.astype(np.float32)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        cf = np.rint((wb / sf).astype(np.float32) + np.float32(1.5))
+    cf = np.where(sf == 0, np.float32(0), cf)
+    c = np.clip(cf, 0, 3).astype(np.uint8).reshape(R, C)
+    return c, s16
+
+
 def fp32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
     """Round fp32 to bf16 (nearest, ties to even); returns the uint16 bit patterns.
     Inputs are finite (the generator never produces NaN or Inf)."""
@@ -136,9 +156,17 @@ class RecordLayout:
     record_bytes: int
 
 
-def record_layout(d: int, f: int) -> RecordLayout:
+FMT_INT8, FMT_Q2 = 0, 1  # record formats: int8 codes, or 2-bit codes (4 per byte)
+
+
+def record_layout(d: int, f: int, fmt: int = FMT_INT8) -> RecordLayout:
+    """fmt FMT_INT8: one byte per code; FMT_Q2: four codes per byte (d and f multiples of 256)."""
     assert d % BLOCK == 0 and f % BLOCK == 0
-    sizes = [f * d, f * d, d * f, f * (d // BLOCK) * 2, f * (d // BLOCK) * 2, d * (f // BLOCK) * 2]
+    cb = 1 if fmt == FMT_INT8 else 4  # codes per byte
+    if fmt == FMT_Q2:
+        assert d % 256 == 0 and f % 256 == 0
+    sizes = [f * d // cb, f * d // cb, d * f // cb, f * (d // BLOCK) * 2, f * (d // BLOCK) * 2,
+             d * (f // BLOCK) * 2]
     offs, o = [], 0
     for n in sizes:
         offs.append(o)
@@ -148,13 +176,15 @@ def record_layout(d: int, f: int) -> RecordLayout:
 
 @dataclass
 class ExpertArrays:
-    """One expert's quantised weights (the oracle's view of a record)."""
+    """One expert's quantised weights (the oracle's view of a record). fmt "int8": codes are int8;
+    fmt "q2": codes are 2-bit values 0..3 (uint8 arrays) of the format w = s (c - 1.5)."""
     gate_q: np.ndarray  # int8 [f][d]
     gate_s: np.ndarray  # fp16 [f][d/32]
     up_q: np.ndarray    # int8 [f][d]
     up_s: np.ndarray    # fp16 [f][d/32]
     down_q: np.ndarray  # int8 [d][f]
     down_s: np.ndarray  # fp16 [d][f/32]
+    fmt: str = "int8"
 
 
 def expert_arrays(seed: int, layer: int, expert: int, d: int, f: int,
@@ -168,6 +198,49 @@ def expert_arrays(seed: int, layer: int, expert: int, d: int, f: int,
     uq, us = quantize_block32(u)
     dq, ds = quantize_block32(w)
     return ExpertArrays(gq, gs, uq, us, dq, ds)
+
+
+def expert_arrays_q2(seed: int, layer: int, expert: int, d: int, f: int,
+                     sigma: float = 0.02) -> ExpertArrays:
+    """The same N(0, sigma) weights as expert_arrays, quantised to the 2-bit format."""
+    g = normal_f32(stream_key(seed, TAG_GATE, layer, expert), 0, f * d, sigma).reshape(f, d)
+    u = normal_f32(stream_key(seed, TAG_UP, layer, expert), 0, f * d, sigma).reshape(f, d)
+    w = normal_f32(stream_key(seed, TAG_DOWN, layer, expert), 0, d * f, sigma).reshape(d, f)
+    gq, gs = quantize_q2_block32(g)
+    uq, us = quantize_q2_block32(u)
+    dq, ds = quantize_q2_block32(w)
+    return ExpertArrays(gq, gs, uq, us, dq, ds, fmt="q2")
+
+
+# stored position of code j (0..7) of a lane's 8 consecutive codes in the 2-bit format: the
+# order (0, 2, 1, 3, 4, 6, 5, 7), two bits each
+_Q2_SLOT = np.array([0, 2, 1, 3, 4, 6, 5, 7])
+
+
+def pack_codes_q2(c: np.ndarray) -> np.ndarray:
+    """Rows of 2-bit codes [R][K] (K a multiple of 256) to their stored bytes [R][K/4]: in each
+    group of 8 blocks (256 codes, 64 bytes), 16-byte chunk q holds for block b = 0..7 one 16-bit
+    little-endian word with codes 8q..8q+7 of block b, code j at bits 2 * slot(j), slot the
+    order (0, 2, 1, 3, 4, 6, 5, 7)."""
+    R, K = c.shape
+    assert K % 256 == 0
+    v = c.astype(np.uint32).reshape(R, K // 256, 8, 4, 8)        # [r][group][block][q][j]
+    words = np.zeros((R, K // 256, 8, 4), dtype=np.uint32)
+    for j in range(8):
+        words |= v[..., j] << np.uint32(2 * _Q2_SLOT[j])
+    words = words.transpose(0, 1, 3, 2).astype(np.uint16)       # [r][group][q][block]
+    return np.ascontiguousarray(words).view(np.uint8).reshape(R, K // 4)
+
+
+def unpack_codes_q2(b: np.ndarray) -> np.ndarray:
+    """The inverse of pack_codes_q2."""
+    R, KB = b.shape
+    K = KB * 4
+    words = np.ascontiguousarray(b).view(np.uint16).reshape(R, K // 256, 4, 8).transpose(0, 1, 3, 2)
+    out = np.zeros((R, K // 256, 8, 4, 8), dtype=np.uint8)
+    for j in range(8):
+        out[..., j] = (words.astype(np.uint32) >> np.uint32(2 * _Q2_SLOT[j])) & 3
+    return out.reshape(R, K)
 
 
 def interleave_codes(q: np.ndarray) -> np.ndarray:
@@ -192,27 +265,35 @@ def deinterleave_codes(q: np.ndarray) -> np.ndarray:
 
 def pack_record(a: ExpertArrays, slot_bytes: int | None = None) -> np.ndarray:
     """Byte record (uint8) of one expert in the layout of record_layout (codes in the stored
-    order of interleave_codes); zero padding."""
+    order of interleave_codes, or of pack_codes_q2 for the 2-bit format); zero padding."""
     f, d = a.gate_q.shape
-    L = record_layout(d, f)
+    q2 = a.fmt == "q2"
+    L = record_layout(d, f, FMT_Q2 if q2 else FMT_INT8)
     n = L.record_bytes if slot_bytes is None else slot_bytes
     assert n >= L.record_bytes
     rec = np.zeros(n, dtype=np.uint8)
-    for off, arr in ((L.gate_q, interleave_codes(a.gate_q)), (L.up_q, interleave_codes(a.up_q)),
-                     (L.down_q, interleave_codes(a.down_q)),
+    pk = pack_codes_q2 if q2 else interleave_codes
+    for off, arr in ((L.gate_q, pk(a.gate_q)), (L.up_q, pk(a.up_q)), (L.down_q, pk(a.down_q)),
                      (L.gate_s, a.gate_s), (L.up_s, a.up_s), (L.down_s, a.down_s)):
         b = np.ascontiguousarray(arr).view(np.uint8).reshape(-1)
         rec[off:off + b.size] = b
     return rec
 
 
-def unpack_record(rec: np.ndarray, d: int, f: int) -> ExpertArrays:
-    L = record_layout(d, f)
+def unpack_record(rec: np.ndarray, d: int, f: int, fmt: int = FMT_INT8) -> ExpertArrays:
+    L = record_layout(d, f, fmt)
     r = np.ascontiguousarray(rec, dtype=np.uint8)
 
     def take(off, n, dt, shape):
         return r[off:off + n * np.dtype(dt).itemsize].view(dt).reshape(shape).copy()
     nb_d, nb_f = d // BLOCK, f // BLOCK
+    if fmt == FMT_Q2:
+        return ExpertArrays(unpack_codes_q2(take(L.gate_q, f * d // 4, np.uint8, (f, d // 4))),
+                            take(L.gate_s, f * nb_d, np.float16, (f, nb_d)),
+                            unpack_codes_q2(take(L.up_q, f * d // 4, np.uint8, (f, d // 4))),
+                            take(L.up_s, f * nb_d, np.float16, (f, nb_d)),
+                            unpack_codes_q2(take(L.down_q, d * f // 4, np.uint8, (d, f // 4))),
+                            take(L.down_s, d * nb_f, np.float16, (d, nb_f)), fmt="q2")
     return ExpertArrays(deinterleave_codes(take(L.gate_q, f * d, np.int8, (f, d))),
                         take(L.gate_s, f * nb_d, np.float16, (f, nb_d)),
                         deinterleave_codes(take(L.up_q, f * d, np.int8, (f, d))),

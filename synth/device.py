@@ -23,7 +23,7 @@ class DeviceLayer:
         if fill == "device":
             from .gpu import fill_expert_records
             fill_expert_records(w.seed, layer, 0, n, w.d, w.f, self.pool.data_ptr(), self.slot_bytes,
-                                w.expert_sigma)
+                                w.expert_sigma, fmt=w.fmt)
         else:
             for e in range(n):
                 rec = pack_record(w.expert(layer, e), self.slot_bytes)

@@ -17,16 +17,21 @@ def _load():
         _lib.synth_fill_expert_records.restype = C.c_int
         _lib.synth_fill_expert_records.argtypes = [C.c_uint64, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                                    C.c_float, C.c_void_p, C.c_uint64, C.c_void_p]
+        _lib.synth_fill_expert_records_fmt.restype = C.c_int
+        _lib.synth_fill_expert_records_fmt.argtypes = [C.c_uint64, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                                       C.c_float, C.c_void_p, C.c_uint64, C.c_int, C.c_void_p]
     return _lib
 
 
 def fill_expert_records(seed: int, layer: int, expert0: int, n_experts: int, d: int, f: int, dst: int,
-                        stride: int, sigma: float = 0.02, stream: int | None = None) -> None:
+                        stride: int, sigma: float = 0.02, stream: int | None = None, fmt: int = 0) -> None:
     """Writes the records of experts expert0 .. expert0+n-1 of `layer` to device address dst,
-    one every `stride` bytes; the same bytes as synth.pack_record(synth.expert_arrays(...))."""
+    one every `stride` bytes; the same bytes as synth.pack_record(synth.expert_arrays(...)), or of
+    expert_arrays_q2 with fmt 1."""
     if stream is None:
         import torch
         stream = torch.cuda.current_stream().cuda_stream
-    rc = _load().synth_fill_expert_records(seed, layer, expert0, n_experts, d, f, sigma, dst, stride, stream)
+    rc = _load().synth_fill_expert_records_fmt(seed, layer, expert0, n_experts, d, f, sigma, dst, stride, fmt,
+                                               stream)
     if rc != 0:
         raise RuntimeError(f"synth_fill_expert_records failed with CUDA error {rc}")

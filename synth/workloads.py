@@ -16,8 +16,8 @@ from dataclasses import dataclass, replace
 
 import numpy as np
 
-from . import (activations_bf16, activations_f32, bf16_bits_to_f32, expert_arrays, record_layout,
-               router_weights)
+from . import (FMT_INT8, FMT_Q2, activations_bf16, activations_f32, bf16_bits_to_f32, expert_arrays,
+               expert_arrays_q2, record_layout, router_weights)
 
 
 @dataclass(frozen=True)
@@ -36,6 +36,7 @@ class Workload:
     slots: int | None = None       # device slot pool size (tiered); None = every expert resident
     seed: int = 0
     expert_sigma: float = 0.02
+    fmt: int = FMT_INT8            # expert record format: FMT_INT8 or FMT_Q2 (2-bit codes)
 
     @property
     def P(self) -> int:
@@ -43,7 +44,7 @@ class Workload:
 
     @property
     def record_bytes(self) -> int:
-        return record_layout(self.d, self.f).record_bytes
+        return record_layout(self.d, self.f, self.fmt).record_bytes
 
     def describe(self) -> str:
         s = f"{self.name}: T={self.T} d={self.d} f={self.f} E={self.E} top-{self.k}"
@@ -52,6 +53,8 @@ class Workload:
             s += f", {self.layers} layers"
         if self.zipf_s:
             s += f", Zipf({self.zipf_s}) routing"
+        if self.fmt == FMT_Q2:
+            s += ", 2-bit block-32 experts (2.5 bits per weight)"
         return s
 
     # ---- inputs -------------------------------------------------------------------------
@@ -71,7 +74,8 @@ class Workload:
 
     def expert(self, layer: int, e: int):
         """Routed expert e < E, or shared expert s as e = E + s."""
-        return expert_arrays(self.seed, layer, e, self.d, self.f, self.expert_sigma)
+        gen = expert_arrays_q2 if self.fmt == FMT_Q2 else expert_arrays
+        return gen(self.seed, layer, e, self.d, self.f, self.expert_sigma)
 
 
 WORKLOADS = {
@@ -80,6 +84,7 @@ WORKLOADS = {
     "stack": Workload("stack", 4, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1, layers=48, residual=True),
     "prefill": Workload("prefill", 8192, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1),
     "tiered": Workload("tiered", 4, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1, layers=48, residual=True, slots=4500),
+    "decode_q2": Workload("decode_q2", 4, 2048, 768, 512, 10, 1, 1.0, fmt=FMT_Q2),
 }
 
 

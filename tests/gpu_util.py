@@ -32,7 +32,7 @@ def run_layer(dl: DeviceLayer, batch: int = 0, mode: int = L.MOE_MODE_AUTO, f32:
     buf = lay.alloc_buffers(s, ydt=L.MOE_F32 if f32 else ydt, odt=odt)
     x = dl.x(batch, torch.float32 if f32 else torch.bfloat16)
     table = L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of if slot_of is None else slot_of,
-                           dl.shared_ptr)
+                           dl.shared_ptr, fmt=w.fmt)
     lay.forward(buf, x, dl.router, table, mode, residual=x if residual else None)
     status = L.moe_read_status(buf.ws)
     torch.cuda.synchronize()
@@ -44,7 +44,7 @@ _EXPERTS: dict = {}
 
 
 def cached_expert(w: Workload, layer: int, e: int):
-    key = (w.seed, w.d, w.f, w.expert_sigma, layer, e)
+    key = (w.seed, w.d, w.f, w.expert_sigma, w.fmt, layer, e)
     if key not in _EXPERTS:
         if len(_EXPERTS) > 256:
             _EXPERTS.pop(next(iter(_EXPERTS)))

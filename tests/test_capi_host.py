@@ -470,3 +470,33 @@ def test_wait_limit_argument_check():
     assert e.value.status == L.MOE_EINVAL and "10 s" in L.moe_last_error_string()
     L.moe_set_wait_limit(5_000_000)
     L.moe_set_wait_limit(0)
+
+
+@pytest.mark.parametrize("d,f", [(256, 256), (2048, 768), (512, 1024)])
+def test_q2_record_layout_matches_generator(d, f):
+    import synth
+    lay = L.moe_get_record_layout(d, f, L.MOE_FMT_Q2)
+    ref = synth.record_layout(d, f, synth.FMT_Q2)
+    assert (lay.gate_q, lay.up_q, lay.down_q, lay.gate_s, lay.up_s, lay.down_s, lay.record_bytes) == \
+        (ref.gate_q, ref.up_q, ref.down_q, ref.gate_s, ref.up_s, ref.down_s, ref.record_bytes)
+    i8 = L.moe_get_record_layout(d, f, L.MOE_FMT_INT8)
+    assert i8.record_bytes == L.moe_get_expert_layout(d, f).record_bytes
+    assert lay.record_bytes < i8.record_bytes / 3
+
+
+def test_q2_format_checks_before_any_launch():
+    for d, f, fmt in ((288, 256, L.MOE_FMT_Q2), (256, 160, L.MOE_FMT_Q2), (256, 256, 7)):
+        with pytest.raises(L.MoeError) as e:
+            L.moe_get_record_layout(d, f, fmt)
+        assert e.value.status == L.MOE_EINVAL
+    fake = 1 << 20
+    lay = L.moe_get_record_layout(256, 256, L.MOE_FMT_Q2)
+    for T, fmt, want in ((16, L.MOE_FMT_Q2, L.MOE_EUNSUPPORTED), (4, 9, L.MOE_EINVAL)):
+        s = L.shape(T, 256, 256, 16, 2, 0)
+        ws = L.moe_workspace_size(s)
+        table = L.expert_table(fake, lay.record_bytes, 16, fake, None, fmt=fmt)
+        with pytest.raises(L.MoeError) as e:
+            L.moe_expert_ffn(s, L.MOE_MODE_AUTO, fake, L.MOE_BF16, table, fake, fake, fake, fake, L.MOE_F32, fake,
+                             ws, 1)
+        assert e.value.status == want, L.moe_last_error_string()
+

@@ -325,3 +325,58 @@ def test_rms_norm_is_per_row_and_scale_free():
     assert np.allclose(np.sqrt(np.mean(out * out, axis=1)), 1.0, rtol=1e-12)
     assert np.allclose(O.rms_norm(x * 19.0, eps=0.0), out, rtol=1e-12)
     assert np.all(np.sign(out) == np.sign(x))
+
+# ------------------------------------------------------------------ 2-bit format ----------
+
+def test_dequantize_q2_levels_and_block_scales():
+    # catches: a level offset other than 1.5, codes read as signed, a block scale applied to the
+    # wrong block, a factor of 2 in the levels
+    c = np.zeros((2, 64), np.uint8)
+    c[0, :4] = [0, 1, 2, 3]
+    c[0, 32:36] = [3, 2, 1, 0]
+    c[1, 40] = 3
+    s = np.array([[2.0, 0.5], [1.0, 4.0]], dtype=np.float16)
+    w = O.dequantize_q2(c, s)
+    assert w[0, :4].tolist() == [-3.0, -1.0, 1.0, 3.0]
+    assert w[0, 32:36].tolist() == [0.75, 0.25, -0.25, -0.75]
+    assert w[0, 4] == -3.0 and w[0, 36] == -0.75  # code 0 is the lowest level, not zero
+    assert w[1, 40] == 6.0 and w[1, 0] == -1.5
+
+
+def test_q2_levels_are_symmetric_and_exact():
+    # catches: asymmetric levels (c - 2 or c - 1), rounding of the level times the scale
+    c = np.tile(np.arange(4, dtype=np.uint8), 8)[None, :]
+    for sv in (1.0, 0.000061035156, 65504.0, 0.1):
+        s = np.array([[sv]], dtype=np.float16)
+        w = O.dequantize_q2(c, s)[0, :4]
+        assert np.array_equal(w, -w[::-1])
+        assert np.array_equal(w, float(s[0, 0]) * np.array([-1.5, -0.5, 0.5, 1.5]))
+
+
+def test_q2_dense_swiglu_hand_example():
+    # catches, in the 2-bit path: the level offset, gate and up swapped, down used transposed,
+    # a scale on the wrong row
+    g = json.load(open(os.path.join(HERE, "golden", "dense_swiglu_q2_d32_f32.json")))
+    d, f = g["d"], g["f"]
+
+    def mat(spec, r, c, dt, default):
+        a = np.full((r, c), default, dtype=dt)
+        for i, row in spec.items():
+            for j, v in row.items():
+                a[int(i), int(j)] = v
+        return a
+    cd, sd = g["code_default"], g["scale_default"]
+    ex = ExpertArrays(mat(g["gate_c"], f, d, np.uint8, cd), mat(g["gate_s"], f, d // 32, np.float16, sd),
+                      mat(g["up_c"], f, d, np.uint8, cd), mat(g["up_s"], f, d // 32, np.float16, sd),
+                      mat(g["down_c"], d, f, np.uint8, cd), mat(g["down_s"], d, f // 32, np.float16, sd), fmt="q2")
+    x = np.zeros((g["T"], d))
+    for t, row in g["x"].items():
+        for i, v in row.items():
+            x[int(t), int(i)] = v
+    want = np.zeros((g["T"], d))
+    for t, row in g["expected_out"].items():
+        for i, v in row.items():
+            want[int(t), int(i)] = v
+    res = O.moe_layer(x, np.ones((d, 1), dtype=np.float32), 1, lambda e: ex)
+    assert np.max(np.abs(res.out - want)) <= g["tolerance_abs"]
+
