@@ -332,10 +332,10 @@ def time_layer(w, dev, K: int, W: int, rot_layers: int, n_batches: int, ydt: int
         L.moe_route_permute(s, x, xdt, dls[l].router, buf.topk_idx, buf.topk_w, None, buf.counts, buf.offsets,
                             buf.sorted_pair, buf.inv_pos, buf.active, buf.ws, buf.ws_bytes, None)
 
-    def seg_ffn_combine(l, x):
-        L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, x, xdt, tables[l], buf.offsets, buf.sorted_pair, buf.active,
-                                 buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, None, buf.out, buf.odt, buf.ws,
-                                 buf.ws_bytes, None)
+    def seg_layer(l, x):  # the whole pass in one C-ABI call
+        L.moe_layer_forward(s, x, xdt, dls[l].router, tables[l], L.MOE_MODE_AUTO, buf.topk_idx, buf.topk_w, None,
+                            buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.y_perm, buf.ydt,
+                            None, buf.out, buf.odt, buf.ws, buf.ws_bytes, None)
 
     def seg_ffn(l, x):
         L.moe_expert_ffn(s, L.MOE_MODE_AUTO, x, xdt, tables[l], buf.offsets, buf.sorted_pair, buf.active,
@@ -347,8 +347,7 @@ def time_layer(w, dev, K: int, W: int, rot_layers: int, n_batches: int, ydt: int
     # active experts per pass (for the algorithmic byte count), from untimed eager passes
     n_active = []
     for l, b in combo:
-        seg_route(l, xs[b])
-        seg_ffn_combine(l, xs[b])
+        seg_layer(l, xs[b])
         torch.cuda.synchronize(dev)
         n_active.append(int(buf.active[0].item()))
         assert L.moe_read_status(buf.ws) == 0
@@ -357,8 +356,7 @@ def time_layer(w, dev, K: int, W: int, rot_layers: int, n_batches: int, ydt: int
     for l, b in combo:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
-            seg_route(l, xs[b])
-            seg_ffn_combine(l, xs[b])
+            seg_layer(l, xs[b])
         layer_graphs.append(g)
         gs = []
         for seg in (seg_route, seg_ffn, seg_comb):
@@ -437,8 +435,7 @@ def time_layer(w, dev, K: int, W: int, rot_layers: int, n_batches: int, ydt: int
         for l in range(rot_layers):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
-                seg_route(l, x_dev)
-                seg_ffn_combine(l, x_dev)
+                seg_layer(l, x_dev)
             e2e_graphs.append(g)
         n_e2e = min(K * R, 4000)
         e2e_s = 0.0
@@ -518,9 +515,8 @@ def run_ours(args, ws, rank, local):
                           "inputs larger than L2: each pass reads all 513 experts (2.57 GB); no flush"),
                    "layers_rotated": 1 if prefill else ROT_LAYERS, "batches": 4 if prefill else N_BATCHES,
                    "mean_active_experts": r["n_active_mean"],
-                   "launch": "one CUDA graph of the two C-ABI calls per pass: moe_route_permute, "
-                             "moe_expert_ffn_combine (stages_ms: route_permute, then the same kernels as "
-                             "moe_expert_ffn and moe_combine; one graph per stage, events between)",
+                   "launch": "one CUDA graph of the one C-ABI call of a pass, moe_layer_forward (stages_ms: "
+                             "moe_route_permute, moe_expert_ffn, moe_combine, one graph per stage, events between)",
                    "parallelism": f"replicas x{ws}"},
         "ms_per_pass": pcts(r["pass_ms"]),
         "roofline": line_roof,
@@ -793,7 +789,7 @@ def run_tiered(args, ws, rank, local, w):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
             x_dev.copy_(x_host[i % n_batches], non_blocking=True)
-            y = ts.forward(x_dev)
+            y = ts.forward(x_dev, prefetch=args.prefetch, prefetch_top=args.prefetch_top)
             if e2e:
                 out_host.copy_(y, non_blocking=True)
             torch.cuda.synchronize(dev)
@@ -801,12 +797,15 @@ def run_tiered(args, ws, rank, local, w):
             # per layer: norm, router GEMV, top-k with bucketing, expert FFN, combine; with misses one
             # more expert FFN (the missed experts after their copies)
             launches[0] += sum(5 + (m > 0) for m in ts.layer_misses)
+            if args.prefetch:  # the next layer's router GEMV and top-k with bucketing
+                launches[0] += 2 * (w.layers - 1)
         return wall
 
     try:
         run(0, W, False)
         launches[0] = 0
         s0 = L.slot_table_stats(ts.table)
+        pf0 = L.slot_table_prefetch_stats(ts.table)
         clocks = ClockSampler(local)
         barrier(ws)
         clocks.start()
@@ -814,7 +813,9 @@ def run_tiered(args, ws, rank, local, w):
         barrier(ws)
         clk = clocks.stop()
         s1 = L.slot_table_stats(ts.table)
-        assert ts.status() == 0, "a kernel reported an error during the timed steps"
+        pf1 = L.slot_table_prefetch_stats(ts.table)
+        st_words = (L.moe_read_status(ts.buf.ws), L.moe_read_status(ts.ws_miss), L.moe_read_status(ts.pbuf.ws))
+        assert not any(st_words), f"a kernel reported an error during the timed steps: {st_words}"
     finally:
         ts.close()
     wall = dist_max(wall, ws, dev)
@@ -840,7 +841,10 @@ def run_tiered(args, ws, rank, local, w):
                       "warm_profile": bool(args.warm_profile), "warm_loads": ts.n_warm,
                       "hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
                       "evictions": s1.evictions - s0.evictions, "h2d_gbs": h2d / wall / 1e9,
-                      "h2d_bytes_per_step": h2d / K, "cold_start_misses": s0.misses},
+                      "h2d_bytes_per_step": h2d / K, "cold_start_misses": s0.misses,
+                      "early_routing_prefetch": bool(args.prefetch), "prefetch_top": args.prefetch_top,
+                      "prefetch_loads": pf1[0] - pf0[0],
+                      "prefetch_used": pf1[1] - pf0[1]},
         "roofline": {"kernel": "miss copies (pinned host to device slots)", "bound": "pcie",
                      "achieved": h2d / wall / 1e9, "peak": pcie, "unit": "GB/s", "frac": h2d / wall / 1e9 / pcie,
                      "peak_kind": "measured 2 GB pinned H2D copy on this box", "traffic": None},
@@ -870,6 +874,10 @@ def main():
     ap.add_argument("--half-life-steps", type=float, default=50.0, help="tiered, freq: half-life of the use counts")
     ap.add_argument("--warm-profile", action="store_true",
                     help="tiered: fill the pool from a usage profile before the first step")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="tiered: route layer l+1 on layer l's input and copy its experts during layer l")
+    ap.add_argument("--prefetch-top", type=int, default=None,
+                    help="tiered, prefetch: load only each token's first N predicted experts")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

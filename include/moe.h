@@ -252,6 +252,20 @@ moe_status moe_expert_ffn_combine(const moe_shape* shape, moe_mode mode, const v
                                   const void* residual_opt, void* out, moe_dtype odt, void* ws,
                                   size_t ws_bytes, moe_stream_t stream);
 
+/* The whole layer in one call: moe_route_permute, then moe_expert_ffn_combine with the same
+ * arguments (the same results, bit for bit). Because the library enqueues every kernel of the
+ * pass itself, the decode expert FFN starts as a programmatic dependent of the bucketing kernel
+ * before it: it stages the activations while the bucketing runs and reads the bucketing's
+ * outputs once that kernel has completed. (The separate calls never start a kernel early on
+ * work the caller enqueued, which could be a copy or an event wait.) out may alias
+ * residual_opt. */
+moe_status moe_layer_forward(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                             const moe_expert_table* experts, moe_mode mode, int32_t* topk_idx, float* topk_w,
+                             float* logits_opt, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                             int32_t* inv_pos, int32_t* active, void* y_perm, moe_dtype ydt,
+                             const void* residual_opt, void* out, moe_dtype odt, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
 /* Combine / unpermute ([P5]: the token's output is the gated mixture of its selected
  * experts; [P2] "三级存储分工": the shared expert applies to every token):
  *   out[t] = sum_{j=0..k-1} topk_w[t][j] * y_perm[inv_pos[t*k+j]]
@@ -347,6 +361,30 @@ moe_status slot_table_update(moe_slot_table* table, int32_t layer, const int32_t
                              int32_t n_active, moe_stream_t copy_stream, moe_event_t ready,
                              int32_t* h_hits, int32_t* n_hits, int32_t* h_misses,
                              int32_t* n_misses, moe_slot_stats* stats_opt);
+
+/* Early loading of the experts a later layer is expected to use, while the current layer
+ * computes ("Strata 性能基准与论文导读125B MoE在消费级硬件上的极限测量与瓶颈分析", section "瓶颈分析
+ * 1️⃣": next-layer experts streamed over PCIe behind the current layer's compute; "Strata 工作
+ * 原理图解GPU内存SSD三级存储如何让125B模型塞进消费级显卡", section "长文本"). For every expert of
+ * h_ids[0..n_ids) (host array, ids of `layer`) that is not resident: a victim slot is chosen as
+ * in slot_table_update (an empty slot first, then the policy's victim) among the slots whose
+ * owner is neither one of h_keep[0..n_keep) of keep_layer (the experts the current layer's
+ * kernels read; keep_layer is ignored when n_keep == 0) nor one of h_ids; the record is copied
+ * on copy_stream and the slot becomes the most recently used. When no slot can be taken the
+ * call loads what it could and returns MOE_OK. Already resident experts are left as they are.
+ * The loads are not uses (no use counts, hits or misses); bytes_h2d and evictions count them.
+ * The changed entries of d_slot_of are written after the copies and `ready` (if not NULL) is
+ * recorded after that: a compute stream must wait on it before it reads a prefetched slot.
+ * *n_loaded (if not NULL) receives the number of experts copied. MOE_EINVAL for bad layers or
+ * ids (nothing changed), MOE_ECUDA if a copy fails (the failed expert is not resident). The
+ * protocol of slot_table_update holds: the kernels that read an evicted slot have completed. */
+moe_status slot_table_prefetch(moe_slot_table* table, int32_t layer, const int32_t* h_ids, int32_t n_ids,
+                               int32_t keep_layer, const int32_t* h_keep, int32_t n_keep, moe_stream_t copy_stream,
+                               moe_event_t ready, int32_t* n_loaded);
+
+/* Prefetched experts so far (*loads), and how many of them a later slot_table_update found
+ * resident and counted as hits before they were evicted (*used). */
+moe_status slot_table_prefetch_stats(const moe_slot_table* table, uint64_t* loads, uint64_t* used);
 
 /* Sets the replacement policy (MOE_SLOT_LRU or MOE_SLOT_FREQ) and the half-life of the use
  * counts, in slot_table_update calls (> 0, finite): a use made h calls ago weighs 2^(-h /

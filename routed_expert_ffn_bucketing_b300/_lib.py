@@ -64,6 +64,8 @@ _SIGS = {
     "moe_expert_ffn": (C.c_int, [C.POINTER(moe_shape), C.c_int, _P, C.c_int, C.POINTER(moe_expert_table), _P, _P, _P,
                                  _P, C.c_int, _P, C.c_size_t, _P]),
     "moe_combine": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, _P, _P, C.c_int, _P]),
+    "moe_layer_forward": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, C.POINTER(moe_expert_table), C.c_int, _P, _P,
+                                    _P, _P, _P, _P, _P, _P, _P, C.c_int, _P, _P, C.c_int, _P, C.c_size_t, _P]),
     "moe_expert_ffn_combine": (C.c_int, [C.POINTER(moe_shape), C.c_int, _P, C.c_int, C.POINTER(moe_expert_table), _P,
                                          _P, _P, _P, C.c_int, _P, _P, _P, _P, C.c_int, _P, C.c_size_t, _P]),
     "moe_rms_norm": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, C.c_int, C.c_float, _P]),
@@ -75,6 +77,8 @@ _SIGS = {
     "slot_table_update": (C.c_int, [_P, C.c_int32, _P, C.c_int32, _P, _P, _P, _P, _P, _P,
                                     C.POINTER(moe_slot_stats)]),
     "slot_table_set_policy": (C.c_int, [_P, C.c_int32, C.c_double]),
+    "slot_table_prefetch": (C.c_int, [_P, C.c_int32, _P, C.c_int32, C.c_int32, _P, C.c_int32, _P, _P, _P]),
+    "slot_table_prefetch_stats": (C.c_int, [_P, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]),
     "slot_table_warm": (C.c_int, [_P, _P, _P, _P, _P]),
     "slot_table_stats": (C.c_int, [_P, C.POINTER(moe_slot_stats)]),
     "slot_table_snapshot": (C.c_int, [_P, _P]),
@@ -190,6 +194,15 @@ def moe_expert_ffn_combine(s, mode, x, xdt, table: moe_expert_table, offsets, so
                                                stream_handle(stream)), "moe_expert_ffn_combine")
 
 
+def moe_layer_forward(s, x, xdt, w_router, table: moe_expert_table, mode, topk_idx, topk_w, logits_opt, counts,
+                      offsets, sorted_pair, inv_pos, active, y_perm, ydt, residual_opt, out, odt, ws, ws_bytes,
+                      stream=None) -> int:
+    return _check(lib().moe_layer_forward(C.byref(s), ptr(x), xdt, ptr(w_router), C.byref(table), mode, ptr(topk_idx),
+                                          ptr(topk_w), ptr(logits_opt), ptr(counts), ptr(offsets), ptr(sorted_pair),
+                                          ptr(inv_pos), ptr(active), ptr(y_perm), ydt, ptr(residual_opt), ptr(out),
+                                          odt, ptr(ws), ws_bytes, stream_handle(stream)), "moe_layer_forward")
+
+
 def moe_combine(s, y_perm, ydt, inv_pos, topk_w, residual_opt, out, odt, stream=None) -> int:
     return _check(lib().moe_combine(C.byref(s), ptr(y_perm), ydt, ptr(inv_pos), ptr(topk_w), ptr(residual_opt),
                                     ptr(out), odt, stream_handle(stream)), "moe_combine")
@@ -241,6 +254,22 @@ def slot_table_update(table, layer, h_active, n_active, copy_stream, ready, h_hi
     if st < 0 and st != MOE_ENOSLOT:
         raise MoeError(st, "slot_table_update", moe_last_error_string())
     return st
+
+
+def slot_table_prefetch(table, layer: int, h_ids, n_ids: int, keep_layer: int, h_keep, n_keep: int, copy_stream=None,
+                        ready=None) -> int:
+    """h_ids, h_keep: host addresses (ints) of int32 arrays, or None. Returns the number of
+    experts copied."""
+    n = C.c_int32()
+    _check(lib().slot_table_prefetch(table, layer, h_ids, n_ids, keep_layer, h_keep, n_keep, copy_stream, ready,
+                                     C.byref(n)), "slot_table_prefetch")
+    return n.value
+
+
+def slot_table_prefetch_stats(table) -> tuple[int, int]:
+    loads, used = C.c_uint64(), C.c_uint64()
+    _check(lib().slot_table_prefetch_stats(table, C.byref(loads), C.byref(used)), "slot_table_prefetch_stats")
+    return loads.value, used.value
 
 
 def slot_table_set_policy(table, policy: int, half_life: float) -> None:

@@ -271,7 +271,7 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t*
   const WsLayout L = ws_layout(*shape);
   cudaError_t e = launch_permute(*shape, topk_idx, counts, offsets, sorted_pair, inv_pos, active,
                                  at<int32_t>(ws, L.perm_cnt), at<uint32_t>(ws, L.perm_keys), at<int>(ws, L.status),
-                                 reinterpret_cast<cudaStream_t>(stream));
+                                 reinterpret_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return cuda_fail(e, "moe_permute: launch");
   return MOE_OK;
 }
@@ -323,7 +323,7 @@ struct CombineReq {
 moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x, moe_dtype xdt,
                            const moe_expert_table* experts, const int32_t* offsets, const int32_t* sorted_pair,
                            const int32_t* active, void* y_perm, moe_dtype ydt, void* ws, size_t ws_bytes,
-                           moe_stream_t stream, const CombineReq* cmb) {
+                           moe_stream_t stream, const CombineReq* cmb, bool pdl_first = false) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   if ((st = check_dtype(xdt, "x")) != MOE_OK) return st;
@@ -410,7 +410,7 @@ moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x,
     const PersistAux px{at<float>(ws, L.part),       at<int32_t>(ws, L.task_cnt), at<uint32_t>(ws, L.hmax),
                         at<int32_t>(ws, L.item_done), sk_tasks * 2 * 128,         sk_tasks,
                         at<int32_t>(ws, L.item_done) + items_max};
-    e = launch_ffn_persist(a, px, device_sm_count(), cs);
+    e = launch_ffn_persist(a, px, device_sm_count(), cs, pdl_first);
   } else if (xdt == MOE_BF16 && stream_supported(a)) {
     const size_t items_max = (P_items(*shape)) + shape->n_shared;
     StreamAux aux{at<__half>(ws, L.x16),    at<float>(ws, L.xunscale), at<uint32_t>(ws, L.hmax),
@@ -428,7 +428,7 @@ moe_status expert_ffn_impl(const moe_shape* shape, moe_mode mode, const void* x,
   }
   if (e != cudaSuccess) return cuda_fail(e, "moe_expert_ffn: launch");
   if (cmb) {
-    e = launch_combine(*shape, y_perm, ydt, cmb->inv_pos, cmb->topk_w, cmb->residual, cmb->out, cmb->odt, cs);
+    e = launch_combine(*shape, y_perm, ydt, cmb->inv_pos, cmb->topk_w, cmb->residual, cmb->out, cmb->odt, cs, true);
     if (e != cudaSuccess) return cuda_fail(e, "moe_expert_ffn_combine: combine launch");
   }
   return MOE_OK;
@@ -464,6 +464,28 @@ moe_status moe_expert_ffn_combine(const moe_shape* shape, moe_mode mode, const v
                          stream, &cmb);
 }
 
+moe_status moe_layer_forward(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                             const moe_expert_table* experts, moe_mode mode, int32_t* topk_idx, float* topk_w,
+                             float* logits_opt, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                             int32_t* inv_pos, int32_t* active, void* y_perm, moe_dtype ydt, const void* residual_opt,
+                             void* out, moe_dtype odt, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_dtype(odt, "out")) != MOE_OK) return st;
+  if (shape->T > 0) {
+    if (!out) return fail(MOE_EINVAL, "moe_layer_forward: NULL out");
+    if (!aligned(out, 16) || (residual_opt && !aligned(residual_opt, 16)))
+      return fail(MOE_EINVAL, "moe_layer_forward: misaligned out or residual");
+  }
+  st = moe_route_permute(shape, x, xdt, w_router, topk_idx, topk_w, logits_opt, counts, offsets, sorted_pair,
+                         inv_pos, active, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  // the kernel before the expert FFN on the stream is the bucketing kernel just enqueued
+  const CombineReq cmb{inv_pos, topk_w, residual_opt, out, odt};
+  return expert_ffn_impl(shape, mode, x, xdt, experts, offsets, sorted_pair, active, y_perm, ydt, ws, ws_bytes,
+                         stream, &cmb, true);
+}
+
 moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt, const int32_t* inv_pos,
                        const float* topk_w, const void* residual_opt, void* out, moe_dtype odt,
                        moe_stream_t stream) {
@@ -477,7 +499,7 @@ moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt
     return fail(MOE_EINVAL, "moe_combine: misaligned y_perm, out or residual");
   if (shape->T == 0) return MOE_OK;
   cudaError_t e = launch_combine(*shape, y_perm, ydt, inv_pos, topk_w, residual_opt, out, odt,
-                                 reinterpret_cast<cudaStream_t>(stream));
+                                 reinterpret_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return cuda_fail(e, "moe_combine: launch");
   return MOE_OK;
 }

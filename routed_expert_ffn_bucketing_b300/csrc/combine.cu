@@ -70,10 +70,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
 }
 
 cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,
-                           const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st) {
+                           const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st,
+                           bool pdl) {
   const int threads = 256;
   dim3 grid((s.d / 4 + threads - 1) / threads, s.T);
-  return launch_pdl(combine_kernel, grid, dim3(threads), 0, st, y, ydt, inv_pos, topk_w, residual, out, odt, s.T, s.d,
+  return launch_maybe_pdl(pdl, combine_kernel, grid, dim3(threads), 0, st, y, ydt, inv_pos, topk_w, residual, out, odt,
+                          s.T, s.d,
                     s.k, s.n_shared);
 }
 

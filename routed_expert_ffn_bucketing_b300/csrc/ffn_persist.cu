@@ -30,8 +30,9 @@
 // The counters (per-item tasks done, stream-K parts, row maxima) hold zeros at launch: moe_route
 // clears them, and every launch leaves them cleared (the finisher of a cut task resets its
 // counter; the last CTA out resets the rest), so no memset stands between the bucketing kernel
-// and this one and the kernel launches as its programmatic dependent. Every wait is bounded: one
-// that runs out sets MOE_DEV_TIMEOUT and the CTA stops before its down work.
+// and this one: in moe_layer_forward the kernel launches as a programmatic dependent of the
+// bucketing kernel and stages x before its dependency wait. Every wait is bounded: one that runs
+// out sets MOE_DEV_TIMEOUT and the CTA stops before its down work.
 #include "decode_mma.cuh"
 #include "sm100_ptx.cuh"
 
@@ -68,17 +69,16 @@ __host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15
 __host__ __device__ inline uint32_t act_stride(int K) { return (((uint32_t)K * 2u + 127u) & ~127u) + 64u; }
 __host__ __device__ inline uint32_t sum_stride(int K) { return (((uint32_t)(K / 32) * 4u + 127u) & ~127u) + 16u; }
 
-// Most h rows one CTA stages for its down work: its range covers at most
-// max(16, 16 * tasks / warps) + 3 tasks, so at most that / (d/16) + 2 items of at most T rows.
+// Most h rows one CTA stages for its down work. A CTA stages the rows [r_lo, r_hi) from its
+// first down item's first row to its last item's last row. The active list may be any subset of
+// the routed experts (e.g. only those a slot table has just loaded), whose rows lie anywhere in
+// [0, P) with other experts' rows between them, so the span is bounded only by all the rows.
 __host__ __device__ inline int p_rows_cap(int T, int d, int items_max, int rows, int n_warps) {
-  const long long tpi = d / 16;
-  const long long tasks = (long long)items_max * tpi;
-  long long per_cta = (16 * tasks + n_warps - 1) / n_warps;
-  if (per_cta < 16) per_cta = 16;
-  per_cta += 3;
-  const long long items = (per_cta + tpi - 1) / tpi + 2;
-  const long long cap = items * T;
-  return cap < rows ? (int)cap : rows;
+  (void)T;
+  (void)d;
+  (void)items_max;
+  (void)n_warps;
+  return rows;
 }
 
 // Shared-memory layout of one CTA (byte offsets), the same on host and device.
@@ -865,7 +865,7 @@ int persist_rows_cap(const FfnArgs& a, int sm_count) {
 }
 
 template <int DG, int DD, int FMT>
-cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st) {
+cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st, bool pdl) {
   const int rows = a.P + a.T * a.n_shared;
   const int items_max = (a.P < a.E ? a.P : a.E) + a.n_shared;
   const int rows_cap = persist_rows_cap(a, sm_count);
@@ -878,11 +878,23 @@ cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int sm_count
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   PAux px{x.part, x.task_cnt, x.hmax, x.item_done, x.part_stride, x.cnt_stride, rows_cap, x.exit};
-  // One CTA per SM (the occupancy check above: a CTA takes every register of its SM), launched as
-  // a programmatic dependent of the bucketing kernel before it: the CTAs stage x while the
-  // bucketing runs and wait for its outputs (griddepcontrol.wait). Every CTA's waits for other
-  // CTAs are bounded, so the grid needs no cooperative launch to be safe.
-  return launch_pdl(ffn_persist_kernel<DG, DD, FMT>, dim3(sm_count), dim3(kPThreads), L.total, st, a, px);
+  // One CTA per SM (the occupancy check above: a CTA takes every register of its SM). With pdl,
+  // a programmatic dependent of the bucketing kernel the caller enqueued just before: the CTAs
+  // stage x while the bucketing runs and wait for its outputs (griddepcontrol.wait); every CTA's
+  // waits for other CTAs are bounded. Otherwise a cooperative launch, which guarantees that all
+  // CTAs are resident at once.
+  if (pdl) return launch_pdl(ffn_persist_kernel<DG, DD, FMT>, dim3(sm_count), dim3(kPThreads), L.total, st, a, px);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sm_count);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ffn_persist_kernel<DG, DD, FMT>, a, px);
 }
 
 }  // namespace
@@ -901,13 +913,13 @@ bool persist_supported(const FfnArgs& a, int sm_count) {
          a.T * (a.d / kQBlock) <= kPThreads && persist_smem_bytes(a, sm_count) <= 200 * 1024;
 }
 
-cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st) {
-  if (a.fmt == 1) return launch_persist_d<8, 8, 1>(a, x, sm_count, st);  // d and f multiples of 256
+cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st, bool pdl) {
+  if (a.fmt == 1) return launch_persist_d<8, 8, 1>(a, x, sm_count, st, pdl);  // d and f multiples of 256
   const bool g8 = (a.d / kQBlock) % 8 == 0, d8 = (a.f / kQBlock) % 8 == 0;
-  if (g8 && d8) return launch_persist_d<8, 8, 0>(a, x, sm_count, st);
-  if (g8) return launch_persist_d<8, 4, 0>(a, x, sm_count, st);
-  if (d8) return launch_persist_d<4, 8, 0>(a, x, sm_count, st);
-  return launch_persist_d<4, 4, 0>(a, x, sm_count, st);
+  if (g8 && d8) return launch_persist_d<8, 8, 0>(a, x, sm_count, st, pdl);
+  if (g8) return launch_persist_d<8, 4, 0>(a, x, sm_count, st, pdl);
+  if (d8) return launch_persist_d<4, 8, 0>(a, x, sm_count, st, pdl);
+  return launch_persist_d<4, 4, 0>(a, x, sm_count, st, pdl);
 }
 
 }  // namespace moe

@@ -59,6 +59,10 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// A kernel is launched as a programmatic dependent only when the library enqueued the kernel
+// before it on the stream in the same call: with anything else between them (a memset, a copy,
+// an event wait) the early start could read inputs that are not there yet. launch_maybe_pdl
+// launches normally when `pdl` is false.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args... args) {
@@ -73,6 +77,14 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+  if (pdl) return launch_pdl(kernel, grid, block, smem, st, args...);
+  kernel<<<grid, block, smem, st>>>(static_cast<KArgs>(args)...);
+  return cudaGetLastError();
 }
 
 __device__ __forceinline__ void flag_status(int* status, int bit) {

@@ -170,14 +170,16 @@ cudaError_t launch_topk(const moe_shape& s, const float* logits, int32_t* idx, f
                         cudaStream_t st);
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
-                           uint32_t* keys, int* status, cudaStream_t st);
+                           uint32_t* keys, int* status, cudaStream_t st, bool pdl = false);
 cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);  // fp32 SIMT (any x dtype)
 // Streaming tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
 cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, int sm_count, cudaStream_t st);
 bool stream_supported(const FfnArgs& a);
 // One persistent cooperative kernel for T <= 8 (bf16 x); persist_supported() says whether the
 // shape fits (its shared-memory copy of the activations included).
-cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st);
+// pdl: launched as a programmatic dependent of the kernel the caller enqueued just before it
+// (else a cooperative launch).
+cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st, bool pdl);
 bool persist_supported(const FfnArgs& a, int sm_count);
 // Tensor-core grouped GEMM for many tokens per expert (bf16 x); prefill_supported() says whether
 // the shape fits (d a multiple of 256, f of 128).
@@ -187,7 +189,8 @@ int device_sm_count();
 // The limit, in nanoseconds, that the next expert-FFN launches give their bounded waits.
 uint64_t wait_limit_ns();
 cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int32_t* inv_pos,
-                           const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st);
+                           const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st,
+                           bool pdl);
 cudaError_t launch_rms_norm(const moe_shape& s, const void* x, int xdt, void* out, int odt, float eps,
                             cudaStream_t st);
 

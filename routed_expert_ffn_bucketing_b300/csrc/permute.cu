@@ -202,12 +202,13 @@ __global__ void __launch_bounds__(CH) bucket_scatter_kernel(int P, const uint32_
 
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
-                           uint32_t* keys, int* status, cudaStream_t st) {
+                           uint32_t* keys, int* status, cudaStream_t st, bool pdl) {
   const int P = s.T * s.k;
   if (P <= 256) {
     const int need = P > s.E ? P : s.E;
     const int n = (need + 31) / 32 * 32;
-    return launch_pdl(bucket_count_kernel, dim3(1), dim3(n), 0, st, topk_idx, P, s.E, counts, offsets, sorted_pair,
+    return launch_maybe_pdl(pdl, bucket_count_kernel, dim3(1), dim3(n), 0, st, topk_idx, P, s.E, counts, offsets,
+                            sorted_pair,
                       inv_pos, active, status);
   }
   if (P <= CH) {

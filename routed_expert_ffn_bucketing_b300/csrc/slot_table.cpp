@@ -66,6 +66,8 @@ struct moe_slot_table {
   std::vector<int64_t> last_use; // [L*E]: call number of the last use, -1 never
   std::vector<int32_t> heap, hpos;  // min-heap of slots by (count, last use, slot); hpos[slot]
   std::vector<uint8_t> pinned;      // [n_slots]: owner is in the current call (never a victim)
+  std::vector<uint8_t> prefetched;  // [n_slots]: loaded by slot_table_prefetch, not yet hit
+  uint64_t pf_loads = 0, pf_used = 0;
 };
 
 namespace {
@@ -225,6 +227,7 @@ moe_status slot_table_create(moe_slot_table** out, int32_t L, int32_t E, int32_t
   t->score.assign((size_t)L * E, 0.0);
   t->last_use.assign((size_t)L * E, -1);
   t->pinned.assign(n_slots, 0);
+  t->prefetched.assign(n_slots, 0);
   t->heap.resize(n_slots);
   t->hpos.resize(n_slots);
   for (int32_t s = 0; s < n_slots; ++s) t->heap[s] = t->hpos[s] = s;
@@ -280,6 +283,10 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
     t->last_use[base + e] = t->calls;
     const int32_t s = t->mirror[base + e];
     if (s >= 0) {
+      if (t->prefetched[s]) {
+        t->prefetched[s] = 0;
+        ++t->pf_used;
+      }
       lru_unlink(t, s);
       lru_push_tail(t, s);
       t->pinned[s] = 1;
@@ -302,6 +309,7 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
       changed.push_back(old);
       t->stats.evictions++;
     }
+    t->prefetched[s] = 0;
     t->owner[s] = -1;
     lru_unlink(t, s);
     lru_push_tail(t, s);
@@ -337,6 +345,99 @@ moe_status slot_table_update(moe_slot_table* t, int32_t layer, const int32_t* h_
   if (n_misses) *n_misses = nm;
   if (stats_opt) *stats_opt = t->stats;
   return rc;
+}
+
+moe_status slot_table_prefetch(moe_slot_table* t, int32_t layer, const int32_t* h_ids, int32_t n_ids,
+                               int32_t keep_layer, const int32_t* h_keep, int32_t n_keep, moe_stream_t copy_stream,
+                               moe_event_t ready, int32_t* n_loaded) {
+  if (!t || n_ids < 0 || n_keep < 0 || (n_ids > 0 && !h_ids) || (n_keep > 0 && !h_keep))
+    return slot_fail(MOE_EINVAL, "slot_table_prefetch: null table or id list, or a negative count");
+  if (layer < 0 || layer >= t->L || (n_keep > 0 && (keep_layer < 0 || keep_layer >= t->L)))
+    return slot_fail(MOE_EINVAL, "slot_table_prefetch: layer %d or keep layer %d not in [0, %d)", layer, keep_layer,
+                     t->L);
+  for (int32_t i = 0; i < n_ids; ++i)
+    if (h_ids[i] < 0 || h_ids[i] >= t->E)
+      return slot_fail(MOE_EINVAL, "slot_table_prefetch: expert id %d out of [0, %d)", h_ids[i], t->E);
+  for (int32_t i = 0; i < n_keep; ++i)
+    if (h_keep[i] < 0 || h_keep[i] >= t->E)
+      return slot_fail(MOE_EINVAL, "slot_table_prefetch: kept expert id %d out of [0, %d)", h_keep[i], t->E);
+  // pin the kept experts' slots and the slots of this call's experts already resident
+  std::vector<int32_t> pins;
+  auto pin = [&](int64_t key) {
+    const int32_t s = t->mirror[key];
+    if (s >= 0 && !t->pinned[s]) {
+      t->pinned[s] = 1;
+      heap_fix(t, s);
+      pins.push_back(s);
+    }
+  };
+  for (int32_t i = 0; i < n_keep; ++i) pin((int64_t)keep_layer * t->E + h_keep[i]);
+  const int64_t base = (int64_t)layer * t->E;
+  for (int32_t i = 0; i < n_ids; ++i) pin(base + h_ids[i]);
+  std::vector<int64_t> changed;
+  moe_status rc = MOE_OK;
+  int32_t loaded = 0;
+  for (int32_t i = 0; i < n_ids; ++i) {
+    const int64_t key = base + h_ids[i];
+    if (t->mirror[key] >= 0) continue;  // resident, or loaded earlier in this call
+    // the victim: LRU, the least recently used unpinned slot; FREQ, the heap's root
+    int32_t s = -1;
+    if (t->policy == MOE_SLOT_FREQ) {
+      if (!t->pinned[t->heap[0]]) s = t->heap[0];
+    } else {
+      for (int32_t c = t->head; c >= 0; c = t->next[c])
+        if (!t->pinned[c]) {
+          s = c;
+          break;
+        }
+    }
+    if (s < 0) break;  // every slot is pinned: nothing more can be loaded
+    const int64_t old = t->owner[s];
+    if (old >= 0) {
+      t->mirror[old] = -1;
+      changed.push_back(old);
+      t->stats.evictions++;
+    }
+    t->owner[s] = -1;
+    lru_unlink(t, s);
+    lru_push_tail(t, s);
+    const int cr = t->copy_fn(t->d_pool + (uint64_t)s * t->slot_bytes, t->h_records[key], t->slot_bytes, copy_stream,
+                              t->copy_user);
+    if (cr != 0) {
+      t->prefetched[s] = 0;
+      heap_fix(t, s);
+      rc = slot_fail(MOE_ECUDA, "slot_table_prefetch: copy of layer %d expert %d failed (%d)", layer, h_ids[i], cr);
+      break;
+    }
+    t->owner[s] = key;
+    t->mirror[key] = s;
+    t->prefetched[s] = 1;
+    t->pinned[s] = 1;
+    heap_fix(t, s);
+    pins.push_back(s);
+    changed.push_back(key);
+    t->stats.bytes_h2d += t->slot_bytes;
+    ++t->pf_loads;
+    ++loaded;
+  }
+  for (const int32_t s : pins) {
+    t->pinned[s] = 0;
+    heap_fix(t, s);
+  }
+  if (write_entries(t, changed, copy_stream) != 0 && rc == MOE_OK)
+    rc = slot_fail(MOE_ECUDA, "slot_table: writing the device table failed");
+  if (ready && cudaEventRecord(reinterpret_cast<cudaEvent_t>(ready), reinterpret_cast<cudaStream_t>(copy_stream)) !=
+                   cudaSuccess && rc == MOE_OK)
+    rc = slot_fail(MOE_ECUDA, "slot_table: recording the ready event failed");
+  if (n_loaded) *n_loaded = loaded;
+  return rc;
+}
+
+moe_status slot_table_prefetch_stats(const moe_slot_table* t, uint64_t* loads, uint64_t* used) {
+  if (!t || !loads || !used) return slot_fail(MOE_EINVAL, "slot_table_prefetch_stats: NULL argument");
+  *loads = t->pf_loads;
+  *used = t->pf_used;
+  return MOE_OK;
 }
 
 moe_status slot_table_set_policy(moe_slot_table* t, int32_t policy, double half_life) {

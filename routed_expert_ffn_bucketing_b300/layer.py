@@ -67,24 +67,19 @@ def alloc_buffers(shape: L.moe_shape, device="cuda", ydt: int = L.MOE_F32, odt: 
 def forward(buf: LayerBuffers, x: torch.Tensor, w_router: torch.Tensor, table: L.moe_expert_table,
             mode: int = L.MOE_MODE_AUTO, residual: torch.Tensor | None = None, stream=None,
             fused: bool = False) -> torch.Tensor:
-    """Runs route -> permute -> expert FFN -> combine on `stream`; returns buf.out. With fused,
-    route and permute are one call (moe_route_permute) and so are the expert FFN and the
-    combine (moe_expert_ffn_combine)."""
+    """Runs route -> permute -> expert FFN -> combine on `stream` as the four separate calls;
+    returns buf.out. With fused, the whole pass is one call (moe_layer_forward)."""
     s = buf.shape
     xdt = L.MOE_F32 if x.dtype == torch.float32 else L.MOE_BF16
     logits = buf.logits if buf.logits.numel() else None
     if fused:
-        L.moe_route_permute(s, x, xdt, w_router, buf.topk_idx, buf.topk_w, logits, buf.counts, buf.offsets,
-                            buf.sorted_pair, buf.inv_pos, buf.active, buf.ws, buf.ws_bytes, stream)
-    else:
-        L.moe_route(s, x, xdt, w_router, buf.topk_idx, buf.topk_w, logits, buf.ws, buf.ws_bytes, stream)
-        L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
-                      buf.ws_bytes, stream)
-    if fused:
-        L.moe_expert_ffn_combine(s, mode, x, xdt, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm,
-                                 buf.ydt, buf.inv_pos, buf.topk_w, residual, buf.out, buf.odt, buf.ws, buf.ws_bytes,
-                                 stream)
+        L.moe_layer_forward(s, x, xdt, w_router, table, mode, buf.topk_idx, buf.topk_w, logits, buf.counts,
+                            buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.y_perm, buf.ydt, residual,
+                            buf.out, buf.odt, buf.ws, buf.ws_bytes, stream)
         return buf.out
+    L.moe_route(s, x, xdt, w_router, buf.topk_idx, buf.topk_w, logits, buf.ws, buf.ws_bytes, stream)
+    L.moe_permute(s, buf.topk_idx, buf.counts, buf.offsets, buf.sorted_pair, buf.inv_pos, buf.active, buf.ws,
+                  buf.ws_bytes, stream)
     L.moe_expert_ffn(s, mode, x, xdt, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm, buf.ydt, buf.ws,
                      buf.ws_bytes, stream)
     L.moe_combine(s, buf.y_perm, buf.ydt, buf.inv_pos, buf.topk_w, residual, buf.out, buf.odt, stream)

@@ -46,12 +46,10 @@ class DecodeStack:
             if keep is not None:
                 keep.append(("in", self.resid.clone()))
             L.moe_rms_norm(s, self.resid, L.MOE_BF16, self.xn, L.MOE_BF16, RMS_EPS, stream)
-            L.moe_route_permute(s, self.xn, L.MOE_BF16, lw.router, b.topk_idx, b.topk_w, None, b.counts, b.offsets,
-                                b.sorted_pair, b.inv_pos, b.active, b.ws, b.ws_bytes, stream)
-            # expert FFN and combine in one call; out aliases the residual: resid <- resid + MoE(n(resid))
-            L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, lw.table, b.offsets, b.sorted_pair,
-                                     b.active, b.y_perm, b.ydt, b.inv_pos, b.topk_w, self.resid, self.resid,
-                                     L.MOE_BF16, b.ws, b.ws_bytes, stream)
+            # the whole layer in one call; out aliases the residual: resid <- resid + MoE(n(resid))
+            L.moe_layer_forward(s, self.xn, L.MOE_BF16, lw.router, lw.table, L.MOE_MODE_AUTO, b.topk_idx, b.topk_w,
+                                None, b.counts, b.offsets, b.sorted_pair, b.inv_pos, b.active, b.y_perm, b.ydt,
+                                self.resid, self.resid, L.MOE_BF16, b.ws, b.ws_bytes, stream)
             if keep is not None:
                 keep.append(("idx", b.topk_idx.clone()))
                 keep.append(("out", self.resid.clone()))
@@ -69,7 +67,15 @@ class TieredStack:
     the slot table (miss copies on the copy stream, `ready` recorded after them). With overlap
     (the default) the expert FFN then runs in two calls: the hit experts and the shared expert
     first, while the copies are in flight, and the missed experts after the compute stream has
-    waited on `ready`. Without overlap one FFN call runs after the wait. Then the combine."""
+    waited on `ready`. Without overlap one FFN call runs after the wait. Then the combine.
+
+    With prefetch (early routing): right after layer l's routing, layer l+1's router is run on
+    layer l's normalised input, which is close to layer l+1's own (the residual stream changes
+    by one MoE output per layer). Its active list comes back with layer l's, and the experts it
+    names that are not resident are copied after layer l's misses (slot_table_prefetch, never
+    evicting layer l's experts), so that PCIe works on layer l+1 while layer l computes. Layer
+    l+1's expert FFN waits for those copies (an event per layer); where the prediction was
+    right its experts are then hits."""
 
     def __init__(self, shape: L.moe_shape, n_layers: int, routers: list[torch.Tensor], h_records: list[int],
                  n_slots: int, slot_bytes: int, shared: list[torch.Tensor], device="cuda",
@@ -102,6 +108,16 @@ class TieredStack:
         self.d_misses = torch.zeros(1 + cap, dtype=torch.int32, device=device)
         self.stats = L.moe_slot_stats()
         self.layer_misses: list[int] = []
+        # early routing: the next layer's predicted routing, its own workspace, and the events
+        # recorded after each layer's prefetch copies
+        self.pbuf = lay.alloc_buffers(shape, device=device, ydt=L.MOE_F32, odt=L.MOE_BF16, keep_logits=False)
+        self.h_pred = torch.empty(1 + cap, dtype=torch.int32).pin_memory()
+        self.h_pred_idx = torch.empty((shape.T, shape.k), dtype=torch.int32).pin_memory()
+        self.h_pf = np.zeros(cap, dtype=np.int32)
+        self.pf_ready = [torch.cuda.Event(), torch.cuda.Event()]
+        for ev in self.pf_ready:
+            ev.record(self.copy_stream)
+        self.layer_prefetched: list[int] = []
         if policy != L.MOE_SLOT_LRU:
             L.slot_table_set_policy(self.table, policy, half_life_steps * n_layers)
         self.n_warm = 0
@@ -113,25 +129,39 @@ class TieredStack:
             self.ready.synchronize()
 
     def status(self) -> int:
-        """The device status words of both workspaces, OR-ed (waits for the current stream)."""
-        return L.moe_read_status(self.buf.ws) | L.moe_read_status(self.ws_miss)
+        """The device status words of the workspaces, OR-ed (waits for the current stream)."""
+        return L.moe_read_status(self.buf.ws) | L.moe_read_status(self.ws_miss) | L.moe_read_status(self.pbuf.ws)
 
     def close(self):
         if self.table:
             L.slot_table_destroy(self.table)
             self.table = None
 
-    def forward(self, x: torch.Tensor, keep: list | None = None, overlap: bool = True) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, keep: list | None = None, overlap: bool = True,
+                prefetch: bool = False, prefetch_top: int | None = None) -> torch.Tensor:
+        """prefetch_top: with prefetch, only the first prefetch_top of each token's predicted top-k
+        experts (descending logit) are loaded early; all of them when None."""
         s, b = self.shape, self.buf
         stream = torch.cuda.current_stream()
         self.resid.copy_(x)
         self.layer_misses = []
+        self.layer_prefetched = []
         for l in range(self.L):
             if keep is not None:
                 keep.append(("in", self.resid.clone()))
             L.moe_rms_norm(s, self.resid, L.MOE_BF16, self.xn, L.MOE_BF16, RMS_EPS, stream)
             L.moe_route_permute(s, self.xn, L.MOE_BF16, self.routers[l], b.topk_idx, b.topk_w, None, b.counts,
                                 b.offsets, b.sorted_pair, b.inv_pos, b.active, b.ws, b.ws_bytes, stream)
+            early = prefetch and l + 1 < self.L
+            if early:  # layer l+1's router on layer l's normalised input
+                pb = self.pbuf
+                L.moe_route_permute(s, self.xn, L.MOE_BF16, self.routers[l + 1], pb.topk_idx, pb.topk_w, None,
+                                    pb.counts, pb.offsets, pb.sorted_pair, pb.inv_pos, pb.active, pb.ws, pb.ws_bytes,
+                                    stream)
+                if prefetch_top is None:
+                    self.h_pred.copy_(pb.active, non_blocking=True)
+                else:
+                    self.h_pred_idx.copy_(pb.topk_idx, non_blocking=True)
             self.h_active.copy_(b.active, non_blocking=True)
             # the host needs the active list, and the previous layer's FFN must be done with the
             # slots before any of them is overwritten: one event wait per layer
@@ -145,6 +175,19 @@ class TieredStack:
                 raise L.MoeError(st, "slot_table_update", L.moe_last_error_string())
             n_miss = int(self.h_misses[0])
             self.layer_misses.append(n_miss)
+            if early:
+                if prefetch_top is None:
+                    pp, n_pf = self.h_pred.data_ptr() + 4, int(self.h_pred[0])
+                else:  # each token's first prefetch_top predicted experts, in first-seen order
+                    ids = dict.fromkeys(self.h_pred_idx.numpy()[:, :prefetch_top].reshape(-1).tolist())
+                    n_pf = len(ids)
+                    self.h_pf[:n_pf] = list(ids)
+                    pp = self.h_pf.ctypes.data
+                self.layer_prefetched.append(
+                    L.slot_table_prefetch(self.table, l + 1, pp, n_pf, l, self.h_active.data_ptr() + 4, n,
+                                          self.copy_stream.cuda_stream, self.pf_ready[(l + 1) % 2].cuda_event))
+            if prefetch and l > 0:  # this layer's experts prefetched during the previous layer
+                stream.wait_event(self.pf_ready[l % 2])
             table = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l],
                                    self.shared[l] if s.n_shared else None)
             # resid <- resid + MoE(n(resid)): the combine is fused into the expert-FFN call where the

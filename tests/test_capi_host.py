@@ -500,3 +500,55 @@ def test_q2_format_checks_before_any_launch():
                              ws, 1)
         assert e.value.status == want, L.moe_last_error_string()
 
+
+
+def _prefetch(h, layer, ids, keep_layer=0, keep=()):
+    a = (C.c_int32 * max(1, len(ids)))(*ids)
+    k = (C.c_int32 * max(1, len(keep)))(*keep)
+    return L.slot_table_prefetch(h, layer, C.addressof(a), len(ids), keep_layer, C.addressof(k), len(keep))
+
+
+@pytest.mark.parametrize("policy", [L.MOE_SLOT_LRU, L.MOE_SLOT_FREQ])
+def test_slot_table_prefetch_keeps_current_layer_and_turns_into_hits(policy):
+    h, cp, hrec = _make_table(2, 8, 4)
+    if policy == L.MOE_SLOT_FREQ:
+        L.slot_table_set_policy(h, policy, 4.0)
+    _update(h, 0, [0, 1, 2])                      # layer 0 uses 3 of the 4 slots
+    n0 = len(cp.records)
+    # layer 1 is expected to use 5, 6, 7: one empty slot, and nothing of layer 0's set may go
+    assert _prefetch(h, 1, [5, 6, 7], keep_layer=0, keep=[0, 1, 2]) == 1
+    assert _resident(h, 2, 8) == {(0, 0), (0, 1), (0, 2), (1, 5)}
+    assert cp.records[n0:] == [(3, hrec[8 + 5])]
+    s = L.slot_table_stats(h)
+    assert (s.hits, s.misses) == (0, 3)          # a prefetch is neither a hit nor a miss
+    # with layer 0 released, the next prefetch may evict its experts
+    assert _prefetch(h, 1, [5, 6, 7]) == 2
+    assert {(1, 5), (1, 6), (1, 7)} <= _resident(h, 2, 8)
+    st, hits, miss = _update(h, 1, [5, 6, 7, 3])
+    assert st == L.MOE_OK and hits == [5, 6, 7] and miss == [3]
+    assert L.slot_table_prefetch_stats(h) == (3, 3)
+    L.slot_table_destroy(h)
+
+
+def test_slot_table_prefetch_stops_when_every_slot_is_kept():
+    h, cp, hrec = _make_table(2, 8, 3)
+    _update(h, 0, [0, 1, 2])
+    n0 = len(cp.records)
+    assert _prefetch(h, 1, [4, 5], keep_layer=0, keep=[0, 1, 2]) == 0
+    assert len(cp.records) == n0 and _resident(h, 2, 8) == {(0, 0), (0, 1), (0, 2)}
+    # already resident experts are left alone (no copy), ids of the call are never victims
+    assert _prefetch(h, 0, [0, 1, 2]) == 0 and len(cp.records) == n0
+    assert _prefetch(h, 1, [4, 5, 6, 7]) == 3
+    assert _resident(h, 2, 8) == {(1, 4), (1, 5), (1, 6)}
+    L.slot_table_destroy(h)
+
+
+def test_slot_table_prefetch_rejects_bad_arguments():
+    h, cp, _ = _make_table(2, 8, 3)
+    for layer, ids, kl, keep in ((2, [1], 0, []), (0, [8], 0, []), (0, [-1], 0, []), (0, [1], 5, [0]),
+                                 (0, [1], 0, [9])):
+        with pytest.raises(L.MoeError) as e:
+            _prefetch(h, layer, ids, kl, keep)
+        assert e.value.status == L.MOE_EINVAL
+    assert len(cp.records) == 0 and _resident(h, 2, 8) == set()
+    L.slot_table_destroy(h)

@@ -11,7 +11,7 @@ from routed_expert_ffn_bucketing_b300 import _lib as L
 from synth.device import DeviceLayer
 from synth.workloads import WORKLOADS, custom
 
-from gpu_util import check_bucketing, check_expert_rows, check_output, check_routing, run_layer
+from gpu_util import GpuRun, check_bucketing, check_expert_rows, check_output, check_routing, run_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -315,4 +315,64 @@ class GpuRunLike:
         self.buf = SimpleNamespace(topk_idx=o[0], topk_w=o[1], logits=o[2], counts=o[3], offsets=o[4],
                                    sorted_pair=o[5], inv_pos=o[6], active=o[7])
         self.x_np = dl.x(1).float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("wl,T", [("decode", 4), ("decode", 1), ("tiny", 16), ("tiny", 300)])
+def test_layer_forward_is_bit_identical(wl, T):
+    # moe_layer_forward (one call; the decode expert FFN a programmatic dependent of the
+    # bucketing) against moe_route, moe_permute, moe_expert_ffn and moe_combine
+    from routed_expert_ffn_bucketing_b300 import layer as lay
+    w = custom(wl, T=T, router_sigma=1.0)
+    dl = DeviceLayer(w)
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    table = L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr)
+    outs = []
+    for fused in (False, True):
+        buf = lay.alloc_buffers(s, ydt=L.MOE_F32, odt=L.MOE_BF16)
+        for batch in range(3):  # repeated calls on one workspace
+            lay.forward(buf, dl.x(batch), dl.router, table, fused=fused)
+        assert L.moe_read_status(buf.ws) == 0
+        torch.cuda.synchronize()
+        outs.append((buf.out.clone(), buf.topk_idx.clone(), buf.y_perm.clone()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_expert_ffn_on_a_sparse_subset_of_experts():
+    # the active list may be any subset of the routed experts (a slot table's misses, say): their
+    # rows lie scattered among the other experts' rows. Every other expert of the full decode layer,
+    # then the complement, each into y_perm; together they equal one call on the whole list
+    from routed_expert_ffn_bucketing_b300 import layer as lay
+    w = custom("decode", T=4)
+    dl = DeviceLayer(w)
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    s0 = L.shape(w.T, w.d, w.f, w.E, w.k, 0)
+    table = L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr)
+    routed = L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, None)
+    buf = lay.alloc_buffers(s)
+    x = dl.x(5)
+    L.moe_route_permute(s, x, L.MOE_BF16, dl.router, buf.topk_idx, buf.topk_w, None, buf.counts, buf.offsets,
+                        buf.sorted_pair, buf.inv_pos, buf.active, buf.ws, buf.ws_bytes)
+    L.moe_expert_ffn(s, L.MOE_MODE_AUTO, x, L.MOE_BF16, table, buf.offsets, buf.sorted_pair, buf.active, buf.y_perm,
+                     buf.ydt, buf.ws, buf.ws_bytes)
+    torch.cuda.synchronize()
+    assert L.moe_read_status(buf.ws) == 0
+    full = buf.y_perm.clone()
+    act = buf.active.cpu().numpy()
+    ids = act[1:1 + act[0]]
+    ws2 = torch.zeros(L.moe_workspace_size(s0), dtype=torch.uint8, device="cuda")
+    buf.y_perm.zero_()
+    for part in (ids[::2], ids[1::2]):
+        sub = torch.tensor(np.concatenate([[part.size], part]).astype(np.int32), device="cuda")
+        L.moe_expert_ffn(s0, L.MOE_MODE_AUTO, x, L.MOE_BF16, routed, buf.offsets, buf.sorted_pair, sub, buf.y_perm,
+                         buf.ydt, ws2, ws2.numel())
+        torch.cuda.synchronize()
+        assert L.moe_read_status(ws2) == 0
+    P = w.P
+    # the same rows as the full call up to the order of fp32 additions (stream-K cuts differ, which
+    # can flip the f16 rounding of an h element: ~2^-11 of it)...
+    assert float(torch.max(torch.abs(buf.y_perm[:P] - full[:P]))) <= 1e-4 * float(torch.max(torch.abs(full[:P])))
+    # ...and every routed expert's rows against the oracle
+    run = GpuRun(buf, 0, x.float().cpu().numpy().astype(np.float64))
+    check_expert_rows(run, w, ids)
 

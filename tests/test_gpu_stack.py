@@ -144,8 +144,9 @@ def test_tiered_step_full_width():
         ts.close()
 
 
-@pytest.mark.parametrize("overlap,freq", [(True, False), (False, False), (True, True)])
-def test_tiered_stack_misses_evictions_and_parity(overlap, freq):
+@pytest.mark.parametrize("overlap,freq,prefetch", [(True, False, False), (False, False, False), (True, True, False),
+                                                   (True, False, True), (True, True, True)])
+def test_tiered_stack_misses_evictions_and_parity(overlap, freq, prefetch):
     # 2 layers x 32 experts, but only 24 device slots: every step evicts and copies. With freq:
     # the decayed-use-count policy, and a usage profile that fills the pool before step 0
     w = custom("stack", d=256, f=128, E=32, k=6, layers=2, T=4)
@@ -167,7 +168,7 @@ def test_tiered_stack_misses_evictions_and_parity(overlap, freq):
     try:
         for step in range(3):
             keep = []
-            ts.forward(dls[0].x(step), keep=keep, overlap=overlap)
+            ts.forward(dls[0].x(step), keep=keep, overlap=overlap, prefetch=prefetch)
             assert ts.status() == 0
             torch.cuda.synchronize()
             check_layers(w, keep, range(w.layers))
@@ -175,7 +176,13 @@ def test_tiered_stack_misses_evictions_and_parity(overlap, freq):
         st = L.slot_table_stats(ts.table)
         assert st.misses > 0 and st.evictions > 0
         assert st.hits + st.misses == lookups
-        assert st.bytes_h2d == (st.misses + ts.n_warm) * rb
+        pf_loads, pf_used = L.slot_table_prefetch_stats(ts.table)
+        assert st.bytes_h2d == (st.misses + ts.n_warm + pf_loads) * rb
+        if prefetch:
+            # layer 1 routed on layer 0's input: most of its experts are loaded before its turn
+            assert pf_loads > 0 and pf_used > 0 and pf_used <= pf_loads
+        else:
+            assert pf_loads == 0
         # every resident expert's slot holds that expert's record
         snap = np.zeros(w.layers * w.E, dtype=np.int32)
         L.slot_table_snapshot(ts.table, snap.ctypes.data)
