@@ -758,6 +758,8 @@ def run_tiered(args, ws, rank, local, w):
             profile[l * w.E + perms[l]] = freq
     ts = TieredStack(s, w.layers, routers, h_records, w.slots, rb, shared, device=dev, policy=policy,
                      half_life_steps=args.half_life_steps, profile=profile)
+    if args.host_threads:
+        ts.host_threads = args.host_threads
     n_batches = 16
     x_host = [torch.from_numpy(w.x_bits(b).astype(np.int16)).view(torch.bfloat16).pin_memory()
               for b in range(n_batches)]
@@ -778,6 +780,7 @@ def run_tiered(args, ws, rank, local, w):
     del pd
 
     launches = [0]
+    host_experts = [0]
 
     def run(step0, n, e2e):
         wall = 0.0
@@ -789,7 +792,8 @@ def run_tiered(args, ws, rank, local, w):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
             x_dev.copy_(x_host[i % n_batches], non_blocking=True)
-            y = ts.forward(x_dev, prefetch=args.prefetch, prefetch_top=args.prefetch_top)
+            y = ts.forward(x_dev, prefetch=args.prefetch, prefetch_top=args.prefetch_top, pcie_frac=args.pcie_frac)
+            host_experts[0] += sum(ts.layer_host)
             if e2e:
                 out_host.copy_(y, non_blocking=True)
             torch.cuda.synchronize(dev)
@@ -804,6 +808,8 @@ def run_tiered(args, ws, rank, local, w):
     try:
         run(0, W, False)
         launches[0] = 0
+        host_experts[0] = 0
+        ts.host_seconds = 0.0
         s0 = L.slot_table_stats(ts.table)
         pf0 = L.slot_table_prefetch_stats(ts.table)
         clocks = ClockSampler(local)
@@ -842,6 +848,9 @@ def run_tiered(args, ws, rank, local, w):
                       "hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
                       "evictions": s1.evictions - s0.evictions, "h2d_gbs": h2d / wall / 1e9,
                       "h2d_bytes_per_step": h2d / K, "cold_start_misses": s0.misses,
+                      "pcie_frac": args.pcie_frac, "host_computed_experts": host_experts[0],
+                      "host_threads": ts.host_threads,
+                      "host_ffn_ms_per_step": 1e3 * ts.host_seconds / K,
                       "early_routing_prefetch": bool(args.prefetch), "prefetch_top": args.prefetch_top,
                       "prefetch_loads": pf1[0] - pf0[0],
                       "prefetch_used": pf1[1] - pf0[1]},
@@ -876,6 +885,10 @@ def main():
                     help="tiered: fill the pool from a usage profile before the first step")
     ap.add_argument("--prefetch", action="store_true",
                     help="tiered: route layer l+1 on layer l's input and copy its experts during layer l")
+    ap.add_argument("--pcie-frac", type=float, default=1.0,
+                    help="tiered: share of each layer's missed experts copied to the device; the host computes the rest")
+    ap.add_argument("--host-threads", type=int, default=0,
+                    help="tiered, pcie-frac < 1: threads of the host expert FFN (0: three quarters of the cores)")
     ap.add_argument("--prefetch-top", type=int, default=None,
                     help="tiered, prefetch: load only each token's first N predicted experts")
     args = ap.parse_args()

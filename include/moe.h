@@ -407,6 +407,27 @@ moe_status slot_table_set_policy(moe_slot_table* table, int32_t policy, double h
 moe_status slot_table_warm(moe_slot_table* table, const float* h_weight, moe_stream_t copy_stream,
                            moe_event_t ready, int32_t* n_loaded);
 
+/* Host computation of missed experts: the bandwidth split of the miss path ([P2] "专家缓存": the
+ * experts a layer misses are divided between PCIe copies into the VRAM cache and computation
+ * where their weights are, in host RAM; the share copied is the pages' --pcie-frac setting,
+ * "Strata 性能基准与论文导读125B MoE在消费级硬件上的极限测量与瓶颈分析", section "如何测量"). Host
+ * only, synchronous, no CUDA call. For each expert h_experts[i] (routed ids, distinct), whose
+ * record (in `format`) is at h_records[i] in host memory, the SwiGLU FFN of each of its tokens:
+ * its rows h_offsets[e] .. h_offsets[e+1]-1 of y_perm, token sorted_pair[row] / k of h_x [T][d]
+ * (xdt), written in fp32 to h_y [T*k][d] at those rows (other rows untouched). fp32 arithmetic on
+ * the exactly expanded weights; n_threads OpenMP threads (0: all). h_offsets [E+1] and
+ * h_sorted_pair [T*k] are host copies of moe_permute's outputs. MOE_EINVAL for NULL arguments,
+ * a bad format, id or offsets. Off the default path: only a caller that asks for the split runs it. */
+moe_status moe_host_expert_ffn(const moe_shape* shape, const void* h_x, moe_dtype xdt,
+                               const void* const* h_records, const int32_t* h_experts, int32_t n_experts,
+                               const int32_t* h_offsets, const int32_t* h_sorted_pair, float* h_y, int32_t format,
+                               int32_t n_threads);
+
+/* Residency of experts of one layer: h_slot[i] (host) = the slot of expert h_ids[i] of `layer`, or
+ * -1 when it is not resident. No state changes. MOE_EINVAL for a bad layer or id. */
+moe_status slot_table_lookup(const moe_slot_table* table, int32_t layer, const int32_t* h_ids, int32_t n,
+                             int32_t* h_slot);
+
 /* Cumulative counters since creation. */
 moe_status slot_table_stats(const moe_slot_table* table, moe_slot_stats* out);
 

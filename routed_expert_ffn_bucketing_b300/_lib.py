@@ -81,6 +81,9 @@ _SIGS = {
     "slot_table_prefetch_stats": (C.c_int, [_P, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]),
     "slot_table_warm": (C.c_int, [_P, _P, _P, _P, _P]),
     "slot_table_stats": (C.c_int, [_P, C.POINTER(moe_slot_stats)]),
+    "slot_table_lookup": (C.c_int, [_P, C.c_int32, _P, C.c_int32, _P]),
+    "moe_host_expert_ffn": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, _P, C.c_int32, _P, _P, _P, C.c_int32,
+                                      C.c_int32]),
     "slot_table_snapshot": (C.c_int, [_P, _P]),
     "slot_table_destroy": (C.c_int, [_P]),
 }
@@ -283,6 +286,19 @@ def slot_table_warm(table, h_weight, copy_stream=None, ready=None) -> int:
     n = C.c_int32()
     _check(lib().slot_table_warm(table, h_weight, copy_stream, ready, C.byref(n)), "slot_table_warm")
     return n.value
+
+
+def slot_table_lookup(table, layer: int, h_ids: int, n: int, h_slot: int) -> None:
+    """h_ids, h_slot: host addresses (ints) of int32 arrays of n entries."""
+    _check(lib().slot_table_lookup(table, layer, h_ids, n, h_slot), "slot_table_lookup")
+
+
+def moe_host_expert_ffn(s, h_x, xdt, h_records, h_experts, n_experts, h_offsets, h_sorted_pair, h_y, fmt=MOE_FMT_INT8,
+                        n_threads=0) -> None:
+    """All pointers are host addresses (ints); h_records: a sequence of n_experts addresses."""
+    recs = (C.c_void_p * max(1, n_experts))(*h_records)
+    _check(lib().moe_host_expert_ffn(C.byref(s), h_x, xdt, recs, h_experts, n_experts, h_offsets, h_sorted_pair, h_y,
+                                     fmt, n_threads), "moe_host_expert_ffn")
 
 
 def slot_table_stats(table) -> moe_slot_stats:

@@ -44,7 +44,8 @@ def _compile(src: str, obj: str, inc: list[str], deps: list[str], verbose: bool)
         return obj
     cmd = [nvcc()] + NVCC_FLAGS + [f"-I{d}" for d in inc] + ["-c", src, "-o", obj]
     if src.endswith(".cpp"):
-        cmd = [nvcc()] + ["-O3", "-std=c++17", "-Xcompiler", "-fPIC,-O2"] + [f"-I{d}" for d in inc] + ["-c", src, "-o", obj]
+        cmd = [nvcc()] + ["-O3", "-std=c++17", "-Xcompiler", "-fPIC,-O3,-fopenmp"] + [f"-I{d}" for d in inc] + \
+            ["-c", src, "-o", obj]
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -67,7 +68,7 @@ def build_lib(name: str, verbose: bool = False) -> str:
         list(ex.map(lambda so: _compile(so[0], so[1], cfg["inc"], hdrs, verbose), zip(srcs, objs)))
     out = cfg["out"]
     if not (os.path.exists(out) and os.path.getmtime(out) >= _newest(objs)):
-        cmd = [nvcc()] + ARCH + ["-shared", "-o", out] + objs + ["-lcudart_static", "-lrt", "-ldl", "-lpthread"]
+        cmd = [nvcc()] + ARCH + ["-shared", "-o", out] + objs + ["-lcudart_static", "-lrt", "-ldl", "-lpthread", "-lgomp"]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)

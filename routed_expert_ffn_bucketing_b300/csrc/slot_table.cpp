@@ -504,6 +504,19 @@ moe_status slot_table_warm(moe_slot_table* t, const float* h_weight, moe_stream_
   return rc;
 }
 
+moe_status slot_table_lookup(const moe_slot_table* t, int32_t layer, const int32_t* h_ids, int32_t n,
+                             int32_t* h_slot) {
+  if (!t || n < 0 || (n > 0 && (!h_ids || !h_slot)))
+    return slot_fail(MOE_EINVAL, "slot_table_lookup: null table or arrays, or n < 0");
+  if (layer < 0 || layer >= t->L) return slot_fail(MOE_EINVAL, "slot_table_lookup: layer %d not in [0, %d)", layer, t->L);
+  for (int32_t i = 0; i < n; ++i) {
+    if (h_ids[i] < 0 || h_ids[i] >= t->E)
+      return slot_fail(MOE_EINVAL, "slot_table_lookup: expert id %d out of [0, %d)", h_ids[i], t->E);
+    h_slot[i] = t->mirror[(int64_t)layer * t->E + h_ids[i]];
+  }
+  return MOE_OK;
+}
+
 moe_status slot_table_stats(const moe_slot_table* t, moe_slot_stats* out) {
   if (!t || !out) return MOE_EINVAL;
   *out = t->stats;

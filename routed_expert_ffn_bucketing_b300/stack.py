@@ -9,6 +9,9 @@ x_l in fp32 and rounds once to bf16, in place.
 """
 from __future__ import annotations
 
+import os
+import time
+
 import ctypes as C
 from dataclasses import dataclass
 
@@ -75,7 +78,12 @@ class TieredStack:
     names that are not resident are copied after layer l's misses (slot_table_prefetch, never
     evicting layer l's experts), so that PCIe works on layer l+1 while layer l computes. Layer
     l+1's expert FFN waits for those copies (an event per layer); where the prediction was
-    right its experts are then hits."""
+    right its experts are then hits.
+
+    With pcie_frac < 1 (the pages' bandwidth split of the miss path): of a layer's missed experts
+    only the first pcie_frac share is copied; the host computes the rest from their pinned
+    records (moe_host_expert_ffn) while the GPU runs the others, and their output rows are copied
+    into y_perm before the combine. Host-computed experts do not become resident."""
 
     def __init__(self, shape: L.moe_shape, n_layers: int, routers: list[torch.Tensor], h_records: list[int],
                  n_slots: int, slot_bytes: int, shared: list[torch.Tensor], device="cuda",
@@ -118,6 +126,20 @@ class TieredStack:
         for ev in self.pf_ready:
             ev.record(self.copy_stream)
         self.layer_prefetched: list[int] = []
+        # bandwidth split: host copies of the layer input and the bucketing, host output rows
+        self.h_records = list(h_records)
+        self.h_xn = torch.empty((shape.T, shape.d), dtype=torch.bfloat16).pin_memory()
+        self.h_offsets = torch.empty(shape.E + 1, dtype=torch.int32).pin_memory()
+        self.h_sorted = torch.empty(max(1, shape.T * shape.k), dtype=torch.int32).pin_memory()
+        self.h_y = torch.empty((shape.T * shape.k, shape.d), dtype=torch.float32).pin_memory()
+        self.h_slot = np.zeros(cap, dtype=np.int32)
+        self.h_upd = np.zeros(cap, dtype=np.int32)
+        self.h_host = np.zeros(cap, dtype=np.int32)
+        self.layer_host: list[int] = []
+        # threads of the host expert FFN: a quarter of the cores stays free for the thread that
+        # drives the GPU and the driver's own threads (with every core busy the host FFN ran ~4x slower)
+        self.host_threads = max(1, (os.cpu_count() or 1) * 3 // 4)
+        self.host_seconds = 0.0  # wall time spent in it, summed over calls
         if policy != L.MOE_SLOT_LRU:
             L.slot_table_set_policy(self.table, policy, half_life_steps * n_layers)
         self.n_warm = 0
@@ -138,14 +160,18 @@ class TieredStack:
             self.table = None
 
     def forward(self, x: torch.Tensor, keep: list | None = None, overlap: bool = True,
-                prefetch: bool = False, prefetch_top: int | None = None) -> torch.Tensor:
+                prefetch: bool = False, prefetch_top: int | None = None, pcie_frac: float = 1.0) -> torch.Tensor:
         """prefetch_top: with prefetch, only the first prefetch_top of each token's predicted top-k
-        experts (descending logit) are loaded early; all of them when None."""
+        experts (descending logit) are loaded early; all of them when None. pcie_frac: the share of
+        each layer's missed experts copied to the device (the rest are computed on the host)."""
+        split = pcie_frac < 1.0
+        assert not split or overlap, "the bandwidth split runs with overlap"
         s, b = self.shape, self.buf
         stream = torch.cuda.current_stream()
         self.resid.copy_(x)
         self.layer_misses = []
         self.layer_prefetched = []
+        self.layer_host = []
         for l in range(self.L):
             if keep is not None:
                 keep.append(("in", self.resid.clone()))
@@ -163,13 +189,31 @@ class TieredStack:
                 else:
                     self.h_pred_idx.copy_(pb.topk_idx, non_blocking=True)
             self.h_active.copy_(b.active, non_blocking=True)
+            if split:  # what the host needs to compute experts itself
+                self.h_xn.copy_(self.xn, non_blocking=True)
+                self.h_offsets.copy_(b.offsets, non_blocking=True)
+                self.h_sorted.copy_(b.sorted_pair[:s.T * s.k], non_blocking=True)
             # the host needs the active list, and the previous layer's FFN must be done with the
             # slots before any of them is overwritten: one event wait per layer
             self.done.record(stream)
             self.done.synchronize()
             n = int(self.h_active[0])
             hp, mp = self.h_hits.data_ptr(), self.h_misses.data_ptr()
-            st = L.slot_table_update(self.table, l, self.h_active.data_ptr() + 4, n, self.copy_stream.cuda_stream,
+            upd_ptr, n_upd, n_host = self.h_active.data_ptr() + 4, n, 0
+            if split and n:
+                # the missed experts, in active-list order; the last (1 - pcie_frac) of them stay on the host
+                L.slot_table_lookup(self.table, l, upd_ptr, n, self.h_slot.ctypes.data)
+                act = self.h_active.numpy()[1:1 + n]
+                miss = act[self.h_slot[:n] < 0]
+                n_host = int(len(miss) * (1.0 - pcie_frac))
+                host_ids = set(miss[len(miss) - n_host:].tolist()) if n_host else set()
+                keep_ids = [e for e in act.tolist() if e not in host_ids]
+                n_upd = len(keep_ids)
+                self.h_upd[:n_upd] = keep_ids
+                self.h_host[:n_host] = sorted(host_ids)
+                upd_ptr = self.h_upd.ctypes.data
+            self.layer_host.append(n_host)
+            st = L.slot_table_update(self.table, l, upd_ptr, n_upd, self.copy_stream.cuda_stream,
                                      self.ready.cuda_event, hp + 4, hp, mp + 4, mp, self.stats)
             if st != L.MOE_OK:
                 raise L.MoeError(st, "slot_table_update", L.moe_last_error_string())
@@ -195,17 +239,30 @@ class TieredStack:
             comb = (b.inv_pos, b.topk_w, self.resid, self.resid, L.MOE_BF16)
             if overlap:
                 self.d_hits.copy_(self.h_hits, non_blocking=True)
-                if n_miss:
+                if n_miss or n_host:
                     L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
                                      self.d_hits, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
-                    stream.wait_event(self.ready)
-                    self.d_misses.copy_(self.h_misses, non_blocking=True)
-                    routed = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l], None)
-                    # the missed experts only (a shape without the shared expert, already done), then
-                    # the combine of the full layer
-                    L.moe_expert_ffn(self.shape_routed, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, routed, b.offsets,
-                                     b.sorted_pair, self.d_misses, b.y_perm, b.ydt, self.ws_miss,
-                                     self.ws_miss.numel(), stream)
+                    if n_miss:
+                        stream.wait_event(self.ready)
+                        self.d_misses.copy_(self.h_misses, non_blocking=True)
+                        routed = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l], None)
+                        # the missed experts only (a shape without the shared expert, already done)
+                        L.moe_expert_ffn(self.shape_routed, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, routed,
+                                         b.offsets, b.sorted_pair, self.d_misses, b.y_perm, b.ydt, self.ws_miss,
+                                         self.ws_miss.numel(), stream)
+                    if n_host:
+                        # meanwhile the host computes the rest of the misses, then their rows go in
+                        ids = self.h_host[:n_host]
+                        recs = [self.h_records[l * s.E + int(e)] for e in ids]
+                        t0 = time.perf_counter()
+                        L.moe_host_expert_ffn(s, self.h_xn.data_ptr(), L.MOE_BF16, recs, ids.ctypes.data, n_host,
+                                              self.h_offsets.data_ptr(), self.h_sorted.data_ptr(),
+                                              self.h_y.data_ptr(), L.MOE_FMT_INT8, self.host_threads)
+                        self.host_seconds += time.perf_counter() - t0
+                        offs = self.h_offsets.numpy()
+                        for e in ids:
+                            r0, r1 = int(offs[e]), int(offs[e + 1])
+                            b.y_perm[r0:r1].copy_(self.h_y[r0:r1], non_blocking=True)
                     L.moe_combine(s, b.y_perm, b.ydt, *comb, stream)
                 else:
                     stream.wait_event(self.ready)

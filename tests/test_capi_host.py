@@ -552,3 +552,59 @@ def test_slot_table_prefetch_rejects_bad_arguments():
         assert e.value.status == L.MOE_EINVAL
     assert len(cp.records) == 0 and _resident(h, 2, 8) == set()
     L.slot_table_destroy(h)
+
+
+@pytest.mark.parametrize("fmt,d,f", [(L.MOE_FMT_INT8, 256, 256), (L.MOE_FMT_Q2, 256, 256),
+                                     (L.MOE_FMT_INT8, 288, 160)])
+def test_host_expert_ffn_matches_oracle(fmt, d, f):
+    # the host half of the bandwidth split: every row of the chosen experts against the oracle's
+    # SwiGLU FFN of the same tokens, with records packed as the device reads them (288 and 160:
+    # rows ending in a block without a partner, stored in order)
+    import synth
+    from oracle import moe_oracle as O
+    from synth.workloads import custom
+    w = custom("tiny", T=5, d=d, f=f, E=8, k=3, fmt=fmt)
+    rng = np.random.default_rng(11)
+    topk = np.stack([rng.choice(w.E, w.k, replace=False) for _ in range(w.T)]).astype(np.int32)
+    flat = topk.reshape(-1)
+    order = np.argsort(flat, kind="stable").astype(np.int32)          # pairs grouped by expert
+    offsets = np.zeros(w.E + 1, np.int32)
+    offsets[1:] = np.cumsum(np.bincount(flat, minlength=w.E))
+    x_bits = w.x_bits(0)
+    x = synth.bf16_bits_to_f32(x_bits).astype(np.float64)
+    experts = np.array([e for e in range(w.E) if offsets[e + 1] > offsets[e]][::2], np.int32)
+    recs = [synth.pack_record(w.expert(0, int(e))) for e in experts]
+    y = np.full((w.P, w.d), np.nan, np.float32)
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, 0)
+    L.moe_host_expert_ffn(s, x_bits.ctypes.data, L.MOE_BF16, [r.ctypes.data for r in recs], experts.ctypes.data,
+                          experts.size, offsets.ctypes.data, order.ctypes.data, y.ctypes.data, fmt, 3)
+    for e in experts:
+        r0, r1 = offsets[e], offsets[e + 1]
+        ref = O.swiglu_ffn(x[order[r0:r1] // w.k], O.dense_expert(w.expert(0, int(e))))
+        got = y[r0:r1].astype(np.float64)
+        assert np.max(np.abs(got - ref)) <= 1e-5 * np.max(np.abs(ref)), e
+    done = set()
+    for e in experts:
+        done |= set(range(offsets[e], offsets[e + 1]))
+    untouched = [r for r in range(w.P) if r not in done]
+    assert np.all(np.isnan(y[untouched]))                              # other rows are left alone
+
+
+def test_host_expert_ffn_and_lookup_argument_checks():
+    s = L.shape(2, 256, 256, 8, 2, 0)
+    z = np.zeros(16, np.int32)
+    with pytest.raises(L.MoeError) as e:
+        L.moe_host_expert_ffn(s, None, L.MOE_BF16, [0], z.ctypes.data, 1, z.ctypes.data, z.ctypes.data, None)
+    assert e.value.status == L.MOE_EINVAL
+    with pytest.raises(L.MoeError):
+        L.moe_host_expert_ffn(s, z.ctypes.data, L.MOE_BF16, [z.ctypes.data], z.ctypes.data, 1, z.ctypes.data,
+                              z.ctypes.data, z.ctypes.data, fmt=5)
+    h, cp, _ = _make_table(2, 8, 3)
+    _update(h, 1, [2, 5])
+    ids = np.array([2, 5, 6], np.int32)
+    out = np.zeros(3, np.int32)
+    L.slot_table_lookup(h, 1, ids.ctypes.data, 3, out.ctypes.data)
+    assert out[0] >= 0 and out[1] >= 0 and out[2] == -1
+    with pytest.raises(L.MoeError):
+        L.slot_table_lookup(h, 2, ids.ctypes.data, 3, out.ctypes.data)
+    L.slot_table_destroy(h)

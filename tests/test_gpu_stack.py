@@ -144,9 +144,11 @@ def test_tiered_step_full_width():
         ts.close()
 
 
-@pytest.mark.parametrize("overlap,freq,prefetch", [(True, False, False), (False, False, False), (True, True, False),
-                                                   (True, False, True), (True, True, True)])
-def test_tiered_stack_misses_evictions_and_parity(overlap, freq, prefetch):
+@pytest.mark.parametrize("overlap,freq,prefetch,pcie_frac", [(True, False, False, 1.0), (False, False, False, 1.0),
+                                                             (True, True, False, 1.0), (True, False, True, 1.0),
+                                                             (True, True, True, 1.0), (True, False, False, 0.5),
+                                                             (True, False, True, 0.0)])
+def test_tiered_stack_misses_evictions_and_parity(overlap, freq, prefetch, pcie_frac):
     # 2 layers x 32 experts, but only 24 device slots: every step evicts and copies. With freq:
     # the decayed-use-count policy, and a usage profile that fills the pool before step 0
     w = custom("stack", d=256, f=128, E=32, k=6, layers=2, T=4)
@@ -165,17 +167,21 @@ def test_tiered_stack_misses_evictions_and_parity(overlap, freq, prefetch):
                      policy=L.MOE_SLOT_FREQ if freq else L.MOE_SLOT_LRU, half_life_steps=2.0, profile=profile)
     assert ts.n_warm == (n_slots if freq else 0)
     lookups = 0
+    n_host = 0
     try:
         for step in range(3):
             keep = []
-            ts.forward(dls[0].x(step), keep=keep, overlap=overlap, prefetch=prefetch)
+            ts.forward(dls[0].x(step), keep=keep, overlap=overlap, prefetch=prefetch, pcie_frac=pcie_frac)
+            n_host += sum(ts.layer_host)
             assert ts.status() == 0
             torch.cuda.synchronize()
             check_layers(w, keep, range(w.layers))
             lookups += sum(np.unique(rec[1].cpu().numpy()).size for rec in keep if rec[0] == "idx")
+        lookups -= n_host  # experts computed on the host are neither hits nor misses of the table
         st = L.slot_table_stats(ts.table)
-        assert st.misses > 0 and st.evictions > 0
+        assert (n_host > 0) == (pcie_frac < 1.0)
         assert st.hits + st.misses == lookups
+        assert st.misses > 0 or pcie_frac == 0.0
         pf_loads, pf_used = L.slot_table_prefetch_stats(ts.table)
         assert st.bytes_h2d == (st.misses + ts.n_warm + pf_loads) * rb
         if prefetch:
