@@ -14,20 +14,22 @@
 //   gemm<DN>: for each (M tile, 256 rows of d): D[128][256] = h16[128][f] . Wd[256][f]^T.
 //
 // The GEMM is persistent (one CTA per SM, a static stride over the work list) and warp
-// specialised, with two shared-memory rings, each with its own full and empty barriers: A (4
-// stages of 16 KB, filled by TMA) and the converted f16 B tile (3 stages of 32 KB). The int8
-// codes never pass through shared memory: its bandwidth is what the tensor core's operand reads
-// (12 KB per M128 x N256 x K16 MMA), the TMA writes and the converters share, and an int8 stage
-// would cost a TMA write plus a converter read for every K step.
+// specialised, with three shared-memory rings, each with its own full and empty barriers: A (4
+// stages of 16 KB, filled by TMA), the int8 codes of B (4 stages of 16 KB, filled by TMA) and the
+// converted f16 B tile (3 stages of 32 KB). The codes come by TMA rather than by per-thread loads
+// into registers: such loads land through L1, and with ~160 KB of shared memory taken the L1
+// left over bounds how many of them are in flight (measured: 48 KB of unused shared memory more
+// made the FFN 1.34x slower), while TMA copies bypass it and the ring sets the prefetch depth.
 //   warp 0, lane 0: TMA of the A tile of each 64-element K step (one pair of 32-element
 //            blocks): 128 rows x 128 bytes of f16 in the 128-byte swizzle; freed by the MMA.
+//   warp 10, lane 0: TMA of the codes of each K step: 256 B rows x 64 bytes; freed by the
+//            converters once they hold them in registers.
 //   warps 1..8: converters. Each thread owns 4 B rows and one 16-byte chunk of each row's 64
 //            stored codes per K step (chunk c holds codes 8c..8c+7 of both blocks of the pair),
-//            loaded with the blocks' fp16 scales from the expert record two pairs of K steps
-//            ahead into registers. It turns them into f16 (q * s, one rounding) and writes them
-//            into the B tile in the 128-byte-swizzled K-major layout the tensor core reads,
-//            then fences them into the async proxy. The int8 codes stay exact until this single
-//            rounding.
+//            with the blocks' fp16 scales loaded from the expert record two pairs of K steps
+//            ahead. It turns them into f16 (q * s, one rounding) and writes them into the B tile
+//            in the 128-byte-swizzled K-major layout the tensor core reads, then fences them
+//            into the async proxy. The int8 codes stay exact until this single rounding.
 //   warp 9, lane 0: issues 4 tcgen05.mma (M = 128, N = 256, K = 16) per K step into one of two
 //            TMEM accumulators (2 x 256 columns) and commits each stage back to the A and B rings.
 //   warps 12..15: epilogue. TMEM lanes 32 q .. 32 q + 31 (q = warp % 4) hold rows of the tile;
@@ -55,13 +57,16 @@ constexpr int kPN = 256;                     // UMMA N
 constexpr int kPK = 64;                      // K elements per stage (128 bytes of f16)
 constexpr int kPAStage = kPM * 128;          // 16 KB
 constexpr int kPBStage = kPN * 128;          // 32 KB
+constexpr int kPQStage = kPN * kPK;          // 16 KB: int8 codes of one K step of the 256 B rows
 constexpr int kPAStages = 4;                 // A ring (TMA; freed by the MMA)
 constexpr int kPBStages = 3;                 // f16 B ring (converters; freed by the MMA)
+constexpr int kPQStages = 4;                 // int8 code ring (TMA; freed by the converters)
 constexpr int kPConv = 8;                    // converter warps
-constexpr int kPThreads = 32 * 16;           // 0: TMA, 1..8: convert, 9: MMA, 12..15: epilogue
+constexpr int kPThreads = 32 * 16;           // 0: A TMA, 1..8: convert, 9: MMA, 10: code TMA, 12..15: epilogue
 constexpr int kPMmaWarp = 9;
+constexpr int kPQWarp = 10;
 constexpr int kPEpiWarp0 = 12;
-constexpr int kPPairsAhead = 2;              // pairs of K steps a converter holds in registers
+constexpr int kPPairsAhead = 2;              // pairs of K steps of scales a converter holds in registers
 
 enum { kPGateUp = 0, kPDown = 1 };
 
@@ -70,6 +75,8 @@ struct PHead {
   uint64_t a_empty[kPAStages];
   uint64_t b_full[kPBStages];
   uint64_t b_empty[kPBStages];
+  uint64_t q_full[kPQStages];
+  uint64_t q_empty[kPQStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;  // the MMA thread's last commit: every MMA it issued has completed
@@ -78,7 +85,9 @@ struct PHead {
 };
 constexpr size_t kPHeadBytes = 1024;
 static_assert(sizeof(PHead) <= kPHeadBytes, "head too large");
-constexpr size_t kPSmem = kPHeadBytes + 1024 + (size_t)kPAStages * kPAStage + (size_t)kPBStages * kPBStage;
+constexpr size_t kPSmem = kPHeadBytes + 1024 + (size_t)kPAStages * kPAStage + (size_t)kPBStages * kPBStage +
+                          (size_t)kPQStages * kPQStage;
+static_assert(kPSmem <= 232448, "shared memory of the GEMM above the per-block limit");
 
 __device__ __forceinline__ float p_pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
@@ -269,38 +278,27 @@ __device__ __forceinline__ bool work_at(const FfnArgs& A, const PrefillAux& X, i
 
 // Loads issued where they stand: the converters' prefetch only hides memory latency if the
 // compiler does not sink these loads down to the first use of their registers.
-__device__ __forceinline__ uint4 p_ld_codes(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
 __device__ __forceinline__ uint2 p_ld_scales(const void* p) {
   uint2 r;
   asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
   return r;
 }
 
-// What one converter thread needs of one pair of K steps (two 32-element blocks each): its
-// 16-byte chunk of the stored codes of each K step, and the four fp16 scales of the pair's four
-// blocks as one 8-byte word, for each of its four B rows.
-struct PPair {
-  uint4 q[2][4];  // [K step of the pair][row]
-  uint2 s[4];     // [row]
+// The four fp16 scales (two K steps, two blocks each) of one converter thread's four B rows for
+// one pair of K steps, one 8-byte word per row.
+struct PScales {
+  uint2 s[4];
 };
 
 // A cursor over the CTA's sequence of (work item, pair of K steps), in the order the MMA consumes
-// them; it loads one thread's PPair straight from the expert record (global memory).
+// them; it loads one thread's PScales straight from the expert record (global memory).
 template <int KIND>
 struct PCursor {
-  const uint8_t* qrow[4];
   const __half* srow[4];
   int w, kc;
 
   __device__ __forceinline__ void seek(const FfnArgs& A, const PrefillAux& X, int w0, int nch, int n_work, int rb,
-                                       int c, int K) {
+                                       int K) {
     const int nb = K / kQBlock;
     for (w = w0; w < n_work; w += gridDim.x) {
       PWork wk;
@@ -309,9 +307,7 @@ struct PCursor {
       for (int i = 0; i < 4; ++i) {
         const int r = rb + 64 * i;
         const int n = KIND == kPGateUp ? wk.n0 + (r & 127) : wk.n0 + r;
-        const uint64_t oq = KIND == kPGateUp ? (r < 128 ? A.o_gate_q : A.o_up_q) : A.o_down_q;
         const uint64_t os = KIND == kPGateUp ? (r < 128 ? A.o_gate_s : A.o_up_s) : A.o_down_s;
-        qrow[i] = wk.rec + oq + (size_t)n * K + c * 16;
         srow[i] = reinterpret_cast<const __half*>(wk.rec + os) + (size_t)n * nb;
       }
       kc = 0;
@@ -319,25 +315,24 @@ struct PCursor {
     }
   }
 
-  // Loads the pair at the cursor and moves one pair forward; false past the CTA's last work.
-  __device__ __forceinline__ bool next(const FfnArgs& A, const PrefillAux& X, int nch, int n_work, int rb, int c,
-                                       int K, PPair& p) {
+  // Loads the scales of the pair at the cursor and moves one pair forward; false past the CTA's
+  // last work.
+  __device__ __forceinline__ bool next(const FfnArgs& A, const PrefillAux& X, int nch, int n_work, int rb, int K,
+                                       PScales& p) {
     if (w >= n_work) return false;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      p.q[0][i] = p_ld_codes(qrow[i] + kc * kPK);
-      p.q[1][i] = p_ld_codes(qrow[i] + kc * kPK + kPK);
-      p.s[i] = p_ld_scales(srow[i] + kc * 2);
-    }
+    for (int i = 0; i < 4; ++i) p.s[i] = p_ld_scales(srow[i] + kc * 2);
     kc += 2;
-    if (kc * kPK >= K) seek(A, X, w + gridDim.x, nch, n_work, rb, c, K);
+    if (kc * kPK >= K) seek(A, X, w + gridDim.x, nch, n_work, rb, K);
     return true;
   }
 };
 
 template <int KIND>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, PrefillAux X,
-                                                                   const __grid_constant__ CUtensorMap tm_a) {
+                                                                   const __grid_constant__ CUtensorMap tm_a,
+                                                                   const __grid_constant__ CUtensorMap tm_q_pool,
+                                                                   const __grid_constant__ CUtensorMap tm_q_shared) {
   extern __shared__ __align__(1024) uint8_t dyn[];
   PHead& H = *reinterpret_cast<PHead*>(dyn);
   uint8_t* base = dyn + kPHeadBytes;
@@ -347,6 +342,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
   }
   uint8_t* ringA = base;
   uint8_t* ringB = ringA + kPAStages * kPAStage;
+  uint8_t* ringQ = ringB + kPBStages * kPBStage;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = KIND == kPGateUp ? A.d : A.f;
   const int KC = K / kPK;
@@ -362,6 +358,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
       mbar_init(&H.b_full[s], kPConv);
       mbar_init(&H.b_empty[s], 1);
     }
+    for (int s = 0; s < kPQStages; ++s) {
+      mbar_init(&H.q_full[s], 1);
+      mbar_init(&H.q_empty[s], kPConv);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&H.acc_full[b], 1);
       mbar_init(&H.acc_empty[b], 4);
@@ -370,6 +370,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
     H.abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_q_pool);
+    prefetch_tmap(&tm_q_shared);
   }
   if (warp == kPMmaWarp) {
     tmem_alloc(&H.tmem, 512);
@@ -407,19 +409,19 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
   } else if (warp >= 1 && warp <= kPConv) {
     // ---------------- converters ----------------
     // Thread ct owns B rows rb + 64 i (i < 4) and 16-byte chunk c of each row's 64 stored codes
-    // per K step. Its codes and scales come straight from global memory, kPPairsAhead pairs of
-    // K steps ahead (crossing into the CTA's next work item), into registers: each slot of the
-    // register ring is consumed and then refilled in place, so no load is waited for early.
+    // per K step (chunk c holds codes 8c..8c+7 of both blocks of the pair). The codes arrive by
+    // TMA in the int8 ring; the blocks' fp16 scales come straight from the expert record,
+    // kPPairsAhead pairs of K steps ahead, into registers.
     const int ct = threadIdx.x - 32;  // 0..255
     const int rb = ct >> 2, c = ct & 3;
-    int sb = 0;
-    uint32_t pb = 0;
+    int sb = 0, sq = 0;
+    uint32_t pb = 0, pq = 0;
     PCursor<KIND> cur;
-    cur.seek(A, X, blockIdx.x, nch, n_work, rb, c, K);
-    PPair pp[kPPairsAhead];
+    cur.seek(A, X, blockIdx.x, nch, n_work, rb, K);
+    PScales ps[kPPairsAhead];
     bool have[kPPairsAhead];
 #pragma unroll
-    for (int j = 0; j < kPPairsAhead; ++j) have[j] = cur.next(A, X, nch, n_work, rb, c, K, pp[j]);
+    for (int j = 0; j < kPPairsAhead; ++j) have[j] = cur.next(A, X, nch, n_work, rb, K, ps[j]);
     bool ok = true;
     while (ok && have[0]) {
 #pragma unroll
@@ -427,38 +429,78 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
         if (!have[j]) break;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const bool w2 = mbar_wait(&H.b_empty[sb], pb ^ 1u, A.wait_ns);
+          const bool w1 = mbar_wait(&H.q_full[sq], pq, A.wait_ns);
+          const bool w2 = w1 && mbar_wait(&H.b_empty[sb], pb ^ 1u, A.wait_ns);
           if (!__all_sync(0xFFFFFFFFu, w2 && !p_aborted(H))) {
             if (lane == 0) p_set_abort(H, A.status);
             ok = false;
             break;
           }
-          uint8_t* dst = ringB + (size_t)sb * kPBStage;
+          const uint8_t* src = ringQ + (size_t)sq * kPQStage;
+          uint4 lo[4], hi[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int r = rb + 64 * i;
             // this K step is one pair of blocks; their scales are the low and high half of one
             // 32-bit word of the pair of K steps' scales
-            const uint32_t sw = h ? pp[j].s[i].y : pp[j].s[i].x;
+            const uint32_t sw = h ? ps[j].s[i].y : ps[j].s[i].x;
             const __half2 s01 = *reinterpret_cast<const __half2*>(&sw);
-            // stored chunk c: codes 8c..8c+7 of both blocks -> K-major chunks c and 4 + c
-            uint4 lo, hi;
-            codes_to_f16(pp[j].q[h][i], __low2half2(s01), __high2half2(s01), &lo, &hi);
-            // odd rows write their high chunk first, so that the 8 lanes of a store phase (two
-            // rows) hit 8 distinct 16-byte bank groups
+            const uint4 q = *reinterpret_cast<const uint4*>(src + r * kPK + c * 16);
+            codes_to_f16(q, __low2half2(s01), __high2half2(s01), &lo[i], &hi[i]);
+          }
+          // every lane has its codes in registers: the code stage goes back to the TMA
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&H.q_empty[sq]);
+          uint8_t* dst = ringB + (size_t)sb * kPBStage;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = rb + 64 * i;
+            // stored chunk c -> K-major chunks c and 4 + c; odd rows write their high chunk
+            // first, so that the 8 lanes of a store phase (two rows) hit 8 distinct 16-byte
+            // bank groups
             const bool odd = (r & 1) != 0;
             const int ch_lo = c ^ (r & 7), ch_hi = (4 + c) ^ (r & 7);
-            *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_hi : ch_lo) << 4)) = odd ? hi : lo;
-            *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_lo : ch_hi) << 4)) = odd ? lo : hi;
+            *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_hi : ch_lo) << 4)) = odd ? hi[i] : lo[i];
+            *reinterpret_cast<uint4*>(dst + r * 128 + ((odd ? ch_lo : ch_hi) << 4)) = odd ? lo[i] : hi[i];
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&H.b_full[sb]);
           if (++sb == kPBStages) { sb = 0; pb ^= 1u; }
+          if (++sq == kPQStages) { sq = 0; pq ^= 1u; }
         }
         if (!ok) break;
-        have[j] = cur.next(A, X, nch, n_work, rb, c, K, pp[j]);
+        have[j] = cur.next(A, X, nch, n_work, rb, K, ps[j]);
       }
+    }
+  } else if (warp == kPQWarp) {
+    // ---------------- TMA producer of the int8 code tiles ----------------
+    // One K step of the work item's 256 B rows: gate rows n0..n0+127 then the same up rows (one
+    // 4-D box), or down rows n0..n0+255 (one 3-D box); 64 bytes per row, rows back to back.
+    if (lane == 0) {
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int w = blockIdx.x; w < n_work && !p_aborted(H); w += gridDim.x) {
+        PWork wk;
+        if (!work_at<KIND>(A, X, w, nch, &wk)) continue;
+        const CUtensorMap* tq = wk.shared ? &tm_q_shared : &tm_q_pool;
+        for (int kc = 0; kc < KC; ++kc) {
+          if (!mbar_wait(&H.q_empty[s], ph ^ 1u, A.wait_ns)) {
+            p_set_abort(H, A.status);
+            break;
+          }
+          mbar_arrive_expect_tx(&H.q_full[s], kPQStage);
+          if (KIND == kPGateUp)
+            tma_load_4d(ringQ + (size_t)s * kPQStage, tq, kc * kPK, wk.n0, 0, wk.slot, &H.q_full[s]);
+          else
+            tma_load_3d(ringQ + (size_t)s * kPQStage, tq, kc * kPK, wk.n0, wk.slot, &H.q_full[s]);
+          ++issued;
+          if (++s == kPQStages) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (p_aborted(H))  // no copy may still be landing in shared memory when the CTA exits
+        for (int j = issued > kPQStages ? issued - kPQStages : 0; j < issued; ++j)
+          mbar_wait(&H.q_full[j % kPQStages], (j / kPQStages) & 1);  // default limit
     }
   } else if (warp == kPMmaWarp) {
     // ---------------- MMA issuer ----------------
@@ -534,7 +576,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
           float hv[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            hv[j] = silu(__uint_as_float(gv[j]) * xs) * (__uint_as_float(uv[j]) * xs);
+            hv[j] = silu_fast(__uint_as_float(gv[j]) * xs) * (__uint_as_float(uv[j]) * xs);
             mx = fmaxf(mx, fabsf(hv[j]));
           }
           if (valid) {
@@ -613,6 +655,28 @@ bool encode_a(CUtensorMap* m, const void* base, int K, int rows) {
                         kPM, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Codes of the gate/up matrices of n records: (K byte, row, gate|up, record), boxes 64 x 128 x 2.
+bool encode_q_gu(CUtensorMap* m, const uint8_t* recs, uint64_t n, const FfnArgs& a) {
+  const cuuint64_t dims[4] = {(cuuint64_t)a.d, (cuuint64_t)a.f, 2, n};
+  const cuuint64_t strides[3] = {(cuuint64_t)a.d, (cuuint64_t)(a.o_up_q - a.o_gate_q), a.slot_bytes};
+  const cuuint32_t box[4] = {kPK, 128, 2, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return p_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(recs + a.o_gate_q), dims, strides,
+                       box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Codes of the down matrix of n records: (K byte, row, record), boxes 64 x 256.
+bool encode_q_dn(CUtensorMap* m, const uint8_t* recs, uint64_t n, const FfnArgs& a) {
+  const cuuint64_t dims[3] = {(cuuint64_t)a.f, (cuuint64_t)a.d, n};
+  const cuuint64_t strides[2] = {(cuuint64_t)a.f, a.slot_bytes};
+  const cuuint32_t box[3] = {kPK, kPN, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return p_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(recs + a.o_down_q), dims, strides,
+                       box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool tmap_available() { return p_encode_fn() != nullptr; }
@@ -635,8 +699,14 @@ bool prefill_supported(const FfnArgs& a) {
 cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, int sm_count, cudaStream_t st) {
   const int rows = a.P + a.T * a.n_shared;
   if (rows == 0) return cudaSuccess;
-  CUtensorMap tm_x, tm_h;
-  if (!encode_a(&tm_x, x.xp16, a.d, rows) || !encode_a(&tm_h, x.h16, a.f, rows)) return cudaErrorInvalidValue;
+  // the shared experts' records follow one another at the pool's record stride
+  CUtensorMap tm_x, tm_h, qgu_pool, qgu_sh, qdn_pool, qdn_sh;
+  const uint8_t* sh = a.n_shared > 0 ? a.shared : a.pool;
+  const uint64_t nsh = a.n_shared > 0 ? (uint64_t)a.n_shared : 1;
+  if (!encode_a(&tm_x, x.xp16, a.d, rows) || !encode_a(&tm_h, x.h16, a.f, rows) ||
+      !encode_q_gu(&qgu_pool, a.pool, a.n_slots, a) || !encode_q_gu(&qgu_sh, sh, nsh, a) ||
+      !encode_q_dn(&qdn_pool, a.pool, a.n_slots, a) || !encode_q_dn(&qdn_sh, sh, nsh, a))
+    return cudaErrorInvalidValue;
   prefill_prepare_kernel<<<a.T, 256, 0, st>>>(a, x);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -647,11 +717,11 @@ cudaError_t launch_ffn_prefill(const FfnArgs& a, const PrefillAux& x, int sm_cou
   auto dn = prefill_gemm_kernel<kPDown>;
   if ((e = ensure_dynamic_smem(reinterpret_cast<const void*>(gu), kPSmem)) != cudaSuccess) return e;
   if ((e = ensure_dynamic_smem(reinterpret_cast<const void*>(dn), kPSmem)) != cudaSuccess) return e;
-  gu<<<sm_count, kPThreads, kPSmem, st>>>(a, x, tm_x);
+  gu<<<sm_count, kPThreads, kPSmem, st>>>(a, x, tm_x, qgu_pool, qgu_sh);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   prefill_convert_h_kernel<<<grid_rows, 256, 0, st>>>(a, x);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dn<<<sm_count, kPThreads, kPSmem, st>>>(a, x, tm_h);
+  dn<<<sm_count, kPThreads, kPSmem, st>>>(a, x, tm_h, qdn_pool, qdn_sh);
   return cudaGetLastError();
 }
 
