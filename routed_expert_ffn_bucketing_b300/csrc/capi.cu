@@ -497,7 +497,6 @@ moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt
   if (!y_perm || !inv_pos || !topk_w || !out) return fail(MOE_EINVAL, "moe_combine: NULL argument");
   if (!aligned(y_perm, 16) || !aligned(out, 16) || (residual_opt && !aligned(residual_opt, 16)))
     return fail(MOE_EINVAL, "moe_combine: misaligned y_perm, out or residual");
-  if (shape->T == 0) return MOE_OK;
   cudaError_t e = launch_combine(*shape, y_perm, ydt, inv_pos, topk_w, residual_opt, out, odt,
                                  reinterpret_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return cuda_fail(e, "moe_combine: launch");
