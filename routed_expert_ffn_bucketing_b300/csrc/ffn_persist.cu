@@ -865,10 +865,10 @@ int persist_rows_cap(const FfnArgs& a, int sm_count) {
 }
 
 template <int DG, int DD, int FMT>
-cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st, bool pdl) {
+cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int n_ctas, cudaStream_t st, bool pdl) {
   const int rows = a.P + a.T * a.n_shared;
   const int items_max = (a.P < a.E ? a.P : a.E) + a.n_shared;
-  const int rows_cap = persist_rows_cap(a, sm_count);
+  const int rows_cap = persist_rows_cap(a, n_ctas);
   const PLayout L = p_layout<DG, DD, FMT>(a.T, a.d, a.f, items_max, rows, rows_cap);
   const void* fn = (const void*)ffn_persist_kernel<DG, DD, FMT>;
   cudaError_t e = ensure_dynamic_smem(fn, L.total);
@@ -878,14 +878,15 @@ cudaError_t launch_persist_d(const FfnArgs& a, const PersistAux& x, int sm_count
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   PAux px{x.part, x.task_cnt, x.hmax, x.item_done, x.part_stride, x.cnt_stride, rows_cap, x.exit};
-  // One CTA per SM (the occupancy check above: a CTA takes every register of its SM). With pdl,
+  // One CTA per SM, n_ctas <= the SM count (the occupancy check above: a CTA takes every
+  // register of its SM). With pdl,
   // a programmatic dependent of the bucketing kernel the caller enqueued just before: the CTAs
   // stage x while the bucketing runs and wait for its outputs (griddepcontrol.wait); every CTA's
   // waits for other CTAs are bounded. Otherwise a cooperative launch, which guarantees that all
   // CTAs are resident at once.
-  if (pdl) return launch_pdl(ffn_persist_kernel<DG, DD, FMT>, dim3(sm_count), dim3(kPThreads), L.total, st, a, px);
+  if (pdl) return launch_pdl(ffn_persist_kernel<DG, DD, FMT>, dim3(n_ctas), dim3(kPThreads), L.total, st, a, px);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sm_count);
+  cfg.gridDim = dim3(n_ctas);
   cfg.blockDim = dim3(kPThreads);
   cfg.dynamicSmemBytes = L.total;
   cfg.stream = st;
@@ -913,13 +914,13 @@ bool persist_supported(const FfnArgs& a, int sm_count) {
          a.T * (a.d / kQBlock) <= kPThreads && persist_smem_bytes(a, sm_count) <= 200 * 1024;
 }
 
-cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st, bool pdl) {
-  if (a.fmt == 1) return launch_persist_d<8, 8, 1>(a, x, sm_count, st, pdl);  // d and f multiples of 256
+cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int n_ctas, cudaStream_t st, bool pdl) {
+  if (a.fmt == 1) return launch_persist_d<8, 8, 1>(a, x, n_ctas, st, pdl);  // d and f multiples of 256
   const bool g8 = (a.d / kQBlock) % 8 == 0, d8 = (a.f / kQBlock) % 8 == 0;
-  if (g8 && d8) return launch_persist_d<8, 8, 0>(a, x, sm_count, st, pdl);
-  if (g8) return launch_persist_d<8, 4, 0>(a, x, sm_count, st, pdl);
-  if (d8) return launch_persist_d<4, 8, 0>(a, x, sm_count, st, pdl);
-  return launch_persist_d<4, 4, 0>(a, x, sm_count, st, pdl);
+  if (g8 && d8) return launch_persist_d<8, 8, 0>(a, x, n_ctas, st, pdl);
+  if (g8) return launch_persist_d<8, 4, 0>(a, x, n_ctas, st, pdl);
+  if (d8) return launch_persist_d<4, 8, 0>(a, x, n_ctas, st, pdl);
+  return launch_persist_d<4, 4, 0>(a, x, n_ctas, st, pdl);
 }
 
 }  // namespace moe

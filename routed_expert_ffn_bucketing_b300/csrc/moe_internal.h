@@ -175,11 +175,11 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);  // fp32 SIMT 
 // Streaming tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
 cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, int sm_count, cudaStream_t st);
 bool stream_supported(const FfnArgs& a);
-// One persistent cooperative kernel for T <= 8 (bf16 x); persist_supported() says whether the
-// shape fits (its shared-memory copy of the activations included).
-// pdl: launched as a programmatic dependent of the kernel the caller enqueued just before it
-// (else a cooperative launch).
-cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int sm_count, cudaStream_t st, bool pdl);
+// One persistent kernel for T <= 8 (bf16 x) on n_ctas SMs (at most the SM count);
+// persist_supported() says whether the shape fits (its shared-memory copy of the activations
+// included). pdl: launched as a programmatic dependent of the kernel the caller enqueued just
+// before it (else a cooperative launch).
+cudaError_t launch_ffn_persist(const FfnArgs& a, const PersistAux& x, int n_ctas, cudaStream_t st, bool pdl);
 bool persist_supported(const FfnArgs& a, int sm_count);
 // Tensor-core grouped GEMM for many tokens per expert (bf16 x); prefill_supported() says whether
 // the shape fits (d a multiple of 256, f of 128).

@@ -63,6 +63,24 @@ __device__ __forceinline__ void sort_desc_regs(uint64_t (&v)[N]) {
       }
 }
 
+// Writes token t's selection, lane j holding its j-th expert and key (j < k), with the
+// renormalised gate weights: exp(l_j - l_0) over their sum (a fixed butterfly order).
+__device__ __forceinline__ void topk_write(int my_e, uint32_t my_key, int k, int t, int32_t* idx, float* wts,
+                                           int* idx_smem) {
+  const int lane = threadIdx.x & 31;
+  const float val = key_logit(my_key);
+  const float m = __shfl_sync(0xFFFFFFFFu, val, 0);
+  const float ex = lane < k ? expf(val - m) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_e;
+    wts[(size_t)t * k + lane] = ex / sum;
+    if (idx_smem) idx_smem[t * k + lane] = my_e;
+  }
+}
+
 // Selection of the k largest keys among the E logits held as PER keys per lane (logit e in
 // lane e % 32, slot e / 32), then the renormalised gate weights; one warp, one token. Each
 // candidate is the 64-bit value (key, ~e): a larger value is a larger logit, or an equal one
@@ -98,17 +116,54 @@ __device__ __forceinline__ void select_topk_warp(uint32_t (&key)[PER], int E, in
       my_key = mk;
     }
   }
-  const float val = key_logit(my_key);
-  const float m = __shfl_sync(0xFFFFFFFFu, val, 0);
-  const float ex = lane < k ? expf(val - m) : 0.0f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-  if (lane < k) {
-    idx[(size_t)t * k + lane] = my_e;
-    wts[(size_t)t * k + lane] = ex / sum;
-    if (idx_smem) idx_smem[t * k + lane] = my_e;
+  topk_write(my_e, my_key, k, t, idx, wts, idx_smem);
+}
+
+// The same selection by every warp of a block at once, for one token whose logits are in
+// shared memory (lg[0, E), E <= 32 * warps, k <= 32): warp w takes the k largest of experts
+// 32w..32w+31 in k rounds of two warp max reductions (one candidate per lane) and lists them
+// best first in cand[w * k ..]; then warp 0 merges the lists, lane l following list l, each
+// round popping the largest head. Every round of both levels takes the largest remaining
+// (key, ~e), so the experts come out in the order select_topk_warp gives, and topk_write
+// makes the weights: the outputs are identical. Returns with warp 0 done (no block barrier
+// after the write).
+__device__ __forceinline__ void select_topk_block(const float* lg, int E, int k, int t, int32_t* idx, float* wts,
+                                                  int* idx_smem, uint64_t* cand, bool* nan) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = (E + 31) / 32;
+  if (warp < nw) {
+    const int e = warp * 32 + lane;
+    uint64_t v = e < E ? ((uint64_t)logit_key(lg[e], nan) << 32) | (uint64_t)(~(uint32_t)e) : 0ull;
+    for (int j = 0; j < k; ++j) {
+      const uint32_t hk = (uint32_t)(v >> 32);
+      const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, hk);
+      const uint32_t lo = hk == mk ? (uint32_t)v : 0u;
+      const uint32_t ml = __reduce_max_sync(0xFFFFFFFFu, lo);
+      if (hk == mk && (uint32_t)v == ml) v = 0ull;  // the unique winner leaves
+      if (lane == 0) cand[warp * k + j] = ((uint64_t)mk << 32) | ml;
+    }
   }
+  __syncthreads();
+  if (warp != 0) return;
+  int ptr = 0;
+  uint64_t head = lane < nw ? cand[lane * k] : 0ull;
+  int my_e = 0;
+  uint32_t my_key = 0u;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t hk = (uint32_t)(head >> 32);
+    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, hk);
+    const uint32_t lo = hk == mk ? (uint32_t)head : 0u;
+    const uint32_t ml = __reduce_max_sync(0xFFFFFFFFu, lo);
+    if (hk == mk && (uint32_t)head == ml) {  // the winning list moves to its next candidate
+      ++ptr;
+      head = ptr < k ? cand[lane * k + ptr] : 0ull;
+    }
+    if (lane == j) {
+      my_e = (int)(~ml);
+      my_key = mk;
+    }
+  }
+  topk_write(my_e, my_key, k, t, idx, wts, idx_smem);
 }
 
 // ------------------------------------------------------------------ split-d GEMV ----------
@@ -413,11 +468,11 @@ __global__ void __launch_bounds__(512) topk_split_kernel(const float* __restrict
 
 // Decode routing tail as one cluster of T CTAs (T <= 8), CTA t for token t: bulk copies bring
 // the token's S split partial sums of the router GEMV, they are added in the fixed order of
-// topk_split_kernel, warp 0 selects the token's top k and writes the experts of its pairs into
-// CTA 0's shared memory (distributed shared memory); after the cluster barrier CTA 0 buckets
-// the T*k pairs with bucket_count_block. The outputs are those of topk_split_kernel followed by
+// topk_split_kernel, the block selects the token's top k (select_topk_block: every warp at
+// once) and warp 0 writes the experts of its pairs into CTA 0's shared memory (distributed
+// shared memory); after the cluster barrier CTA 0 buckets the T*k pairs with
+// bucket_count_block. The outputs are those of topk_split_kernel followed by
 // bucket_count_kernel, bit for bit, from one launch instead of two.
-template <int PER>
 __global__ void __launch_bounds__(512) route_tail_kernel(const float* __restrict__ partial, int S, int T, int E,
                                                           int k, int32_t* __restrict__ idx, float* __restrict__ wts,
                                                           float* __restrict__ logits_out, int32_t* counts,
@@ -428,6 +483,7 @@ __global__ void __launch_bounds__(512) route_tail_kernel(const float* __restrict
   __shared__ int ex[256];
   __shared__ int cs[512];
   __shared__ int warp_sums[33];
+  __shared__ uint64_t cand[512];
   __shared__ int nan_any;
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x, t = blockIdx.x;
@@ -455,15 +511,9 @@ __global__ void __launch_bounds__(512) route_tail_kernel(const float* __restrict
     if (v != v) nan_any = 1;
   }
   __syncthreads();
-  if (tid < 32) {
-    uint32_t key[PER];
+  {
     bool nan = false;
-#pragma unroll
-    for (int p = 0; p < PER; ++p) {
-      const int e = tid + 32 * p;
-      key[p] = e < E ? logit_key(lg[e], &nan) : 0u;
-    }
-    select_topk_warp<PER>(key, E, k, t, idx, wts, cluster.map_shared_rank(ex, 0));
+    select_topk_block(lg, E, k, t, idx, wts, cluster.map_shared_rank(ex, 0), cand, &nan);
   }
   if (tid == 0 && nan_any) flag_status(status, MOE_DEV_NAN_LOGIT_BIT);
   cluster.sync();  // every token's experts are in CTA 0's ex[]
@@ -533,17 +583,11 @@ cudaError_t launch_route_tail(const moe_shape& s, const float* partial, int spli
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-#define L_TAIL(P)                                                                                          \
-  do {                                                                                                     \
-    const cudaError_t e = ensure_dynamic_smem((const void*)route_tail_kernel<P>, smem);                    \
-    if (e != cudaSuccess) return e;                                                                        \
-    const cudaError_t e2 = cudaLaunchKernelEx(&cfg, route_tail_kernel<P>, partial, splits, s.T, s.E, s.k, idx, \
-                                              wts, logits_out, counts, offsets, sorted_pair, inv_pos, active, \
-                                              status);                                                     \
-    if (e2 != cudaSuccess) return e2;                                                                      \
-  } while (0)
-  MOE_TOPK_DISPATCH(L_TAIL);
-#undef L_TAIL
+  cudaError_t e = ensure_dynamic_smem((const void*)route_tail_kernel, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaLaunchKernelEx(&cfg, route_tail_kernel, partial, splits, s.T, s.E, s.k, idx, wts, logits_out, counts, offsets,
+                         sorted_pair, inv_pos, active, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
