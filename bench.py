@@ -595,7 +595,7 @@ def run_stack(args, ws, rank, local, w):
 
     dev = torch.device("cuda", local)
     K, W = args.steps, args.warmup
-    hbm_peak, _, peak_kind = peaks()
+    hbm_peak, _, _, peak_kind = peaks()
     need = w.layers * (w.E + w.n_shared) * w.record_bytes
     free, _ = torch.cuda.mem_get_info(dev)
     if need > free - (4 << 30):
@@ -648,17 +648,19 @@ def run_stack(args, ws, rank, local, w):
     step_bytes = [sum(layer_bytes[i % n_batches]) for i in range(K)]
     achieved = sum(step_bytes) / (sum(step_ms) / 1e3) / 1e9
 
-    # end to end: pinned x in, the eager stack through the public API, bf16 out back
+    # end to end: each step copies its pinned x into the step graph's input, replays the graph of
+    # the stack's calls and copies the bf16 output back, the stream synchronised
     x_host = [x.cpu().pin_memory() for x in xs]
     out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(xs[0])
     K_e2e = min(K, 50)
     e2e_s = 0.0
     for i in range(W + K_e2e):
+        b = i % n_batches
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        x_dev.copy_(x_host[i % n_batches], non_blocking=True)
-        out_host.copy_(st.forward(x_dev), non_blocking=True)
+        xs[b].copy_(x_host[b], non_blocking=True)
+        graphs[b].replay()
+        out_host.copy_(st.resid, non_blocking=True)
         torch.cuda.synchronize(dev)
         if i >= W:
             e2e_s += time.perf_counter() - t0
@@ -674,8 +676,8 @@ def run_stack(args, ws, rank, local, w):
                    "resident_gb": need / 1e9, "activations": "bf16 residual stream",
                    "l2": "inputs larger than L2 (each step reads every layer's selected experts, ~10 GB)",
                    "batches": n_batches, "mean_active_experts_per_layer": float(np.mean(n_active)),
-                   "launch": f"one CUDA graph of the {4 * w.layers} C-ABI calls of a step (norm, route, permute, "
-                             "expert FFN with the combine, per layer)",
+                   "launch": f"one CUDA graph of the {2 * w.layers} C-ABI calls of a step (per layer: moe_rms_norm, "
+                             "then moe_layer_forward: route, bucketing, expert FFN, combine)",
                    "block": "pre-norm residual: x + MoE(rms_norm(x)), eps 1e-6, no gain",
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"kernel": f"whole {w.layers}-layer step (route, permute, expert FFN, combine per layer)",
@@ -683,7 +685,8 @@ def run_stack(args, ws, rank, local, w):
                      "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
                      "bytes_per_step": float(np.mean(step_bytes)), "ms_per_step": sum(step_ms) / K},
         "e2e": {"value": ws * w.T * K_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
-                "d2h_bytes_per_step": w.T * w.d * 2, "steps": K_e2e, "launch": "eager C-ABI calls"},
+                "d2h_bytes_per_step": w.T * w.d * 2, "steps": K_e2e,
+                "launch": "per step: pinned x copied in, the step's CUDA graph, bf16 output copied out, stream synchronised"},
         "cpu_baseline": cpu,
         "gpu_launches": 5 * w.layers * K,  # per layer: norm, router GEMV, top-k with bucketing, expert FFN, combine
         "clocks": clk,

@@ -32,7 +32,8 @@ def main() -> None:
         raise SystemExit(f"{args.workload} is a multi-layer workload; profile one of its layers as 'decode'")
     dl = DeviceLayer(w)
     s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
-    buf = lay.alloc_buffers(s, ydt=L.MOE_F32, odt=L.MOE_BF16, keep_logits=False)
+    # y_perm as bench.py runs each workload: fp32 for decode, bf16 for prefill
+    buf = lay.alloc_buffers(s, ydt=L.MOE_BF16 if w.T > 16 else L.MOE_F32, odt=L.MOE_BF16, keep_logits=False)
     table = L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr, fmt=w.fmt)
     xs = [dl.x(b) for b in range(min(args.passes, 4))]
     for i in range(args.passes):
