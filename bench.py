@@ -486,7 +486,7 @@ def run_ours(args, ws, rank, local):
         nested = {"workload": wp.describe(), "value": ws * wp.T * 10 * rp["R"] / rp["total_s"], "unit": "tokens/s",
                   "steps": 10, "passes_per_step": rp["R"], "ms_per_pass": pcts(rp["pass_ms"]),
                   "roofline": roof_p, **extra_p, "clocks": rp["clocks"],
-                  "gpu_launches": 11 * 10 * rp["R"]}
+                  "gpu_launches": 12 * 10 * rp["R"]}
     nested_q2 = None
     if not prefill and not args.no_q2 and args.workload == "decode":
         # the same decode pass on 2-bit expert records (2.5 bits per weight)
@@ -499,6 +499,28 @@ def run_ours(args, ws, rank, local):
                      "record_bytes": wq.record_bytes, "steps": K, "passes_per_step": rq["R"],
                      "ms_per_pass": pcts(rq["pass_ms"]), "roofline": roof_q, **extra_q, "clocks": rq["clocks"],
                      "gpu_launches": 4 * K * rq["R"]}
+    nested_more = {}
+    if not prefill and not args.no_stack and args.workload == "decode":
+        # the 48-layer stack and the tiered slot pool, short runs, each line's own fields kept
+        import copy
+        keep = ("workload", "value", "unit", "steps", "warmup", "ms_per_step", "roofline", "e2e", "slot_pool",
+                "gpu_launches", "clocks")
+        runs = [("stack", "stack", dict(steps=10, warmup=3)),
+                ("tiered", "tiered", dict(steps=40, warmup=5, host_gb=8.0)),
+                ("tiered_count_warm_split", "tiered",
+                 dict(steps=40, warmup=5, host_gb=8.0, slot_policy="freq", warm_profile=True, pcie_frac=0.6,
+                      host_threads=8))]
+        for key, wname, over in runs:
+            torch.cuda.empty_cache()
+            sub_args = copy.copy(args)
+            sub_args.no_cpu_baseline = True
+            for k_, v_ in over.items():
+                setattr(sub_args, k_, v_)
+            wn = WORKLOADS[wname]
+            ln = (run_tiered if wn.slots else run_stack)(sub_args, ws, rank, local, wn, nested=True)
+            if ln is not None:
+                cfg = ln["config"]
+                nested_more[key] = {"workload": cfg["workload"], **{k_: ln[k_] for k_ in keep[1:] if k_ in ln}}
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_line(w, args)
@@ -525,14 +547,16 @@ def run_ours(args, ws, rank, local):
         "e2e": e2e,
         "cpu_baseline": cpu,
         # kernels per pass: decode 4 (router GEMV, top-k with bucketing, persistent expert FFN,
-        # combine); prefill 11 (router GEMM, top-k, 3 bucketing, 5 expert FFN, combine)
-        "gpu_launches": (11 if prefill else 4) * K * R,
+        # combine); prefill 12 (router weight split, router GEMM, top-k, 3 bucketing, 5 expert
+        # FFN, combine)
+        "gpu_launches": (12 if prefill else 4) * K * R,
         "clocks": r["clocks"],
     }
     if nested is not None:
         line["prefill"] = nested
     if nested_q2 is not None:
         line["decode_q2"] = nested_q2
+    line.update(nested_more)
     print(json.dumps(line), flush=True)
 
 
@@ -586,7 +610,7 @@ def stack_cpu_baseline(w, rank, args):
     return cpu_baseline_line(w, args)
 
 
-def run_stack(args, ws, rank, local, w):
+def run_stack(args, ws, rank, local, w, nested: bool = False):
     """L resident layers on a residual stream; one CUDA graph of the whole L-layer step."""
     import torch
     from routed_expert_ffn_bucketing_b300 import _lib as L
@@ -691,6 +715,8 @@ def run_stack(args, ws, rank, local, w):
         "gpu_launches": 5 * w.layers * K,  # per layer: norm, router GEMV, top-k with bucketing, expert FFN, combine
         "clocks": clk,
     }
+    if nested:
+        return line
     print(json.dumps(line), flush=True)
 
 
@@ -714,7 +740,7 @@ def _host_images(w, n_img: int, dev):
     return host
 
 
-def run_tiered(args, ws, rank, local, w):
+def run_tiered(args, ws, rank, local, w, nested: bool = False):
     """L layers, experts in pinned host memory, a device pool of w.slots slots; Zipf routing
     whose hot set drifts every few steps. Wall-clock tokens/s, hit rate and H2D GB/s."""
     import torch
@@ -866,6 +892,8 @@ def run_tiered(args, ws, rank, local, w):
         "gpu_launches": launches[0],
         "clocks": clk,
     }
+    if nested:
+        return line
     print(json.dumps(line), flush=True)
 
 
@@ -880,6 +908,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="decode: skip the nested prefill measurement")
     ap.add_argument("--no-q2", action="store_true", help="decode: skip the nested 2-bit-format measurement")
+    ap.add_argument("--no-stack", action="store_true",
+                    help="decode: skip the nested 48-layer stack and tiered slot-pool measurements")
     ap.add_argument("--host-gb", type=float, default=24.0, help="pinned host memory for expert images (tiered)")
     ap.add_argument("--slot-policy", choices=["lru", "freq"], default="lru",
                     help="tiered: replacement policy of the slot pool (LRU, or decayed use count)")
