@@ -44,10 +44,16 @@ ROT_LAYERS = 4         # decode: layers whose weights rotate between passes
 MIN_TIMED_MS = 300.0   # the K timed steps last at least this long
 MAX_ORACLE_WORKERS = 32
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernel,
-# from one ncu capture of the kernel as it is now built, or None when the kernel has changed
-# since its last capture.
-TRAFFIC = {"decode": None, "prefill": None}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant kernel, from one ncu
+# capture of the kernel as it is now built (None once the kernel has changed since). Decode: the
+# capture's bytes per expert record it streamed (41 records: 40 routed + the shared one, input
+# batch 2), scaled in the line by the records of an average launch. Prefill: the two GEMM launches
+# (gate/up + SwiGLU, down) of one pass at T = 8192.
+TRAFFIC = {
+    "decode": {"per_record": (206_294_528 + 3_836_672) / 41},
+    "decode_q2": {"per_record": (60_635_136 + 845_568) / 41},
+    "prefill": {"per_launch": 2_099_562_000 + 248_561_000 + 996_717_000 + 323_050_000},
+}
 
 
 def peaks():
@@ -579,7 +585,9 @@ def layer_roofline(w, r, hbm_peak, bf16_peak, bf16_sus, peak_kind):
                 "int8_peak": None,
                 "int8_note": "tcgen05.mma kind::i8 does not exist for sm_103a (ptxas: Feature '.kind::i8' not "
                              "supported on .target 'sm_103a'); the int8 codes enter f16 MMAs exactly",
-                "traffic": TRAFFIC["prefill"], "flops_per_launch": flops, "ms_per_launch": sum(ffn_ms) / n}
+                "traffic": (TRAFFIC["prefill"] or {}).get("per_launch"),
+                "traffic_kernels": "prefill_gemm_kernel<0> + <1> (ncu, one pass)",
+                "flops_per_launch": flops, "ms_per_launch": sum(ffn_ms) / n}
         extra = {"stages_ms": stages,
                  "router": {"ms": pcts(r["route_ms"])["median"], "flops": router_flops,
                             "tflops": router_flops / (np.median(r["route_ms"]) / 1e3) / 1e12,
@@ -591,7 +599,9 @@ def layer_roofline(w, r, hbm_peak, bf16_peak, bf16_sus, peak_kind):
         roof = {"kernel": "moe_expert_ffn (persistent kernel: gate/up + SwiGLU, down)", "bound": "hbm",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_kind": f"{peak_kind} copy bandwidth", "frac_of_8tbs": achieved / 8000.0,
-                "traffic": TRAFFIC["decode"], "bytes_per_launch": float(np.mean(byts)),
+                "traffic": (TRAFFIC.get(w.name) or {}).get("per_record", 0.0) * float(np.mean(r["n_active"]) + w.n_shared)
+                if TRAFFIC.get(w.name) else None,
+                "bytes_per_launch": float(np.mean(byts)),
                 "ms_per_launch": sum(ffn_ms) / n}
         router_bytes = w.d * w.E * 4
         step_bytes = [(na + w.n_shared) * w.record_bytes + small + router_bytes for na in r["n_active"]]
