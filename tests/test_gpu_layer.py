@@ -277,10 +277,12 @@ def test_fused_combine_is_bit_identical(wl, mode, residual, odt, ydt):
 
 @pytest.mark.parametrize("wl,T,E,k", [("decode", 4, 512, 10), ("decode", 1, 512, 10), ("decode", 16, 512, 10),
                                       ("tiny", 16, 16, 2), ("tiny", 7, 40, 5), ("decode", 16, 1024, 32),
-                                      ("tiny", 300, 64, 10)])
+                                      ("tiny", 300, 64, 10), ("decode", 8, 512, 32), ("tiny", 3, 36, 7)])
 def test_route_permute_is_bit_identical(wl, T, E, k):
     # moe_route_permute against moe_route followed by moe_permute: the same bits in every output,
-    # on shapes inside the one-kernel tail (T <= 16, T*k <= 256), at its edges and beyond it
+    # on shapes inside the one-kernel tail (T <= 8, T*k <= 256), at its edges and beyond it; the
+    # tail's block-wide selection with its largest candidate table (16 warps x k = 32) and with a
+    # warp holding fewer experts than k (E = 36)
     from routed_expert_ffn_bucketing_b300 import layer as lay
     w = custom(wl, T=T, E=E, k=k, n_shared=0, router_sigma=1.0)
     dl = DeviceLayer(w, fill="host" if w.d * w.f * (w.E + w.n_shared) < (1 << 26) else "device")
