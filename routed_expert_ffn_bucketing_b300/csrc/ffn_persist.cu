@@ -188,7 +188,7 @@ struct Ring {
 constexpr int kQ2Ahead = 4;  // groups of 2-bit codes a warp has requested ahead of the one it multiplies
 template <>
 struct Ring<8, 1> {
-  uint4 lo[kQ2Ahead], hi[kQ2Ahead];  // [0]: the group being multiplied
+  uint4 lo[kQ2Ahead], hi[kQ2Ahead];  // group G0 + m kQ2Ahead + q of a range at position q
 };
 
 // Requests group gs of task p: D blocks of both rows into the ring, and the 16 rows' D scales
@@ -528,102 +528,109 @@ __device__ __forceinline__ void p_stream_q2(const FfnArgs& A, const PAux& X, con
   int tl = -1;  // task of the group requested ahead
   PTask la = cur;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (long long G = G0; G < G1; ++G) {
-    const int gs = (int)(G - (long long)t * gpt);
-    cp_async_wait<kQ2Ahead - 1>();  // this group's scales have landed
-    __syncwarp();
-    if (cur.valid) {
-      const uint16_t* sp = sring_p + (size_t)((int)(G % kQ2Ahead) * 16) * 8;
-      const uint4 sa = *reinterpret_cast<const uint4*>(sp + g * 8);
-      const uint4 sb = *reinterpret_cast<const uint4*>(sp + (8 + g) * 8);
-      const uint32_t slo[4] = {sa.x, sa.y, sa.z, sa.w}, shi[4] = {sb.x, sb.y, sb.z, sb.w};
-      const uint32_t qlo[4] = {ring.lo[0].x, ring.lo[0].y, ring.lo[0].z, ring.lo[0].w};
-      const uint32_t qhi[4] = {ring.hi[0].x, ring.hi[0].y, ring.hi[0].z, ring.hi[0].w};
-      float4 c0, c1, xu;
+  // kQ2Ahead groups per outer step: group G0 + m kQ2Ahead + q sits at queue position q (as
+  // q2_prime placed the first ones), so every position is a fixed register set; the group
+  // requested kQ2Ahead ahead refills the position just consumed
+  for (long long Gb = G0; Gb < G1; Gb += kQ2Ahead) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int b = gs * 8 + j;
-        if ((j & 3) == 0) {
-          c0 = *reinterpret_cast<const float4*>(psm + cur.cs0 + b * 4);
-          c1 = *reinterpret_cast<const float4*>(psm + cur.cs1 + b * 4);
-          if (KIND == kGU) xu = *reinterpret_cast<const float4*>(psm + xe + b * 4);
-        }
-        const uint4 xv =
-            cur.has ? *reinterpret_cast<const uint4*>(psm + cur.xrow + b * kQBlock * 2) : make_uint4(0, 0, 0, 0);
-        const int jj = j & 3;
-        const float ca = jj == 0 ? c0.x : jj == 1 ? c0.y : jj == 2 ? c0.z : c0.w;
-        const float cb = jj == 0 ? c1.x : jj == 1 ? c1.y : jj == 2 ? c1.z : c1.w;
-        float dd[4];
-        const uint32_t wl = qlo[j >> 1], wh = qhi[j >> 1];
-        block_mma_q2(dd, (j & 1) ? (wl >> 16) : (wl & 0xFFFFu), (j & 1) ? (wh >> 16) : (wh & 0xFFFFu), xv, ca, cb);
-        const uint32_t sl = slo[j >> 1], sh = shi[j >> 1];
-        float s_lo = __half2float(__ushort_as_half((unsigned short)((j & 1) ? (sl >> 16) : (sl & 0xFFFFu))));
-        float s_hi = __half2float(__ushort_as_half((unsigned short)((j & 1) ? (sh >> 16) : (sh & 0xFFFFu))));
-        if (KIND == kGU) {
-          const float u = jj == 0 ? xu.x : jj == 1 ? xu.y : jj == 2 ? xu.z : xu.w;
-          s_lo *= u;
-          s_hi *= u;
-        }
-        acc[0] = fmaf(s_lo, dd[0], acc[0]);
-        acc[1] = fmaf(s_lo, dd[1], acc[1]);
-        acc[2] = fmaf(s_hi, dd[2], acc[2]);
-        acc[3] = fmaf(s_hi, dd[3], acc[3]);
-      }
-    }
-    // the queue moves one place; group G + kQ2Ahead goes to its end, its scales into the slot this
-    // group's scales occupied (every lane has read them)
-#pragma unroll
-    for (int i = 0; i + 1 < kQ2Ahead; ++i) {
-      ring.lo[i] = ring.lo[i + 1];
-      ring.hi[i] = ring.hi[i + 1];
-    }
-    __syncwarp();
-    const long long Gl = G + kQ2Ahead;
-    if (Gl < G1) {
-      const int tn = (int)(Gl / gpt);
-      if (tn != tl) {
-        tl = tn;
-        la = tl == t ? cur : make_task<KIND, 1>(A, items, rowtok, sx, sc, tl, lane);
-      }
-      q2_request(la, dhi, (int)(Gl - (long long)tl * gpt), ring.lo[kQ2Ahead - 1], ring.hi[kQ2Ahead - 1], sring_w,
-                 (int)(Gl % kQ2Ahead), lane);
-    } else {
-      cp_async_commit();
-    }
-    if (gs == gpt - 1 || G + 1 == G1) {
-      // the task ends in this range: finish it, or publish this part of a cut task
+    for (int q = 0; q < kQ2Ahead; ++q) {
+      const long long G = Gb + q;
+      if (G >= G1) break;
+      const int gs = (int)(G - (long long)t * gpt);
+      cp_async_wait<kQ2Ahead - 1>();  // this group's scales have landed
+      __syncwarp();
       if (cur.valid) {
-        const long long t0 = (long long)t * gpt;
-        const bool first = G0 <= t0, last = G1 >= t0 + gpt;
-        bool finish = true;
-        if (!(first && last)) {
-          const int my = first ? 0 : 1;
-          float4* slot_p = reinterpret_cast<float4*>(part + ((size_t)t * 2 + my) * 128);
-          slot_p[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-          __threadfence();
-          __syncwarp();
-          int second = 0;
-          if (lane == 0) {
-            second = atomicAdd(cnt + t, 1) == 1;
-            if (second) cnt[t] = 0;  // both parts are in: the counter is free for the next launch
+        const uint16_t* sp = sring_p + (size_t)((int)(G % kQ2Ahead) * 16) * 8;
+        const uint4 sa = *reinterpret_cast<const uint4*>(sp + g * 8);
+        const uint4 sb = *reinterpret_cast<const uint4*>(sp + (8 + g) * 8);
+        const uint32_t slo[4] = {sa.x, sa.y, sa.z, sa.w}, shi[4] = {sb.x, sb.y, sb.z, sb.w};
+        const uint32_t qlo[4] = {ring.lo[q].x, ring.lo[q].y, ring.lo[q].z, ring.lo[q].w};
+        const uint32_t qhi[4] = {ring.hi[q].x, ring.hi[q].y, ring.hi[q].z, ring.hi[q].w};
+        float4 c0, c1, xu;
+        float2 f_lo, f_hi;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int b = gs * 8 + j;
+          if ((j & 3) == 0) {
+            c0 = *reinterpret_cast<const float4*>(psm + cur.cs0 + b * 4);
+            c1 = *reinterpret_cast<const float4*>(psm + cur.cs1 + b * 4);
+            if (KIND == kGU) xu = *reinterpret_cast<const float4*>(psm + xe + b * 4);
           }
-          finish = __shfl_sync(0xFFFFFFFFu, second, 0) != 0;
-          if (finish) {
-            __threadfence();
-            const float4 p0 = __ldcg(reinterpret_cast<const float4*>(part + (size_t)t * 2 * 128) + lane);
-            const float4 p1 = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)t * 2 + 1) * 128) + lane);
-            acc[0] = p0.x + p1.x;
-            acc[1] = p0.y + p1.y;
-            acc[2] = p0.z + p1.z;
-            acc[3] = p0.w + p1.w;
+          if ((j & 1) == 0) {  // the scales of blocks j and j + 1, rows g and g + 8
+            f_lo = __half22float2(*reinterpret_cast<const __half2*>(&slo[j >> 1]));
+            f_hi = __half22float2(*reinterpret_cast<const __half2*>(&shi[j >> 1]));
           }
+          const uint4 xv =
+              cur.has ? *reinterpret_cast<const uint4*>(psm + cur.xrow + b * kQBlock * 2) : make_uint4(0, 0, 0, 0);
+          const int jj = j & 3;
+          const float ca = jj == 0 ? c0.x : jj == 1 ? c0.y : jj == 2 ? c0.z : c0.w;
+          const float cb = jj == 0 ? c1.x : jj == 1 ? c1.y : jj == 2 ? c1.z : c1.w;
+          float dd[4];
+          const uint32_t wl = qlo[j >> 1], wh = qhi[j >> 1];
+          block_mma_q2(dd, (j & 1) ? (wl >> 16) : (wl & 0xFFFFu), (j & 1) ? (wh >> 16) : (wh & 0xFFFFu), xv, ca, cb);
+          float s_lo = (j & 1) ? f_lo.y : f_lo.x;
+          float s_hi = (j & 1) ? f_hi.y : f_hi.x;
+          if (KIND == kGU) {
+            const float u = jj == 0 ? xu.x : jj == 1 ? xu.y : jj == 2 ? xu.z : xu.w;
+            s_lo *= u;
+            s_hi *= u;
+          }
+          acc[0] = fmaf(s_lo, dd[0], acc[0]);
+          acc[1] = fmaf(s_lo, dd[1], acc[1]);
+          acc[2] = fmaf(s_hi, dd[2], acc[2]);
+          acc[3] = fmaf(s_hi, dd[3], acc[3]);
         }
-        if (finish) p_epilogue<KIND>(A, X, cur, hexp, lane, acc, s_done);
       }
-      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-      if (G + 1 < G1) {
-        t = (int)((G + 1) / gpt);
-        cur = tl == t ? la : make_task<KIND, 1>(A, items, rowtok, sx, sc, t, lane);
+      // group G + kQ2Ahead goes to position q, its scales into the slot this group's scales
+      // occupied (every lane has read them)
+      __syncwarp();
+      const long long Gl = G + kQ2Ahead;
+      if (Gl < G1) {
+        const int tn = (int)(Gl / gpt);
+        if (tn != tl) {
+          tl = tn;
+          la = tl == t ? cur : make_task<KIND, 1>(A, items, rowtok, sx, sc, tl, lane);
+        }
+        q2_request(la, dhi, (int)(Gl - (long long)tl * gpt), ring.lo[q], ring.hi[q], sring_w, (int)(Gl % kQ2Ahead),
+                   lane);
+      } else {
+        cp_async_commit();
+      }
+      if (gs == gpt - 1 || G + 1 == G1) {
+        // the task ends in this range: finish it, or publish this part of a cut task
+        if (cur.valid) {
+          const long long t0 = (long long)t * gpt;
+          const bool first = G0 <= t0, last = G1 >= t0 + gpt;
+          bool finish = true;
+          if (!(first && last)) {
+            const int my = first ? 0 : 1;
+            float4* slot_p = reinterpret_cast<float4*>(part + ((size_t)t * 2 + my) * 128);
+            slot_p[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            __threadfence();
+            __syncwarp();
+            int second = 0;
+            if (lane == 0) {
+              second = atomicAdd(cnt + t, 1) == 1;
+              if (second) cnt[t] = 0;  // both parts are in: the counter is free for the next launch
+            }
+            finish = __shfl_sync(0xFFFFFFFFu, second, 0) != 0;
+            if (finish) {
+              __threadfence();
+              const float4 p0 = __ldcg(reinterpret_cast<const float4*>(part + (size_t)t * 2 * 128) + lane);
+              const float4 p1 = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)t * 2 + 1) * 128) + lane);
+              acc[0] = p0.x + p1.x;
+              acc[1] = p0.y + p1.y;
+              acc[2] = p0.z + p1.z;
+              acc[3] = p0.w + p1.w;
+            }
+          }
+          if (finish) p_epilogue<KIND>(A, X, cur, hexp, lane, acc, s_done);
+        }
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        if (G + 1 < G1) {
+          t = (int)((G + 1) / gpt);
+          cur = tl == t ? la : make_task<KIND, 1>(A, items, rowtok, sx, sc, t, lane);
+        }
       }
     }
   }
