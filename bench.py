@@ -516,7 +516,8 @@ def run_ours(args, ws, rank, local):
                 ("tiered", "tiered", dict(steps=40, warmup=5, host_gb=8.0)),
                 ("tiered_count_warm_split", "tiered",
                  dict(steps=40, warmup=5, host_gb=8.0, slot_policy="freq", warm_profile=True, pcie_frac=0.6,
-                      host_threads=8))]
+                      host_threads=8)),
+                ("tiered_q2", "tiered_q2", dict(steps=40, warmup=5, host_gb=8.0))]
         for key, wname, over in runs:
             torch.cuda.empty_cache()
             sub_args = copy.copy(args)
@@ -751,7 +752,7 @@ def _host_images(w, n_img: int, dev):
     while i < n_img:
         l, e = divmod(i, w.E)
         n = min(chunk, n_img - i, w.E - e)
-        fill_expert_records(w.seed, l, e, n, w.d, w.f, tmp.data_ptr(), rb, w.expert_sigma)
+        fill_expert_records(w.seed, l, e, n, w.d, w.f, tmp.data_ptr(), rb, w.expert_sigma, fmt=w.fmt)
         host[i:i + n].copy_(tmp[:n])
         i += n
     torch.cuda.synchronize(dev)
@@ -780,7 +781,7 @@ def run_tiered(args, ws, rank, local, w, nested: bool = False):
     for l in range(w.layers):
         t = torch.empty(max(w.n_shared, 1) * rb, dtype=torch.uint8, device=dev)
         if w.n_shared:
-            fill_expert_records(w.seed, l, w.E, w.n_shared, w.d, w.f, t.data_ptr(), rb, w.expert_sigma)
+            fill_expert_records(w.seed, l, w.E, w.n_shared, w.d, w.f, t.data_ptr(), rb, w.expert_sigma, fmt=w.fmt)
         shared.append(t)
     base = [torch.from_numpy(synth.router_weights_unscaled(w.seed, l, w.d, w.E, w.router_sigma)).to(dev)
             for l in range(w.layers)]
@@ -804,7 +805,7 @@ def run_tiered(args, ws, rank, local, w, nested: bool = False):
         for l in range(w.layers):
             profile[l * w.E + perms[l]] = freq
     ts = TieredStack(s, w.layers, routers, h_records, w.slots, rb, shared, device=dev, policy=policy,
-                     half_life_steps=args.half_life_steps, profile=profile)
+                     half_life_steps=args.half_life_steps, profile=profile, fmt=w.fmt)
     if args.host_threads:
         ts.host_threads = args.host_threads
     n_batches = 16
@@ -883,8 +884,10 @@ def run_tiered(args, ws, rank, local, w, nested: bool = False):
         "ms_per_step": 1e3 * wall / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE, "data": "synthetic (seeded)",
         "config": {"workload": w.describe() + f", {w.slots} device slots, drift every {synth.DRIFT_EVERY} steps",
-                   "tokens_per_step": w.T, "weights": "int8 block-32 + fp16 scales",
-                   "pool_gb": w.slots * rb / 1e9, "host_images": n_img,
+                   "tokens_per_step": w.T,
+                   "weights": "int8 block-32 + fp16 scales" if w.fmt == 0 else
+                              "2-bit block-32 codes + fp16 scales (2.5 bits per weight)",
+                   "record_bytes": rb, "pool_gb": w.slots * rb / 1e9, "host_images": n_img,
                    "host_mapping": "(l*E + e) mod host_images" if n_img < n_all else "one image per expert",
                    "timing": "wall clock per step (the host reads each layer's active list), x copied in and "
                              "the output copied out inside every step",

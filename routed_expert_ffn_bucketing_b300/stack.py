@@ -83,12 +83,18 @@ class TieredStack:
     With pcie_frac < 1 (the pages' bandwidth split of the miss path): of a layer's missed experts
     only the first pcie_frac share is copied; the host computes the rest from their pinned
     records (moe_host_expert_ffn) while the GPU runs the others, and their output rows are copied
-    into y_perm before the combine. Host-computed experts do not become resident."""
+    into y_perm before the combine. Host-computed experts do not become resident.
+
+    fmt: the record format of every expert (MOE_FMT_INT8, or MOE_FMT_Q2: 2-bit codes, 2.5 bits
+    per weight, so that the same pool bytes hold 3.4x more experts and a miss copies 3.4x fewer
+    bytes). slot_bytes is at least the format's record size."""
 
     def __init__(self, shape: L.moe_shape, n_layers: int, routers: list[torch.Tensor], h_records: list[int],
                  n_slots: int, slot_bytes: int, shared: list[torch.Tensor], device="cuda",
-                 policy: int = L.MOE_SLOT_LRU, half_life_steps: float = 50.0, profile=None):
+                 policy: int = L.MOE_SLOT_LRU, half_life_steps: float = 50.0, profile=None,
+                 fmt: int = L.MOE_FMT_INT8):
         self.shape, self.L, self.routers = shape, n_layers, routers
+        self.fmt = fmt
         self.shape_routed = L.shape(shape.T, shape.d, shape.f, shape.E, shape.k, 0)
         self.n_slots, self.slot_bytes = n_slots, slot_bytes
         self.pool = torch.empty(n_slots * slot_bytes, dtype=torch.uint8, device=device)
@@ -233,7 +239,7 @@ class TieredStack:
             if prefetch and l > 0:  # this layer's experts prefetched during the previous layer
                 stream.wait_event(self.pf_ready[l % 2])
             table = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l],
-                                   self.shared[l] if s.n_shared else None)
+                                   self.shared[l] if s.n_shared else None, fmt=self.fmt)
             # resid <- resid + MoE(n(resid)): the combine is fused into the expert-FFN call where the
             # layer makes only one
             comb = (b.inv_pos, b.topk_w, self.resid, self.resid, L.MOE_BF16)
@@ -245,7 +251,8 @@ class TieredStack:
                     if n_miss:
                         stream.wait_event(self.ready)
                         self.d_misses.copy_(self.h_misses, non_blocking=True)
-                        routed = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l], None)
+                        routed = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l], None,
+                                                fmt=self.fmt)
                         # the missed experts only (a shape without the shared expert, already done)
                         L.moe_expert_ffn(self.shape_routed, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, routed,
                                          b.offsets, b.sorted_pair, self.d_misses, b.y_perm, b.ydt, self.ws_miss,
@@ -257,7 +264,7 @@ class TieredStack:
                         t0 = time.perf_counter()
                         L.moe_host_expert_ffn(s, self.h_xn.data_ptr(), L.MOE_BF16, recs, ids.ctypes.data, n_host,
                                               self.h_offsets.data_ptr(), self.h_sorted.data_ptr(),
-                                              self.h_y.data_ptr(), L.MOE_FMT_INT8, self.host_threads)
+                                              self.h_y.data_ptr(), self.fmt, self.host_threads)
                         self.host_seconds += time.perf_counter() - t0
                         offs = self.h_offsets.numpy()
                         for e in ids:

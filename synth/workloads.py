@@ -7,8 +7,10 @@ for this path.
   stack    48 decode layers, router columns scaled for Zipf(1.1) popularity, residual stream
   prefill  T=8192 chunk, d=2048, f=768, E=512, top-10 + 1 shared, Zipf(1.1) routing
   tiered   the stack with a 4,500-slot device pool, the rest in pinned host memory
-Experts are N(0, 0.02) quantised to int8 blocks of 32 with fp16 scales. Activations are
-N(0, 1) rounded to bf16.
+  decode_q2, tiered_q2   decode and tiered with 2-bit expert records (2.5 bits per weight); the
+           tiered pool has the same bytes (22.56 GB), so 15,300 slots
+Experts are N(0, 0.02) quantised to int8 blocks of 32 with fp16 scales (or to the 2-bit format).
+Activations are N(0, 1) rounded to bf16.
 """
 from __future__ import annotations
 
@@ -84,6 +86,9 @@ WORKLOADS = {
     "stack": Workload("stack", 4, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1, layers=48, residual=True),
     "prefill": Workload("prefill", 8192, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1),
     "tiered": Workload("tiered", 4, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1, layers=48, residual=True, slots=4500),
+    # the same device pool bytes (4,500 x 5,013,504 B) holding 2-bit records of 1,474,560 B
+    "tiered_q2": Workload("tiered_q2", 4, 2048, 768, 512, 10, 1, 1.0, zipf_s=1.1, layers=48, residual=True,
+                          slots=15300, fmt=FMT_Q2),
     "decode_q2": Workload("decode_q2", 4, 2048, 768, 512, 10, 1, 1.0, fmt=FMT_Q2),
 }
 

@@ -199,3 +199,42 @@ def test_tiered_stack_misses_evictions_and_parity(overlap, freq, prefetch, pcie_
             assert np.array_equal(pool[slot * rb:(slot + 1) * rb], host[i].numpy())
     finally:
         ts.close()
+
+
+@pytest.mark.parametrize("pcie_frac", [1.0, 0.5])
+def test_tiered_stack_two_bit_records(pcie_frac):
+    # the tiered path on 2-bit expert records (2.5 bits per weight): slots of the 2-bit record
+    # size, misses copied and (pcie_frac < 1) computed on the host from 2-bit records; every
+    # layer against the oracle on the same dequantised weights
+    w = custom("stack", d=256, f=256, E=32, k=6, layers=2, T=4, fmt=synth.FMT_Q2)
+    n_slots = 24
+    rb = w.record_bytes
+    host = torch.empty((w.layers * w.E, rb), dtype=torch.uint8).pin_memory()
+    for l in range(w.layers):
+        for e in range(w.E):
+            host[l * w.E + e].copy_(torch.from_numpy(synth.pack_record(cached_expert(w, l, e))))
+    h_records = [host[i].data_ptr() for i in range(w.layers * w.E)]
+    dls = [DeviceLayer(w, layer=l) for l in range(w.layers)]
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    shared = [dl.pool[w.E * rb:(w.E + w.n_shared) * rb] for dl in dls]
+    ts = TieredStack(s, w.layers, [dl.router for dl in dls], h_records, n_slots, rb, shared, fmt=L.MOE_FMT_Q2)
+    n_host = 0
+    try:
+        for step in range(3):
+            keep = []
+            ts.forward(dls[0].x(step), keep=keep, pcie_frac=pcie_frac)
+            n_host += sum(ts.layer_host)
+            assert ts.status() == 0
+            torch.cuda.synchronize()
+            check_layers(w, keep, range(w.layers))
+        st = L.slot_table_stats(ts.table)
+        assert st.misses > 0 and st.evictions > 0
+        assert (n_host > 0) == (pcie_frac < 1.0)
+        snap = np.zeros(w.layers * w.E, dtype=np.int32)
+        L.slot_table_snapshot(ts.table, snap.ctypes.data)
+        pool = ts.pool.cpu().numpy()
+        for i in np.nonzero(snap >= 0)[0][:8]:
+            slot = int(snap[i])
+            assert np.array_equal(pool[slot * rb:(slot + 1) * rb], host[i].numpy())
+    finally:
+        ts.close()
