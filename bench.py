@@ -804,8 +804,10 @@ def run_tiered(args, ws, rank, local, w, nested: bool = False):
         profile = np.zeros(n_all, dtype=np.float32)
         for l in range(w.layers):
             profile[l * w.E + perms[l]] = freq
+    # the library's executor runs the step (moe_tiered_forward); early routing needs the Python loop
+    native = not args.prefetch and not args.python_loop
     ts = TieredStack(s, w.layers, routers, h_records, w.slots, rb, shared, device=dev, policy=policy,
-                     half_life_steps=args.half_life_steps, profile=profile, fmt=w.fmt)
+                     half_life_steps=args.half_life_steps, profile=profile, fmt=w.fmt, native=native)
     if args.host_threads:
         ts.host_threads = args.host_threads
     n_batches = 16
@@ -891,6 +893,7 @@ def run_tiered(args, ws, rank, local, w, nested: bool = False):
                    "host_mapping": "(l*E + e) mod host_images" if n_img < n_all else "one image per expert",
                    "timing": "wall clock per step (the host reads each layer's active list), x copied in and "
                              "the output copied out inside every step",
+                   "executor": "moe_tiered_forward (C++)" if native else "TieredStack Python loop",
                    "parallelism": f"replicas x{ws}"},
         "slot_pool": {"policy": "LRU" if policy == L.MOE_SLOT_LRU else
                       f"decayed use count (half-life {args.half_life_steps:g} steps)",
@@ -943,6 +946,8 @@ def main():
                     help="tiered: share of each layer's missed experts copied to the device; the host computes the rest")
     ap.add_argument("--host-threads", type=int, default=0,
                     help="tiered, pcie-frac < 1: threads of the host expert FFN (0: three quarters of the cores)")
+    ap.add_argument("--python-loop", action="store_true",
+                    help="tiered: run the step with TieredStack's Python loop instead of the library's executor")
     ap.add_argument("--prefetch-top", type=int, default=None,
                     help="tiered, prefetch: load only each token's first N predicted experts")
     args = ap.parse_args()

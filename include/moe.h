@@ -423,6 +423,49 @@ moe_status moe_host_expert_ffn(const moe_shape* shape, const void* h_x, moe_dtyp
                                const int32_t* h_offsets, const int32_t* h_sorted_pair, float* h_y, int32_t format,
                                int32_t n_threads);
 
+/* ------------------------------------------------------------------------------------
+ * Native executor of a tiered L-layer stack (all layers of one step in one call): per layer
+ * the RMS norm of the residual stream, routing and bucketing, the active list read back, the
+ * slot table's update (miss copies on the executor's own copy stream), the expert FFN of the
+ * hit experts and the shared expert while the copies run, the missed experts after them, and
+ * the combine into the residual stream ("Strata 工作原理图解GPU内存SSD三级存储如何让125B模型塞进
+ * 消费级显卡", sections "三级存储分工" and "专家缓存"). Optionally the bandwidth split of the
+ * miss path: the last floor((1 - pcie_frac) n) of a layer's n misses are computed on the host
+ * (moe_host_expert_ffn) instead of copied ("Strata 性能基准与论文导读125B MoE在消费级硬件上的极限
+ * 测量与瓶颈分析", section "如何测量"). The executor allocates its buffers (device and pinned
+ * host) at creation; a forward call allocates nothing.
+ * ------------------------------------------------------------------------------------ */
+typedef struct moe_tiered moe_tiered;
+
+/* shape: one layer (T, d, f, E, k, n_shared); routers: n_layers device pointers, fp32 [d][E];
+ * shared: n_layers device pointers to each layer's n_shared records (NULL when n_shared = 0);
+ * table, pool, slot_bytes, n_slots, slot_of: the slot table and the device pool and table
+ * [n_layers][E] it manages (the caller owns them and keeps them alive); h_records: the
+ * n_layers * E pinned host records, (layer, expert) order; format: MOE_FMT_INT8 or MOE_FMT_Q2;
+ * eps: the RMS norm's epsilon. MOE_EINVAL for a NULL pointer, a bad shape or slot size. */
+moe_status moe_tiered_create(const moe_shape* shape, int32_t n_layers, const float* const* routers,
+                             const void* const* shared, moe_slot_table* table, void* pool, uint64_t slot_bytes,
+                             uint64_t n_slots, int32_t* slot_of, const void* const* h_records, int32_t format,
+                             float eps, moe_tiered** out);
+
+/* The bandwidth split: pcie_frac in [0, 1] (1: every miss is copied, the default) and the host
+ * threads of the host expert FFN (0: the OpenMP default). MOE_EINVAL otherwise. */
+moe_status moe_tiered_set_split(moe_tiered* t, double pcie_frac, int32_t host_threads);
+
+/* One step: every layer on the residual stream resid (device bf16 [T][d], updated in place),
+ * launched on `stream`. The host waits once per layer for that layer's routing (the active
+ * list); the call returns with the last layer's work enqueued. h_layer_misses / h_layer_host
+ * (optional, host int32 [n_layers]): each layer's copied misses and host-computed experts. */
+moe_status moe_tiered_forward(moe_tiered* t, void* resid, moe_stream_t stream, int32_t* h_layer_misses,
+                              int32_t* h_layer_host);
+
+/* Waits for `stream`; *h_status = the OR of the device status words of the executor's
+ * workspaces. MOE_OK when zero, MOE_EDEVICE if not. */
+moe_status moe_tiered_status(moe_tiered* t, moe_stream_t stream, int32_t* h_status);
+
+/* Waits for the executor's copy stream and frees its buffers. NULL is accepted. */
+moe_status moe_tiered_destroy(moe_tiered* t);
+
 /* Residency of experts of one layer: h_slot[i] (host) = the slot of expert h_ids[i] of `layer`, or
  * -1 when it is not resident. No state changes. MOE_EINVAL for a bad layer or id. */
 moe_status slot_table_lookup(const moe_slot_table* table, int32_t layer, const int32_t* h_ids, int32_t n,

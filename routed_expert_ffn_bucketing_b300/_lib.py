@@ -86,6 +86,12 @@ _SIGS = {
                                       C.c_int32]),
     "slot_table_snapshot": (C.c_int, [_P, _P]),
     "slot_table_destroy": (C.c_int, [_P]),
+    "moe_tiered_create": (C.c_int, [C.POINTER(moe_shape), C.c_int32, _P, _P, _P, _P, C.c_uint64, C.c_uint64, _P, _P,
+                                    C.c_int32, C.c_float, C.POINTER(_P)]),
+    "moe_tiered_set_split": (C.c_int, [_P, C.c_double, C.c_int32]),
+    "moe_tiered_forward": (C.c_int, [_P, _P, _P, _P, _P]),
+    "moe_tiered_status": (C.c_int, [_P, _P, C.POINTER(C.c_int32)]),
+    "moe_tiered_destroy": (C.c_int, [_P]),
 }
 
 _lib = None
@@ -313,3 +319,37 @@ def slot_table_snapshot(table, h_out) -> None:
 
 def slot_table_destroy(table) -> None:
     _check(lib().slot_table_destroy(table), "slot_table_destroy")
+
+
+def moe_tiered_create(s, n_layers, routers, shared, table, pool, slot_bytes, n_slots, slot_of, h_records,
+                      fmt=MOE_FMT_INT8, eps=1e-6) -> int:
+    """routers / shared: sequences of n_layers device tensors or addresses (shared may be None
+    when s.n_shared == 0); h_records: n_layers * E host addresses. Returns the opaque handle."""
+    r = (C.c_void_p * n_layers)(*[ptr(x) for x in routers])
+    sh = (C.c_void_p * n_layers)(*[ptr(x) for x in shared]) if shared is not None else None
+    rec = (C.c_void_p * len(h_records))(*h_records)
+    out = C.c_void_p()
+    _check(lib().moe_tiered_create(C.byref(s), n_layers, r, sh, table, ptr(pool), slot_bytes, n_slots, ptr(slot_of),
+                                   rec, fmt, eps, C.byref(out)), "moe_tiered_create")
+    return out.value
+
+
+def moe_tiered_set_split(t, pcie_frac: float, host_threads: int = 0) -> int:
+    return _check(lib().moe_tiered_set_split(t, pcie_frac, host_threads), "moe_tiered_set_split")
+
+
+def moe_tiered_forward(t, resid, stream=None, h_layer_misses=None, h_layer_host=None) -> int:
+    return _check(lib().moe_tiered_forward(t, ptr(resid), stream_handle(stream), h_layer_misses, h_layer_host),
+                  "moe_tiered_forward")
+
+
+def moe_tiered_status(t, stream=None) -> int:
+    v = C.c_int32()
+    st = lib().moe_tiered_status(t, stream_handle(stream), C.byref(v))
+    if st not in (MOE_OK, MOE_EDEVICE):
+        _check(st, "moe_tiered_status")
+    return v.value
+
+
+def moe_tiered_destroy(t) -> int:
+    return _check(lib().moe_tiered_destroy(t), "moe_tiered_destroy")

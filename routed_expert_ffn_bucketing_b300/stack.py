@@ -87,12 +87,16 @@ class TieredStack:
 
     fmt: the record format of every expert (MOE_FMT_INT8, or MOE_FMT_Q2: 2-bit codes, 2.5 bits
     per weight, so that the same pool bytes hold 3.4x more experts and a miss copies 3.4x fewer
-    bytes). slot_bytes is at least the format's record size."""
+    bytes). slot_bytes is at least the format's record size.
+
+    native: forward() runs the library's executor (moe_tiered_forward: the same steps, overlap
+    mode, bit for bit, with the per-layer host work in C++) instead of this class's loop; keep,
+    prefetch and overlap=False need the loop."""
 
     def __init__(self, shape: L.moe_shape, n_layers: int, routers: list[torch.Tensor], h_records: list[int],
                  n_slots: int, slot_bytes: int, shared: list[torch.Tensor], device="cuda",
                  policy: int = L.MOE_SLOT_LRU, half_life_steps: float = 50.0, profile=None,
-                 fmt: int = L.MOE_FMT_INT8):
+                 fmt: int = L.MOE_FMT_INT8, native: bool = False):
         self.shape, self.L, self.routers = shape, n_layers, routers
         self.fmt = fmt
         self.shape_routed = L.shape(shape.T, shape.d, shape.f, shape.E, shape.k, 0)
@@ -155,12 +159,26 @@ class TieredStack:
             self.n_warm = L.slot_table_warm(self.table, w.ctypes.data, self.copy_stream.cuda_stream,
                                             self.ready.cuda_event)
             self.ready.synchronize()
+        self.native = None
+        self._split = None
+        if native:
+            self.native = L.moe_tiered_create(shape, n_layers, routers, shared if shape.n_shared else None, self.table,
+                                              self.pool, slot_bytes, n_slots, self.slot_of, self.h_records, fmt,
+                                              RMS_EPS)
+            self.h_layer_misses = np.zeros(n_layers, dtype=np.int32)
+            self.h_layer_host = np.zeros(n_layers, dtype=np.int32)
 
     def status(self) -> int:
         """The device status words of the workspaces, OR-ed (waits for the current stream)."""
-        return L.moe_read_status(self.buf.ws) | L.moe_read_status(self.ws_miss) | L.moe_read_status(self.pbuf.ws)
+        st = L.moe_read_status(self.buf.ws) | L.moe_read_status(self.ws_miss) | L.moe_read_status(self.pbuf.ws)
+        if self.native:
+            st |= L.moe_tiered_status(self.native)
+        return st
 
     def close(self):
+        if getattr(self, "native", None):
+            L.moe_tiered_destroy(self.native)
+            self.native = None
         if self.table:
             L.slot_table_destroy(self.table)
             self.table = None
@@ -175,6 +193,17 @@ class TieredStack:
         s, b = self.shape, self.buf
         stream = torch.cuda.current_stream()
         self.resid.copy_(x)
+        if self.native:
+            assert keep is None and not prefetch and overlap, "keep, prefetch and overlap=False need the Python loop"
+            if self._split != (pcie_frac, self.host_threads):
+                L.moe_tiered_set_split(self.native, pcie_frac, self.host_threads)
+                self._split = (pcie_frac, self.host_threads)
+            L.moe_tiered_forward(self.native, self.resid, stream, self.h_layer_misses.ctypes.data,
+                                 self.h_layer_host.ctypes.data)
+            self.layer_misses = self.h_layer_misses.tolist()
+            self.layer_host = self.h_layer_host.tolist()
+            self.layer_prefetched = []
+            return self.resid
         self.layer_misses = []
         self.layer_prefetched = []
         self.layer_host = []

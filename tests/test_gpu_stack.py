@@ -238,3 +238,46 @@ def test_tiered_stack_two_bit_records(pcie_frac):
             assert np.array_equal(pool[slot * rb:(slot + 1) * rb], host[i].numpy())
     finally:
         ts.close()
+
+
+@pytest.mark.parametrize("fmt,pcie_frac,freq", [(0, 1.0, False), (0, 0.5, False), (1, 1.0, True), (1, 0.5, False)])
+def test_tiered_native_executor_is_bit_identical(fmt, pcie_frac, freq):
+    # moe_tiered_forward (the library's executor: the per-layer host work in C++) against the
+    # Python loop of TieredStack, on two identical fresh stacks: the same outputs bit for bit, the
+    # same misses and host-computed experts per layer, the same slot-table counters
+    w = custom("stack", d=256, f=256, E=32, k=6, layers=3, T=4, fmt=fmt)
+    n_slots = 24
+    rb = w.record_bytes
+    host = torch.empty((w.layers * w.E, rb), dtype=torch.uint8).pin_memory()
+    for l in range(w.layers):
+        for e in range(w.E):
+            host[l * w.E + e].copy_(torch.from_numpy(synth.pack_record(cached_expert(w, l, e))))
+    h_records = [host[i].data_ptr() for i in range(w.layers * w.E)]
+    dls = [DeviceLayer(w, layer=l) for l in range(w.layers)]
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    shared = [dl.pool[w.E * rb:(w.E + w.n_shared) * rb] for dl in dls]
+    profile = np.random.default_rng(3).random(w.layers * w.E).astype(np.float32) if freq else None
+    runs = []
+    for native in (False, True):
+        ts = TieredStack(s, w.layers, [dl.router for dl in dls], h_records, n_slots, rb, shared, fmt=fmt,
+                         policy=L.MOE_SLOT_FREQ if freq else L.MOE_SLOT_LRU, half_life_steps=2.0, profile=profile,
+                         native=native)
+        ts.host_threads = 2
+        try:
+            outs, misses, hosts = [], [], []
+            for step in range(4):
+                outs.append(ts.forward(dls[0].x(step % 2), pcie_frac=pcie_frac).clone())
+                torch.cuda.synchronize()
+                assert ts.status() == 0
+                misses.append(list(ts.layer_misses))
+                hosts.append(list(ts.layer_host))
+            st = L.slot_table_stats(ts.table)
+            runs.append((outs, misses, hosts, (st.hits, st.misses, st.evictions, st.bytes_h2d)))
+        finally:
+            ts.close()
+    (o0, m0, h0, s0), (o1, m1, h1, s1) = runs
+    for a, b in zip(o0, o1):
+        assert torch.equal(a, b)
+    assert m0 == m1 and h0 == h1 and s0 == s1
+    assert sum(map(sum, m0)) > 0
+    assert (sum(map(sum, h0)) > 0) == (pcie_frac < 1.0)
