@@ -423,6 +423,15 @@ moe_status moe_host_expert_ffn(const moe_shape* shape, const void* h_x, moe_dtyp
                                const int32_t* h_offsets, const int32_t* h_sorted_pair, float* h_y, int32_t format,
                                int32_t n_threads);
 
+/* The resident experts of one layer's active list: out (device int32 [1 + n]) = [m, e...] with
+ * the experts e of active ([n, e_0 .. e_{n-1}], device) whose slot_of[e] (device int32 [E],
+ * one row of a slot table's device table) is >= 0, in active-list order. Launched on
+ * `stream`: run before the slot table's update of that layer, it lists the experts the update
+ * will count as hits, so their expert FFN can start before the host has read the active list.
+ * MOE_EINVAL for a NULL pointer, E <= 0 or out aliasing active. */
+moe_status moe_filter_resident(const int32_t* active, const int32_t* slot_of, int32_t E, int32_t* out,
+                               moe_stream_t stream);
+
 /* ------------------------------------------------------------------------------------
  * Native executor of a tiered L-layer stack (all layers of one step in one call): per layer
  * the RMS norm of the residual stream, routing and bucketing, the active list read back, the

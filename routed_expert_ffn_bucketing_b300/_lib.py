@@ -86,6 +86,7 @@ _SIGS = {
                                       C.c_int32]),
     "slot_table_snapshot": (C.c_int, [_P, _P]),
     "slot_table_destroy": (C.c_int, [_P]),
+    "moe_filter_resident": (C.c_int, [_P, _P, C.c_int32, _P, _P]),
     "moe_tiered_create": (C.c_int, [C.POINTER(moe_shape), C.c_int32, _P, _P, _P, _P, C.c_uint64, C.c_uint64, _P, _P,
                                     C.c_int32, C.c_float, C.POINTER(_P)]),
     "moe_tiered_set_split": (C.c_int, [_P, C.c_double, C.c_int32]),
@@ -353,3 +354,8 @@ def moe_tiered_status(t, stream=None) -> int:
 
 def moe_tiered_destroy(t) -> int:
     return _check(lib().moe_tiered_destroy(t), "moe_tiered_destroy")
+
+
+def moe_filter_resident(active, slot_of_row, E: int, out, stream=None) -> int:
+    return _check(lib().moe_filter_resident(ptr(active), ptr(slot_of_row), E, ptr(out), stream_handle(stream)),
+                  "moe_filter_resident")

@@ -530,6 +530,15 @@ moe_status moe_rms_norm(const moe_shape* shape, const void* x, moe_dtype xdt, vo
   return MOE_OK;
 }
 
+moe_status moe_filter_resident(const int32_t* active, const int32_t* slot_of, int32_t E, int32_t* out,
+                               moe_stream_t stream) {
+  if (!active || !slot_of || !out || E <= 0) return fail(MOE_EINVAL, "moe_filter_resident: NULL argument or E <= 0");
+  if (out == active) return fail(MOE_EINVAL, "moe_filter_resident: out must not alias active");
+  const cudaError_t e = launch_filter_resident(active, slot_of, E, out, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_filter_resident: launch");
+  return MOE_OK;
+}
+
 moe_status moe_set_wait_limit(uint64_t ns) {
   if (ns > kMaxWaitNs) return fail(MOE_EINVAL, "moe_set_wait_limit: %llu ns is above 10 s", (unsigned long long)ns);
   g_wait_ns.store(ns ? ns : kDefaultWaitNs, std::memory_order_relaxed);

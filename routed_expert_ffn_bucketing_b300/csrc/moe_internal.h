@@ -171,6 +171,9 @@ cudaError_t launch_topk(const moe_shape& s, const float* logits, int32_t* idx, f
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
                            uint32_t* keys, int* status, cudaStream_t st, bool pdl = false);
+// The resident experts (slot_of >= 0) of an active list, in order, as an active list.
+cudaError_t launch_filter_resident(const int32_t* active, const int32_t* slot_of, int E, int32_t* out,
+                                   cudaStream_t st);
 cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);  // fp32 SIMT (any x dtype)
 // Streaming tensor-core kernels (bf16 x); stream_supported() says whether the shape fits
 cudaError_t launch_ffn_stream(const FfnArgs& a, const StreamAux& x, int sm_count, cudaStream_t st);

@@ -200,6 +200,35 @@ __global__ void __launch_bounds__(CH) bucket_scatter_kernel(int P, const uint32_
   }
 }
 
+// The resident experts of an active list ([n, e_0, ..., e_{n-1}]), in the same order, as a list
+// of the same form: the experts whose slot_of entry is >= 0. One warp, ballots in chunks of 32.
+__global__ void __launch_bounds__(32) filter_resident_kernel(const int32_t* __restrict__ active,
+                                                             const int32_t* __restrict__ slot_of, int E,
+                                                             int32_t* __restrict__ out) {
+  const int lane = threadIdx.x;
+  const int n = active[0];
+  int m = 0;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    int e = -1;
+    bool res = false;
+    if (i < n) {
+      e = active[1 + i];
+      res = e >= 0 && e < E && slot_of[e] >= 0;
+    }
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, res);
+    if (res) out[1 + m + __popc(b & ((1u << lane) - 1u))] = e;
+    m += __popc(b);
+  }
+  if (lane == 0) out[0] = m;
+}
+
+cudaError_t launch_filter_resident(const int32_t* active, const int32_t* slot_of, int E, int32_t* out,
+                                   cudaStream_t st) {
+  filter_resident_kernel<<<1, 32, 0, st>>>(active, slot_of, E, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, int32_t* cnt,
                            uint32_t* keys, int* status, cudaStream_t st, bool pdl) {

@@ -3,10 +3,11 @@
 // "三级存储分工" and "专家缓存"). One moe_tiered_forward call runs every layer of one step:
 //
 //   per layer l: RMS norm of the residual stream; routing and bucketing (moe_route_permute);
-//   the active list back to the host; the slot table's update (its miss copies on the copy
-//   stream, `ready` recorded after them); the expert FFN of the hit experts and the shared
-//   expert while the copies are in flight; after the compute stream has waited on `ready`, the
-//   missed experts; the combine into the residual stream.
+//   the resident experts of the active list (moe_filter_resident) and, launched before the host
+//   has read anything back, the expert FFN of those hit experts and the shared expert; the
+//   active list back to the host, one event wait; the slot table's update (its miss copies on
+//   the copy stream, `ready` recorded after them); after the compute stream has waited on
+//   `ready`, the missed experts; the combine into the residual stream.
 //
 // With a bandwidth split (pcie_frac < 1, the pages' --pcie-frac: "Strata 性能基准与论文导读125B
 // MoE在消费级硬件上的极限测量与瓶颈分析", section "如何测量"), the last floor((1 - pcie_frac) n)
@@ -17,6 +18,8 @@
 // The steps and their order are those of the Python TieredStack (overlap mode), so both give
 // the same results bit for bit; this one keeps the per-layer host work (one event wait, the
 // slot update, the launches) in C++. The executor owns its buffers, allocated at creation.
+// The hit FFN reads only slots of this layer's resident experts, which the update never evicts
+// (its victims are never experts of the call), so it may run while the miss copies land.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -216,9 +219,19 @@ moe_status moe_tiered_forward(moe_tiered* t, void* resid, moe_stream_t stream_h,
     if ((e = (x)) != cudaSuccess) return cuda_err(e, what); \
   } while (0)
   for (int l = 0; l < t->L; ++l) {
+    moe_expert_table tab{};
+    tab.pool = t->pool;
+    tab.slot_bytes = t->slot_bytes;
+    tab.slot_of = t->slot_of + (size_t)l * E;
+    tab.shared = s.n_shared > 0 ? t->shared[l] : nullptr;
+    tab.n_slots = t->n_slots;
+    tab.format = (uint32_t)t->fmt;
     MOE_T_CALL(moe_rms_norm(&s, resid, MOE_BF16, t->xn, MOE_BF16, t->eps, stream));
     MOE_T_CALL(moe_route_permute(&s, t->xn, MOE_BF16, t->routers[l], t->topk_idx, t->topk_w, nullptr, t->counts,
                                  t->offsets, t->sorted_pair, t->inv_pos, t->active, t->ws, t->ws_bytes, stream));
+    // the experts resident now are the ones the slot update below counts as hits (the device
+    // table is current: every earlier update's entries were waited for, or changed nothing)
+    MOE_T_CALL(moe_filter_resident(t->active, tab.slot_of, E, t->d_hits, stream));
     MOE_T_CUDA(cudaMemcpyAsync(t->h_active, t->active, (size_t)cap1 * 4, cudaMemcpyDeviceToHost, stream), "active list");
     if (split) {  // what the host needs to compute experts itself
       MOE_T_CUDA(cudaMemcpyAsync(t->h_xn, t->xn, (size_t)s.T * s.d * 2, cudaMemcpyDeviceToHost, stream), "x copy");
@@ -227,9 +240,11 @@ moe_status moe_tiered_forward(moe_tiered* t, void* resid, moe_stream_t stream_h,
       MOE_T_CUDA(cudaMemcpyAsync(t->h_sorted, t->sorted_pair, (size_t)t->P * 4, cudaMemcpyDeviceToHost, stream),
                  "pairs copy");
     }
-    // the host needs the active list, and the previous layer's FFN must be done with the slots
-    // before any of them is overwritten: one event wait per layer
+    // the host waits for the routing and for the previous layer's FFN (no slot it read may be
+    // overwritten before); the hit experts' FFN, enqueued after the event, runs meanwhile
     MOE_T_CUDA(cudaEventRecord(t->done, stream), "event record");
+    MOE_T_CALL(moe_expert_ffn(&s, MOE_MODE_AUTO, t->xn, MOE_BF16, &tab, t->offsets, t->sorted_pair, t->d_hits,
+                              t->y_perm, MOE_F32, t->ws, t->ws_bytes, stream));
     MOE_T_CUDA(cudaEventSynchronize(t->done), "event wait");
     const int n = t->h_active[0];
     const int32_t* upd = t->h_active + 1;
@@ -262,47 +277,30 @@ moe_status moe_tiered_forward(moe_tiered* t, void* resid, moe_stream_t stream_h,
                                  t->h_misses + 1, t->h_misses, nullptr));
     const int n_miss = t->h_misses[0];
     if (h_layer_misses) h_layer_misses[l] = n_miss;
-    moe_expert_table tab{};
-    tab.pool = t->pool;
-    tab.slot_bytes = t->slot_bytes;
-    tab.slot_of = t->slot_of + (size_t)l * E;
-    tab.shared = s.n_shared > 0 ? t->shared[l] : nullptr;
-    tab.n_slots = t->n_slots;
-    tab.format = (uint32_t)t->fmt;
-    MOE_T_CUDA(cudaMemcpyAsync(t->d_hits, t->h_hits, (size_t)cap1 * 4, cudaMemcpyHostToDevice, stream), "hits copy");
-    if (n_miss || n_host) {
-      MOE_T_CALL(moe_expert_ffn(&s, MOE_MODE_AUTO, t->xn, MOE_BF16, &tab, t->offsets, t->sorted_pair, t->d_hits,
-                                t->y_perm, MOE_F32, t->ws, t->ws_bytes, stream));
-      if (n_miss) {
-        MOE_T_CUDA(cudaStreamWaitEvent(stream, t->ready, 0), "wait for the miss copies");
-        MOE_T_CUDA(cudaMemcpyAsync(t->d_misses, t->h_misses, (size_t)cap1 * 4, cudaMemcpyHostToDevice, stream),
-                   "misses copy");
-        moe_expert_table routed = tab;
-        routed.shared = nullptr;
-        // the missed experts only (a shape without the shared expert, already done)
-        MOE_T_CALL(moe_expert_ffn(&t->s_routed, MOE_MODE_AUTO, t->xn, MOE_BF16, &routed, t->offsets, t->sorted_pair,
-                                  t->d_misses, t->y_perm, MOE_F32, t->ws_miss, t->ws_miss_bytes, stream));
-      }
-      if (n_host) {
-        // meanwhile the host computes the rest of the misses, then their rows go in
-        for (int i = 0; i < n_host; ++i) t->h_host_recs[i] = t->h_records[(size_t)l * E + t->h_host[i]];
-        MOE_T_CALL(moe_host_expert_ffn(&s, t->h_xn, MOE_BF16, t->h_host_recs.data(), t->h_host.data(), n_host,
-                                       t->h_offsets, t->h_sorted, t->h_y, t->fmt, t->host_threads));
-        for (int i = 0; i < n_host; ++i) {
-          const int ex = t->h_host[i], r0 = t->h_offsets[ex], r1 = t->h_offsets[ex + 1];
-          if (r1 > r0)
-            MOE_T_CUDA(cudaMemcpyAsync(t->y_perm + (size_t)r0 * s.d, t->h_y + (size_t)r0 * s.d,
-                                       (size_t)(r1 - r0) * s.d * 4, cudaMemcpyHostToDevice, stream),
-                       "host rows copy");
-        }
-      }
-      MOE_T_CALL(moe_combine(&s, t->y_perm, MOE_F32, t->inv_pos, t->topk_w, resid, resid, MOE_BF16, stream));
-    } else {
-      MOE_T_CUDA(cudaStreamWaitEvent(stream, t->ready, 0), "wait for the copies");
-      MOE_T_CALL(moe_expert_ffn_combine(&s, MOE_MODE_AUTO, t->xn, MOE_BF16, &tab, t->offsets, t->sorted_pair,
-                                        t->d_hits, t->y_perm, MOE_F32, t->inv_pos, t->topk_w, resid, resid, MOE_BF16,
-                                        t->ws, t->ws_bytes, stream));
+    if (n_miss) {
+      MOE_T_CUDA(cudaStreamWaitEvent(stream, t->ready, 0), "wait for the miss copies");
+      MOE_T_CUDA(cudaMemcpyAsync(t->d_misses, t->h_misses, (size_t)cap1 * 4, cudaMemcpyHostToDevice, stream),
+                 "misses copy");
+      moe_expert_table routed = tab;
+      routed.shared = nullptr;
+      // the missed experts only (a shape without the shared expert, already done)
+      MOE_T_CALL(moe_expert_ffn(&t->s_routed, MOE_MODE_AUTO, t->xn, MOE_BF16, &routed, t->offsets, t->sorted_pair,
+                                t->d_misses, t->y_perm, MOE_F32, t->ws_miss, t->ws_miss_bytes, stream));
     }
+    if (n_host) {
+      // the host computes the rest of the misses, then their rows go in
+      for (int i = 0; i < n_host; ++i) t->h_host_recs[i] = t->h_records[(size_t)l * E + t->h_host[i]];
+      MOE_T_CALL(moe_host_expert_ffn(&s, t->h_xn, MOE_BF16, t->h_host_recs.data(), t->h_host.data(), n_host,
+                                     t->h_offsets, t->h_sorted, t->h_y, t->fmt, t->host_threads));
+      for (int i = 0; i < n_host; ++i) {
+        const int ex = t->h_host[i], r0 = t->h_offsets[ex], r1 = t->h_offsets[ex + 1];
+        if (r1 > r0)
+          MOE_T_CUDA(cudaMemcpyAsync(t->y_perm + (size_t)r0 * s.d, t->h_y + (size_t)r0 * s.d,
+                                     (size_t)(r1 - r0) * s.d * 4, cudaMemcpyHostToDevice, stream),
+                     "host rows copy");
+      }
+    }
+    MOE_T_CALL(moe_combine(&s, t->y_perm, MOE_F32, t->inv_pos, t->topk_w, resid, resid, MOE_BF16, stream));
   }
 #undef MOE_T_CALL
 #undef MOE_T_CUDA

@@ -68,9 +68,11 @@ class TieredStack:
 
     Per layer: route and bucket on the compute stream; read the active list on the host; update
     the slot table (miss copies on the copy stream, `ready` recorded after them). With overlap
-    (the default) the expert FFN then runs in two calls: the hit experts and the shared expert
-    first, while the copies are in flight, and the missed experts after the compute stream has
-    waited on `ready`. Without overlap one FFN call runs after the wait. Then the combine.
+    (the default) the expert FFN runs in two calls: the hit experts (those resident before the
+    update, listed on the device by moe_filter_resident) and the shared expert are launched right
+    after the routing, before the host has read the active list, so they compute during the host's
+    wait and the miss copies; the missed experts follow once the compute stream has waited on
+    `ready`. Without overlap one FFN call runs after the wait. Then the combine.
 
     With prefetch (early routing): right after layer l's routing, layer l+1's router is run on
     layer l's normalised input, which is close to layer l+1's own (the residual stream changes
@@ -223,14 +225,26 @@ class TieredStack:
                     self.h_pred.copy_(pb.active, non_blocking=True)
                 else:
                     self.h_pred_idx.copy_(pb.topk_idx, non_blocking=True)
+            table = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l],
+                                   self.shared[l] if s.n_shared else None, fmt=self.fmt)
+            if overlap:
+                if prefetch and l > 0:  # this layer's experts prefetched during the previous layer
+                    stream.wait_event(self.pf_ready[l % 2])
+                # the experts resident now: the ones the slot update below counts as hits
+                L.moe_filter_resident(b.active, self.slot_of[l], s.E, self.d_hits, stream)
             self.h_active.copy_(b.active, non_blocking=True)
             if split:  # what the host needs to compute experts itself
                 self.h_xn.copy_(self.xn, non_blocking=True)
                 self.h_offsets.copy_(b.offsets, non_blocking=True)
                 self.h_sorted.copy_(b.sorted_pair[:s.T * s.k], non_blocking=True)
             # the host needs the active list, and the previous layer's FFN must be done with the
-            # slots before any of them is overwritten: one event wait per layer
+            # slots before any of them is overwritten: one event wait per layer. With overlap, the
+            # hit experts' FFN (and the shared expert's), enqueued after the event, runs meanwhile:
+            # it reads only slots of this layer's resident experts, which the update never evicts
             self.done.record(stream)
+            if overlap:
+                L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
+                                 self.d_hits, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
             self.done.synchronize()
             n = int(self.h_active[0])
             hp, mp = self.h_hits.data_ptr(), self.h_misses.data_ptr()
@@ -265,47 +279,36 @@ class TieredStack:
                 self.layer_prefetched.append(
                     L.slot_table_prefetch(self.table, l + 1, pp, n_pf, l, self.h_active.data_ptr() + 4, n,
                                           self.copy_stream.cuda_stream, self.pf_ready[(l + 1) % 2].cuda_event))
-            if prefetch and l > 0:  # this layer's experts prefetched during the previous layer
-                stream.wait_event(self.pf_ready[l % 2])
-            table = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l],
-                                   self.shared[l] if s.n_shared else None, fmt=self.fmt)
             # resid <- resid + MoE(n(resid)): the combine is fused into the expert-FFN call where the
             # layer makes only one
             comb = (b.inv_pos, b.topk_w, self.resid, self.resid, L.MOE_BF16)
             if overlap:
-                self.d_hits.copy_(self.h_hits, non_blocking=True)
-                if n_miss or n_host:
-                    L.moe_expert_ffn(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
-                                     self.d_hits, b.y_perm, b.ydt, b.ws, b.ws_bytes, stream)
-                    if n_miss:
-                        stream.wait_event(self.ready)
-                        self.d_misses.copy_(self.h_misses, non_blocking=True)
-                        routed = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l], None,
-                                                fmt=self.fmt)
-                        # the missed experts only (a shape without the shared expert, already done)
-                        L.moe_expert_ffn(self.shape_routed, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, routed,
-                                         b.offsets, b.sorted_pair, self.d_misses, b.y_perm, b.ydt, self.ws_miss,
-                                         self.ws_miss.numel(), stream)
-                    if n_host:
-                        # meanwhile the host computes the rest of the misses, then their rows go in
-                        ids = self.h_host[:n_host]
-                        recs = [self.h_records[l * s.E + int(e)] for e in ids]
-                        t0 = time.perf_counter()
-                        L.moe_host_expert_ffn(s, self.h_xn.data_ptr(), L.MOE_BF16, recs, ids.ctypes.data, n_host,
-                                              self.h_offsets.data_ptr(), self.h_sorted.data_ptr(),
-                                              self.h_y.data_ptr(), self.fmt, self.host_threads)
-                        self.host_seconds += time.perf_counter() - t0
-                        offs = self.h_offsets.numpy()
-                        for e in ids:
-                            r0, r1 = int(offs[e]), int(offs[e + 1])
-                            b.y_perm[r0:r1].copy_(self.h_y[r0:r1], non_blocking=True)
-                    L.moe_combine(s, b.y_perm, b.ydt, *comb, stream)
-                else:
+                if n_miss:
                     stream.wait_event(self.ready)
-                    L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets,
-                                             b.sorted_pair, self.d_hits, b.y_perm, b.ydt, *comb, b.ws, b.ws_bytes,
-                                             stream)
+                    self.d_misses.copy_(self.h_misses, non_blocking=True)
+                    routed = L.expert_table(self.pool, self.slot_bytes, self.n_slots, self.slot_of[l], None,
+                                            fmt=self.fmt)
+                    # the missed experts only (a shape without the shared expert, already done)
+                    L.moe_expert_ffn(self.shape_routed, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, routed,
+                                     b.offsets, b.sorted_pair, self.d_misses, b.y_perm, b.ydt, self.ws_miss,
+                                     self.ws_miss.numel(), stream)
+                if n_host:
+                    # meanwhile the host computes the rest of the misses, then their rows go in
+                    ids = self.h_host[:n_host]
+                    recs = [self.h_records[l * s.E + int(e)] for e in ids]
+                    t0 = time.perf_counter()
+                    L.moe_host_expert_ffn(s, self.h_xn.data_ptr(), L.MOE_BF16, recs, ids.ctypes.data, n_host,
+                                          self.h_offsets.data_ptr(), self.h_sorted.data_ptr(),
+                                          self.h_y.data_ptr(), self.fmt, self.host_threads)
+                    self.host_seconds += time.perf_counter() - t0
+                    offs = self.h_offsets.numpy()
+                    for e in ids:
+                        r0, r1 = int(offs[e]), int(offs[e + 1])
+                        b.y_perm[r0:r1].copy_(self.h_y[r0:r1], non_blocking=True)
+                L.moe_combine(s, b.y_perm, b.ydt, *comb, stream)
             else:
+                if prefetch and l > 0:
+                    stream.wait_event(self.pf_ready[l % 2])
                 stream.wait_event(self.ready)
                 L.moe_expert_ffn_combine(s, L.MOE_MODE_AUTO, self.xn, L.MOE_BF16, table, b.offsets, b.sorted_pair,
                                          b.active, b.y_perm, b.ydt, *comb, b.ws, b.ws_bytes, stream)
