@@ -378,3 +378,23 @@ def test_expert_ffn_on_a_sparse_subset_of_experts():
     run = GpuRun(buf, 0, x.float().cpu().numpy().astype(np.float64))
     check_expert_rows(run, w, ids)
 
+
+
+@pytest.mark.parametrize("n,E", [(0, 16), (5, 16), (40, 512), (77, 512), (300, 1024)])
+def test_filter_resident_keeps_order_and_drops_missing(n, E):
+    # moe_filter_resident against the plain filter on the host: the active experts whose slot is
+    # >= 0, in active-list order, counted in element 0 (several 32-entry chunks for n > 32)
+    rng = np.random.default_rng(n + E)
+    ids = rng.choice(E, size=n, replace=False).astype(np.int32)
+    slot = np.where(rng.random(E) < 0.6, rng.integers(0, 1000, E), -1).astype(np.int32)
+    active = torch.tensor(np.concatenate([[n], ids]).astype(np.int32), device="cuda")
+    d_slot = torch.tensor(slot, device="cuda")
+    out = torch.full((1 + max(n, 1),), -7, dtype=torch.int32, device="cuda")
+    L.moe_filter_resident(active, d_slot, E, out)
+    torch.cuda.synchronize()
+    want = [int(e) for e in ids if slot[e] >= 0]
+    got = out.cpu().numpy()
+    assert got[0] == len(want)
+    assert got[1:1 + len(want)].tolist() == want
+    with pytest.raises(L.MoeError):
+        L.moe_filter_resident(active, d_slot, E, active)
