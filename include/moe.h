@@ -1,27 +1,34 @@
 /*
  * moe.h: C-ABI of the B300 (sm_103a) sparse MoE layer forward pass.
  *
- * One MoE layer's forward pass runs as five calls on one CUDA stream:
+ * One MoE layer's forward pass runs as four calls on one CUDA stream:
  *
  *   moe_route       router logits (fp32), top-k and renormalised gate weights
  *   moe_permute     bucketing: group the (token, slot) pairs by expert
- *   moe_expert_ffn  each selected expert's SwiGLU FFN over int8 block-32 weights, looked up
- *                   through the resident slot table, plus the always-on shared experts
+ *   moe_expert_ffn  each selected expert's SwiGLU FFN over int8 (or 2-bit) block-32 weights,
+ *                   looked up through the resident slot table, plus the always-on shared experts
  *   moe_combine     weighted sum of the expert outputs per token (unpermute)
- *   moe_expert_ffn_combine  the last two in one call
+ *
+ * or fused: moe_route_permute (the first two), moe_expert_ffn_combine (the last two),
+ * moe_layer_forward (all four in one call). Around them:
  *   moe_rms_norm    (stacks of layers) the normalised input of a pre-norm residual block
  *   slot_table_*    host-side slot pool for experts that do not all fit on the device: a miss
- *                   is copied from pinned host memory on a side stream
+ *                   is copied from pinned host memory on a side stream; early loading of a
+ *                   later layer's experts; residency lookups
+ *   moe_filter_resident  the resident experts of an active list, on the device
+ *   moe_host_expert_ffn  the expert FFN on the host CPU (the bandwidth split of the miss path)
+ *   moe_tiered_*    a native executor of a whole tiered L-layer step
+ *   moe_permute_static  bucketing without a caller workspace
  *
  * Sources. The pages on the Strata engine describe the method:
- *   [P5] "单张RTX 5090跑125B大模型：Strata实测Qwen3.8 Flash Next", section "MoE专家按需调度":
+ *   [run-5090] "单张RTX 5090跑125B大模型：Strata实测Qwen3.8 Flash Next", section "MoE专家按需调度":
  *        a light router picks the top-K experts per token and the other experts take no part;
  *        experts not selected can leave VRAM and are brought back when the router picks them.
- *   [P2] "Strata 工作原理图解GPU内存SSD三级存储如何让125B模型塞进消费级显卡":
+ *   [tiers] "Strata 工作原理图解GPU内存SSD三级存储如何让125B模型塞进消费级显卡":
  *        section "三级存储分工": router and shared expert resident in VRAM, all experts pinned in RAM;
  *        section "专家缓存": a VRAM expert cache of the most used experts; misses live in RAM;
  *        section "长文本": the next layer's experts stream over PCIe while the current layer computes.
- *   [P3] "Strata 性能基准与论文导读125B MoE在消费级硬件上的极限测量与瓶颈分析", section "瓶颈分析 1️⃣":
+ *   [bench] "Strata 性能基准与论文导读125B MoE在消费级硬件上的极限测量与瓶颈分析", section "瓶颈分析 1️⃣":
  *        quantised expert matmuls on tensor cores without a separate dequantisation pass.
  * The pages leave the FFN form, weight format, gate and tie-break open. The readings taken
  * here are: SwiGLU without biases; int8 codes with one fp16 scale per 32 elements of the
@@ -30,7 +37,8 @@
  *
  * Conventions for every call:
  *  - All pointers are DEVICE pointers unless the name starts with h_. The caller owns all
- *    memory, and the library allocates nothing on any of these calls.
+ *    memory, and the library allocates nothing on the calls of a pass (slot_table_create and
+ *    moe_tiered_create allocate their own state once, at creation).
  *  - Arrays are dense and row-major. x, y_perm, out, w_router and the workspace must be
  *    16-byte aligned (the workspace 256-byte aligned). Expert records are 256-byte aligned.
  *  - Calls are asynchronous on `stream` and return at once. A negative moe_status is a
@@ -139,7 +147,7 @@ moe_status moe_get_record_layout(int32_t d, int32_t f, int32_t format, moe_exper
  *             `format`; a zero-filled table means MOE_FMT_INT8)
  *  slot_bytes stride of the pool: >= record_bytes and a multiple of 256
  *  slot_of    device int32 [E]: slot of routed expert e, or -1 when it is not resident
- *             (the row of one layer of the slot table; [P2] "专家缓存")
+ *             (the row of one layer of the slot table; [tiers] "专家缓存")
  *  shared     device: n_shared records at shared + s * slot_bytes; NULL iff n_shared == 0
  *  n_slots    number of slots in the pool (> 0). A slot_of entry >= n_slots is an error
  *             (MOE_DEV_BAD_SLOT) and that expert's rows are not written.
@@ -163,7 +171,7 @@ typedef struct {
  * moe_route with that shape comes first. */
 moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes);
 
-/* Router and top-k ([P5] "MoE专家按需调度": the router picks the top-K experts per token).
+/* Router and top-k ([run-5090] "MoE专家按需调度": the router picks the top-K experts per token).
  *  x          [T][d], bf16 (xdt = MOE_BF16) or fp32 (MOE_F32)
  *  w_router   fp32 [d][E]
  *  topk_idx   out int32 [T][k]: the k experts with the largest fp32 logits, descending
@@ -179,7 +187,7 @@ moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const
                      moe_stream_t stream);
 
 /* Bucketing and permutation of the P = T*k pairs by expert, so that each selected expert's
- * weights are streamed once for all of its tokens ([P2] "专家缓存": the GPU computes the
+ * weights are streamed once for all of its tokens ([tiers] "专家缓存": the GPU computes the
  * experts the cache holds). Deterministic and free of atomics.
  *  topk_idx    int32 [T][k]; pair p = t*k + j routes token t to expert topk_idx[p]
  *  counts      out int32 [E]: pairs routed to each expert
@@ -222,9 +230,9 @@ moe_status moe_permute_static(const moe_shape* shape, const int32_t* topk_idx, i
                               int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos,
                               int32_t* active, int32_t* status, moe_stream_t stream);
 
-/* Expert FFN ([P5] "MoE专家按需调度": only the experts the router picked compute for a token;
- * [P2] "专家缓存": each is computed from its copy in the VRAM expert cache, found through the
- * slot table; [P2] "三级存储分工": the resident shared expert applies to every token): for
+/* Expert FFN ([run-5090] "MoE专家按需调度": only the experts the router picked compute for a token;
+ * [tiers] "专家缓存": each is computed from its copy in the VRAM expert cache, found through the
+ * slot table; [tiers] "三级存储分工": the resident shared expert applies to every token): for
  * every expert in `active` (and every shared expert), for each of its rows
  * y = W_down (silu(W_gate x) * (W_up x)), silu(z) = z / (1 + e^-z), W = q * s per block of 32.
  * The expert's record is found through the slot table (experts->slot_of).
@@ -266,8 +274,8 @@ moe_status moe_layer_forward(const moe_shape* shape, const void* x, moe_dtype xd
                              const void* residual_opt, void* out, moe_dtype odt, void* ws, size_t ws_bytes,
                              moe_stream_t stream);
 
-/* Combine / unpermute ([P5]: the token's output is the gated mixture of its selected
- * experts; [P2] "三级存储分工": the shared expert applies to every token):
+/* Combine / unpermute ([run-5090]: the token's output is the gated mixture of its selected
+ * experts; [tiers] "三级存储分工": the shared expert applies to every token):
  *   out[t] = sum_{j=0..k-1} topk_w[t][j] * y_perm[inv_pos[t*k+j]]
  *            + sum_s y_perm[P + s*T + t] + (residual_opt ? residual_opt[t] : 0)
  * summed in fp32 in exactly that order, then rounded once to odt (bf16: nearest-even).
@@ -307,10 +315,10 @@ const char* moe_last_error_string(void);
 
 /* ------------------------------------------------------------------------------------
  * Slot table: an expert cache for experts that do not all fit in device memory
- * ([P2] "专家缓存" and "三级存储分工": the most used experts stay in VRAM, all experts
- * sit pinned in host RAM; [P2] "长文本": expert copies overlap with computation).
+ * ([tiers] "专家缓存" and "三级存储分工": the most used experts stay in VRAM, all experts
+ * sit pinned in host RAM; [tiers] "长文本": expert copies overlap with computation).
  * The table keeps, on the host, the owner (layer, expert) of each of n_slots device slots,
- * their LRU order, and a decayed use count of every (layer, expert) ([P2] "专家缓存": the
+ * their LRU order, and a decayed use count of every (layer, expert) ([tiers] "专家缓存": the
  * cache starts from a ranking of expert use and adapts to what the session uses most). The
  * device table d_slot_of [L][E] lives in caller memory. Row `layer` of it is what
  * moe_expert_ffn reads through moe_expert_table.slot_of.
@@ -392,7 +400,7 @@ moe_status slot_table_prefetch_stats(const moe_slot_table* table, uint64_t* load
  * half-life is set), so the policy can change at any time. MOE_EINVAL otherwise. */
 moe_status slot_table_set_policy(moe_slot_table* table, int32_t policy, double half_life);
 
-/* Warm start from a usage profile ([P2] "专家缓存": a shipped ranking of expert use decides
+/* Warm start from a usage profile ([tiers] "专家缓存": a shipped ranking of expert use decides
  * which experts start in VRAM). h_weight: host float [L*E] of use weights (>= 0, finite;
  * one use = 1), added to the use counts. Then the empty slots, lowest index first, take the
  * non-resident experts of positive weight in decreasing order of use count (ties: lower
@@ -407,7 +415,7 @@ moe_status slot_table_set_policy(moe_slot_table* table, int32_t policy, double h
 moe_status slot_table_warm(moe_slot_table* table, const float* h_weight, moe_stream_t copy_stream,
                            moe_event_t ready, int32_t* n_loaded);
 
-/* Host computation of missed experts: the bandwidth split of the miss path ([P2] "专家缓存": the
+/* Host computation of missed experts: the bandwidth split of the miss path ([tiers] "专家缓存": the
  * experts a layer misses are divided between PCIe copies into the VRAM cache and computation
  * where their weights are, in host RAM; the share copied is the pages' --pcie-frac setting,
  * "Strata 性能基准与论文导读125B MoE在消费级硬件上的极限测量与瓶颈分析", section "如何测量"). Host
@@ -464,7 +472,9 @@ moe_status moe_tiered_set_split(moe_tiered* t, double pcie_frac, int32_t host_th
 /* One step: every layer on the residual stream resid (device bf16 [T][d], updated in place),
  * launched on `stream`. The host waits once per layer for that layer's routing (the active
  * list); the call returns with the last layer's work enqueued. h_layer_misses / h_layer_host
- * (optional, host int32 [n_layers]): each layer's copied misses and host-computed experts. */
+ * (optional, host int32 [n_layers]): each layer's copied misses and host-computed experts.
+ * An error returns at once with the layers before it enqueued and none after; kernels'
+ * errors are in the status words (moe_tiered_status). */
 moe_status moe_tiered_forward(moe_tiered* t, void* resid, moe_stream_t stream, int32_t* h_layer_misses,
                               int32_t* h_layer_host);
 
