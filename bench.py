@@ -678,7 +678,8 @@ def run_stack(args, ws, rank, local, w, nested: bool = False):
     dls = [DeviceLayer(w, layer=l, device=str(dev)) for l in range(w.layers)]
     s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
     st = DecodeStack(s, [LayerWeights(dl.router, L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of,
-                                                                dl.shared_ptr)) for dl in dls], device=dev)
+                                                                dl.shared_ptr)) for dl in dls], device=dev,
+                     native=not args.python_loop)
     n_batches = 4
     xs = [dls[0].x(b) for b in range(n_batches)]
     stream = torch.cuda.current_stream(dev)
@@ -757,8 +758,11 @@ def run_stack(args, ws, rank, local, w, nested: bool = False):
                    "resident_gb": need / 1e9, "activations": "bf16 residual stream",
                    "l2": "inputs larger than L2 (each step reads every layer's selected experts, ~10 GB)",
                    "batches": n_batches, "mean_active_experts_per_layer": float(np.mean(n_active)),
-                   "launch": f"one CUDA graph of the {2 * w.layers} C-ABI calls of a step (per layer: moe_rms_norm, "
-                             "then moe_layer_forward: route, bucketing, expert FFN, combine)",
+                   "launch": ("one CUDA graph of one moe_stack_forward call: per layer norm, router GEMV, top-k "
+                              "with bucketing, expert FFN, combine, all in one chain of programmatic dependents"
+                              if st.native else
+                              f"one CUDA graph of the {2 * w.layers} C-ABI calls of a step (per layer: moe_rms_norm, "
+                              "then moe_layer_forward: route, bucketing, expert FFN, combine)"),
                    "block": "pre-norm residual: x + MoE(rms_norm(x)), eps 1e-6, no gain",
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"kernel": f"whole {w.layers}-layer step (route, permute, expert FFN, combine per layer)",
@@ -986,7 +990,8 @@ def main():
     ap.add_argument("--host-threads", type=int, default=0,
                     help="tiered, pcie-frac < 1: threads of the host expert FFN (0: three quarters of the cores)")
     ap.add_argument("--python-loop", action="store_true",
-                    help="tiered: run the step with TieredStack's Python loop instead of the library's executor")
+                    help="stack / tiered: run the step as per-layer calls (stack) or with TieredStack's Python loop "
+                         "(tiered) instead of the library's executor")
     ap.add_argument("--prefetch-top", type=int, default=None,
                     help="tiered, prefetch: load only each token's first N predicted experts")
     args = ap.parse_args()

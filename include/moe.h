@@ -12,6 +12,7 @@
  * or fused: moe_route_permute (the first two), moe_expert_ffn_combine (the last two),
  * moe_layer_forward (all four in one call). Around them:
  *   moe_rms_norm    (stacks of layers) the normalised input of a pre-norm residual block
+ *   moe_stack_forward  L resident layers in one call (norm and layer per layer, one chain)
  *   slot_table_*    host-side slot pool for experts that do not all fit on the device: a miss
  *                   is copied from pinned host memory on a side stream; early loading of a
  *                   later layer's experts; residency lookups
@@ -295,6 +296,32 @@ moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt
  *  eps  finite and >= 0 (MOE_EINVAL otherwise). */
 moe_status moe_rms_norm(const moe_shape* shape, const void* x, moe_dtype xdt, void* out,
                         moe_dtype odt, float eps, moe_stream_t stream);
+
+/* A stack of n_layers resident MoE layers ([run-5090]: the router runs per layer of the
+ * transformer; [tiers] "三级存储分工": every layer's router and shared expert stay in VRAM),
+ * on the pre-norm residual reading of moe_rms_norm:
+ *   for l = 0 .. n_layers-1:  resid <- resid + MoE_l(rms_norm(resid))
+ * Each layer is moe_rms_norm(resid -> xn) followed by moe_layer_forward(xn, w_routers[l],
+ * experts[l], residual = out = resid), with the same results bit for bit. The library
+ * enqueues the whole chain itself, so from the second kernel on every kernel starts as a
+ * programmatic dependent of the one before it (layer l+1's norm overlaps the end of layer l's
+ * combine; the router overlaps the norm); each waits for its predecessor before touching
+ * memory that an earlier kernel uses.
+ *  n_layers    >= 0 (0, or T == 0: only the status word is cleared)
+ *  w_routers   HOST array of n_layers device pointers, each fp32 [d][E], 16-byte aligned
+ *  experts     HOST array of n_layers expert tables (see moe_expert_table)
+ *  resid       in/out [T][d] in rdt's type (MOE_BF16 or MOE_F32); xn: [T][d] rdt scratch that
+ *              holds the last layer's normalised input afterwards; neither may alias the other
+ *  eps         the RMS norm's eps (finite, >= 0)
+ *  topk_idx .. active, y_perm, ws: one set for all layers (as in moe_layer_forward); after the
+ *              call they hold the last layer's routing, bucketing and expert outputs
+ * The status word is cleared once, at the first layer, and gathers the flags of every layer.
+ * A host-side error at layer l returns at once; the earlier layers' kernels stay enqueued. */
+moe_status moe_stack_forward(const moe_shape* shape, int32_t n_layers, const float* const* w_routers,
+                             const moe_expert_table* experts, moe_mode mode, void* resid, moe_dtype rdt,
+                             float eps, void* xn, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                             int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int32_t* active,
+                             void* y_perm, moe_dtype ydt, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Limit of the bounded waits inside the expert-FFN kernels (a CTA waiting for work that other
  * CTAs or its own warps publish), in nanoseconds, for every moe_expert_ffn /

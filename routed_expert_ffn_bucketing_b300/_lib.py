@@ -69,6 +69,9 @@ _SIGS = {
     "moe_expert_ffn_combine": (C.c_int, [C.POINTER(moe_shape), C.c_int, _P, C.c_int, C.POINTER(moe_expert_table), _P,
                                          _P, _P, _P, C.c_int, _P, _P, _P, _P, C.c_int, _P, C.c_size_t, _P]),
     "moe_rms_norm": (C.c_int, [C.POINTER(moe_shape), _P, C.c_int, _P, C.c_int, C.c_float, _P]),
+    "moe_stack_forward": (C.c_int, [C.POINTER(moe_shape), C.c_int32, _P, C.POINTER(moe_expert_table), C.c_int, _P,
+                                    C.c_int, C.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_int, _P, C.c_size_t,
+                                    _P]),
     "moe_read_status": (C.c_int, [_P, _P, C.POINTER(C.c_int32)]),
     "moe_set_wait_limit": (C.c_int, [C.c_uint64]),
     "moe_last_error_string": (C.c_char_p, []),
@@ -221,6 +224,20 @@ def moe_combine(s, y_perm, ydt, inv_pos, topk_w, residual_opt, out, odt, stream=
 def moe_rms_norm(s, x, xdt, out, odt, eps: float, stream=None) -> int:
     return _check(lib().moe_rms_norm(C.byref(s), ptr(x), xdt, ptr(out), odt, C.c_float(eps), stream_handle(stream)),
                   "moe_rms_norm")
+
+
+def moe_stack_forward(s, routers, tables, mode, resid, rdt, eps: float, xn, topk_idx, topk_w, counts, offsets,
+                      sorted_pair, inv_pos, active, y_perm, ydt, ws, ws_bytes, stream=None) -> int:
+    """routers: n_layers device tensors (or addresses); tables: n_layers moe_expert_table."""
+    n = len(routers)
+    if len(tables) != n:
+        raise ValueError("moe_stack_forward: routers and tables differ in length")
+    r = (C.c_void_p * max(1, n))(*[ptr(x) for x in routers])
+    t = (moe_expert_table * max(1, n))(*tables)
+    return _check(lib().moe_stack_forward(C.byref(s), n, r, t, mode, ptr(resid), rdt, C.c_float(eps), ptr(xn),
+                                          ptr(topk_idx), ptr(topk_w), ptr(counts), ptr(offsets), ptr(sorted_pair),
+                                          ptr(inv_pos), ptr(active), ptr(y_perm), ydt, ptr(ws), ws_bytes,
+                                          stream_handle(stream)), "moe_stack_forward")
 
 
 def moe_read_status(ws, stream=None) -> int:

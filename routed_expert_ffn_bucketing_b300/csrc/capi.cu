@@ -230,9 +230,16 @@ moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
   return MOE_OK;
 }
 
-moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
-                     int32_t* topk_idx, float* topk_w, float* logits_opt, void* ws, size_t ws_bytes,
-                     moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// moe_route, with two options a stack of layers uses: pdl_gemv launches the split-d router GEMV as
+// a programmatic dependent of the kernel before it (the stack's RMS norm), and clear_status false
+// leaves the status word as the earlier layers left it.
+moe_status route_impl(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                      int32_t* topk_idx, float* topk_w, float* logits_opt, void* ws, size_t ws_bytes,
+                      moe_stream_t stream, bool pdl_gemv, bool clear_status) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   if ((st = check_dtype(xdt, "x")) != MOE_OK) return st;
@@ -247,7 +254,7 @@ moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const
   int* status = at<int>(ws, L.status);
   cudaError_t e;
   if (shape->T == 0) {
-    e = cudaMemsetAsync(status, 0, sizeof(int), s);
+    e = clear_status ? cudaMemsetAsync(status, 0, sizeof(int), s) : cudaSuccess;
     if (e != cudaSuccess) return cuda_fail(e, "moe_route: clearing the status word");
     return MOE_OK;
   }
@@ -256,19 +263,29 @@ moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const
   if (shape->T <= kRouteGemvMaxT) {
     float* partial = at<float>(ws, L.route_partial);
     e = launch_route_gemv(*shape, x, xdt, w_router, partial, status, at<uint8_t>(ws, L.zero), L.zero_end - L.zero,
-                          s);
+                          s, pdl_gemv, clear_status);
     if (e == cudaSuccess)
       e = launch_topk_split(*shape, partial, route_splits(shape->d), topk_idx, topk_w, logits_opt, status, s);
   } else {
     float* logits = logits_opt ? logits_opt : at<float>(ws, L.logits);
     if (route_tc_supported(*shape, xdt))
-      e = launch_route_tc(*shape, x, w_router, at<uint8_t>(ws, L.wparts), logits, status, s);
+      e = launch_route_tc(*shape, x, w_router, at<uint8_t>(ws, L.wparts), logits, status, s, clear_status);
     else
-      e = launch_route_gemm(*shape, x, xdt, w_router, logits, status, s);
+      e = launch_route_gemm(*shape, x, xdt, w_router, logits, status, s, clear_status);
     if (e == cudaSuccess) e = launch_topk(*shape, logits, topk_idx, topk_w, status, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "moe_route: launch");
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_route(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                     int32_t* topk_idx, float* topk_w, float* logits_opt, void* ws, size_t ws_bytes,
+                     moe_stream_t stream) {
+  return route_impl(shape, x, xdt, w_router, topk_idx, topk_w, logits_opt, ws, ws_bytes, stream, false, true);
 }
 
 moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
@@ -287,16 +304,22 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t*
   return MOE_OK;
 }
 
-moe_status moe_route_permute(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
-                             int32_t* topk_idx, float* topk_w, float* logits_opt, int32_t* counts, int32_t* offsets,
-                             int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, void* ws, size_t ws_bytes,
-                             moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// moe_route_permute with route_impl's two stack options.
+moe_status route_permute_impl(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                              int32_t* topk_idx, float* topk_w, float* logits_opt, int32_t* counts,
+                              int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, void* ws,
+                              size_t ws_bytes, moe_stream_t stream, bool pdl_gemv, bool clear_status) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   if ((st = check_dtype(xdt, "x")) != MOE_OK) return st;
   if ((st = check_ws(shape, ws, ws_bytes)) != MOE_OK) return st;
   if (shape->T == 0 || !route_tail_supported(*shape)) {
-    st = moe_route(shape, x, xdt, w_router, topk_idx, topk_w, logits_opt, ws, ws_bytes, stream);
+    st = route_impl(shape, x, xdt, w_router, topk_idx, topk_w, logits_opt, ws, ws_bytes, stream, pdl_gemv,
+                    clear_status);
     if (st != MOE_OK) return st;
     return moe_permute(shape, topk_idx, counts, offsets, sorted_pair, inv_pos, active, ws, ws_bytes, stream);
   }
@@ -309,12 +332,24 @@ moe_status moe_route_permute(const moe_shape* shape, const void* x, moe_dtype xd
   int* status = at<int>(ws, L.status);
   float* partial = at<float>(ws, L.route_partial);
   cudaError_t e = launch_route_gemv(*shape, x, xdt, w_router, partial, status, at<uint8_t>(ws, L.zero),
-                                    L.zero_end - L.zero, s);
+                                    L.zero_end - L.zero, s, pdl_gemv, clear_status);
   if (e == cudaSuccess)
     e = launch_route_tail(*shape, partial, route_splits(shape->d), topk_idx, topk_w, logits_opt, counts, offsets,
                           sorted_pair, inv_pos, active, status, s);
   if (e != cudaSuccess) return cuda_fail(e, "moe_route_permute: launch");
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_route_permute(const moe_shape* shape, const void* x, moe_dtype xdt, const float* w_router,
+                             int32_t* topk_idx, float* topk_w, float* logits_opt, int32_t* counts, int32_t* offsets,
+                             int32_t* sorted_pair, int32_t* inv_pos, int32_t* active, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+  return route_permute_impl(shape, x, xdt, w_router, topk_idx, topk_w, logits_opt, counts, offsets, sorted_pair,
+                            inv_pos, active, ws, ws_bytes, stream, false, true);
 }
 
 }  // extern "C"
@@ -495,6 +530,47 @@ moe_status moe_layer_forward(const moe_shape* shape, const void* x, moe_dtype xd
   const CombineReq cmb{inv_pos, topk_w, residual_opt, out, odt};
   return expert_ffn_impl(shape, mode, x, xdt, experts, offsets, sorted_pair, active, y_perm, ydt, ws, ws_bytes,
                          stream, &cmb, true);
+}
+
+moe_status moe_stack_forward(const moe_shape* shape, int32_t n_layers, const float* const* w_routers,
+                             const moe_expert_table* experts, moe_mode mode, void* resid, moe_dtype rdt,
+                             float eps, void* xn, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                             int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int32_t* active,
+                             void* y_perm, moe_dtype ydt, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_dtype(rdt, "resid")) != MOE_OK) return st;
+  if ((st = check_ws(shape, ws, ws_bytes)) != MOE_OK) return st;
+  if (n_layers < 0) return fail(MOE_EINVAL, "moe_stack_forward: n_layers %d < 0", (int)n_layers);
+  if (!(eps >= 0.0f) || !isfinite(eps)) return fail(MOE_EINVAL, "moe_stack_forward: eps must be finite and >= 0");
+  if (n_layers > 0 && (!w_routers || !experts)) return fail(MOE_EINVAL, "moe_stack_forward: NULL layer arrays");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(*shape);
+  if (shape->T == 0 || n_layers == 0) {
+    const cudaError_t e = cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_stack_forward: clearing the status word");
+    return MOE_OK;
+  }
+  if (!resid || !xn) return fail(MOE_EINVAL, "moe_stack_forward: NULL resid or xn");
+  if (!aligned(resid, 16) || !aligned(xn, 16)) return fail(MOE_EINVAL, "moe_stack_forward: misaligned resid or xn");
+  if (xn == resid) return fail(MOE_EINVAL, "moe_stack_forward: xn must not alias resid");
+  for (int32_t l = 0; l < n_layers; ++l) {
+    // resid <- resid + MoE_l(rms_norm(resid)). From the second layer on every kernel is a
+    // programmatic dependent of the one before it (each waits for its predecessor before it
+    // reads or writes anything that kernel, or an earlier one, touches), and the status word is
+    // kept, so after the call it holds the flags of every layer.
+    cudaError_t e = launch_rms_norm(*shape, resid, rdt, xn, rdt, eps, s, l > 0);
+    if (e != cudaSuccess)
+      return fail(MOE_ECUDA, "moe_stack_forward: RMS norm launch (layer %d): %s", (int)l, cudaGetErrorString(e));
+    st = route_permute_impl(shape, xn, rdt, w_routers[l], topk_idx, topk_w, nullptr, counts, offsets, sorted_pair,
+                            inv_pos, active, ws, ws_bytes, stream, true, l == 0);
+    if (st != MOE_OK) return st;
+    const CombineReq cmb{inv_pos, topk_w, resid, resid, rdt};
+    st = expert_ffn_impl(shape, mode, xn, rdt, &experts[l], offsets, sorted_pair, active, y_perm, ydt, ws, ws_bytes,
+                         stream, &cmb, true);
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
 }
 
 moe_status moe_combine(const moe_shape* shape, const void* y_perm, moe_dtype ydt, const int32_t* inv_pos,

@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(const void* x, int xdt, v
   __shared__ float wsum[8];
   __shared__ float inv_s;
   const int t = blockIdx.x;
+  pdl_trigger();  // the router may launch; it waits for this grid before reading out
+  pdl_wait();     // x from the kernel before (a layer's combine in a stack)
   const size_t row = (size_t)t * d;
   float ss = 0.0f;
   for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
@@ -125,9 +127,8 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(const void* x, int xdt, v
 }
 
 cudaError_t launch_rms_norm(const moe_shape& s, const void* x, int xdt, void* out, int odt, float eps,
-                            cudaStream_t st) {
-  rms_norm_kernel<<<s.T, 256, 0, st>>>(x, xdt, out, odt, s.d, eps);
-  return cudaGetLastError();
+                            cudaStream_t st, bool pdl) {
+  return launch_maybe_pdl(pdl, rms_norm_kernel, dim3(s.T), dim3(256), 0, st, x, xdt, out, odt, s.d, eps);
 }
 
 }  // namespace moe

@@ -143,10 +143,14 @@ struct PrefillAux {
 };
 
 // Launchers; each returns cudaSuccess or the launch error.
-// The router GEMV also sets *status to 0 and clears zero[0, zero_bytes) (16-byte aligned, a
-// multiple of 16 bytes) before any other kernel of the layer reads them.
+// The router GEMV also sets *status to 0 (unless clear_status is false: a stack keeps the word
+// across its layers) and clears zero[0, zero_bytes) (16-byte aligned, a multiple of 16 bytes)
+// before any other kernel of the layer reads them.
+// pdl: launched as a programmatic dependent of the kernel before it (the kernel waits for it
+// before reading x or clearing anything).
 cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
-                              int* status, void* zero, size_t zero_bytes, cudaStream_t st);
+                              int* status, void* zero, size_t zero_bytes, cudaStream_t st, bool pdl = false,
+                              bool clear_status = true);
 // Top-k from the router GEMV's split partial sums [splits][T][E]: one CTA per token.
 cudaError_t launch_topk_split(const moe_shape& s, const float* partial, int splits, int32_t* idx, float* wts,
                               float* logits_out, int* status, cudaStream_t st);
@@ -157,14 +161,14 @@ cudaError_t launch_route_tail(const moe_shape& s, const float* partial, int spli
                               float* logits_out, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
                               int32_t* inv_pos, int32_t* active, int* status, cudaStream_t st);
 // Router logits for T > 16 on the tensor cores (bf16 x; d a multiple of 256): the fp32 weights
-// split into three exact bf16 parts in `parts` (route_tc_parts_bytes), then a tcgen05 GEMM. Also
-// clears *status.
+// split into three exact bf16 parts in `parts` (route_tc_parts_bytes), then a tcgen05 GEMM. Both
+// this and the SIMT GEMM also clear *status when clear_status is true.
 bool route_tc_supported(const moe_shape& s, int xdt);
 size_t route_tc_parts_bytes(const moe_shape& s);
 cudaError_t launch_route_tc(const moe_shape& s, const void* x, const float* w, void* parts, float* logits, int* status,
-                            cudaStream_t st);
+                            cudaStream_t st, bool clear_status = true);
 cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const float* w, float* logits,
-                              int* status, cudaStream_t st);
+                              int* status, cudaStream_t st, bool clear_status = true);
 // Top-k of logits already summed (after the router GEMM): one warp per token.
 cudaError_t launch_topk(const moe_shape& s, const float* logits, int32_t* idx, float* wts, int* status,
                         cudaStream_t st);
@@ -195,6 +199,6 @@ cudaError_t launch_combine(const moe_shape& s, const void* y, int ydt, const int
                            const float* topk_w, const void* residual, void* out, int odt, cudaStream_t st,
                            bool pdl);
 cudaError_t launch_rms_norm(const moe_shape& s, const void* x, int xdt, void* out, int odt, float eps,
-                            cudaStream_t st);
+                            cudaStream_t st, bool pdl = false);
 
 }  // namespace moe

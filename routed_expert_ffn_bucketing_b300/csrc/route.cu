@@ -197,14 +197,19 @@ template <int TT, int VEC>
 __global__ void __launch_bounds__(256) router_gemv_kernel(const void* __restrict__ x, int xdt,
                                                           const float* __restrict__ w,
                                                           float* __restrict__ partial, int T, int d,
-                                                          int E, int* status, uint4* zero, int zero_n16) {
+                                                          int E, int* status, int clear_status, uint4* zero,
+                                                          int zero_n16) {
   constexpr int R = kRouteRowsPerSplit;  // rows of d per CTA
   pdl_trigger();  // the top-k kernel may launch now; it waits for this grid before reading
-  // this launch is ordered after every earlier kernel of the stream: clear the layer's status
-  // word and the expert FFN's counters here, so no memset precedes the pass
+  // launched as a programmatic dependent (a stack's RMS norm before it), this grid may start
+  // early: it waits for that kernel, and with it for every earlier kernel of the stream, before
+  // it reads x or clears anything (at once when launched normally)
+  pdl_wait();
+  // ordered after every earlier kernel of the stream: clear the layer's status word (unless a
+  // stack keeps it across layers) and the expert FFN's counters here, so no memset precedes the pass
   {
     const int cta = blockIdx.y * gridDim.x + blockIdx.x, n_cta = gridDim.x * gridDim.y;
-    if (cta == 0 && threadIdx.x == 0) *status = 0;
+    if (clear_status && cta == 0 && threadIdx.x == 0) *status = 0;
     for (int i = cta * blockDim.x + threadIdx.x; i < zero_n16; i += n_cta * blockDim.x) zero[i] = make_uint4(0, 0, 0, 0);
   }
   constexpr int COLS = 32 * VEC;         // experts per CTA
@@ -270,32 +275,33 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const void* __restrict
 
 template <int TT, int VEC>
 static cudaError_t gemv_launch(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
-                               int* status, void* zero, size_t zero_bytes, cudaStream_t st) {
+                               int* status, int clear, void* zero, size_t zero_bytes, cudaStream_t st, bool pdl) {
   constexpr int COLS = 32 * VEC;
   const size_t smem = sizeof(float) * (TT * kRouteRowsPerSplit + 8 * TT * COLS);
   auto kern = router_gemv_kernel<TT, VEC>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   dim3 grid((s.E + COLS - 1) / COLS, route_splits(s.d));
-  kern<<<grid, 256, smem, st>>>(x, xdt, w, partial, s.T, s.d, s.E, status, static_cast<uint4*>(zero),
-                                (int)(zero_bytes / 16));
-  return cudaGetLastError();
+  return launch_maybe_pdl(pdl, kern, grid, dim3(256), smem, st, x, xdt, w, partial, s.T, s.d, s.E, status, clear,
+                          static_cast<uint4*>(zero), (int)(zero_bytes / 16));
 }
 
 template <int VEC>
 static cudaError_t gemv_dispatch_t(const moe_shape& s, const void* x, int xdt, const float* w, float* p, int* status,
-                                   void* z, size_t zb, cudaStream_t st) {
-  if (s.T <= 1) return gemv_launch<1, VEC>(s, x, xdt, w, p, status, z, zb, st);
-  if (s.T <= 2) return gemv_launch<2, VEC>(s, x, xdt, w, p, status, z, zb, st);
-  if (s.T <= 4) return gemv_launch<4, VEC>(s, x, xdt, w, p, status, z, zb, st);
-  if (s.T <= 8) return gemv_launch<8, VEC>(s, x, xdt, w, p, status, z, zb, st);
-  return gemv_launch<16, VEC>(s, x, xdt, w, p, status, z, zb, st);
+                                   int c, void* z, size_t zb, cudaStream_t st, bool pdl) {
+  if (s.T <= 1) return gemv_launch<1, VEC>(s, x, xdt, w, p, status, c, z, zb, st, pdl);
+  if (s.T <= 2) return gemv_launch<2, VEC>(s, x, xdt, w, p, status, c, z, zb, st, pdl);
+  if (s.T <= 4) return gemv_launch<4, VEC>(s, x, xdt, w, p, status, c, z, zb, st, pdl);
+  if (s.T <= 8) return gemv_launch<8, VEC>(s, x, xdt, w, p, status, c, z, zb, st, pdl);
+  return gemv_launch<16, VEC>(s, x, xdt, w, p, status, c, z, zb, st, pdl);
 }
 
 cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const float* w, float* partial,
-                              int* status, void* zero, size_t zero_bytes, cudaStream_t st) {
-  if (s.E % 4 == 0) return gemv_dispatch_t<4>(s, x, xdt, w, partial, status, zero, zero_bytes, st);
-  return gemv_dispatch_t<1>(s, x, xdt, w, partial, status, zero, zero_bytes, st);
+                              int* status, void* zero, size_t zero_bytes, cudaStream_t st, bool pdl,
+                              bool clear_status) {
+  const int c = clear_status ? 1 : 0;
+  if (s.E % 4 == 0) return gemv_dispatch_t<4>(s, x, xdt, w, partial, status, c, zero, zero_bytes, st, pdl);
+  return gemv_dispatch_t<1>(s, x, xdt, w, partial, status, c, zero, zero_bytes, st, pdl);
 }
 
 // ------------------------------------------------------------------ tiled GEMM -------------
@@ -305,9 +311,9 @@ cudaError_t launch_route_gemv(const moe_shape& s, const void* x, int xdt, const 
 __global__ void __launch_bounds__(256) router_gemm_kernel(const void* __restrict__ x, int xdt,
                                                           const float* __restrict__ w,
                                                           float* __restrict__ out, int T, int d, int E,
-                                                          int* status) {
+                                                          int* status, int clear_status) {
   // ordered after every earlier kernel of the stream, and before the top-k that flags NaNs
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
+  if (clear_status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
   __shared__ __align__(16) float As[2][8][128];  // [k][token]
   __shared__ __align__(16) float Bs[2][8][128];  // [k][expert]
   const int tid = threadIdx.x;
@@ -391,9 +397,9 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const void* __restrict
 }
 
 cudaError_t launch_route_gemm(const moe_shape& s, const void* x, int xdt, const float* w, float* logits,
-                              int* status, cudaStream_t st) {
+                              int* status, cudaStream_t st, bool clear_status) {
   dim3 grid((s.E + 127) / 128, (s.T + 127) / 128);
-  router_gemm_kernel<<<grid, 256, 0, st>>>(x, xdt, w, logits, s.T, s.d, s.E, status);
+  router_gemm_kernel<<<grid, 256, 0, st>>>(x, xdt, w, logits, s.T, s.d, s.E, status, clear_status ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -75,11 +75,12 @@ __device__ __forceinline__ void r_set_abort(RHead& H, int* status) {
 }
 
 // parts[p][e][i] (bf16) for w[i][e] (fp32): 32 x 32 tiles through shared memory. Also clears the
-// status word: this kernel is the first of the layer on the stream.
+// status word (unless a stack keeps it across layers): this kernel is the first of the layer on
+// the stream.
 __global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ w, __nv_bfloat16* parts,
-                                                           int d, int E, int* status) {
+                                                           int d, int E, int* status, int clear_status) {
   __shared__ float tile[32][33];
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
+  if (clear_status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
   const int e0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows per pass
   for (int r = ty; r < 32; r += 8) {
@@ -239,7 +240,7 @@ bool route_tc_supported(const moe_shape& s, int xdt) {
 size_t route_tc_parts_bytes(const moe_shape& s) { return sizeof(__nv_bfloat16) * 3 * (size_t)s.E * s.d; }
 
 cudaError_t launch_route_tc(const moe_shape& s, const void* x, const float* w, void* parts, float* logits, int* status,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool clear_status) {
   CUtensorMap tm_x, tm_w;
   if (!tmap_encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)s.d, (uint64_t)s.T, (uint64_t)s.d * 2,
                       kRK, kRM, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -247,7 +248,7 @@ cudaError_t launch_route_tc(const moe_shape& s, const void* x, const float* w, v
                       (uint64_t)s.d * 2, kRK, kRN, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   router_split_kernel<<<dim3((s.E + 31) / 32, (s.d + 31) / 32), 256, 0, st>>>(
-      w, static_cast<__nv_bfloat16*>(parts), s.d, s.E, status);
+      w, static_cast<__nv_bfloat16*>(parts), s.d, s.E, status, clear_status ? 1 : 0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if ((e = ensure_dynamic_smem(reinterpret_cast<const void*>(router_tc_kernel), kRSmem)) != cudaSuccess) return e;

@@ -34,17 +34,27 @@ class LayerWeights:
 class DecodeStack:
     """L MoE layers run one after another on a residual stream of T tokens."""
 
-    def __init__(self, shape: L.moe_shape, layers: list[LayerWeights], device="cuda"):
+    def __init__(self, shape: L.moe_shape, layers: list[LayerWeights], device="cuda", native: bool = True):
         self.shape, self.layers = shape, layers
         self.buf = lay.alloc_buffers(shape, device=device, ydt=L.MOE_F32, odt=L.MOE_BF16, keep_logits=False)
         self.resid = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=device)
         self.xn = torch.empty_like(self.resid)
+        # native: one moe_stack_forward call runs every layer (one chain of programmatic
+        # dependents); otherwise a moe_rms_norm and a moe_layer_forward call per layer
+        self.native = native
 
     def forward(self, x: torch.Tensor, stream=None, keep: list | None = None) -> torch.Tensor:
         """Runs every layer on x (bf16 [T][d], left unchanged); returns the residual stream after
-        the last layer. With keep (a list), appends a copy of each layer's input and output."""
+        the last layer. With keep (a list), appends a copy of each layer's input and output
+        (that runs the per-layer calls)."""
         self.resid.copy_(x)
         s, b = self.shape, self.buf
+        if self.native and keep is None:
+            L.moe_stack_forward(s, [lw.router for lw in self.layers], [lw.table for lw in self.layers],
+                                L.MOE_MODE_AUTO, self.resid, L.MOE_BF16, RMS_EPS, self.xn, b.topk_idx, b.topk_w,
+                                b.counts, b.offsets, b.sorted_pair, b.inv_pos, b.active, b.y_perm, b.ydt, b.ws,
+                                b.ws_bytes, stream)
+            return self.resid
         for lw in self.layers:
             if keep is not None:
                 keep.append(("in", self.resid.clone()))

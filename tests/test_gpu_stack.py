@@ -111,6 +111,93 @@ def test_decode_stack_full_shape_three_layers():
         check_layers(w, keep, range(w.layers))
 
 
+def _stack_layers(w):
+    dls = [DeviceLayer(w, layer=l) for l in range(w.layers)]
+    s = L.shape(w.T, w.d, w.f, w.E, w.k, w.n_shared)
+    layers = [LayerWeights(dl.router, L.expert_table(dl.pool, dl.slot_bytes, dl.n_slots, dl.slot_of, dl.shared_ptr))
+              for dl in dls]
+    return dls, s, layers
+
+
+@pytest.mark.parametrize("full", [False, True])
+def test_stack_forward_is_bit_identical_to_layer_calls(full):
+    # moe_stack_forward (one chain of programmatic dependents over all layers) against the
+    # per-layer moe_rms_norm + moe_layer_forward calls, whose layers the oracle checks above: the
+    # same residual stream, routing and bucketing, bit for bit
+    w = custom("stack", layers=3) if full else custom("stack", d=256, f=128, E=32, k=4, layers=3)
+    dls, s, layers = _stack_layers(w)
+    per_layer = DecodeStack(s, layers, native=False)
+    chain = DecodeStack(s, layers, native=True)
+    for batch in (0, 1, 2):
+        x = dls[0].x(batch)
+        want = per_layer.forward(x).clone()
+        got = chain.forward(x).clone()
+        assert L.moe_read_status(chain.buf.ws) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(got, want), batch
+        for name in ("topk_idx", "topk_w", "counts", "offsets", "sorted_pair", "inv_pos"):
+            assert torch.equal(getattr(chain.buf, name), getattr(per_layer.buf, name)), (batch, name)
+        n = int(per_layer.buf.active[0])  # the list is [count, ids...]; the rest is not written
+        assert torch.equal(chain.buf.active[:1 + n], per_layer.buf.active[:1 + n]), batch
+        assert torch.equal(chain.xn, per_layer.xn)
+        # x itself is left unchanged
+        assert torch.equal(x, dls[0].x(batch))
+
+
+def test_stack_forward_keeps_every_layers_status():
+    # layer 0 has no resident slot for any routed expert (MOE_DEV_MISSING_SLOT; its routed rows
+    # are not written), the later layers are clean: the flag survives their router kernels,
+    # which clear the word in a single-layer call
+    w = custom("stack", d=256, f=128, E=32, k=4, layers=3)
+    dls, s, layers = _stack_layers(w)
+    missing = torch.full_like(dls[0].slot_of, -1)
+    d0 = dls[0]
+    layers[0] = LayerWeights(d0.router, L.expert_table(d0.pool, d0.slot_bytes, d0.n_slots, missing, d0.shared_ptr))
+    st = DecodeStack(s, layers, native=True)
+    st.buf.y_perm.zero_()
+    st.forward(dls[0].x(0))
+    assert L.moe_read_status(st.buf.ws) == L.MOE_DEV_MISSING_SLOT
+    # a clean stack clears it again at its first layer
+    clean = DecodeStack(s, [LayerWeights(d.router, L.expert_table(d.pool, d.slot_bytes, d.n_slots, d.slot_of,
+                                                                  d.shared_ptr)) for d in dls], native=True)
+    clean.buf = st.buf
+    clean.forward(dls[0].x(0))
+    assert L.moe_read_status(st.buf.ws) == 0
+
+
+def test_stack_forward_degenerate_and_bad_arguments():
+    w = custom("stack", d=256, f=128, E=32, k=4, layers=2)
+    dls, s, layers = _stack_layers(w)
+    st = DecodeStack(s, layers, native=True)
+    b = st.buf
+    x = dls[0].x(0)
+    st.resid.copy_(x)
+    # no layers: nothing but the status word is touched
+    L.moe_stack_forward(s, [], [], L.MOE_MODE_AUTO, st.resid, L.MOE_BF16, 1e-6, st.xn, b.topk_idx, b.topk_w,
+                        b.counts, b.offsets, b.sorted_pair, b.inv_pos, b.active, b.y_perm, b.ydt, b.ws, b.ws_bytes)
+    assert L.moe_read_status(b.ws) == 0
+    assert torch.equal(st.resid, x)
+    # T == 0
+    s0 = L.shape(0, w.d, w.f, w.E, w.k, w.n_shared)
+    L.moe_stack_forward(s0, [l.router for l in layers], [l.table for l in layers], L.MOE_MODE_AUTO, None,
+                        L.MOE_BF16, 1e-6, None, None, None, b.counts, b.offsets, None, None, b.active, None, b.ydt,
+                        b.ws, b.ws_bytes)
+    bad = [
+        dict(eps=-1.0),
+        dict(xn=st.resid),   # xn aliases resid
+        dict(rdt=7),
+    ]
+    for kw in bad:
+        args = dict(eps=1e-6, xn=st.xn, rdt=L.MOE_BF16)
+        args.update(kw)
+        with pytest.raises(L.MoeError):
+            L.moe_stack_forward(s, [l.router for l in layers], [l.table for l in layers], L.MOE_MODE_AUTO, st.resid,
+                                args["rdt"], args["eps"], args["xn"], b.topk_idx, b.topk_w, b.counts, b.offsets,
+                                b.sorted_pair, b.inv_pos, b.active, b.y_perm, b.ydt, b.ws, b.ws_bytes)
+    torch.cuda.synchronize()
+    assert torch.equal(st.resid, x)
+
+
 def test_tiered_step_full_width():
     # the tiered path at the full layer width (d = 2048, f = 768, top-10 + 1 shared): 2 layers of
     # 64 experts in pinned host memory, 48 device slots, so a step's two layers (about 36
