@@ -130,15 +130,16 @@ struct PersistAux {
 
 // Workspace buffers of the prefill (tensor-core GEMM) expert FFN.
 struct PrefillAux {
-  __half* xp16;       // [P + T*n_shared][d]: activation rows in expert order, f16, rescaled per token
+  __half* xp16;       // [P + T*n_shared][d]: activation rows in expert order, f16, rescaled per token,
+                      // each 64-element K step in the records' stored code order
   float* xunscale;    // [T]: 2^e of each token's rescale
   int32_t* xexp;      // [T]: e
   uint32_t* hmax;     // [P + T*n_shared]: bits of max |h| per row
   ItemRec* items;
   int32_t* row_tok;
-  __half* h16;        // [P + T*n_shared][f]: h rescaled per row (natural order)
+  __half* h16;        // [P + T*n_shared][f]: h rescaled per row, in the stored code order like xp16
   int32_t* hexp;      // [P + T*n_shared]
-  int2* tiles;        // M tiles: (item, first row within the item)
+  int2* tiles;        // token tiles of up to 128 rows: (item, first row within the item)
   int32_t* n_tiles;   // [1]
 };
 

@@ -208,11 +208,12 @@ def test_prefill_layer_full_size():
     assert n_checked >= w.T - 8
     check_bucketing(run, w)
     check_output(run, w, tokens=np.array([0, 1, 77, 1023, 3333, 4096, 5000, 8191]))
-    # whole experts' rows of y_perm, chosen to cover the GEMM's tile walk at full size (6
-    # column tiles of gate/up at f = 768, 8 of down at d = 2048): the heaviest Zipf expert
-    # (every one of its 128-row M tiles, the partial last one included), a mid-rank expert, the
-    # three experts with the fewest rows (one partial M tile each), the last three experts of
-    # the tile list, and the shared expert's first and last M tiles
+    # whole experts' rows of y_perm, chosen to cover the GEMM's tile walk at full size (12
+    # chunks of 64 columns of gate/up at f = 768, 16 of 128 rows of down at d = 2048): the
+    # heaviest Zipf expert (every one of its 128-row token tiles, the partial last one
+    # included), a mid-rank expert, the three experts with the fewest rows (one partial token
+    # tile each, N of 16), the last three experts of the tile list, and the shared expert's
+    # first and last token tiles
     counts = run.buf.counts.cpu().numpy()
     act = np.nonzero(counts)[0]
     heavy = int(act[np.argmax(counts[act])])
