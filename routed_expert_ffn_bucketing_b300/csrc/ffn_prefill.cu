@@ -49,7 +49,7 @@
 //            tensor memory) per stage, the commit that frees the stage's X and A slots, and the
 //            one that hands a finished accumulator to the epilogue.
 //   warps 12..15: epilogue. Tensor-memory lanes 32 q .. 32 q + 31 (q = warp % 4) are weight
-//            rows; tcgen05.ld 32 token columns at a time, the next load in flight while the
+//            rows; tcgen05.ld 16 token columns at a time, the next load in flight while the
 //            current columns are processed.
 // Activations enter as f16 exactly (bf16 has 8 significant bits; each row is rescaled by a power
 // of two that puts its max |x| in [2^14, 2^15)), and h is rescaled per row the same way.
@@ -705,22 +705,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
           }
         }
       };
-      // 32 columns per tcgen05.ld, two register sets: the next load is in flight while the
-      // current columns are processed (columns past n_cols are read, in bounds, and ignored)
-      uint32_t va[32], vb[32];
-      tmem_ld32(t_row, va);
-      tmem_ld_wait32(va);
-      for (int ch = 0; ch < n_cols; ch += 64) {
-        const bool more1 = ch + 32 < n_cols, more2 = ch + 64 < n_cols;
-        if (more1) tmem_ld32(t_row + ch + 32, vb);
+      // 16 columns per tcgen05.ld, two register sets: the next load is in flight while the
+      // current columns are processed. (Loads of 32 columns, two sets of 32 registers, made
+      // the FFN 1.11x slower: 115 registers per thread against 72.)
+      uint32_t va[16], vb[16];
+      tmem_ld16(t_row, va);
+      tmem_ld_wait16(va);
+      for (int ch = 0; ch < n_cols; ch += 32) {
+        const bool more1 = ch + 16 < n_cols, more2 = ch + 32 < n_cols;
+        if (more1) tmem_ld16(t_row + ch + 16, vb);
         process16(va, ch);
-        if (ch + 16 < n_cols) process16(va + 16, ch + 16);
         if (more1) {
-          tmem_ld_wait32(vb);
-          if (more2) tmem_ld32(t_row + ch + 64, va);
-          process16(vb, ch + 32);
-          if (ch + 48 < n_cols) process16(vb + 16, ch + 48);
-          if (more2) tmem_ld_wait32(va);
+          tmem_ld_wait16(vb);
+          if (more2) tmem_ld16(t_row + ch + 32, va);
+          process16(vb, ch + 16);
+          if (more2) tmem_ld_wait16(va);
         }
       }
       tc_fence_before();
