@@ -51,8 +51,8 @@ MAX_ORACLE_WORKERS = 32
 # (gate/up + SwiGLU, down) of one pass at T = 8192.
 TRAFFIC = {
     "decode": {"per_record": (206_294_528 + 3_836_672) / 41},
-    "decode_q2": {"per_record": (60_635_136 + 845_568) / 41},
-    "prefill": {"per_launch": 2_099_562_000 + 248_561_000 + 996_717_000 + 323_050_000},
+    "decode_q2": {"per_record": (60_700_928 + 694_272) / 41},
+    "prefill": {"per_launch": 2_091_546_000 + 250_737_408 + 1_000_237_000 + 326_405_376},
 }
 
 

@@ -171,7 +171,7 @@ __device__ __forceinline__ void codes_to_f16(const uint4& q, __half2 s_lo, __hal
 // ------------------------------------------------------------------ prepare / gather ------
 
 // CTA t: exponent and unscale of token t. All CTAs: hmax[r] = 0 and row_tok[r]. CTA 0: items
-// and the M-tile list (tiles in item order, then by row).
+// and the token-tile list (tiles of up to 128 rows, in item order, then by row).
 __global__ void __launch_bounds__(256) prefill_prepare_kernel(FfnArgs A, PrefillAux X) {
   __shared__ float wmax[8];
   __shared__ int scan[257];

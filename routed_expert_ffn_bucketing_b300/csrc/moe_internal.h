@@ -46,7 +46,7 @@ struct WsLayout {
                          // then the task counters of the two streaming kernels
   size_t xp16;           // f16 [P + T*n_shared][d]: prefill activations gathered by row, rescaled per token
   size_t xexp;           // int32 [T]: the exponent of each token's rescale (prefill)
-  size_t tiles;          // int2 [P/128 + items + 2]: prefill M tiles (item, first row), then the count
+  size_t tiles;          // int2 [P/128 + items + 2]: prefill token tiles (item, first row), then the count
   size_t part;           // fp32 [2][tasks][2][128]: stream-K partial sums (T <= 8 only)
   size_t cx;             // fp32 [T][d/32]: MMA accumulator inputs of the x16 blocks
   size_t ch;             // fp32 [P + T*n_shared][f/32]: MMA accumulator inputs of the h16 blocks
