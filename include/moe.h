@@ -90,8 +90,9 @@ typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
  *           (the fp32 debug mode), and DECODE asked for explicitly with T > 16, run the fp32
  *           SIMT kernels instead: exact-weight fp32 arithmetic, far slower than either
  *           tensor-core path.
- *  PREFILL  many tokens per expert: a tcgen05 grouped GEMM (activations by TMA, int8 weights
- *           converted to f16 into shared memory, fp32 accumulators in tensor memory). Needs
+ *  PREFILL  many tokens per expert: a tcgen05 grouped GEMM (int8 codes and token rows by TMA,
+ *           the codes converted to f16 straight into tensor memory as the MMA's A operand, the
+ *           token tile as its N, fp32 accumulators in tensor memory). Needs
  *           xdt = MOE_BF16, d a multiple of 256 and f of 128 (else MOE_EUNSUPPORTED).
  *  AUTO     xdt = MOE_F32: the fp32 SIMT kernels. xdt = MOE_BF16: DECODE for T <= 16 and
  *           PREFILL for T > 16; a shape that PREFILL does not take with T > 16 returns
