@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(FfnArgs A, P
       };
       // 16 columns per tcgen05.ld, two register sets: the next load is in flight while the
       // current columns are processed. (Loads of 32 columns, two sets of 32 registers, made
-      // the FFN 1.11x slower: 115 registers per thread against 72.)
+      // the FFN 1.11x slower: 115 registers per thread against 80.)
       uint32_t va[16], vb[16];
       tmem_ld16(t_row, va);
       tmem_ld_wait16(va);
