@@ -202,7 +202,12 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
         tmem_ld16(t_row + kRN + c, v1);
         tmem_ld16(t_row + 2 * kRN + c, v2);
         tmem_ld16(t_row + 3 * kRN + c, v3);
-        tmem_ld_wait();
+        // one wait for the four loads; the other three only tie their registers to it, so that
+        // no use of them is scheduled above the wait
+        tmem_ld_wait16(v0);
+        tmem_ld_wait16(v1);
+        tmem_ld_wait16(v2);
+        tmem_ld_wait16(v3);
         if (m < T) {
           float v[16];
 #pragma unroll

@@ -189,7 +189,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // tcgen05.wait::ld that also names the 16 registers of the load it waits for, so that the
 // compiler cannot move their uses above it.
 __device__ __forceinline__ void tmem_ld_wait16(uint32_t* r) {
