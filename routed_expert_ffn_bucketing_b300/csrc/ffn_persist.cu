@@ -253,7 +253,7 @@ __device__ __forceinline__ void load_bf16_block(const uint16_t* p, float* v) {
   const uint4* src = reinterpret_cast<const uint4*>(p);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 u = __ldg(src + q);
+    const uint4 u = __ldcg(src + q);  // through L2: an earlier kernel may have rewritten x
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int z = 0; z < 4; ++z) {
@@ -687,8 +687,10 @@ __global__ void __launch_bounds__(kPThreads, 1) ffn_persist_kernel(FfnArgs A, PA
   // ---- phase 0 --------------------------------------------------------------------------
   // Before the kernel's inputs from the bucketing kernel are complete (programmatic dependent
   // launch: this grid may start while that kernel runs): x to f16 in shared memory, with one
-  // power of two per block over all tokens. x itself was written before the layer's first
-  // kernel started. (CTAs start at different blocks, so they do not all read the same lines.)
+  // power of two per block over all tokens. x was written by a kernel that has completed: the
+  // kernel before this one lets it launch only after its own wait, which returns once every
+  // kernel before that one has completed. (CTAs start at different blocks, so they do not all
+  // read the same lines.)
   const int rot = (int)((blockIdx.x * 7u) % (uint32_t)nbd);
   const bool xmine = tid < T * nbd;
   const int xb = (tid / T + rot) % nbd, xt = tid % T;

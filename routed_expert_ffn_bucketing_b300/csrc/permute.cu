@@ -106,8 +106,10 @@ __global__ void __launch_bounds__(1024) bucket_count_kernel(const int32_t* __res
   __shared__ int cs[1024];
   __shared__ int warp_sums[33];
   const int i = threadIdx.x;
-  pdl_trigger();  // the expert FFN may launch and stage its activations meanwhile
   pdl_wait();  // topk_idx from the router
+  // the expert FFN may launch now and stage its activations meanwhile: after the wait, so that
+  // every kernel before this one has completed when it reads them
+  pdl_trigger();
   if (i < P) {
     int e = topk_idx[i];
     if (e < 0 || e >= E) {

@@ -500,8 +500,12 @@ __global__ void __launch_bounds__(512) route_tail_kernel(const float* __restrict
     nan_any = 0;
   }
   __syncthreads();
-  pdl_trigger();  // the expert FFN may launch and stage its activations meanwhile
-  pdl_wait();     // the router GEMV's partial sums
+  pdl_wait();  // the router GEMV's partial sums
+  // The expert FFN may launch now and stage its activations meanwhile. It reads them before its
+  // own wait, so it may start only once every kernel before this one has completed: after this
+  // wait, not before it (the router GEMV has completed, and it completed only after its own wait
+  // for the kernel before it, e.g. the RMS norm that wrote those activations).
+  pdl_trigger();
   if (tid == 0) {
     mbar_arrive_expect_tx(&bar, (uint32_t)(S * E * 4));
     for (int sp = 0; sp < S; ++sp)
